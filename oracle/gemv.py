@@ -1,0 +1,89 @@
+"""Oracle GEMV and element-wise tails (fp64).  Test infrastructure only.
+
+Definition followed ("feat(cuda): fuse activations and residual add into mmv f/q
+epilogues", Summary and What changed; "ggml-cpu: fuse element-wise epilogues (ADD,
+MUL, SILU) into ggml_compute_forward_mul_mat", What):
+
+    y[c, i]   = sum_k W[i, k] * x[c, k]            (decode case: one column, or a
+                                                   small batch of independent columns)
+    out[c, i] = tail(y[c, i])  with tail one of
+        NONE      y
+        SIGMOID   1 / (1 + exp(-y))
+        SILU      y * sigmoid(y)
+        SILU_MUL  silu(y) * m[c, i]    (activation, then the per-row multiplicand;
+                                        never silu(y * m))
+        ADD       y + r[c, i]          (residual add; the reshape view in between is an
+                                        index identity on contiguous memory)
+
+All arithmetic is float64; exp is libm's (numpy).  The dot product is numpy's own
+(non-BLAS) einsum loop, one thread.
+"""
+
+import numpy as np
+
+from . import quant
+
+EPI_NONE, EPI_SIGMOID, EPI_SILU, EPI_SILU_MUL, EPI_ADD = 0, 1, 2, 3, 4
+EPI_NAMES = {EPI_NONE: "none", EPI_SIGMOID: "sigmoid", EPI_SILU: "silu",
+             EPI_SILU_MUL: "silu_mul", EPI_ADD: "add"}
+NEEDS_AUX = (EPI_SILU_MUL, EPI_ADD)
+
+
+def sigmoid(y):
+    y = np.asarray(y, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-y))
+
+
+def silu(y):
+    y = np.asarray(y, dtype=np.float64)
+    return y * sigmoid(y)
+
+
+def apply_epilogue(y, epilogue, aux=None):
+    """The fused tail applied to the fp64 GEMV result y (any shape; aux same shape)."""
+    y = np.asarray(y, dtype=np.float64)
+    if epilogue == EPI_NONE:
+        return y.copy()
+    if epilogue == EPI_SIGMOID:
+        return sigmoid(y)
+    if epilogue == EPI_SILU:
+        return silu(y)
+    if epilogue in NEEDS_AUX:
+        a = np.asarray(aux, dtype=np.float64)
+        if a.shape != y.shape:
+            raise ValueError("aux must have the output's shape (no broadcast)")
+        return silu(y) * a if epilogue == EPI_SILU_MUL else y + a
+    raise ValueError("unknown epilogue %r" % (epilogue,))
+
+
+def _as_cols(v, n):
+    v = np.asarray(v, dtype=np.float64)
+    return v.reshape(-1, n)
+
+
+def gemv(raw, wtype, x, M, K, epilogue=EPI_NONE, aux=None, rows=None):
+    """out[c, i] for columns c of x (shape [ncols, K] or [K]) and rows i (all, or the
+    listed subset).  Returns float64 [ncols, len(rows)].  aux has shape [ncols, M]."""
+    W = quant.dequantize(raw, wtype, M, K, rows)          # [R, K] float64
+    X = _as_cols(x, K)                                    # [ncols, K]
+    y = np.einsum("ik,ck->ci", W, X)                      # plain sum over k, per (c, i)
+    a = None
+    if epilogue in NEEDS_AUX:
+        a = _as_cols(aux, M)
+        if rows is not None:
+            a = a[:, np.asarray(rows, dtype=np.int64)]
+    return apply_epilogue(y, epilogue, a)
+
+
+def abs_dot(raw, wtype, x, M, K, rows=None):
+    """sum_k |W[i,k] * x[c,k]| in fp64: the scale of the parity tolerance."""
+    W = quant.dequantize(raw, wtype, M, K, rows)
+    X = _as_cols(x, K)
+    return np.einsum("ik,ck->ci", np.abs(W), np.abs(X))
+
+
+def abs_w_dot(raw, wtype, e, M, K, rows=None):
+    """sum_k |W[i,k]| * e[c,k] for a non-negative per-element error e [ncols, K]."""
+    W = quant.dequantize(raw, wtype, M, K, rows)
+    return np.einsum("ik,ck->ci", np.abs(W), _as_cols(e, K))
