@@ -1,0 +1,467 @@
+// C ABI of gemvfuse: argument validation (sizes, alignment, the aliasing contract),
+// kernel planning for the TMA-streamed GEMV, dispatch, and the device error word.
+//
+// Aliasing contract ("feat(cuda): fuse activations and residual add into mmv f/q
+// epilogues", What changed): dst may alias the mul/add operand only as the same
+// element index (dst == aux, in place), and may not overlap the product inputs W and x,
+// which are read across the whole reduction.  Every call is validated on its own; no
+// overlap-guard state is kept between calls.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemvfuse.h"
+#include "gf_device.cuh"
+#include "gf_internal.h"
+
+namespace gf {
+
+__device__ unsigned int g_error_word;
+
+static thread_local int t_last_cuda_error = 0;
+
+static int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return GF_ERR_CUDA;
+}
+
+unsigned* device_error_word() {
+  static std::mutex mu;
+  static unsigned* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned*>(p);
+  }
+  return addr[dev];
+}
+
+static DeviceLimits device_limits() {
+  static std::mutex mu;
+  static DeviceLimits lim[64];
+  static bool have[64] = {false};
+  DeviceLimits fallback{152, 232448};  // GB300: 152 SMs, 227 KB opt-in shared memory
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return fallback;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev]) {
+    DeviceLimits l = fallback;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      l.sm_count = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess && v > 0)
+      l.smem_optin = v;
+    cudaGetLastError();
+    lim[dev] = l;
+    have[dev] = true;
+  }
+  return lim[dev];
+}
+
+// ------------------------------------------------------------------ helpers
+
+static int64_t row_bytes_of(int wtype, int64_t K) {
+  switch (wtype) {
+    case GF_F32: return 4 * K;
+    case GF_F16: return 2 * K;
+    case GF_Q8_0: return (K / 32) * 34;
+    default: return (K / 32) * 18;
+  }
+}
+
+static bool ranges_overlap(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+  if (!a || !b || abytes <= 0 || bbytes <= 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+static bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+static bool is_pow2(int64_t v) { return v >= 1 && (v & (v - 1)) == 0; }
+
+struct Call {
+  const void* W;
+  int wtype;
+  const float* x;
+  int64_t M, K;
+  int epi;
+  const float* aux;
+  const float* dst;
+  int64_t ncols;
+  const float* signs;
+  int64_t fwht_block, nsigns;
+  uint32_t flags;
+};
+
+static int validate(const Call& c) {
+  if (c.wtype < GF_F32 || c.wtype > GF_Q4_0) return GF_ERR_INVALID;
+  if (c.epi < GF_EPI_NONE || c.epi > GF_EPI_ADD) return GF_ERR_INVALID;
+  if (c.M < 0 || c.K < 0) return GF_ERR_INVALID;
+  if (c.M > INT32_MAX || c.K > INT32_MAX / 8) return GF_ERR_UNSUPPORTED;
+  if (c.ncols < 1 || c.ncols > kMaxCols) return c.ncols < 1 ? GF_ERR_INVALID : GF_ERR_UNSUPPORTED;
+  if ((c.wtype == GF_Q8_0 || c.wtype == GF_Q4_0) && c.K % 32 != 0) return GF_ERR_UNSUPPORTED;
+  const bool need_aux = (c.epi == GF_EPI_SILU_MUL || c.epi == GF_EPI_ADD);
+  if (c.M > 0) {
+    if (!c.dst) return GF_ERR_INVALID;
+    if (need_aux && !c.aux) return GF_ERR_INVALID;
+    if (c.K > 0 && (!c.W || !c.x)) return GF_ERR_INVALID;
+  }
+  const uintptr_t walign = c.wtype == GF_F32 ? 4 : 2;
+  if (c.W && !aligned(c.W, walign)) return GF_ERR_ALIGN;
+  if ((c.x && !aligned(c.x, 4)) || (c.dst && !aligned(c.dst, 4)) || (need_aux && c.aux && !aligned(c.aux, 4)))
+    return GF_ERR_ALIGN;
+  if (c.signs) {
+    if (!aligned(c.signs, 4)) return GF_ERR_ALIGN;
+    if (!is_pow2(c.fwht_block)) return GF_ERR_INVALID;
+    if (c.fwht_block > kMaxFusedFwhtBlock) return GF_ERR_UNSUPPORTED;
+    if (c.nsigns < 1) return GF_ERR_INVALID;
+    if (c.K % c.fwht_block != 0 || c.K % c.nsigns != 0) return GF_ERR_INVALID;
+  }
+  // aliasing: dst against W, x, signs (never) and aux (only exactly equal)
+  const int64_t dbytes = c.ncols * c.M * 4;
+  const int64_t wbytes = c.M * row_bytes_of(c.wtype, c.K);
+  const int64_t xbytes = c.ncols * c.K * 4;
+  if (ranges_overlap(c.dst, dbytes, c.W, wbytes)) return GF_ERR_ALIAS;
+  if (ranges_overlap(c.dst, dbytes, c.x, xbytes)) return GF_ERR_ALIAS;
+  if (c.signs && ranges_overlap(c.dst, dbytes, c.signs, c.nsigns * 4)) return GF_ERR_ALIAS;
+  if (need_aux && c.aux != c.dst && ranges_overlap(c.dst, dbytes, c.aux, dbytes)) return GF_ERR_ALIAS;
+  return GF_OK;
+}
+
+// Pick the number of consumer warps: no idle units per thread if possible, then more warps.
+static int choose_ncw(int units, int max_cw) {
+  int best = max_cw, best_waste = INT32_MAX;
+  for (int w = max_cw; w >= 4; --w) {
+    const int nt = 32 * w;
+    const int per = (units + nt - 1) / nt;
+    const int waste = per * nt - units;
+    if (waste < best_waste) {
+      best_waste = waste;
+      best = w;
+    }
+  }
+  return best;
+}
+
+static int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Plan the TMA-streamed kernel; returns false if the shape/alignment needs the generic one.
+static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
+  const int nc = static_cast<int>(c.ncols);
+  const int K = static_cast<int>(c.K);
+  const int64_t rb = row_bytes_of(c.wtype, c.K);
+  if (c.K < 8 || K % 8 != 0) return false;
+  if (rb % 16 != 0 || !aligned(c.W, 16) || !aligned(c.x, 16)) return false;
+  if (rb > INT32_MAX / 2) return false;
+  const bool quant = c.wtype == GF_Q8_0 || c.wtype == GF_Q4_0;
+  auto seg_of = [&](int klen) -> int { return static_cast<int>(row_bytes_of(c.wtype, klen)); };
+  // K chunk: whole K if x fits and the row fits a stage; else a multiple of the granule
+  int gran = 256;
+  if (c.signs) gran = std::max<int>(gran, static_cast<int>(c.fwht_block));
+  int kc = K;
+  const int64_t xs_cap = kXsMaxBytes / (4 * nc);
+  if (static_cast<int64_t>(K) > xs_cap || seg_of(K) > kSegMaxBytes) {
+    if (quant && K % 256 != 0) return false;
+    int bytes_per_gran = seg_of(gran);
+    int g_by_x = static_cast<int>(xs_cap / gran);
+    int g_by_seg = kSegMaxBytes / bytes_per_gran;
+    int g = std::min(g_by_x, g_by_seg);
+    if (g < 1) return false;
+    kc = g * gran;
+  }
+  const int n_kc = (K + kc - 1) / kc;
+  const int seg_full = seg_of(kc);
+  if (seg_full % 16 != 0) return false;
+  if (n_kc > 1) {
+    const int last = K - (n_kc - 1) * kc;
+    if (seg_of(last) % 16 != 0 || last % 8 != 0) return false;
+  }
+  const int max_cw = stream_max_cw(nc);
+  const int ncw = choose_ncw(kc / 8, max_cw);
+  const int grid = static_cast<int>(std::min<int64_t>(lim.sm_count, c.M));
+  const int rows_base = static_cast<int>(c.M / grid);
+  const int rows_extra = static_cast<int>(c.M % grid);
+  const int rows_max = rows_base + (rows_extra ? 1 : 0);
+  int RC = std::min(rows_max, std::max(1, kRedMaxBytes / (ncw * nc * 4)));
+  RC = std::min(RC, 256);
+  const int rmax = stream_rmax(nc);
+  int R = std::max(1, std::min(rmax, kStageTargetBytes / seg_full));
+  R = std::min(R, RC);
+  const int xs_bytes = round_up(nc * kc * 4, 128);
+  const int aux_bytes = round_up(nc * RC * 4, 128);
+  const int red_bytes = round_up(RC * ncw * nc * 4, 128);
+  const int fixed = kBarBytes + xs_bytes + aux_bytes + red_bytes;
+  int stage_bytes = round_up(R * seg_full, 128);
+  int NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
+  while (NS < 2 && R > 1) {
+    --R;
+    stage_bytes = round_up(R * seg_full, 128);
+    NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
+  }
+  if (NS < 2) return false;
+  p.path = PATH_STREAM;
+  p.grid = grid;
+  p.threads = stream_threads(nc);
+  p.smem = fixed + NS * stage_bytes;
+  StreamArgs& s = p.s;
+  std::memset(&s, 0, sizeof(s));
+  s.M = c.M;
+  s.K = K;
+  s.epi = c.epi;
+  s.row_bytes = static_cast<int>(rb);
+  s.kc_len = kc;
+  s.n_kc = n_kc;
+  s.R = R;
+  s.NS = NS;
+  s.stage_bytes = stage_bytes;
+  s.RC = RC;
+  s.ncw = ncw;
+  s.rows_base = rows_base;
+  s.rows_extra = rows_extra;
+  s.fwht_B = c.signs ? static_cast<int>(c.fwht_block) : 0;
+  s.nsigns = c.signs ? static_cast<int>(c.nsigns) : 1;
+  s.fwht_scale = c.signs ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.fwht_block))) : 1.0f;
+  s.off_xs = kBarBytes;
+  s.off_aux = s.off_xs + xs_bytes;
+  s.off_red = s.off_aux + aux_bytes;
+  s.off_ring = s.off_red + red_bytes;
+  // launch threads: producer warp + consumer warps actually used
+  p.threads = 32 * (1 + ncw);
+  return true;
+}
+
+static int plan_call(const Call& c, Plan& p, int* generic_smem, int* generic_grid) {
+  const DeviceLimits lim = device_limits();
+  if (plan_stream(c, lim, p)) return PATH_STREAM;
+  const int64_t smem = c.ncols * c.K * 4;
+  if (smem > lim.smem_optin) return GF_ERR_UNSUPPORTED;
+  *generic_smem = static_cast<int>(smem);
+  const int64_t rows_per_cta = 8;  // one row per warp of the 256-thread generic CTA
+  int64_t grid = (c.M + rows_per_cta - 1) / rows_per_cta;
+  grid = std::min<int64_t>(grid, 2 * lim.sm_count);
+  *generic_grid = static_cast<int>(std::max<int64_t>(grid, 1));
+  p.path = PATH_GENERIC;
+  return PATH_GENERIC;
+}
+
+static int launch_call(const Call& c, float* dst, cudaStream_t st) {
+  Plan p;
+  int gsmem = 0, ggrid = 0;
+  const int path = plan_call(c, p, &gsmem, &ggrid);
+  if (path < 0) return path;
+  unsigned* err = device_error_word();
+  if (!err) return cuda_fail(cudaGetLastError());
+  const bool pdl = (c.flags & GF_FLAG_PDL) != 0;
+  int e;
+  if (path == PATH_STREAM) {
+    StreamArgs& s = p.s;
+    s.W = static_cast<const uint8_t*>(c.W);
+    s.x = c.x;
+    s.aux = c.aux;
+    s.dst = dst;
+    s.signs = c.signs;
+    s.err = err;
+    e = (c.wtype == GF_F32 || c.wtype == GF_F16) ? launch_stream_float(c.wtype, static_cast<int>(c.ncols), p, st, pdl)
+                                               : launch_stream_block(c.wtype, static_cast<int>(c.ncols), p, st, pdl);
+  } else {
+    GenericArgs g;
+    g.W = static_cast<const uint8_t*>(c.W);
+    g.x = c.x;
+    g.aux = c.aux;
+    g.dst = dst;
+    g.signs = c.signs;
+    g.err = err;
+    g.M = c.M;
+    g.K = static_cast<int>(c.K);
+    g.epi = c.epi;
+    g.row_bytes = row_bytes_of(c.wtype, c.K);
+    g.fwht_B = c.signs ? static_cast<int>(c.fwht_block) : 0;
+    g.nsigns = c.signs ? static_cast<int>(c.nsigns) : 1;
+    g.fwht_scale = c.signs ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.fwht_block))) : 1.0f;
+    e = launch_generic(c.wtype, static_cast<int>(c.ncols), g, ggrid, gsmem, st, pdl);
+  }
+  if (e != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(e));
+  return GF_OK;
+}
+
+static Call make_call(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
+                      const float* aux, const float* dst, const gf_opts* opts) {
+  Call c;
+  c.W = W;
+  c.wtype = wtype;
+  c.x = x;
+  c.M = M;
+  c.K = K;
+  c.epi = epilogue;
+  c.aux = (epilogue == GF_EPI_SILU_MUL || epilogue == GF_EPI_ADD) ? aux : nullptr;
+  c.dst = dst;
+  c.ncols = 1;
+  c.signs = nullptr;
+  c.fwht_block = 0;
+  c.nsigns = 0;
+  c.flags = 0;
+  if (opts) {
+    c.ncols = opts->ncols == 0 ? 1 : opts->ncols;
+    c.signs = opts->fwht_signs;
+    c.fwht_block = opts->fwht_block;
+    c.nsigns = opts->nsigns;
+    c.flags = opts->flags;
+  }
+  return c;
+}
+
+static int check_view(const gf_opts* opts, int64_t M) {
+  if (!opts) return GF_OK;
+  bool any = false;
+  int64_t prod = 1;
+  for (int i = 0; i < 4; ++i) {
+    const int64_t v = opts->view_ne[i];
+    if (v < 0) return GF_ERR_INVALID;
+    if (v > 0) {
+      any = true;
+      if (prod > INT64_MAX / v) return GF_ERR_INVALID;
+      prod *= v;
+    }
+  }
+  if (any && prod != M) return GF_ERR_INVALID;
+  return GF_OK;
+}
+
+}  // namespace gf
+
+using namespace gf;
+
+extern "C" {
+
+int gemv_fused_ex(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
+                  const float* aux, float* dst, const gf_opts* opts, void* stream) {
+  const Call c = make_call(W, wtype, x, M, K, epilogue, aux, dst, opts);
+  int v = validate(c);
+  if (v != GF_OK) return v;
+  v = check_view(opts, M);
+  if (v != GF_OK) return v;
+  if (M == 0) return GF_OK;
+  return launch_call(c, dst, static_cast<cudaStream_t>(stream));
+}
+
+int gemv_fused(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
+               const float* aux, float* dst, void* stream) {
+  return gemv_fused_ex(W, wtype, x, M, K, epilogue, aux, dst, nullptr, stream);
+}
+
+int gf_plan(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue, const float* aux,
+            const float* dst, const gf_opts* opts, int64_t info[8]) {
+  const Call c = make_call(W, wtype, x, M, K, epilogue, aux, dst, opts);
+  int v = validate(c);
+  if (v != GF_OK) return v;
+  v = check_view(opts, M);
+  if (v != GF_OK) return v;
+  if (M == 0) return 0;  // nothing would be launched
+  Plan p;
+  int gsmem = 0, ggrid = 0;
+  const int path = plan_call(c, p, &gsmem, &ggrid);
+  if (path < 0) return path;
+  if (info) {
+    for (int i = 0; i < 8; ++i) info[i] = 0;
+    if (path == PATH_STREAM) {
+      info[0] = p.grid; info[1] = p.threads; info[2] = p.s.R; info[3] = p.s.NS;
+      info[4] = p.s.kc_len; info[5] = p.smem; info[6] = p.s.RC;
+    } else {
+      info[0] = ggrid; info[1] = 256; info[5] = gsmem;
+    }
+  }
+  return path;
+}
+
+int fwht_signed(const float* x, const float* signs, float* dst, int64_t n, int64_t block, int64_t nsigns,
+                void* stream) {
+  if (n < 0 || !is_pow2(block)) return GF_ERR_INVALID;
+  if (block > 16384) return GF_ERR_UNSUPPORTED;
+  if (n % block != 0) return GF_ERR_INVALID;
+  if (signs && (nsigns < 1 || n % nsigns != 0)) return GF_ERR_INVALID;
+  if (n == 0) return GF_OK;
+  if (!x || !dst) return GF_ERR_INVALID;
+  if (!aligned(x, 4) || !aligned(dst, 4) || (signs && !aligned(signs, 4))) return GF_ERR_ALIGN;
+  if (x != dst && ranges_overlap(x, n * 4, dst, n * 4)) return GF_ERR_ALIAS;
+  if (signs && ranges_overlap(signs, nsigns * 4, dst, n * 4)) return GF_ERR_ALIAS;
+  if (n > INT32_MAX) return GF_ERR_UNSUPPORTED;
+  const int e = launch_fwht(x, signs, dst, n, static_cast<int>(block), signs ? static_cast<int>(nsigns) : 1,
+                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(e));
+  return GF_OK;
+}
+
+int gf_elementwise(int op, const float* a, const float* b, int64_t nb, float* dst, int64_t n, void* stream) {
+  if (op < GF_EW_SIGMOID || op > GF_EW_ADD) return GF_ERR_INVALID;
+  if (n < 0) return GF_ERR_INVALID;
+  const bool binary = (op == GF_EW_MUL || op == GF_EW_ADD);
+  if (binary && (nb < 1 || n % nb != 0)) return GF_ERR_INVALID;
+  if (n == 0) return GF_OK;
+  if (!a || !dst || (binary && !b)) return GF_ERR_INVALID;
+  if (!aligned(a, 4) || !aligned(dst, 4) || (binary && !aligned(b, 4))) return GF_ERR_ALIGN;
+  if (a != dst && ranges_overlap(a, n * 4, dst, n * 4)) return GF_ERR_ALIAS;
+  if (binary && b != dst && ranges_overlap(b, nb * 4, dst, n * 4)) return GF_ERR_ALIAS;
+  const int e = launch_elementwise(op, a, binary ? b : nullptr, binary ? nb : 1, dst, n,
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(e));
+  return GF_OK;
+}
+
+int gf_dequantize(const void* W, int wtype, int64_t M, int64_t K, float* out, void* stream) {
+  if (wtype < GF_F32 || wtype > GF_Q4_0) return GF_ERR_INVALID;
+  if (M < 0 || K < 0) return GF_ERR_INVALID;
+  if ((wtype == GF_Q8_0 || wtype == GF_Q4_0) && K % 32 != 0) return GF_ERR_UNSUPPORTED;
+  if (M == 0 || K == 0) return GF_OK;
+  if (!W || !out) return GF_ERR_INVALID;
+  if (!aligned(W, wtype == GF_F32 ? 4 : 2) || !aligned(out, 4)) return GF_ERR_ALIGN;
+  const int64_t rb = row_bytes_of(wtype, K);
+  if (ranges_overlap(W, M * rb, out, M * K * 4)) return GF_ERR_ALIAS;
+  const int e = launch_dequantize(wtype, static_cast<const uint8_t*>(W), M, K, rb, out,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(e));
+  return GF_OK;
+}
+
+int gf_device_status(int reset) {
+  unsigned* err = device_error_word();
+  if (!err) return cuda_fail(cudaGetLastError());
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned v = 0;
+  e = cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (reset) {
+    e = cudaMemset(err, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return (v & ERRBIT_TIMEOUT) ? GF_ERR_TIMEOUT : GF_OK;
+}
+
+const char* gf_status_string(int status) {
+  switch (status) {
+    case GF_OK: return "GF_OK";
+    case GF_ERR_INVALID: return "GF_ERR_INVALID: bad argument";
+    case GF_ERR_ALIAS: return "GF_ERR_ALIAS: dst overlaps an input it may not alias";
+    case GF_ERR_UNSUPPORTED: return "GF_ERR_UNSUPPORTED: shape or option not implemented";
+    case GF_ERR_ALIGN: return "GF_ERR_ALIGN: misaligned pointer";
+    case GF_ERR_CUDA: return "GF_ERR_CUDA: CUDA call failed";
+    case GF_ERR_TIMEOUT: return "GF_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+    default: return "unknown gf_status";
+  }
+}
+
+int gf_last_cuda_error(void) { return t_last_cuda_error; }
+
+int gf_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,265 @@
+// TMA-streamed persistent GEMV with fused prologue/epilogue.
+//
+// One CTA per SM owns a contiguous range of rows.  Warp 0 is the producer: one lane
+// streams the CTA's weight bytes, tile by tile (R rows x one K chunk), into a ring of
+// shared-memory stages with 1-D bulk async copies (no multicast), signalling a "full"
+// mbarrier per stage.  Warps 1..ncw are consumers: each thread owns fixed 8-weight
+// units of the K chunk, keeps the matching x values in registers while it walks the
+// R rows of a stage, decodes the weights (F32/F16/Q8_0/Q4_0) and accumulates with
+// packed f32x2 FMAs.  Per tile, each warp reduces its per-row partial sums with
+// shuffles and stores them to shared memory; after the last K chunk the partials of
+// the consumer warps are added in a fixed order (deterministic), the fused tail is
+// applied with the prefetched aux operand, and dst is written once.
+//
+// x (all columns of one K chunk) is staged in shared memory with a bulk copy; with a
+// signed-FWHT prologue the consumers transform it in place before use, so x' never
+// leaves the chip.  Every wait is bounded; a timeout sets the device error word and
+// the kernel returns after draining its own copies.
+#pragma once
+
+#include "gf_device.cuh"
+#include "gf_internal.h"
+
+namespace gf {
+
+template <int WT>
+__host__ __device__ constexpr int seg_bytes_of(int klen) {
+  return WT == WT_F32 ? 4 * klen : WT == WT_F16 ? 2 * klen : WT == WT_Q8_0 ? (klen / 32) * 34 : (klen / 32) * 18;
+}
+
+template <int WT, int NC, int RMAX>
+__device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int units, int ctid,
+                                             int nt, const float* xs, int xstride,
+                                             float2 (&acc)[RMAX][NC]) {
+  for (int u = ctid; u < units; u += nt) {
+    uint32_t e0, e1;
+    unit_x_offsets<WT>(static_cast<uint32_t>(u), e0, e1);
+    float2 xv[NC][4];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const float4 p = *reinterpret_cast<const float4*>(xs + c * xstride + e0);
+      const float4 q = *reinterpret_cast<const float4*>(xs + c * xstride + e1);
+      xv[c][0] = make_float2(p.x, p.y);
+      xv[c][1] = make_float2(p.z, p.w);
+      xv[c][2] = make_float2(q.x, q.y);
+      xv[c][3] = make_float2(q.z, q.w);
+    }
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      if (r < rows) {
+        const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+        float2 v[4];
+        float d;
+        decode_unit<WT>(ld, static_cast<uint32_t>(u), v, d);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          if constexpr (WT == WT_F32 || WT == WT_F16) {
+            float2 t = acc[r][c];
+            t = ffma2(v[0], xv[c][0], t);
+            t = ffma2(v[1], xv[c][1], t);
+            t = ffma2(v[2], xv[c][2], t);
+            t = ffma2(v[3], xv[c][3], t);
+            acc[r][c] = t;
+          } else {
+            // block partial first, then scaled by d into the running sum
+            float2 p = make_float2(0.0f, 0.0f);
+            p = ffma2(v[0], xv[c][0], p);
+            p = ffma2(v[1], xv[c][1], p);
+            p = ffma2(v[2], xv[c][2], p);
+            p = ffma2(v[3], xv[c][3], p);
+            acc[r][c] = ffma2(make_float2(d, d), p, acc[r][c]);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int WT, int NC, int RMAX>
+__global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(const StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t full0 = sbase, empty0 = sbase + 8u * a.NS, xbar = sbase + 16u * a.NS;
+  float* xs = reinterpret_cast<float*>(smem + a.off_xs);
+  float* auxs = reinterpret_cast<float*>(smem + a.off_aux);
+  float* red = reinterpret_cast<float*>(smem + a.off_red);
+  const uint32_t ring = sbase + static_cast<uint32_t>(a.off_ring);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarBytes - 8);
+
+  const int cta = blockIdx.x;
+  const int64_t r0 = static_cast<int64_t>(cta) * a.rows_base + min(cta, a.rows_extra);
+  const int nrows = a.rows_base + (cta < a.rows_extra ? 1 : 0);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < a.NS; ++i) {
+      mbar_init(full0 + 8u * i, 1);
+      mbar_init(empty0 + 8u * i, static_cast<uint32_t>(a.ncw));
+    }
+    mbar_init(xbar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      int it = 0;
+      bool ok = true;
+      for (int rc0 = 0; rc0 < nrows && ok; rc0 += a.RC) {
+        const int nrc = min(a.RC, nrows - rc0);
+        for (int kc = 0; kc < a.n_kc && ok; ++kc) {
+          const int klen = min(a.kc_len, a.K - kc * a.kc_len);
+          const int seg = seg_bytes_of<WT>(klen);
+          const int64_t segoff = seg_bytes_of<WT>(kc * a.kc_len);
+          for (int t0 = 0; t0 < nrc; t0 += a.R) {
+            const int rows = min(a.R, nrc - t0);
+            const int slot = it % a.NS, round = it / a.NS;
+            if (!mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1),
+                                    abort_flag, a.err)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = full0 + 8u * slot;
+            const uint32_t dst = ring + static_cast<uint32_t>(slot) * a.stage_bytes;
+            const int64_t row = r0 + rc0 + t0;
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(rows * seg));
+            if (a.n_kc == 1) {
+              bulk_g2s(dst, a.W + row * a.row_bytes, static_cast<uint32_t>(rows * seg), full, pol);
+            } else {
+              for (int r = 0; r < rows; ++r)
+                bulk_g2s(dst + static_cast<uint32_t>(r * seg), a.W + (row + r) * a.row_bytes + segoff,
+                         static_cast<uint32_t>(seg), full, pol);
+            }
+            ++it;
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: wait (bounded) until every copy this thread issued has landed.
+        for (int i = max(0, it - a.NS); i < it; ++i)
+          (void)mbar_wait(full0 + 8u * (i % a.NS), static_cast<uint32_t>((i / a.NS) & 1));
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    // Every consumer thread runs the same sequence of named barriers whether or not a
+    // wait gave up; after an abort the remaining work is skipped, not the barriers.
+    const int cw = warp - 1, ctid = threadIdx.x - 32, nt = a.ncw * 32;
+    const bool need_aux = (a.epi == EPI_SILU_MUL || a.epi == EPI_ADD);
+    pdl_wait();  // x, aux and dst may belong to the preceding grid
+    int it = 0;
+    uint32_t xphase = 0;
+    bool ok = true;
+    auto cbar = [&]() { named_bar_sync(1, static_cast<uint32_t>(nt)); };
+    for (int rc0 = 0; rc0 < nrows; rc0 += a.RC) {
+      const int nrc = min(a.RC, nrows - rc0);
+      if (need_aux)
+        for (int i = ctid; i < nrc * NC; i += nt) {
+          const int c = i / nrc, r = i - c * nrc;
+          auxs[c * a.RC + r] = a.aux[c * a.M + r0 + rc0 + r];  // plain load: aux may alias dst
+        }
+      for (int kc = 0; kc < a.n_kc; ++kc) {
+        const int klen = min(a.kc_len, a.K - kc * a.kc_len);
+        if (a.n_kc > 1 || rc0 == 0) {
+          cbar();  // nobody still reads the previous x chunk
+          if (ctid == 0 && !*abort_flag) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(NC * klen * 4));
+            for (int c = 0; c < NC; ++c)
+              bulk_g2s(smem_u32(xs + c * klen), a.x + static_cast<int64_t>(c) * a.K + kc * a.kc_len,
+                       static_cast<uint32_t>(klen * 4), xbar);
+          }
+          ok = ok && mbar_wait_or_abort(xbar, xphase, abort_flag, a.err);
+          xphase ^= 1u;
+          if (a.fwht_B > 0)
+            fwht_smem(xs, NC * klen, a.fwht_B, klen, static_cast<int64_t>(kc) * a.kc_len, a.signs,
+                      a.nsigns, a.fwht_scale, ctid, nt, cbar);
+          else
+            cbar();
+        }
+        const int units = klen / 8;
+        const int seg = seg_bytes_of<WT>(klen);
+        for (int t0 = 0; t0 < nrc; t0 += a.R, ++it) {
+          const int rows = min(a.R, nrc - t0);
+          const int slot = it % a.NS, round = it / a.NS;
+          ok = ok && mbar_wait_or_abort(full0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag,
+                                        a.err);
+          float2 acc[RMAX][NC];
+#pragma unroll
+          for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[r][c] = make_float2(0.0f, 0.0f);
+          if (ok)
+            consume_tile<WT, NC, RMAX>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows,
+                                       units, ctid, nt, xs, klen, acc);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+          // warp reduction of the RMAX*NC partial sums, up to 32 values at a time
+          constexpr int V = RMAX * NC;
+          constexpr int G = V >= 32 ? 32 : V > 8 ? 16 : V > 4 ? 8 : V > 2 ? 4 : V > 1 ? 2 : 1;
+#pragma unroll
+          for (int g0 = 0; g0 < V; g0 += G) {
+            float vals[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+              const int idx = g0 + j < V ? g0 + j : 0;
+              vals[j] = g0 + j < V ? acc[idx / NC][idx % NC].x + acc[idx / NC][idx % NC].y : 0.0f;
+            }
+            const float s = WarpVecReduce<G>::run(vals, lane);
+            const int j = lane >> (5 - WarpVecReduce<G>::kLog);
+            if (lane == WarpVecReduce<G>::owner(j) && g0 + j < V) {
+              const int r = (g0 + j) / NC, c = (g0 + j) % NC;
+              if (r < rows) {
+                float* p = red + ((t0 + r) * a.ncw + cw) * NC + c;
+                *p = (kc == 0) ? s : (*p + s);
+              }
+            }
+          }
+        }
+      }
+      cbar();  // all partial sums of this row chunk are in `red`
+      if (ok) {
+        for (int i = ctid; i < nrc * NC; i += nt) {
+          const int c = i / nrc, r = i - c * nrc;
+          float y = 0.0f;
+          for (int w = 0; w < a.ncw; ++w) y += red[(r * a.ncw + w) * NC + c];
+          const float av = need_aux ? auxs[c * a.RC + r] : 0.0f;
+          a.dst[c * a.M + r0 + rc0 + r] = apply_tail(a.epi, y, av);
+        }
+      }
+      cbar();  // red / auxs may be reused by the next row chunk
+    }
+  }
+  __syncthreads();
+}
+
+template <int WT, int NC>
+int launch_stream_t(const Plan& p, cudaStream_t st, bool pdl) {
+  constexpr int RMAX = stream_rmax(NC);
+  auto kern = gemv_stream_kernel<WT, NC, RMAX>;
+  static int configured_smem[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && configured_smem[dev] < p.smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
+    if (e != cudaSuccess) return e;
+    configured_smem[dev] = p.smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, p.s);
+}
+
+}  // namespace gf

@@ -1,0 +1,410 @@
+// Device helpers shared by the gemvfuse kernels: inline-PTX wrappers (mbarrier,
+// bulk async copy, programmatic dependent launch, packed f32x2 arithmetic), the
+// weight unit decoders, the fused tails and the shared-memory Walsh-Hadamard passes.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace gf {
+
+enum { WT_F32 = 0, WT_F16 = 1, WT_Q8_0 = 2, WT_Q4_0 = 3 };
+enum { EPI_NONE = 0, EPI_SIGMOID = 1, EPI_SILU = 2, EPI_SILU_MUL = 3, EPI_ADD = 4 };
+enum { ERRBIT_TIMEOUT = 1u };
+
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// As mbar_wait, but also gives up as soon as *abort is set, and sets *abort (and the
+// error word) when its own time limit runs out, so the rest of the CTA stops waiting.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort, unsigned* err) {
+  if (*abort) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      if (err) atomicOr(err, static_cast<unsigned>(ERRBIT_TIMEOUT));
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 1-D bulk async copy global -> shared (no multicast), completion counted on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's memory; allow the
+// following grid to launch.  Both are no-ops without a programmatic dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+__device__ __forceinline__ void set_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// Packed two-lane fp32 arithmetic (one instruction, two IEEE-rounded results).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// ------------------------------------------------------------------ loaders
+// The unit decoders read weight bytes through a loader so the same decode code runs
+// on a shared-memory stage (the streaming kernel) and on global memory (dequantize).
+
+struct SmemLoader {
+  uint32_t base;  // shared-state-space address of row start
+  __device__ __forceinline__ uint32_t u16(uint32_t off) const {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(base + off));
+    return v;
+  }
+  __device__ __forceinline__ uint4 v4(uint32_t off) const {  // 16-byte aligned
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(base + off));
+    return v;
+  }
+  // 32 bits at a 2-byte-aligned offset.
+  __device__ __forceinline__ uint32_t u32_a2(uint32_t off) const {
+    return __byte_perm(u16(off), u16(off + 2), 0x5410);
+  }
+};
+
+struct GmemLoader {
+  const uint8_t* base;
+  __device__ __forceinline__ uint32_t u16(uint32_t off) const {
+    return *reinterpret_cast<const uint16_t*>(base + off);
+  }
+  __device__ __forceinline__ uint4 v4(uint32_t off) const {
+    return *reinterpret_cast<const uint4*>(base + off);
+  }
+  __device__ __forceinline__ uint32_t u32_a2(uint32_t off) const {
+    return __byte_perm(u16(off), u16(off + 2), 0x5410);
+  }
+};
+
+// ------------------------------------------------------------------ unit decoders
+// A "unit" is 8 weights of one row.  Unit u covers, within a row (or K chunk):
+//   F32, F16, Q8_0 : elements 8u .. 8u+7
+//   Q4_0           : block b = u/4, word i = u%4 of its 16 code bytes:
+//                    elements 32b+4i .. +3 (low nibbles) and 32b+16+4i .. +3 (high)
+// decode_unit() returns the 8 values as four float2 pairs in that element order,
+// together with the block scale (1 for F32/F16).  Quant codes are turned into floats
+// exactly: the byte is placed in the low mantissa bits of 2^23 and 2^23 (+ offset)
+// is subtracted, which is exact for every code.
+
+constexpr float kMagic = 8388608.0f;  // 2^23
+
+__device__ __forceinline__ float2 magic_pair(uint32_t w, uint32_t sel0, float bias) {
+  const float a = __uint_as_float(__byte_perm(w, 0x4B000000u, sel0));
+  const float b = __uint_as_float(__byte_perm(w, 0x4B000000u, sel0 + 1));
+  return fadd2(make_float2(a, b), make_float2(bias, bias));
+}
+
+__device__ __forceinline__ float h2f(uint32_t bits16) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+}
+
+template <int WT, class L>
+__device__ __forceinline__ void decode_unit(const L& ld, uint32_t u, float2 (&v)[4], float& d) {
+  if constexpr (WT == WT_F32) {
+    const uint4 a = ld.v4(u * 32u);
+    const uint4 b = ld.v4(u * 32u + 16u);
+    v[0] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
+    v[1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
+    v[2] = make_float2(__uint_as_float(b.x), __uint_as_float(b.y));
+    v[3] = make_float2(__uint_as_float(b.z), __uint_as_float(b.w));
+    d = 1.0f;
+  } else if constexpr (WT == WT_F16) {
+    const uint4 a = ld.v4(u * 16u);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h;
+      *reinterpret_cast<uint32_t*>(&h) = w[i];
+      v[i] = __half22float2(h);
+    }
+    d = 1.0f;
+  } else if constexpr (WT == WT_Q8_0) {
+    const uint32_t b = u >> 2, i = u & 3u;
+    const uint32_t off = b * 34u;
+    d = h2f(ld.u16(off));
+    const uint32_t w0 = ld.u32_a2(off + 2u + 8u * i) ^ 0x80808080u;  // bytes q + 128
+    const uint32_t w1 = ld.u32_a2(off + 6u + 8u * i) ^ 0x80808080u;
+    const float bias = -(kMagic + 128.0f);
+    v[0] = magic_pair(w0, 0x7540u, bias);
+    v[1] = magic_pair(w0, 0x7542u, bias);
+    v[2] = magic_pair(w1, 0x7540u, bias);
+    v[3] = magic_pair(w1, 0x7542u, bias);
+  } else {  // WT_Q4_0
+    const uint32_t b = u >> 2, i = u & 3u;
+    const uint32_t off = b * 18u;
+    d = h2f(ld.u16(off));
+    const uint32_t w = ld.u32_a2(off + 2u + 4u * i);
+    const uint32_t lo = w & 0x0F0F0F0Fu;
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+    const float bias = -(kMagic + 8.0f);
+    v[0] = magic_pair(lo, 0x7540u, bias);
+    v[1] = magic_pair(lo, 0x7542u, bias);
+    v[2] = magic_pair(hi, 0x7540u, bias);
+    v[3] = magic_pair(hi, 0x7542u, bias);
+  }
+}
+
+// Element offsets (within the row / chunk) of unit u's first and second group of 4.
+template <int WT>
+__device__ __forceinline__ void unit_x_offsets(uint32_t u, uint32_t& e0, uint32_t& e1) {
+  if constexpr (WT == WT_Q4_0) {
+    e0 = (u >> 2) * 32u + (u & 3u) * 4u;
+    e1 = e0 + 16u;
+  } else {
+    e0 = u * 8u;
+    e1 = e0 + 4u;
+  }
+}
+
+// Scalar decode of element k of a row in global memory (generic kernel).
+template <int WT>
+__device__ __forceinline__ float decode_elem(const uint8_t* row, int64_t k) {
+  if constexpr (WT == WT_F32) {
+    return reinterpret_cast<const float*>(row)[k];
+  } else if constexpr (WT == WT_F16) {
+    return __half2float(reinterpret_cast<const __half*>(row)[k]);
+  } else if constexpr (WT == WT_Q8_0) {
+    const int64_t b = k >> 5;
+    const int j = static_cast<int>(k & 31);
+    const uint8_t* blk = row + b * 34;
+    const float d = h2f(*reinterpret_cast<const uint16_t*>(blk));
+    return d * static_cast<float>(static_cast<int8_t>(blk[2 + j]));
+  } else {
+    const int64_t b = k >> 5;
+    const int j = static_cast<int>(k & 31);
+    const uint8_t* blk = row + b * 18;
+    const float d = h2f(*reinterpret_cast<const uint16_t*>(blk));
+    const uint32_t byte = blk[2 + (j & 15)];
+    const int q = static_cast<int>(j < 16 ? (byte & 15u) : (byte >> 4));
+    return d * static_cast<float>(q - 8);
+  }
+}
+
+// ------------------------------------------------------------------ fused tails
+// One definition each, used by the fused epilogue and by the unfused element-wise
+// control kernel so the two paths round identically.
+
+__device__ __forceinline__ float tail_sigmoid(float y) { return 1.0f / (1.0f + expf(-y)); }
+__device__ __forceinline__ float tail_silu(float y) { return y * tail_sigmoid(y); }
+
+__device__ __forceinline__ float apply_tail(int epi, float y, float a) {
+  switch (epi) {
+    case EPI_SIGMOID: return tail_sigmoid(y);
+    case EPI_SILU: return tail_silu(y);
+    case EPI_SILU_MUL: return tail_silu(y) * a;
+    case EPI_ADD: return y + a;
+    default: return y;
+  }
+}
+
+// ------------------------------------------------------------------ warp reduction
+// Sums V per-lane values over the 32 lanes of a warp.  Lanes trade halves of their
+// value vector (V - 1 shuffles in total for V <= 32) and finish with a butterfly.
+// Afterwards lane l holds the total of value index (l >> (5 - log2 V)) & (V - 1) for
+// V <= 32; red_owner() says which lane holds value j.
+template <int V>
+struct WarpVecReduce {
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be a power of two <= 32");
+  static constexpr int kLog = (V >= 32) ? 5 : (V >= 16) ? 4 : (V >= 8) ? 3 : (V >= 4) ? 2 : (V >= 2) ? 1 : 0;
+  __device__ __forceinline__ static float run(float (&v)[V], int lane) {
+    int n = V;
+#pragma unroll
+    for (int step = 0; step < kLog; ++step) {
+      const int off = 16 >> step;
+      const bool upper = (lane & off) != 0;
+      const int half = V >> (step + 1);
+#pragma unroll
+      for (int j = 0; j < half; ++j) {
+        const float send = upper ? v[j] : v[j + half];
+        const float keep = upper ? v[j + half] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+      n >>= 1;
+    }
+    float s = v[0];
+#pragma unroll
+    for (int off = 16 >> kLog; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    return s;
+  }
+  __device__ __forceinline__ static int owner(int j) { return j << (5 - kLog); }
+};
+
+// ------------------------------------------------------------------ Walsh-Hadamard
+// In-place transform of `total` floats in shared memory, laid out as segments of
+// `seg_len` elements (one per column), each a whole number of blocks of B (a power of
+// two).  Element e of a segment sits at column position koff + e.  The first pass
+// multiplies by signs[(koff + e) % nsigns] while loading (signs may be null), the
+// last multiplies by `scale` while storing.  Radix-4 passes (two butterfly stages
+// (a, b) -> (a + b, a - b) at strides h and 2h), then one radix-2 pass if log2 B is
+// odd.  `sync()` must be a barrier over the `nthr` participating threads; it is
+// called after every pass.
+template <class Sync>
+__device__ __forceinline__ void fwht_smem(float* buf, int total, int B, int seg_len, int64_t koff,
+                                          const float* __restrict__ signs, int nsigns, float scale,
+                                          int tid, int nthr, Sync sync) {
+  int log2b = 0;
+  while ((1 << log2b) < B) ++log2b;
+  const int npass = (log2b >> 1) + (log2b & 1);
+  auto sign_of = [&](int p) -> float {
+    if (signs == nullptr) return 1.0f;
+    const int64_t pos = koff + (p % seg_len);
+    return __ldg(signs + (pos % nsigns));
+  };
+  if (log2b == 0) {
+    for (int p = tid; p < total; p += nthr) buf[p] = buf[p] * sign_of(p) * scale;
+    sync();
+    return;
+  }
+  int h = 1;
+  for (int pass = 0; pass < npass; ++pass) {
+    const bool first = (pass == 0), last = (pass == npass - 1);
+    const bool radix4 = (h * 4 <= B);
+    if (radix4) {
+      const int per_blk = B >> 2;
+      for (int g = tid; g < (total >> 2); g += nthr) {
+        const int blk = g / per_blk, gi = g - blk * per_blk;
+        const int lo = gi & (h - 1), hi = gi / h;
+        const int p0 = blk * B + hi * (4 * h) + lo;
+        float a0 = buf[p0], a1 = buf[p0 + h], a2 = buf[p0 + 2 * h], a3 = buf[p0 + 3 * h];
+        if (first) {
+          a0 *= sign_of(p0); a1 *= sign_of(p0 + h);
+          a2 *= sign_of(p0 + 2 * h); a3 *= sign_of(p0 + 3 * h);
+        }
+        const float b0 = a0 + a1, b1 = a0 - a1, b2 = a2 + a3, b3 = a2 - a3;
+        float c0 = b0 + b2, c1 = b1 + b3, c2 = b0 - b2, c3 = b1 - b3;
+        if (last) { c0 *= scale; c1 *= scale; c2 *= scale; c3 *= scale; }
+        buf[p0] = c0; buf[p0 + h] = c1; buf[p0 + 2 * h] = c2; buf[p0 + 3 * h] = c3;
+      }
+      h *= 4;
+    } else {  // final radix-2 stage, h == B / 2
+      const int per_blk = B >> 1;
+      for (int g = tid; g < (total >> 1); g += nthr) {
+        const int blk = g / per_blk, lo = g - blk * per_blk;
+        const int p0 = blk * B + lo;
+        float a0 = buf[p0], a1 = buf[p0 + h];
+        if (first) { a0 *= sign_of(p0); a1 *= sign_of(p0 + h); }
+        float c0 = a0 + a1, c1 = a0 - a1;
+        if (last) { c0 *= scale; c1 *= scale; }
+        buf[p0] = c0; buf[p0 + h] = c1;
+      }
+      h *= 2;
+    }
+    sync();
+  }
+}
+
+}  // namespace gf

@@ -1,0 +1,93 @@
+// Host/device shared declarations for the gemvfuse library (not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gf {
+
+// Kernel-side limits of the TMA-streamed GEMV.
+constexpr int kMaxCols = 8;
+constexpr int kMaxStages = 8;
+constexpr int kBarBytes = 256;              // mbarrier area at the start of shared memory
+constexpr int kXsMaxBytes = 64 * 1024;      // x chunk (all columns) kept in shared memory
+constexpr int kSegMaxBytes = 32 * 1024;     // bytes of one row's K chunk
+constexpr int kStageTargetBytes = 32 * 1024;
+constexpr int kRedMaxBytes = 16 * 1024;
+constexpr int kMaxFusedFwhtBlock = 8192;
+
+// Rows per tile and consumer warps, as functions of the column count.
+__host__ __device__ constexpr int stream_rmax(int nc) { return nc == 1 ? 16 : nc == 2 ? 8 : 4; }
+__host__ __device__ constexpr int stream_max_cw(int nc) { return nc <= 2 ? 16 : 8; }
+__host__ __device__ constexpr int stream_threads(int nc) { return 32 * (1 + stream_max_cw(nc)); }
+
+struct StreamArgs {
+  const uint8_t* W;
+  const float* x;
+  const float* aux;
+  float* dst;
+  const float* signs;
+  unsigned* err;
+  int64_t M;
+  int K;
+  int epi;
+  int row_bytes;     // bytes of a full row
+  int kc_len;        // elements per K chunk
+  int n_kc;          // K chunks
+  int R;             // rows per tile
+  int NS;            // ring stages
+  int stage_bytes;   // bytes reserved per stage
+  int RC;            // rows per finalize chunk
+  int ncw;           // consumer warps
+  int rows_base;     // rows per CTA (the first rows_extra CTAs take one more)
+  int rows_extra;
+  int fwht_B;        // 0 = no prologue
+  int nsigns;
+  float fwht_scale;
+  int off_xs, off_aux, off_red, off_ring;
+};
+
+struct GenericArgs {
+  const uint8_t* W;
+  const float* x;
+  const float* aux;
+  float* dst;
+  const float* signs;
+  unsigned* err;
+  int64_t M;
+  int K;
+  int epi;
+  int64_t row_bytes;
+  int fwht_B;
+  int nsigns;
+  float fwht_scale;
+};
+
+enum { PATH_STREAM = 1, PATH_GENERIC = 2 };
+
+struct Plan {
+  int path;
+  int grid, threads, smem;
+  StreamArgs s;   // valid when path == PATH_STREAM (pointers filled by the caller)
+};
+
+struct DeviceLimits {
+  int sm_count;
+  int smem_optin;
+};
+
+// Launchers (return cudaError_t).  `pdl` requests programmatic stream serialization.
+int launch_stream_float(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);  // F32, F16
+int launch_stream_block(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);  // Q8_0, Q4_0
+int launch_generic(int wtype, int ncols, const GenericArgs& a, int grid, int smem,
+                   cudaStream_t st, bool pdl);
+int launch_fwht(const float* x, const float* signs, float* dst, int64_t n, int B, int nsigns,
+                cudaStream_t st);
+int launch_elementwise(int op, const float* a, const float* b, int64_t nb, float* dst, int64_t n,
+                       cudaStream_t st);
+int launch_dequantize(int wtype, const uint8_t* W, int64_t M, int64_t K, int64_t row_bytes,
+                      float* out, cudaStream_t st);
+
+unsigned* device_error_word();  // this device's error word (nullptr on failure)
+
+}  // namespace gf

@@ -1,0 +1,140 @@
+// Stand-alone kernels: the signed FWHT, the unfused element-wise control ops and the
+// dequantize test hook.
+#include "gf_device.cuh"
+#include "gf_internal.h"
+
+namespace gf {
+
+// ------------------------------------------------------------------ signed FWHT
+// Each CTA transforms E consecutive elements (a whole number of blocks) in shared
+// memory: load (coalesced), sign-multiply on the first pass, radix-4/radix-2 passes,
+// scale on the last pass, store.  dst may equal x: a CTA reads its whole segment
+// before the first barrier and writes only after the last one.
+constexpr int kFwhtThreads = 256;
+
+__global__ void __launch_bounds__(kFwhtThreads) fwht_signed_kernel(const float* x, const float* signs,
+                                                                   float* dst, int64_t n, int B, int nsigns,
+                                                                   float scale, int E) {
+  extern __shared__ __align__(16) float buf[];
+  pdl_wait();
+  pdl_trigger();
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * E;
+  const int len = static_cast<int>(min(static_cast<int64_t>(E), n - base));
+  for (int i = threadIdx.x; i < len; i += blockDim.x) buf[i] = x[base + i];
+  __syncthreads();
+  fwht_smem(buf, len, B, len, base, signs, nsigns, scale, threadIdx.x, blockDim.x,
+            []() { __syncthreads(); });
+  for (int i = threadIdx.x; i < len; i += blockDim.x) dst[base + i] = buf[i];
+}
+
+int launch_fwht(const float* x, const float* signs, float* dst, int64_t n, int B, int nsigns,
+                cudaStream_t st) {
+  // one block per CTA for large blocks; several small blocks (up to 4096 elements) per CTA
+  int64_t E = B >= 1024 ? B : (4096 / B) * B;
+  if (E > n) E = n;
+  const int64_t grid = (n + E - 1) / E;
+  const int smem = static_cast<int>(E * 4);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem > 48 * 1024 && dev < 64 && configured[dev] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(fwht_signed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = smem;
+  }
+  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(B)));
+  fwht_signed_kernel<<<static_cast<unsigned>(grid), kFwhtThreads, smem, st>>>(x, signs, dst, n, B, nsigns,
+                                                                            scale, static_cast<int>(E));
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ element-wise control
+__global__ void elementwise_kernel(int op, const float* a, const float* b, int64_t nb, float* dst,
+                                   int64_t n) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float av = a[i];
+    float r;
+    switch (op) {
+      case 1: r = tail_sigmoid(av); break;                 // GF_EW_SIGMOID
+      case 2: r = tail_silu(av); break;                    // GF_EW_SILU
+      case 3: r = av * b[nb == n ? i : i % nb]; break;     // GF_EW_MUL
+      default: r = av + b[nb == n ? i : i % nb]; break;    // GF_EW_ADD
+    }
+    dst[i] = r;
+  }
+}
+
+int launch_elementwise(int op, const float* a, const float* b, int64_t nb, float* dst, int64_t n,
+                       cudaStream_t st) {
+  int64_t grid = (n + 255) / 256;
+  if (grid > 152 * 16) grid = 152 * 16;
+  elementwise_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(op, a, b, nb, dst, n);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dequantize hook
+// Same unit decoders as the streaming kernel (through a global-memory loader), one
+// thread per 8-weight unit; the product with the block scale is exact in fp32.
+template <int WT>
+__global__ void dequantize_units_kernel(const uint8_t* W, int64_t M, int64_t K, int64_t row_bytes,
+                                        float* out) {
+  const int64_t units_per_row = K / 8;
+  const int64_t total = M * units_per_row;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total; t += stride) {
+    const int64_t row = t / units_per_row;
+    const uint32_t u = static_cast<uint32_t>(t - row * units_per_row);
+    const GmemLoader ld{W + row * row_bytes};
+    float2 v[4];
+    float d;
+    decode_unit<WT>(ld, u, v, d);
+    uint32_t e0, e1;
+    unit_x_offsets<WT>(u, e0, e1);
+    float* o = out + row * K;
+    o[e0 + 0] = v[0].x * d; o[e0 + 1] = v[0].y * d; o[e0 + 2] = v[1].x * d; o[e0 + 3] = v[1].y * d;
+    o[e1 + 0] = v[2].x * d; o[e1 + 1] = v[2].y * d; o[e1 + 2] = v[3].x * d; o[e1 + 3] = v[3].y * d;
+  }
+}
+
+// Element-wise decode for F32/F16 rows whose K is not a multiple of 8.
+template <int WT>
+__global__ void dequantize_elems_kernel(const uint8_t* W, int64_t M, int64_t K, int64_t row_bytes,
+                                        float* out) {
+  const int64_t total = M * K;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total; t += stride) {
+    const int64_t row = t / K, k = t - row * K;
+    out[t] = decode_elem<WT>(W + row * row_bytes, k);
+  }
+}
+
+int launch_dequantize(int wtype, const uint8_t* W, int64_t M, int64_t K, int64_t row_bytes, float* out,
+                      cudaStream_t st) {
+  const bool by_unit = (K % 8 == 0) &&
+                       ((wtype != WT_F32 && wtype != WT_F16) ||
+                        (reinterpret_cast<uintptr_t>(W) % 16 == 0 && row_bytes % 16 == 0));
+  const int64_t work = by_unit ? M * (K / 8) : M * K;
+  int64_t grid = (work + 255) / 256;
+  if (grid > 152 * 16) grid = 152 * 16;
+  if (grid < 1) grid = 1;
+  const unsigned g = static_cast<unsigned>(grid);
+  switch (wtype) {
+    case WT_F32:
+      if (by_unit) dequantize_units_kernel<WT_F32><<<g, 256, 0, st>>>(W, M, K, row_bytes, out);
+      else dequantize_elems_kernel<WT_F32><<<g, 256, 0, st>>>(W, M, K, row_bytes, out);
+      break;
+    case WT_F16:
+      if (by_unit) dequantize_units_kernel<WT_F16><<<g, 256, 0, st>>>(W, M, K, row_bytes, out);
+      else dequantize_elems_kernel<WT_F16><<<g, 256, 0, st>>>(W, M, K, row_bytes, out);
+      break;
+    case WT_Q8_0: dequantize_units_kernel<WT_Q8_0><<<g, 256, 0, st>>>(W, M, K, row_bytes, out); break;
+    case WT_Q4_0: dequantize_units_kernel<WT_Q4_0><<<g, 256, 0, st>>>(W, M, K, row_bytes, out); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gf

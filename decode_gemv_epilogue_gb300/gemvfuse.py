@@ -1,0 +1,171 @@
+"""Thin ctypes binding over libgemvfuse.so (the C ABI in include/gemvfuse.h).
+
+Argument marshalling only: every computation runs in the library's CUDA kernels.
+Arrays are passed as torch CUDA tensors (or raw integer device addresses); the
+stream defaults to torch's current CUDA stream.  Importing this module loads the
+library and raises ImportError if it has not been built -- there is no fallback.
+"""
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgemvfuse.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libgemvfuse.so is not built (run __graft_entry__.build()): %s" % LIB_PATH)
+_lib = ctypes.CDLL(LIB_PATH)
+
+# enums (include/gemvfuse.h)
+F32, F16, Q8_0, Q4_0 = 0, 1, 2, 3
+EPI_NONE, EPI_SIGMOID, EPI_SILU, EPI_SILU_MUL, EPI_ADD = 0, 1, 2, 3, 4
+EW_SIGMOID, EW_SILU, EW_MUL, EW_ADD = 1, 2, 3, 4
+OK, ERR_INVALID, ERR_ALIAS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+FLAG_PDL = 1
+PATH_NONE, PATH_STREAM, PATH_GENERIC = 0, 1, 2
+
+_vp, _i64, _i32, _u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
+
+
+class GfOpts(ctypes.Structure):
+    _fields_ = [("ncols", _i64), ("fwht_signs", _vp), ("fwht_block", _i64), ("nsigns", _i64),
+                ("view_ne", _i64 * 4), ("flags", _u32)]
+
+
+def _sig(name, args, res=_i32):
+    f = getattr(_lib, name)
+    f.argtypes = args
+    f.restype = res
+    return f
+
+
+_gemv_fused = _sig("gemv_fused", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, _vp])
+_gemv_fused_ex = _sig("gemv_fused_ex", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp,
+                                        ctypes.POINTER(GfOpts), _vp])
+_fwht_signed = _sig("fwht_signed", [_vp, _vp, _vp, _i64, _i64, _i64, _vp])
+_elementwise = _sig("gf_elementwise", [_i32, _vp, _vp, _i64, _vp, _i64, _vp])
+_dequantize = _sig("gf_dequantize", [_vp, _i32, _i64, _i64, _vp, _vp])
+_plan = _sig("gf_plan", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, ctypes.POINTER(GfOpts),
+                         ctypes.POINTER(_i64 * 8)])
+_device_status = _sig("gf_device_status", [_i32])
+_status_string = _sig("gf_status_string", [_i32], ctypes.c_char_p)
+_last_cuda_error = _sig("gf_last_cuda_error", [])
+_version = _sig("gf_version", [])
+
+#: the raw C functions, for callers that want the status codes themselves
+raw = _lib
+
+
+class GemvFuseError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        msg = "%s: %s" % (what, status_string(status))
+        if status == ERR_CUDA:
+            msg += " (cudaError %d)" % _last_cuda_error()
+        super().__init__(msg)
+
+
+def status_string(status):
+    return _status_string(int(status)).decode()
+
+
+def version():
+    return _version()
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    return a.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st, what):
+    if st != OK:
+        raise GemvFuseError(st, what)
+
+
+def make_opts(ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, view=None, pdl=False):
+    o = GfOpts()
+    o.ncols = ncols
+    o.fwht_signs = _ptr(fwht_signs)
+    o.fwht_block = fwht_block
+    if nsigns is None:
+        nsigns = fwht_block if fwht_signs is not None and isinstance(fwht_signs, int) \
+            else (fwht_signs.numel() if fwht_signs is not None else 0)
+    o.nsigns = nsigns
+    v = list(view or ())
+    for i in range(4):
+        o.view_ne[i] = v[i] if i < len(v) else 0
+    o.flags = FLAG_PDL if pdl else 0
+    return o
+
+
+def gemv_fused(W, wtype, x, M, K, epilogue, aux, dst, stream=None, check=True):
+    st = _gemv_fused(_ptr(W), wtype, _ptr(x), M, K, epilogue, _ptr(aux), _ptr(dst), _stream(stream))
+    if check:
+        _check(st, "gemv_fused")
+    return st
+
+
+def gemv_fused_ex(W, wtype, x, M, K, epilogue, aux, dst, ncols=1, fwht_signs=None, fwht_block=0,
+                  nsigns=None, view=None, pdl=False, stream=None, check=True):
+    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, view, pdl)
+    st = _gemv_fused_ex(_ptr(W), wtype, _ptr(x), M, K, epilogue, _ptr(aux), _ptr(dst),
+                        ctypes.byref(o), _stream(stream))
+    if check:
+        _check(st, "gemv_fused_ex")
+    return st
+
+
+def fwht_signed(x, signs, dst, n, block, nsigns=None, stream=None, check=True):
+    if nsigns is None:
+        nsigns = 0 if signs is None else (block if isinstance(signs, int) else signs.numel())
+    st = _fwht_signed(_ptr(x), _ptr(signs), _ptr(dst), n, block, nsigns, _stream(stream))
+    if check:
+        _check(st, "fwht_signed")
+    return st
+
+
+def elementwise(op, a, b, dst, n, nb=None, stream=None, check=True):
+    if nb is None:
+        nb = n if b is None or isinstance(b, int) else b.numel()
+    st = _elementwise(op, _ptr(a), _ptr(b), nb, _ptr(dst), n, _stream(stream))
+    if check:
+        _check(st, "gf_elementwise")
+    return st
+
+
+def dequantize(W, wtype, M, K, out, stream=None, check=True):
+    st = _dequantize(_ptr(W), wtype, M, K, _ptr(out), _stream(stream))
+    if check:
+        _check(st, "gf_dequantize")
+    return st
+
+
+def plan(W, wtype, x, M, K, epilogue, aux, dst, **opts):
+    """(path, info) without launching: path 1 = TMA-streamed, 2 = generic, <0 = error."""
+    o = make_opts(**opts)
+    info = (_i64 * 8)()
+    path = _plan(_ptr(W), wtype, _ptr(x), M, K, epilogue, _ptr(aux), _ptr(dst), ctypes.byref(o),
+                 ctypes.byref(info))
+    keys = ("grid", "threads", "stage_rows", "stages", "k_chunk", "smem", "row_chunk")
+    return path, dict(zip(keys, list(info)[:7]))
+
+
+def device_status(reset=False):
+    return _device_status(1 if reset else 0)
+
+
+def last_cuda_error():
+    return _last_cuda_error()

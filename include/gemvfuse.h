@@ -1,0 +1,160 @@
+/*
+ * gemvfuse -- decode-path GEMV with a fused element-wise epilogue and a signed
+ * Walsh-Hadamard prologue, for GB300 (sm_103a).  C ABI.
+ *
+ * Operations defined by the pages this library restates (cited by title, section):
+ *  [EPI]  "feat(cuda): fuse activations and residual add into mmv f/q epilogues",
+ *         Summary / What changed: y = W x for one output column (ncols_dst == 1), with
+ *         the tail sigmoid | silu | silu(y)*m | y + r folded into the GEMV; a reshape
+ *         between the product and the tail is an index identity; the destination may
+ *         alias the mul/add operand (same element index) but never the product inputs.
+ *  [FWHT] "vulkan: fuse the sign multiply into the Hadamard FWHT", Overview: the sign
+ *         vector is multiplied in while the row is loaded, before the transform, and is
+ *         broadcast over its own length.
+ *  [CPU]  "ggml-cpu: fuse element-wise epilogues (ADD, MUL, SILU) into
+ *         ggml_compute_forward_mul_mat", Guards / Correctness: epilogue operands are F32,
+ *         same shape, contiguous; F32/F16/Q8_0/Q4_0 weights; fused == unfused values.
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller.  The library never
+ *    allocates, frees or keeps a pointer after the call returns.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is enqueued
+ *    asynchronously; the call returns once it is launched.
+ *  - Arguments are validated on the host before anything is launched.  A non-zero
+ *    return means nothing was launched, except GF_ERR_CUDA (launch failure; see
+ *    gf_last_cuda_error()).
+ *  - Vectors are contiguous float32.  A batch of ncols columns is column-major:
+ *    x is [ncols][K], aux and dst are [ncols][M].
+ *  - The library holds no state between calls other than per-device launch limits
+ *    and a device error word (see gf_device_status()).
+ */
+#ifndef GEMVFUSE_H
+#define GEMVFUSE_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GF_API __attribute__((visibility("default")))
+#else
+#define GF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight storage formats; each row of W holds K elements, rows are contiguous.
+ *  GF_F32  : float32 [M][K].
+ *  GF_F16  : IEEE binary16 [M][K].
+ *  GF_Q8_0 : per 32 elements a 34-byte block {binary16 d; int8 q[32]}; w = d*q.
+ *  GF_Q4_0 : per 32 elements an 18-byte block {binary16 d; uint8 qs[16]}; byte j holds
+ *            element j (low nibble) and element j+16 (high nibble); w = d*(nibble-8).
+ * (Format names from [CPU] Correctness; the layouts are the ggml block convention.) */
+typedef enum { GF_F32 = 0, GF_F16 = 1, GF_Q8_0 = 2, GF_Q4_0 = 3 } gf_wtype;
+
+/* Fused tails ([EPI] What changed; [CPU] What):
+ *  NONE      dst = y
+ *  SIGMOID   dst = 1/(1+exp(-y))
+ *  SILU      dst = y*sigmoid(y)
+ *  SILU_MUL  dst = silu(y)*aux          (aux = the per-row activation_mul operand)
+ *  ADD       dst = y + aux              (residual add; dst == aux allowed, in place) */
+typedef enum {
+  GF_EPI_NONE = 0, GF_EPI_SIGMOID = 1, GF_EPI_SILU = 2, GF_EPI_SILU_MUL = 3, GF_EPI_ADD = 4
+} gf_epilogue;
+
+/* Stand-alone element-wise ops (the unfused control path): dst[i] = op(a[i], b[i % nb]). */
+typedef enum { GF_EW_SIGMOID = 1, GF_EW_SILU = 2, GF_EW_MUL = 3, GF_EW_ADD = 4 } gf_ewop;
+
+typedef enum {
+  GF_OK = 0,
+  GF_ERR_INVALID = -1,      /* bad enum, size, null pointer or view shape            */
+  GF_ERR_ALIAS = -2,        /* dst overlaps an input it may not alias                */
+  GF_ERR_UNSUPPORTED = -3,  /* valid but outside what is implemented (e.g. K%32 != 0 */
+                            /* for a block format, ncols > 8, FWHT block > 8192)     */
+  GF_ERR_ALIGN = -4,        /* pointer not aligned to its element type               */
+  GF_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed                  */
+  GF_ERR_TIMEOUT = -6       /* a kernel gave up on a bounded wait (device status)    */
+} gf_status;
+
+/* gf_opts.flags */
+#define GF_FLAG_PDL 1u   /* launch with programmatic dependent launch: the kernel may
+                            start while the previous kernel in `stream` still runs and
+                            streams W before waiting for it.  Only valid when no kernel
+                            still running in `stream` writes W. */
+
+typedef struct {
+  int64_t ncols;             /* columns in the batch, 1..8 (0 is read as 1)            */
+  const float* fwht_signs;   /* non-NULL: signed-FWHT prologue on every column of x     */
+  int64_t fwht_block;        /* FWHT block B: power of two, 1..8192, K % B == 0         */
+  int64_t nsigns;            /* length of fwht_signs; K % nsigns == 0; element k of a   */
+                             /* column uses fwht_signs[k % nsigns]                      */
+  int64_t view_ne[4];        /* optional view of each dst column (all 0 = none); the    */
+                             /* product of the non-zero entries must equal M. A view of */
+                             /* contiguous memory is an index identity ([EPI] What      */
+                             /* changed: result written with the matmul geometry).      */
+  uint32_t flags;            /* GF_FLAG_*                                              */
+} gf_opts;
+
+/* y = W x with the fused tail, one column.  [EPI] Summary, What changed.
+ *  W    : device, M rows in format `wtype` (see gf_wtype).  Alignment: 4 B for F32,
+ *         2 B otherwise; 16 B (and K % 256 == 0 for block formats) selects the
+ *         TMA-streamed fast kernel, anything else the generic kernel.
+ *  x    : device float32 [K].           aux : device float32 [M], required iff the
+ *  dst  : device float32 [M].                 epilogue is SILU_MUL or ADD.
+ *  Aliasing: dst may equal aux exactly; any other overlap of dst with W, x or aux
+ *  returns GF_ERR_ALIAS.  M == 0 launches nothing.  K == 0 gives y = 0. */
+GF_API int gemv_fused(const void* W, int wtype, const float* x, int64_t M, int64_t K,
+               int epilogue, const float* aux, float* dst, void* stream);
+
+/* gemv_fused plus the options in `opts` (may be NULL): a batch of ncols independent
+ * columns sharing one pass over W; the signed-FWHT prologue
+ *     x'_c[b*B + j] = (1/sqrt(B)) sum_t H_B[j][t] s[(b*B + t) % nsigns] x_c[b*B + t]
+ * (Sylvester H, [FWHT] Overview) applied to each column before the product, with x'
+ * kept on chip; the dst view check; and GF_FLAG_PDL.  fwht_signs must not overlap dst. */
+GF_API int gemv_fused_ex(const void* W, int wtype, const float* x, int64_t M, int64_t K,
+                  int epilogue, const float* aux, float* dst, const gf_opts* opts,
+                  void* stream);
+
+/* Signed FWHT, stand-alone ([FWHT] Overview): for every block of `block` consecutive
+ * elements of x[0..n), dst_b = H_block (x_b * s) / sqrt(block), with element i using
+ * signs[i % nsigns]; signs == NULL means all +1 (the plain normalised transform).
+ *  block : power of two, 1..16384, n % block == 0;  n % nsigns == 0 when signs != NULL.
+ *  dst == x is allowed (in place); other overlaps with x or signs: GF_ERR_ALIAS. */
+GF_API int fwht_signed(const float* x, const float* signs, float* dst, int64_t n,
+                int64_t block, int64_t nsigns, void* stream);
+
+/* Unfused control ([CPU] Correctness compares fused against unfused outputs):
+ * dst[i] = op(a[i], b[i % nb]) for i < n; SIGMOID and SILU ignore b.  Uses the same
+ * device functions as the fused tails.  dst may equal a or b exactly. */
+GF_API int gf_elementwise(int op, const float* a, const float* b, int64_t nb, float* dst,
+                   int64_t n, void* stream);
+
+/* Test hook: out[i*K + k] = decoded W[i][k] as float32, through the same unit decoders
+ * the fast GEMV kernel uses.  Every decoded value is exact in float32. */
+GF_API int gf_dequantize(const void* W, int wtype, int64_t M, int64_t K, float* out, void* stream);
+
+/* Which kernel gemv_fused_ex would launch for these arguments (host only, launches
+ * nothing): 0 = none (M == 0), 1 = TMA-streamed kernel, 2 = generic kernel, <0 = the
+ * gf_status the call would return.  `info` (may be NULL) receives
+ *   {grid, block_threads, stage_rows, stages, k_chunk, smem_bytes, row_chunk, 0}. */
+GF_API int gf_plan(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
+            const float* aux, const float* dst, const gf_opts* opts, int64_t info[8]);
+
+/* Device error word of the current device: GF_OK, or GF_ERR_TIMEOUT if a kernel gave up
+ * on a bounded wait since the last reset.  Synchronises with the device.  reset != 0
+ * clears it. */
+GF_API int gf_device_status(int reset);
+
+/* Human-readable name of a gf_status value. */
+GF_API const char* gf_status_string(int status);
+
+/* cudaError_t of the last failing CUDA call made by this library in this thread. */
+GF_API int gf_last_cuda_error(void);
+
+/* Library ABI version. */
+GF_API int gf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GEMVFUSE_H */

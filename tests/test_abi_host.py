@@ -1,0 +1,160 @@
+"""Host-side tests of the C ABI that need no GPU: the library loads and exports every
+declared entry point, and argument validation (sizes, alignment, the aliasing contract
+of "feat(cuda): fuse activations and residual add into mmv f/q epilogues", What changed)
+returns the documented status before anything is launched.  Pointers here are fake,
+well-separated device addresses; no call below reaches a CUDA launch."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "gemvfuse.h")
+# fake, non-overlapping device addresses (validation never dereferences them)
+W, X, A, D, S = (1 << 40), (2 << 40), (3 << 40), (4 << 40), (5 << 40)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"GF_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_abi():
+    names = set(declared_functions())
+    assert {"gemv_fused", "gemv_fused_ex", "fwht_signed", "gf_elementwise", "gf_dequantize", "gf_plan",
+            "gf_device_status", "gf_status_string", "gf_last_cuda_error", "gf_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(so, name), name
+
+
+def test_library_hides_internal_symbols(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm not available")
+    exported = {l.split()[-1] for l in out.stdout.splitlines() if " T " in l}
+    assert set(declared_functions()) <= exported
+    assert not any(n.startswith("_ZN2gf") for n in exported)
+
+
+def test_status_strings(lib):
+    assert lib.status_string(0) == "GF_OK"
+    for s in (-1, -2, -3, -4, -5, -6):
+        assert lib.status_string(s).startswith("GF_ERR_")
+    assert lib.version() == 1
+
+
+def g(lib, *a, **k):
+    return lib.gemv_fused_ex(*a, check=False, stream=0, **k)
+
+
+@pytest.mark.parametrize("args,kw,expect", [
+    ((W, 7, X, 16, 32, 0, None, D), {}, -1),                    # bad weight type
+    ((W, 0, X, 16, 32, 9, None, D), {}, -1),                    # bad epilogue
+    ((W, 0, X, -1, 32, 0, None, D), {}, -1),                    # negative M
+    ((W, 2, X, 16, 48, 0, None, D), {}, -3),                    # Q8_0 with K % 32 != 0
+    ((W, 3, X, 16, 33, 0, None, D), {}, -3),                    # Q4_0 with K % 32 != 0
+    ((W, 1, X, 16, 32, 0, None, D), {"ncols": 9}, -3),          # more than 8 columns
+    ((W, 1, X, 16, 32, 0, None, D), {"ncols": -1}, -1),
+    ((W, 1, X, 16, 32, 0, None, None), {}, -1),                 # null dst
+    ((W, 1, X, 16, 32, 4, None, D), {}, -1),                    # ADD without operand
+    ((W, 1, X, 16, 32, 3, None, D), {}, -1),                    # SILU_MUL without operand
+    ((None, 1, X, 16, 32, 0, None, D), {}, -1),                 # null W
+    ((W + 1, 1, X, 16, 32, 0, None, D), {}, -4),                # W not 2-byte aligned
+    ((W + 2, 0, X, 16, 32, 0, None, D), {}, -4),                # F32 W not 4-byte aligned
+    ((W, 1, X + 2, 16, 32, 0, None, D), {}, -4),                # x misaligned
+    ((W, 1, X, 16, 32, 0, None, D + 1), {}, -4),                # dst misaligned
+    ((W, 1, X, 16, 32, 0, None, W + 4), {}, -2),                # dst inside W
+    ((W, 1, X, 16, 32, 0, None, X + 64), {}, -2),               # dst overlaps x
+    ((W, 1, X, 16, 32, 4, A, A + 4), {}, -2),                   # dst partially overlaps aux
+    ((W, 1, X, 16, 32, 3, A, A + 60), {}, -2),
+    ((W, 1, X, 16, 32, 0, None, D), {"view": (4, 5)}, -1),      # view product != M
+    ((W, 1, X, 16, 32, 0, None, D), {"view": (-4, 4)}, -1),
+    ((W, 1, X, 16, 32, 0, None, D), {"fwht_signs": S, "fwht_block": 12, "nsigns": 12}, -1),
+    ((W, 1, X, 16, 32, 0, None, D), {"fwht_signs": S, "fwht_block": 64, "nsigns": 64}, -1),   # K % B
+    ((W, 1, X, 16, 16384, 0, None, D), {"fwht_signs": S, "fwht_block": 16384, "nsigns": 16384}, -3),
+    ((W, 1, X, 16, 32, 0, None, D), {"fwht_signs": S, "fwht_block": 32, "nsigns": 0}, -1),
+    ((W, 1, X, 16, 32, 0, None, D), {"fwht_signs": S, "fwht_block": 32, "nsigns": 5}, -1),
+    ((W, 1, X, 16, 32, 0, None, S + 8), {"fwht_signs": S, "fwht_block": 32, "nsigns": 32}, -2),
+])
+def test_gemv_validation(lib, args, kw, expect):
+    assert g(lib, *args, **kw) == expect
+
+
+def test_gemv_accepts_exact_in_place_and_empty(lib):
+    # M == 0: nothing to launch, OK without touching the device
+    assert g(lib, W, 1, X, 0, 32, 4, A, A) == 0
+    assert g(lib, None, 1, None, 0, 0, 0, None, None) == 0
+    # dst == aux exactly is allowed; plan says which kernel would run
+    path, info = lib.plan(W, 1, X, 4096, 4096, 4, A, A, view=(32, 128))
+    assert path == lib.PATH_STREAM and info["grid"] > 0
+    # dst adjacent to (not overlapping) W is fine
+    path, _ = lib.plan(W, 1, X, 16, 32, 0, None, W + 16 * 64)
+    assert path in (lib.PATH_STREAM, lib.PATH_GENERIC)
+
+
+@pytest.mark.parametrize("wt,K,w,expect_path", [
+    (1, 4096, W, 1), (3, 4096, W, 1), (2, 4096, W, 1), (0, 512, W, 1),
+    (1, 36, W, 2), (1, 4096, W + 2, 2), (3, 96, W, 2), (2, 224, W, 2), (0, 4, W, 2),
+])
+def test_plan_path_selection(lib, wt, K, w, expect_path):
+    path, info = lib.plan(w, wt, X, 1000, K, 0, None, D)
+    assert path == expect_path
+    if path == lib.PATH_STREAM:
+        assert info["smem"] <= 232448 and 2 <= info["stages"] <= 8
+        assert info["threads"] % 32 == 0 and info["threads"] <= 544
+
+
+def test_plan_k_chunks_for_batches_and_long_rows(lib):
+    _, info = lib.plan(W, 1, X, 5120, 5120, 4, A, A, ncols=8, fwht_signs=S, fwht_block=1024, nsigns=1024)
+    assert info["k_chunk"] % 1024 == 0 and info["k_chunk"] < 5120
+    _, info = lib.plan(W, 0, X, 4096, 14336, 0, None, D)
+    assert info["k_chunk"] < 14336
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((X, None, D, 100, 3), -1),        # block not a power of two
+    ((X, None, D, 100, 64), -1),       # n % block
+    ((X, None, D, 1 << 16, 32768), -3),
+    ((X, S, D, 64, 32, 0), -1),        # nsigns 0
+    ((X, S, D, 64, 32, 3), -1),        # n % nsigns
+    ((X + 2, None, D, 64, 32), -4),
+    ((X, None, X + 4, 64, 32), -2),    # partial overlap with x
+    ((X, S, S, 64, 32, 32), -2),       # dst over the signs
+    ((None, None, D, 64, 32), -1),
+])
+def test_fwht_validation(lib, args, expect):
+    x, s, d, n, b = args[:5]
+    ns = args[5] if len(args) > 5 else (32 if s else None)
+    assert lib.fwht_signed(x, s, d, n, b, nsigns=ns, stream=0, check=False) == expect
+
+
+def test_fwht_empty_is_ok(lib):
+    assert lib.fwht_signed(None, None, None, 0, 1024, stream=0, check=False) == 0
+
+
+@pytest.mark.parametrize("op,a,b,nb,d,n,expect", [
+    (0, X, None, 1, D, 16, -1), (5, X, None, 1, D, 16, -1),
+    (3, X, None, 16, D, 16, -1),            # MUL without b
+    (4, X, A, 5, D, 16, -1),                # n % nb
+    (1, X, None, 1, X + 4, 16, -2),         # partial overlap
+    (4, X, A, 16, A + 8, 16, -2),
+    (1, X + 1, None, 1, D, 16, -4),
+])
+def test_elementwise_validation(lib, op, a, b, nb, d, n, expect):
+    assert lib.elementwise(op, a, b, d, n, nb=nb, stream=0, check=False) == expect
+
+
+def test_dequantize_validation(lib):
+    assert lib.dequantize(W, 9, 4, 32, D, stream=0, check=False) == -1
+    assert lib.dequantize(W, 3, 4, 40, D, stream=0, check=False) == -3
+    assert lib.dequantize(W, 3, 4, 32, W + 8, stream=0, check=False) == -2
+    assert lib.dequantize(W + 1, 1, 4, 32, D, stream=0, check=False) == -4
+    assert lib.dequantize(W, 1, 0, 32, D, stream=0, check=False) == 0
