@@ -1,0 +1,653 @@
+#!/usr/bin/env python
+"""Benchmark of the fused decode GEMV path on GB300.
+
+One step = one pass over every operation of the hot path at full size, each through
+the C ABI (weights resident in HBM, ~357 MB per step, more than the 129 MB L2, so
+every launch streams its weights from HBM):
+
+  f16 4096x4096  residual add in place through a [32,128] view      (1 launch)
+  f16 4096x4096  sigmoid tail                                        (1)
+  Q8_0 11008x4096  silu(y) * m                                      (1)
+  Q4_0 decode-layer chain, d_model 4096, ffn 14336: q, k, v, o+add,
+       up, gate silu*up, down+add, beta sigmoid (M=32)               (8)
+  signed FWHT(1024) prologue + f16 5120x5120 + add in place, 1 column (1)
+  the same with a batch of 8 columns                                 (1)
+
+value = algorithmic bytes of the step (W + x + aux + dst, each once) / step time, GB/s,
+with the step captured in a CUDA graph (launches chained with programmatic dependent
+launch) and replayed.  Also reported: per-kernel CUDA-event durations and the roofline
+of the dominant kernel, microseconds per decode layer (fused and unfused chains), the
+epilogue cost against the tail-free GEMV, an end-to-end number through host buffers,
+SM clocks during the timed region, and the fp64 CPU oracle timed on the host cores.
+
+Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+(N > 1 under torch.distributed.run; every rank runs the same step on its own GPU.)
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMV HBM GB/s & % of GB300 peak; µs per decode layer chain"
+UNIT = "GB/s"
+WORKLOAD = ("decode_step: f16 4096x4096 add-in-place via [32,128] view + sigmoid; "
+            "Q8_0 11008x4096 silu*m; Q4_0 decode-layer chain (d_model 4096, ffn 14336, 8 GEMVs); "
+            "signed FWHT(1024) + f16 5120x5120 add-in-place, ncols 1 and 8")
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- workload spec
+
+def step_spec():
+    """(name, wtype, M, K, epilogue, ncols, fwht) for every launch of one step, in order."""
+    F16, Q8, Q4 = 1, 2, 3
+    NONE, SIG, SILU_MUL, ADD = 0, 1, 3, 4
+    d, f = 4096, 14336
+    return [
+        ("f16_add_view", F16, 4096, 4096, ADD, 1, False),
+        ("f16_sigmoid", F16, 4096, 4096, SIG, 1, False),
+        ("q8_0_silu_mul", Q8, 11008, 4096, SILU_MUL, 1, False),
+        ("chain_q", Q4, d, d, NONE, 1, False),
+        ("chain_k", Q4, d, d, NONE, 1, False),
+        ("chain_v", Q4, d, d, NONE, 1, False),
+        ("chain_o_add", Q4, d, d, ADD, 1, False),
+        ("chain_up", Q4, f, d, NONE, 1, False),
+        ("chain_gate_silu_mul", Q4, f, d, SILU_MUL, 1, False),
+        ("chain_down_add", Q4, d, f, ADD, 1, False),
+        ("chain_beta_sigmoid", Q4, 32, d, SIG, 1, False),
+        ("fwht_f16_add_n1", F16, 5120, 5120, ADD, 1, True),
+        ("fwht_f16_add_n8", F16, 5120, 5120, ADD, 8, True),
+    ]
+
+
+def row_bytes(wt, K):
+    return {0: 4 * K, 1: 2 * K, 2: (K // 32) * 34, 3: (K // 32) * 18}[wt]
+
+
+def algo_bytes(wt, M, K, epi, ncols, fwht):
+    """W once + x once + aux once (read) + dst once (write)."""
+    b = M * row_bytes(wt, K) + ncols * K * 4 + ncols * M * 4
+    if epi in (3, 4):
+        b += ncols * M * 4
+    if fwht:
+        b += 1024 * 4
+    return b
+
+
+WT_NAME = {0: "f32", 1: "f16", 2: "q8_0", 3: "q4_0"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Step:
+    """Device buffers and the list of ABI calls of one step."""
+
+    def __init__(self, G, torch, seed0=0, layer_seed=100):
+        from decode_gemv_epilogue_gb300 import synth
+        self.G, self.torch = G, torch
+        dev = torch.device("cuda")
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        spec = step_spec()
+        self.spec = spec
+        self.W = {}
+        for i, (name, wt, M, K, epi, nc, fw) in enumerate(spec):
+            seed = (layer_seed + i) if name.startswith("chain_") else (seed0 + 10 * i)
+            self.W[name] = up(synth.weights(wt, M, K, seed=seed))
+        self.x4096 = up(synth.normal(4096, seed=seed0 + 1))
+        self.r4096 = up(synth.normal(4096, seed=seed0 + 2))
+        self.xsig = up(synth.normal(4096, seed=seed0 + 3))
+        self.xq8 = up(synth.normal(4096, seed=seed0 + 4))
+        self.m = up(synth.normal(11008, seed=seed0 + 5))
+        self.gate_out = torch.empty(11008, device=dev)
+        self.sig_out = torch.empty(4096, device=dev)
+        # chain
+        self.cx = up(synth.normal(4096, seed=seed0 + 6))
+        self.ca = up(synth.normal(4096, seed=seed0 + 7))
+        self.cr = up(synth.normal(4096, seed=seed0 + 8))
+        self.cq, self.ck, self.cv = (torch.empty(4096, device=dev) for _ in range(3))
+        self.cup = torch.empty(14336, device=dev)
+        self.cg = torch.empty(14336, device=dev)
+        self.cbeta = torch.empty(32, device=dev)
+        # FWHT + f16 5120
+        self.signs = up(synth.rademacher(1024, seed=seed0 + 9))
+        self.fx1 = up(synth.normal(5120, seed=seed0 + 10))
+        self.fr1 = up(synth.normal(5120, seed=seed0 + 11))
+        self.fx8 = up(synth.normal(8 * 5120, seed=seed0 + 12))
+        self.fr8 = up(synth.normal(8 * 5120, seed=seed0 + 13))
+        self.bytes = {n: algo_bytes(wt, M, K, e, nc, fw) for (n, wt, M, K, e, nc, fw) in spec}
+        self.step_bytes = sum(self.bytes.values())
+        self.keys = {}
+        for (n, wt, M, K, e, nc, fw) in spec:
+            path, _ = G.plan(self.W[n], wt, self.cx, M, K, e, None, self.cq, ncols=nc,
+                             fwht_signs=self.signs if fw else None, fwht_block=1024 if fw else 0)
+            kind = "gemv_stream_kernel" if path == G.PATH_STREAM else "gemv_generic_kernel"
+            self.keys[n] = "%s<%s,%d>" % (kind, WT_NAME[wt], nc)
+
+    def calls(self, pdl=True):
+        G, W = self.G, self.W
+        c = []
+        add = lambda name, fn: c.append((name, fn))
+        add("f16_add_view", lambda: G.gemv_fused_ex(W["f16_add_view"], 1, self.x4096, 4096, 4096, 4,
+                                                    self.r4096, self.r4096, view=(32, 128), pdl=pdl))
+        add("f16_sigmoid", lambda: G.gemv_fused_ex(W["f16_sigmoid"], 1, self.xsig, 4096, 4096, 1, None,
+                                                   self.sig_out, pdl=pdl))
+        add("q8_0_silu_mul", lambda: G.gemv_fused_ex(W["q8_0_silu_mul"], 2, self.xq8, 11008, 4096, 3, self.m,
+                                                     self.gate_out, pdl=pdl))
+        add("chain_q", lambda: G.gemv_fused_ex(W["chain_q"], 3, self.cx, 4096, 4096, 0, None, self.cq, pdl=pdl))
+        add("chain_k", lambda: G.gemv_fused_ex(W["chain_k"], 3, self.cx, 4096, 4096, 0, None, self.ck, pdl=pdl))
+        add("chain_v", lambda: G.gemv_fused_ex(W["chain_v"], 3, self.cx, 4096, 4096, 0, None, self.cv, pdl=pdl))
+        add("chain_o_add", lambda: G.gemv_fused_ex(W["chain_o_add"], 3, self.ca, 4096, 4096, 4, self.cr,
+                                                   self.cr, pdl=pdl))
+        add("chain_up", lambda: G.gemv_fused_ex(W["chain_up"], 3, self.cr, 14336, 4096, 0, None, self.cup,
+                                                pdl=pdl))
+        add("chain_gate_silu_mul", lambda: G.gemv_fused_ex(W["chain_gate_silu_mul"], 3, self.cr, 14336, 4096,
+                                                           3, self.cup, self.cg, pdl=pdl))
+        add("chain_down_add", lambda: G.gemv_fused_ex(W["chain_down_add"], 3, self.cg, 4096, 14336, 4,
+                                                      self.cr, self.cr, pdl=pdl))
+        add("chain_beta_sigmoid", lambda: G.gemv_fused_ex(W["chain_beta_sigmoid"], 3, self.cx, 32, 4096, 1,
+                                                          None, self.cbeta, pdl=pdl))
+        add("fwht_f16_add_n1", lambda: G.gemv_fused_ex(W["fwht_f16_add_n1"], 1, self.fx1, 5120, 5120, 4,
+                                                       self.fr1, self.fr1, fwht_signs=self.signs,
+                                                       fwht_block=1024, pdl=pdl))
+        add("fwht_f16_add_n8", lambda: G.gemv_fused_ex(W["fwht_f16_add_n8"], 1, self.fx8, 5120, 5120, 4,
+                                                       self.fr8, self.fr8, ncols=8, fwht_signs=self.signs,
+                                                       fwht_block=1024, pdl=pdl))
+        return c
+
+    # host-resident per-step activations for the end-to-end leg
+    def e2e_buffers(self):
+        torch = self.torch
+        ins = [self.x4096, self.r4096, self.xsig, self.xq8, self.m, self.cx, self.ca, self.cr,
+               self.fx1, self.fr1, self.fx8, self.fr8]
+        outs = [self.r4096, self.sig_out, self.gate_out, self.cq, self.ck, self.cv, self.cr, self.cbeta,
+                self.fr1, self.fr8]
+        h_in = [torch.empty(t.numel(), dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for t in ins]
+        h_out = [torch.empty(t.numel(), dtype=t.dtype, pin_memory=True) for t in outs]
+        return ins, outs, h_in, h_out
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [t.strip() for t in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def ncu_traffic(kernel_key):
+    """dram read+write bytes per launch from the committed ncu summary, if it still
+    matches the kernel source (profiles/traffic.txt: key, bytes, source hash)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_gemv_epilogue_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(f.read())
+    src = h.hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_key and parts[2] == src:
+                return float(parts[1])
+    return None
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    from decode_gemv_epilogue_gb300 import gemvfuse as G
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    step = Step(G, torch)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    calls = step.calls(pdl=True)
+    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+
+    with torch.cuda.stream(s):
+        for _ in range(max(args.warmup, 3)):
+            for _, fn in calls:
+                fn()
+    s.synchronize()
+    assert G.device_status(reset=True) == 0
+    # capture one step in a CUDA graph (launches chained with programmatic dependencies)
+    graph = torch.cuda.CUDAGraph()
+    mode = "cuda_graph+pdl"
+    try:
+        with torch.cuda.graph(graph, stream=s):
+            for _, fn in calls:
+                fn()
+        graph.replay()
+        s.synchronize()
+    except Exception as e:  # report and fall back to eager launches
+        graph = None
+        mode = "eager+pdl (graph capture failed: %s)" % str(e).splitlines()[0][:120]
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            for _, fn in calls:
+                fn()
+
+    sampler.start()
+    with torch.cuda.stream(s):
+        soak_end = time.time() + 1.0
+        while time.time() < soak_end:
+            for _ in range(50):
+                run_step()
+            s.synchronize()
+    # ---------------------------------------------------------------- timed region
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        ev0.record(s)
+        for _ in range(args.steps):
+            run_step()
+        ev1.record(s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    sampler.stop()
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * step.step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # ---------------------------------------------------------------- per-kernel durations
+    kb = min(args.steps, 200)
+    nl = len(calls)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
+           for _ in range(kb)]
+    with torch.cuda.stream(s):
+        for k in range(kb):
+            for i, (_, fn) in enumerate(calls):
+                evs[k][i][0].record(s)
+                fn()
+                evs[k][i][1].record(s)
+    s.synchronize()
+    per_call = {}
+    for i, (name, _) in enumerate(calls):
+        per_call[name] = statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(kb))
+    per_kernel = {}
+    for name, ms_i in per_call.items():
+        key = step.keys[name]
+        d = per_kernel.setdefault(key, {"launches_per_step": 0, "ms_per_step": 0.0, "bytes_per_step": 0})
+        d["launches_per_step"] += 1
+        d["ms_per_step"] += ms_i
+        d["bytes_per_step"] += step.bytes[name]
+    total_k = sum(d["ms_per_step"] for d in per_kernel.values())
+    for d in per_kernel.values():
+        d["share"] = d["ms_per_step"] / total_k
+        d["gbs"] = d["bytes_per_step"] / (d["ms_per_step"] * 1e-3) / 1e9
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_per_step"])
+    peak, peak_kind = measured_peaks()
+    dk = per_kernel[dom]
+    achieved = dk["gbs"]
+    traffic = ncu_traffic(dom)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else
+                "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": round(dk["bytes_per_step"] / dk["launches_per_step"]),
+                "launch_us": round(1e3 * dk["ms_per_step"] / dk["launches_per_step"], 3)}
+    per_workload = {n: {"us": round(1e3 * per_call[n], 3), "bytes": step.bytes[n],
+                        "gbs": round(step.bytes[n] / (per_call[n] * 1e-3) / 1e9, 1),
+                        "frac_of_peak": round(step.bytes[n] / (per_call[n] * 1e-3) / 1e9 / peak, 4)}
+                    for n in per_call}
+
+    # ---------------------------------------------------------------- decode-layer chain
+    chain = chain_measure(G, torch, step, s, args)
+    # ---------------------------------------------------------------- epilogue cost
+    epi_cost = epilogue_cost(G, torch, s)
+    # ---------------------------------------------------------------- end to end (host buffers)
+    e2e = e2e_measure(G, torch, step, s, args)
+    assert G.device_status() == 0, "a kernel reported a bounded-wait timeout"
+
+    launches = nl * args.steps
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; weight distributions of the workload; weights resident in HBM)",
+        "config": {"workload": WORKLOAD, "model": None, "bytes_per_step": step.step_bytes,
+                   "l2": "inputs larger than L2: %.0f MB of weights per step vs 129 MB L2; each launch "
+                         "reads a distinct weight buffer" % (step.step_bytes / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "launch_mode": mode, "launches_per_step": nl, "soak_s_before_timing": 1.0},
+        "roofline": roofline,
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "gpu_launches": launches,
+        "us_per_layer": chain["fused_us"], "launches_per_layer": 8,
+        "us_per_layer_unfused": chain["unfused_us"], "launches_per_layer_unfused": 13,
+        "chain": chain, "epilogue_cost": epi_cost, "per_kernel": per_kernel, "per_workload": per_workload,
+        "e2e": e2e, "clocks": sampler.summary(),
+    }
+    if dist is not None:
+        dist.destroy_process_group()
+    return out
+
+
+def chain_measure(G, torch, step, s, args):
+    """Microseconds per decode layer: the 8 fused launches vs the 13-launch unfused
+    chain (separate GEMV, add, silu, mul, sigmoid kernels), each captured in a CUDA
+    graph, two layers' weights alternating so nothing stays in L2."""
+    from decode_gemv_epilogue_gb300 import synth
+    dev = torch.device("cuda")
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    names = ["chain_q", "chain_k", "chain_v", "chain_o_add", "chain_up", "chain_gate_silu_mul",
+             "chain_down_add", "chain_beta_sigmoid"]
+    shapes = {n: (M, K) for (n, wt, M, K, e, nc, fw) in step_spec() if n in names}
+    layers = [{n: step.W[n] for n in names},
+              {n: up(synth.weights(3, shapes[n][0], shapes[n][1], seed=300 + i)) for i, n in enumerate(names)}]
+    x, a, r = step.cx, step.ca, step.cr
+    q, k, v, u, g, beta = step.cq, step.ck, step.cv, step.cup, step.cg, step.cbeta
+    y4 = torch.empty(4096, device=dev)
+    y14 = torch.empty(14336, device=dev)
+
+    def fused(Wl):
+        G.gemv_fused_ex(Wl["chain_q"], 3, x, 4096, 4096, 0, None, q, pdl=True)
+        G.gemv_fused_ex(Wl["chain_k"], 3, x, 4096, 4096, 0, None, k, pdl=True)
+        G.gemv_fused_ex(Wl["chain_v"], 3, x, 4096, 4096, 0, None, v, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_up"], 3, r, 14336, 4096, 0, None, u, pdl=True)
+        G.gemv_fused_ex(Wl["chain_gate_silu_mul"], 3, r, 14336, 4096, 3, u, g, pdl=True)
+        G.gemv_fused_ex(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_beta_sigmoid"], 3, x, 32, 4096, 1, None, beta, pdl=True)
+
+    def unfused(Wl):
+        G.gemv_fused(Wl["chain_q"], 3, x, 4096, 4096, 0, None, q)
+        G.gemv_fused(Wl["chain_k"], 3, x, 4096, 4096, 0, None, k)
+        G.gemv_fused(Wl["chain_v"], 3, x, 4096, 4096, 0, None, v)
+        G.gemv_fused(Wl["chain_o_add"], 3, a, 4096, 4096, 0, None, y4)
+        G.elementwise(G.EW_ADD, y4, r, r, 4096)
+        G.gemv_fused(Wl["chain_up"], 3, r, 14336, 4096, 0, None, u)
+        G.gemv_fused(Wl["chain_gate_silu_mul"], 3, r, 14336, 4096, 0, None, y14)
+        G.elementwise(G.EW_SILU, y14, None, y14, 14336)
+        G.elementwise(G.EW_MUL, y14, u, g, 14336)
+        G.gemv_fused(Wl["chain_down_add"], 3, g, 4096, 14336, 0, None, y4)
+        G.elementwise(G.EW_ADD, y4, r, r, 4096)
+        G.gemv_fused(Wl["chain_beta_sigmoid"], 3, x, 32, 4096, 0, None, beta)
+        G.elementwise(G.EW_SIGMOID, beta, None, beta, 32)
+
+    res = {}
+    reps = max(20, min(args.steps, 500))
+    for label, fn in (("fused", fused), ("unfused", unfused)):
+        with torch.cuda.stream(s):
+            fn(layers[0]); fn(layers[1])
+        s.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            fn(layers[0])
+            fn(layers[1])
+        for _ in range(3):
+            gr.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(reps):
+                gr.replay()
+            e1.record(s)
+        s.synchronize()
+        res[label + "_us"] = round(1e3 * e0.elapsed_time(e1) / (2 * reps), 3)
+    layer_bytes = sum(step.bytes[n] for n in names)
+    res["layer_bytes"] = layer_bytes
+    res["fused_gbs"] = round(layer_bytes / (res["fused_us"] * 1e-6) / 1e9, 1)
+    res["layers_timed"] = 2 * reps
+    return res
+
+
+def epilogue_cost(G, torch, s):
+    """Fused tail vs the tail-free GEMV of the same shape (per-launch CUDA-event mean over
+    launches cycling through enough weight copies to exceed L2)."""
+    from decode_gemv_epilogue_gb300 import synth
+    dev = torch.device("cuda")
+    out = {}
+    for label, wt, M, K, epi in (("f16_4096_add", 1, 4096, 4096, 4), ("q8_0_11008_silu_mul", 2, 11008, 4096, 3),
+                                 ("q4_0_14336_silu_mul", 3, 14336, 4096, 3)):
+        base = torch.from_numpy(synth.weights(wt, M, K, seed=500)).to(dev)
+        ncopy = max(2, int(2 * L2_BYTES // base.numel()) + 1)
+        Ws = [base.clone() for _ in range(ncopy)]
+        x = torch.from_numpy(synth.normal(K, seed=501)).to(dev)
+        aux = torch.from_numpy(synth.normal(M, seed=502)).to(dev)
+        dst = torch.empty(M, device=dev)
+        times = {}
+        for e in (0, epi):
+            def run(Wc, e=e):
+                G.gemv_fused(Wc, wt, x, M, K, e, aux if e in (3, 4) else None, aux if e == 4 else dst)
+            with torch.cuda.stream(s):
+                for Wc in Ws:
+                    run(Wc)
+            s.synchronize()
+            reps = 4
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                e0.record(s)
+                for _ in range(reps):
+                    for Wc in Ws:
+                        run(Wc)
+                e1.record(s)
+            s.synchronize()
+            times[e] = e0.elapsed_time(e1) / (reps * len(Ws))
+        out[label] = {"none_us": round(1e3 * times[0], 3), "fused_us": round(1e3 * times[epi], 3),
+                      "cost": round(times[epi] / times[0] - 1.0, 4)}
+        del Ws
+    return out
+
+
+def e2e_measure(G, torch, step, s, args):
+    """The same step through the public API from pinned host buffers: every step copies its
+    activations host->device, runs the 13 ABI calls and copies every result back."""
+    ins, outs, h_in, h_out = step.e2e_buffers()
+    calls = step.calls(pdl=True)
+    reps = max(5, min(args.steps, 200))
+
+    def one():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        for _, fn in calls:
+            fn()
+        for d, h in zip(outs, h_out):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            one()
+    s.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(reps):
+            one()
+        e1.record(s)
+    s.synchronize()
+    wall = time.perf_counter() - t0
+    ms = e0.elapsed_time(e1) / reps
+    bi = sum(t.numel() * t.element_size() for t in h_in)
+    bo = sum(t.numel() * t.element_size() for t in h_out)
+    return {"value": round(step.step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 6), "wall_ms_per_step": round(1e3 * wall / reps, 6),
+            "steps": reps, "launch_mode": "eager+pdl via the C ABI"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(seed0=0):
+    """Seeded inputs of every launch of the step (generated once per process)."""
+    from decode_gemv_epilogue_gb300 import synth
+    if seed0 not in _ORACLE_INPUTS:
+        items = []
+        for i, (name, wt, M, K, epi, nc, fw) in enumerate(step_spec()):
+            raw = synth.weights(wt, M, K, seed=seed0 + 10 * i)
+            X = synth.normal(nc * K, seed=seed0 + 1).reshape(nc, K)
+            aux = synth.normal(nc * M, seed=seed0 + 2).reshape(nc, M) if epi in (3, 4) else None
+            s = synth.rademacher(1024, seed=seed0 + 9) if fw else None
+            items.append((raw, X, aux, s))
+        _ORACLE_INPUTS[seed0] = items
+    return _ORACLE_INPUTS[seed0]
+
+
+def oracle_step(frac, seed0=0):
+    """Run the fp64 oracle on a row sample (every frac-th row) of every launch of the
+    step; returns (algorithmic bytes of the sample, seconds of oracle work)."""
+    from oracle import fwht as ofwht
+    from oracle import gemv as ogemv
+    total_b, total_t = 0, 0.0
+    for (name, wt, M, K, epi, nc, fw), (raw, X, aux, s) in zip(step_spec(), _oracle_inputs(seed0)):
+        rows = np.arange(0, M, frac)
+        t = time.perf_counter()
+        if fw:
+            X = np.stack([ofwht.fwht_signed(X[c], s, 1024) for c in range(nc)])
+        for r0 in range(0, rows.size, 2048):
+            ogemv.gemv(raw, wt, X, M, K, epi, aux, rows=rows[r0:r0 + 2048])
+        total_t += time.perf_counter() - t
+        total_b += algo_bytes(wt, rows.size, K, epi, nc, fw)
+    return total_b, total_t
+
+
+def cpu_baseline(frac=2):
+    b, t = oracle_step(frac)
+    return {"value": round(b / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "every %d%s row of every launch of one decode step (%.0f MB of the step's "
+                      "algorithmic bytes), numpy fp64 oracle, one thread" % (frac, "nd" if frac == 2 else "th",
+                                                                           b / 1e6),
+            "seconds": round(t, 2)}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    frac = 16
+    _oracle_inputs()
+    for _ in range(max(args.warmup, 0)):
+        oracle_step(frac)
+    tb, wall = 0, 0.0
+    for _ in range(args.steps):
+        b, t = oracle_step(frac)
+        tb += b
+        wall += t
+    value = tb / wall / 1e9
+    cb = {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+          "sample": "every 16th row of every launch of one decode step per step (%d steps)" % args.steps}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * wall / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "1/16 of the rows of each launch"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and "WORLD_SIZE" in os.environ:
+        print("warning: --gpus %d but WORLD_SIZE %d" % (args.gpus, world), file=sys.stderr)
+    if args.impl == "reference":
+        out = reference_arm(args, rank, world)
+        if out is not None:
+            print(json.dumps(out))
+        return 0
+    out = gpu_arm(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(out))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

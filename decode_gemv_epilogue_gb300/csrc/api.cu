@@ -136,21 +136,6 @@ static int validate(const Call& c) {
   return GF_OK;
 }
 
-// Pick the number of consumer warps: no idle units per thread if possible, then more warps.
-static int choose_ncw(int units, int max_cw) {
-  int best = max_cw, best_waste = INT32_MAX;
-  for (int w = max_cw; w >= 4; --w) {
-    const int nt = 32 * w;
-    const int per = (units + nt - 1) / nt;
-    const int waste = per * nt - units;
-    if (waste < best_waste) {
-      best_waste = waste;
-      best = w;
-    }
-  }
-  return best;
-}
-
 static int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
 // Plan the TMA-streamed kernel; returns false if the shape/alignment needs the generic one.
@@ -158,58 +143,58 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
   const int nc = static_cast<int>(c.ncols);
   const int K = static_cast<int>(c.K);
   const int64_t rb = row_bytes_of(c.wtype, c.K);
-  if (c.K < 8 || K % 8 != 0) return false;
+  if (c.K < kUnitElems || K % kUnitElems != 0) return false;
   if (rb % 16 != 0 || !aligned(c.W, 16) || !aligned(c.x, 16)) return false;
   if (rb > INT32_MAX / 2) return false;
-  const bool quant = c.wtype == GF_Q8_0 || c.wtype == GF_Q4_0;
+  const int U = stream_u(c.wtype, nc), RT = stream_rt(c.wtype, nc);
+  const int max_cw = stream_max_cw(nc);
   auto seg_of = [&](int klen) -> int { return static_cast<int>(row_bytes_of(c.wtype, klen)); };
-  // K chunk: whole K if x fits and the row fits a stage; else a multiple of the granule
+  // K chunk: the whole row if x, one row's bytes and the units all fit; else a multiple
+  // of the granule (256 elements, or the FWHT block) that does.
   int gran = 256;
   if (c.signs) gran = std::max<int>(gran, static_cast<int>(c.fwht_block));
+  const int64_t cap_x = kXsMaxBytes / (4 * nc);
+  const int64_t cap_units = static_cast<int64_t>(kUnitElems) * U * 32 * max_cw;
+  const int cap_seg = std::min(kSegMaxBytes, kStageMaxBytes / RT);  // RT rows fit one stage
   int kc = K;
-  const int64_t xs_cap = kXsMaxBytes / (4 * nc);
-  if (static_cast<int64_t>(K) > xs_cap || seg_of(K) > kSegMaxBytes) {
-    if (quant && K % 256 != 0) return false;
-    int bytes_per_gran = seg_of(gran);
-    int g_by_x = static_cast<int>(xs_cap / gran);
-    int g_by_seg = kSegMaxBytes / bytes_per_gran;
-    int g = std::min(g_by_x, g_by_seg);
-    if (g < 1) return false;
-    kc = g * gran;
+  if (K > cap_x || seg_of(K) > cap_seg || K > cap_units) {
+    const int g_x = static_cast<int>(cap_x / gran);
+    const int g_seg = cap_seg / seg_of(gran);
+    const int g_u = static_cast<int>(cap_units / gran);
+    const int gch = std::min(std::min(g_x, g_seg), g_u);
+    if (gch < 1) return false;
+    kc = gch * gran;
   }
   const int n_kc = (K + kc - 1) / kc;
   const int seg_full = seg_of(kc);
   if (seg_full % 16 != 0) return false;
   if (n_kc > 1) {
     const int last = K - (n_kc - 1) * kc;
-    if (seg_of(last) % 16 != 0 || last % 8 != 0) return false;
+    if (seg_of(last) % 16 != 0 || last % kUnitElems != 0) return false;
   }
-  const int max_cw = stream_max_cw(nc);
-  const int ncw = choose_ncw(kc / 8, max_cw);
+  const int units = kc / kUnitElems;
+  const int wpg = (((units + U - 1) / U) + 31) / 32;
+  if (wpg > max_cw) return false;
   const int grid = static_cast<int>(std::min<int64_t>(lim.sm_count, c.M));
   const int rows_base = static_cast<int>(c.M / grid);
   const int rows_extra = static_cast<int>(c.M % grid);
   const int rows_max = rows_base + (rows_extra ? 1 : 0);
-  int RC = std::min(rows_max, std::max(1, kRedMaxBytes / (ncw * nc * 4)));
-  RC = std::min(RC, 256);
-  const int rmax = stream_rmax(nc);
-  int R = std::max(1, std::min(rmax, kStageTargetBytes / seg_full));
-  R = std::min(R, RC);
+  int G = std::max(1, std::min(max_cw / wpg, (rows_max + RT - 1) / RT));
+  while (G > 1 && G * RT * seg_full > kStageMaxBytes) --G;
+  const int ncw = G * wpg;
+  int R = G * RT;
+  int RC = std::min(rows_max, std::max(R, kRedMaxBytes / (wpg * nc * 4)));
+  RC = std::min(RC, 512);
   const int xs_bytes = round_up(nc * kc * 4, 128);
   const int aux_bytes = round_up(nc * RC * 4, 128);
-  const int red_bytes = round_up(RC * ncw * nc * 4, 128);
-  const int fixed = kBarBytes + xs_bytes + aux_bytes + red_bytes;
-  int stage_bytes = round_up(R * seg_full, 128);
-  int NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
-  while (NS < 2 && R > 1) {
-    --R;
-    stage_bytes = round_up(R * seg_full, 128);
-    NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
-  }
+  const int red_bytes = round_up(RC * wpg * nc * 4, 128);
+  const int fixed = kBarBytes + xs_bytes + aux_bytes + red_bytes + kRingSlackBytes;
+  const int stage_bytes = round_up(R * seg_full, 128);
+  const int NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
   if (NS < 2) return false;
   p.path = PATH_STREAM;
   p.grid = grid;
-  p.threads = stream_threads(nc);
+  p.threads = 32 * (1 + ncw);
   p.smem = fixed + NS * stage_bytes;
   StreamArgs& s = p.s;
   std::memset(&s, 0, sizeof(s));
@@ -220,6 +205,8 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
   s.kc_len = kc;
   s.n_kc = n_kc;
   s.R = R;
+  s.G = G;
+  s.wpg = wpg;
   s.NS = NS;
   s.stage_bytes = stage_bytes;
   s.RC = RC;
@@ -233,8 +220,6 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
   s.off_aux = s.off_xs + xs_bytes;
   s.off_red = s.off_aux + aux_bytes;
   s.off_ring = s.off_red + red_bytes;
-  // launch threads: producer warp + consumer warps actually used
-  p.threads = 32 * (1 + ncw);
   return true;
 }
 

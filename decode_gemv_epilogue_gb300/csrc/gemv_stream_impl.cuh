@@ -27,56 +27,92 @@ __host__ __device__ constexpr int seg_bytes_of(int klen) {
   return WT == WT_F32 ? 4 * klen : WT == WT_F16 ? 2 * klen : WT == WT_Q8_0 ? (klen / 32) * 34 : (klen / 32) * 18;
 }
 
-template <int WT, int NC, int RMAX>
-__device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int units, int ctid,
-                                             int nt, const float* xs, int xstride,
-                                             float2 (&acc)[RMAX][NC]) {
-  for (int u = ctid; u < units; u += nt) {
-    uint32_t e0, e1;
-    unit_x_offsets<WT>(static_cast<uint32_t>(u), e0, e1);
-    float2 xv[NC][4];
+// x values of one unit (all columns) as eight float2 pairs per column, matching the
+// pair order of decode_unit().
+template <int WT, int NC>
+__device__ __forceinline__ void load_unit_x(const float* xs, int xstride, int u, uint32_t qr,
+                                            float2 (&xv)[NC][8]) {
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const float4 p = *reinterpret_cast<const float4*>(xs + c * xstride + e0);
-      const float4 q = *reinterpret_cast<const float4*>(xs + c * xstride + e1);
-      xv[c][0] = make_float2(p.x, p.y);
-      xv[c][1] = make_float2(p.z, p.w);
-      xv[c][2] = make_float2(q.x, q.y);
-      xv[c][3] = make_float2(q.z, q.w);
+  for (int c = 0; c < NC; ++c) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 t = *reinterpret_cast<const float4*>(
+          xs + c * xstride + unit_pair_elem<WT>(static_cast<uint32_t>(u), 2 * static_cast<int>((q + qr) & 3u)));
+      xv[c][2 * q] = make_float2(t.x, t.y);
+      xv[c][2 * q + 1] = make_float2(t.z, t.w);
     }
+  }
+}
+
+// acc[c] += sum of the unit's 16 products for each column c (quant formats: the block
+// partial first, then scaled by d into the running sum).
+template <int WT, int NC>
+__device__ __forceinline__ void unit_rows_fma(const float2 (&v)[8], float d, const float2 (&xv)[NC][8],
+                                              float2 (&acc)[NC]) {
 #pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-      if (r < rows) {
-        const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
-        float2 v[4];
-        float d;
-        decode_unit<WT>(ld, static_cast<uint32_t>(u), v, d);
+  for (int c = 0; c < NC; ++c) {
+    if constexpr (WT == WT_F32 || WT == WT_F16) {
+      float2 t = acc[c];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          if constexpr (WT == WT_F32 || WT == WT_F16) {
-            float2 t = acc[r][c];
-            t = ffma2(v[0], xv[c][0], t);
-            t = ffma2(v[1], xv[c][1], t);
-            t = ffma2(v[2], xv[c][2], t);
-            t = ffma2(v[3], xv[c][3], t);
-            acc[r][c] = t;
-          } else {
-            // block partial first, then scaled by d into the running sum
-            float2 p = make_float2(0.0f, 0.0f);
-            p = ffma2(v[0], xv[c][0], p);
-            p = ffma2(v[1], xv[c][1], p);
-            p = ffma2(v[2], xv[c][2], p);
-            p = ffma2(v[3], xv[c][3], p);
-            acc[r][c] = ffma2(make_float2(d, d), p, acc[r][c]);
+      for (int k = 0; k < 8; ++k) t = ffma2(v[k], xv[c][k], t);
+      acc[c] = t;
+    } else {
+      float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        p0 = ffma2(v[k], xv[c][k], p0);
+        p1 = ffma2(v[k + 1], xv[c][k + 1], p1);
+      }
+      acc[c] = ffma2(make_float2(d, d), fadd2(p0, p1), acc[c]);
+    }
+  }
+}
+
+// x held in registers for the whole K chunk when it fits (U units x NC columns x 16).
+template <int WT, int NC, int U>
+__host__ __device__ constexpr bool stream_xreg() { return U * NC * 16 <= 32; }
+
+// One thread's share of a tile: U units (16 weights each, stride tg_n within the row
+// group) times RT rows (stride G within the tile).  x comes either from registers
+// loaded once per K chunk (xr) or, for wide batches, from shared memory once per tile
+// and unit, reused for the RT rows.
+template <int WT, int NC, int U, int RT>
+__device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int units, int tg, int tg_n,
+                                             int g, int G, const float* xs, int xstride, uint32_t qr,
+                                             const float2 (&xr)[U][NC][8], float2 (&acc)[RT][NC]) {
+  constexpr bool XREG = stream_xreg<WT, NC, U>();
+#pragma unroll
+  for (int i = 0; i < U; ++i) {
+    const int u = tg + i * tg_n;
+    if (u < units) {
+      auto rows_of_unit = [&](const float2 (&xv)[NC][8]) {
+#pragma unroll
+        for (int j = 0; j < RT; ++j) {
+          const int r = g + j * G;
+          if (r < rows) {
+            const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+            float2 v[8];
+            float d;
+            decode_unit<WT>(ld, static_cast<uint32_t>(u), v, d, qr);
+            unit_rows_fma<WT, NC>(v, d, xv, acc[j]);
           }
         }
+      };
+      if constexpr (XREG) {
+        rows_of_unit(xr[i]);
+      } else {
+        float2 xt[NC][8];
+        load_unit_x<WT, NC>(xs, xstride, u, qr, xt);
+        rows_of_unit(xt);
       }
     }
   }
 }
 
-template <int WT, int NC, int RMAX>
+template <int WT, int NC>
 __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(const StreamArgs a) {
+  constexpr int U = stream_u(WT, NC);
+  constexpr int RT = stream_rt(WT, NC);
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
@@ -149,23 +185,23 @@ __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(cons
     // Every consumer thread runs the same sequence of named barriers whether or not a
     // wait gave up; after an abort the remaining work is skipped, not the barriers.
     const int cw = warp - 1, ctid = threadIdx.x - 32, nt = a.ncw * 32;
+    const int g = cw / a.wpg;                  // row group of this warp
+    const int wg = cw - g * a.wpg;             // warp within the group
+    const int tg = wg * 32 + lane, tg_n = a.wpg * 32;
+    const uint32_t qr = lane_quad_rot<WT>(lane);
     const bool need_aux = (a.epi == EPI_SILU_MUL || a.epi == EPI_ADD);
     pdl_wait();  // x, aux and dst may belong to the preceding grid
     int it = 0;
     uint32_t xphase = 0;
     bool ok = true;
+    bool x_loaded = false;
     auto cbar = [&]() { named_bar_sync(1, static_cast<uint32_t>(nt)); };
     for (int rc0 = 0; rc0 < nrows; rc0 += a.RC) {
       const int nrc = min(a.RC, nrows - rc0);
-      if (need_aux)
-        for (int i = ctid; i < nrc * NC; i += nt) {
-          const int c = i / nrc, r = i - c * nrc;
-          auxs[c * a.RC + r] = a.aux[c * a.M + r0 + rc0 + r];  // plain load: aux may alias dst
-        }
       for (int kc = 0; kc < a.n_kc; ++kc) {
         const int klen = min(a.kc_len, a.K - kc * a.kc_len);
-        if (a.n_kc > 1 || rc0 == 0) {
-          cbar();  // nobody still reads the previous x chunk
+        if (a.n_kc > 1 || !x_loaded) {
+          if (x_loaded) cbar();  // nobody still reads the previous x chunk
           if (ctid == 0 && !*abort_flag) {
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(NC * klen * 4));
@@ -173,50 +209,62 @@ __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(cons
               bulk_g2s(smem_u32(xs + c * klen), a.x + static_cast<int64_t>(c) * a.K + kc * a.kc_len,
                        static_cast<uint32_t>(klen * 4), xbar);
           }
+          x_loaded = true;
+          if (kc == 0 && need_aux)  // aux loads overlap the x copy
+            for (int i = ctid; i < nrc * NC; i += nt) {
+              const int c = i / nrc, r = i - c * nrc;
+              auxs[c * a.RC + r] = a.aux[c * a.M + r0 + rc0 + r];  // plain load: aux may alias dst
+            }
           ok = ok && mbar_wait_or_abort(xbar, xphase, abort_flag, a.err);
           xphase ^= 1u;
           if (a.fwht_B > 0)
             fwht_smem(xs, NC * klen, a.fwht_B, klen, static_cast<int64_t>(kc) * a.kc_len, a.signs,
                       a.nsigns, a.fwht_scale, ctid, nt, cbar);
-          else
-            cbar();
+        } else if (kc == 0 && need_aux) {
+          for (int i = ctid; i < nrc * NC; i += nt) {
+            const int c = i / nrc, r = i - c * nrc;
+            auxs[c * a.RC + r] = a.aux[c * a.M + r0 + rc0 + r];
+          }
         }
-        const int units = klen / 8;
+        const int units = klen / kUnitElems;
         const int seg = seg_bytes_of<WT>(klen);
+        float2 xr[U][NC][8];
+        if constexpr (stream_xreg<WT, NC, U>()) {
+#pragma unroll
+          for (int i = 0; i < U; ++i) {
+            const int u = tg + i * tg_n;
+            if (u < units) load_unit_x<WT, NC>(xs, klen, u, qr, xr[i]);
+          }
+        }
         for (int t0 = 0; t0 < nrc; t0 += a.R, ++it) {
           const int rows = min(a.R, nrc - t0);
           const int slot = it % a.NS, round = it / a.NS;
           ok = ok && mbar_wait_or_abort(full0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag,
                                         a.err);
-          float2 acc[RMAX][NC];
+          float2 acc[RT][NC];
 #pragma unroll
-          for (int r = 0; r < RMAX; ++r)
+          for (int j = 0; j < RT; ++j)
 #pragma unroll
-            for (int c = 0; c < NC; ++c) acc[r][c] = make_float2(0.0f, 0.0f);
+            for (int c = 0; c < NC; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
           if (ok)
-            consume_tile<WT, NC, RMAX>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows,
-                                       units, ctid, nt, xs, klen, acc);
+            consume_tile<WT, NC, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units,
+                                        tg, tg_n, g, a.G, xs, klen, qr, xr, acc);
           __syncwarp();
           if (lane == 0) mbar_arrive(empty0 + 8u * slot);
-          // warp reduction of the RMAX*NC partial sums, up to 32 values at a time
-          constexpr int V = RMAX * NC;
-          constexpr int G = V >= 32 ? 32 : V > 8 ? 16 : V > 4 ? 8 : V > 2 ? 4 : V > 1 ? 2 : 1;
+          // warp reduction of the RT*NC partial sums (padded to a power of two)
+          constexpr int V = RT * NC;
+          constexpr int VP = V > 16 ? 32 : V > 8 ? 16 : V > 4 ? 8 : V > 2 ? 4 : V > 1 ? 2 : 1;
+          float vals[VP];
 #pragma unroll
-          for (int g0 = 0; g0 < V; g0 += G) {
-            float vals[G];
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-              const int idx = g0 + j < V ? g0 + j : 0;
-              vals[j] = g0 + j < V ? acc[idx / NC][idx % NC].x + acc[idx / NC][idx % NC].y : 0.0f;
-            }
-            const float s = WarpVecReduce<G>::run(vals, lane);
-            const int j = lane >> (5 - WarpVecReduce<G>::kLog);
-            if (lane == WarpVecReduce<G>::owner(j) && g0 + j < V) {
-              const int r = (g0 + j) / NC, c = (g0 + j) % NC;
-              if (r < rows) {
-                float* p = red + ((t0 + r) * a.ncw + cw) * NC + c;
-                *p = (kc == 0) ? s : (*p + s);
-              }
+          for (int j = 0; j < VP; ++j)
+            vals[j] = j < V ? acc[j / NC][j % NC].x + acc[j / NC][j % NC].y : 0.0f;
+          const float sum = WarpVecReduce<VP>::run(vals, lane);
+          const int jv = lane >> (5 - WarpVecReduce<VP>::kLog);
+          if (lane == WarpVecReduce<VP>::owner(jv) && jv < V) {
+            const int r = g + (jv / NC) * a.G, c = jv % NC;
+            if (r < rows) {
+              float* p = red + ((t0 + r) * a.wpg + wg) * NC + c;
+              *p = (kc == 0) ? sum : (*p + sum);
             }
           }
         }
@@ -226,7 +274,7 @@ __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(cons
         for (int i = ctid; i < nrc * NC; i += nt) {
           const int c = i / nrc, r = i - c * nrc;
           float y = 0.0f;
-          for (int w = 0; w < a.ncw; ++w) y += red[(r * a.ncw + w) * NC + c];
+          for (int w = 0; w < a.wpg; ++w) y += red[(r * a.wpg + w) * NC + c];
           const float av = need_aux ? auxs[c * a.RC + r] : 0.0f;
           a.dst[c * a.M + r0 + rc0 + r] = apply_tail(a.epi, y, av);
         }
@@ -239,8 +287,7 @@ __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(cons
 
 template <int WT, int NC>
 int launch_stream_t(const Plan& p, cudaStream_t st, bool pdl) {
-  constexpr int RMAX = stream_rmax(NC);
-  auto kern = gemv_stream_kernel<WT, NC, RMAX>;
+  auto kern = gemv_stream_kernel<WT, NC>;
   static int configured_smem[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);

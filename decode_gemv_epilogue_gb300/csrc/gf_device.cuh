@@ -156,12 +156,22 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
 // ------------------------------------------------------------------ loaders
 // The unit decoders read weight bytes through a loader so the same decode code runs
 // on a shared-memory stage (the streaming kernel) and on global memory (dequantize).
+// words<N>(start) returns N consecutive 32-bit words starting at a 2-byte-aligned
+// offset.  The shared-memory loader reads the N+1 aligned words around them and
+// funnel-shifts (it may read up to 3 bytes past the last byte: the stage ring keeps
+// slack for that); the global-memory loader assembles them from 16-bit loads and
+// never reads outside the requested bytes.
 
 struct SmemLoader {
   uint32_t base;  // shared-state-space address of row start
   __device__ __forceinline__ uint32_t u16(uint32_t off) const {
     uint16_t v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(base + off));
+    return v;
+  }
+  __device__ __forceinline__ uint32_t u32(uint32_t off) const {  // 4-byte aligned
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(base + off));
     return v;
   }
   __device__ __forceinline__ uint4 v4(uint32_t off) const {  // 16-byte aligned
@@ -171,9 +181,14 @@ struct SmemLoader {
                  : "r"(base + off));
     return v;
   }
-  // 32 bits at a 2-byte-aligned offset.
-  __device__ __forceinline__ uint32_t u32_a2(uint32_t off) const {
-    return __byte_perm(u16(off), u16(off + 2), 0x5410);
+  template <int N>
+  __device__ __forceinline__ void words(uint32_t start, uint32_t (&w)[N]) const {
+    const uint32_t a = start & ~3u, sh = (start & 3u) * 8u;
+    uint32_t r[N + 1];
+#pragma unroll
+    for (int i = 0; i <= N; ++i) r[i] = u32(a + 4u * i);
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], sh);
   }
 };
 
@@ -185,20 +200,23 @@ struct GmemLoader {
   __device__ __forceinline__ uint4 v4(uint32_t off) const {
     return *reinterpret_cast<const uint4*>(base + off);
   }
-  __device__ __forceinline__ uint32_t u32_a2(uint32_t off) const {
-    return __byte_perm(u16(off), u16(off + 2), 0x5410);
+  template <int N>
+  __device__ __forceinline__ void words(uint32_t start, uint32_t (&w)[N]) const {
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = __byte_perm(u16(start + 4u * i), u16(start + 4u * i + 2u), 0x5410);
   }
 };
 
 // ------------------------------------------------------------------ unit decoders
-// A "unit" is 8 weights of one row.  Unit u covers, within a row (or K chunk):
-//   F32, F16, Q8_0 : elements 8u .. 8u+7
-//   Q4_0           : block b = u/4, word i = u%4 of its 16 code bytes:
-//                    elements 32b+4i .. +3 (low nibbles) and 32b+16+4i .. +3 (high)
-// decode_unit() returns the 8 values as four float2 pairs in that element order,
-// together with the block scale (1 for F32/F16).  Quant codes are turned into floats
-// exactly: the byte is placed in the low mantissa bits of 2^23 and 2^23 (+ offset)
-// is subtracted, which is exact for every code.
+// A "unit" is 16 weights of one row (half a quant block).  Unit u covers, within a
+// row (or K chunk):
+//   F32, F16, Q8_0 : elements 16u .. 16u+15
+//   Q4_0           : block b = u/2, half h = u%2: code bytes 8h .. 8h+7 of the block,
+//                    i.e. elements 32b+8h .. +7 (low nibbles) and 32b+16+8h .. +7 (high)
+// decode_unit() returns the 16 values as eight float2 pairs (pair k = elements
+// unit_pair_elem(u, k) and +1) together with the block scale d (1 for F32/F16).  Quant
+// codes are turned into floats exactly: the byte goes into the low mantissa bits of
+// 2^23 and 2^23 + offset is subtracted with a packed add, exact for every code.
 
 constexpr float kMagic = 8388608.0f;  // 2^23
 
@@ -212,61 +230,80 @@ __device__ __forceinline__ float h2f(uint32_t bits16) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
 }
 
+__device__ __forceinline__ float2 h2pair(uint32_t w) {
+  __half2 h;
+  *reinterpret_cast<uint32_t*>(&h) = w;
+  return __half22float2(h);
+}
+
+// qr (F32/F16 only) rotates the order in which a thread visits the unit's four 16-byte
+// quads: slot quad q holds natural quad (q + qr) & 3.  Lanes of a quarter warp use
+// different rotations so their 16-byte shared-memory reads hit distinct banks; the x
+// values are loaded with the same rotation, so every product pairs the same element.
 template <int WT, class L>
-__device__ __forceinline__ void decode_unit(const L& ld, uint32_t u, float2 (&v)[4], float& d) {
+__device__ __forceinline__ void decode_unit(const L& ld, uint32_t u, float2 (&v)[8], float& d,
+                                            uint32_t qr = 0) {
   if constexpr (WT == WT_F32) {
-    const uint4 a = ld.v4(u * 32u);
-    const uint4 b = ld.v4(u * 32u + 16u);
-    v[0] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
-    v[1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
-    v[2] = make_float2(__uint_as_float(b.x), __uint_as_float(b.y));
-    v[3] = make_float2(__uint_as_float(b.z), __uint_as_float(b.w));
-    d = 1.0f;
-  } else if constexpr (WT == WT_F16) {
-    const uint4 a = ld.v4(u * 16u);
-    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __half2 h;
-      *reinterpret_cast<uint32_t*>(&h) = w[i];
-      v[i] = __half22float2(h);
+    for (int q = 0; q < 4; ++q) {
+      const uint4 a = ld.v4(u * 64u + 16u * ((q + qr) & 3u));
+      v[2 * q] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
+      v[2 * q + 1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
     }
     d = 1.0f;
+  } else if constexpr (WT == WT_F16) {
+    const uint32_t h0 = (qr >> 1) & 1u;
+    const uint4 a = ld.v4(u * 32u + 16u * h0);
+    const uint4 b = ld.v4(u * 32u + 16u * (h0 ^ 1u));
+    v[0] = h2pair(a.x); v[1] = h2pair(a.y); v[2] = h2pair(a.z); v[3] = h2pair(a.w);
+    v[4] = h2pair(b.x); v[5] = h2pair(b.y); v[6] = h2pair(b.z); v[7] = h2pair(b.w);
+    d = 1.0f;
   } else if constexpr (WT == WT_Q8_0) {
-    const uint32_t b = u >> 2, i = u & 3u;
+    const uint32_t b = u >> 1, h = u & 1u;
     const uint32_t off = b * 34u;
     d = h2f(ld.u16(off));
-    const uint32_t w0 = ld.u32_a2(off + 2u + 8u * i) ^ 0x80808080u;  // bytes q + 128
-    const uint32_t w1 = ld.u32_a2(off + 6u + 8u * i) ^ 0x80808080u;
+    uint32_t w[4];
+    ld.template words<4>(off + 2u + 16u * h, w);
     const float bias = -(kMagic + 128.0f);
-    v[0] = magic_pair(w0, 0x7540u, bias);
-    v[1] = magic_pair(w0, 0x7542u, bias);
-    v[2] = magic_pair(w1, 0x7540u, bias);
-    v[3] = magic_pair(w1, 0x7542u, bias);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t t = w[i] ^ 0x80808080u;  // bytes q + 128
+      v[2 * i] = magic_pair(t, 0x7540u, bias);
+      v[2 * i + 1] = magic_pair(t, 0x7542u, bias);
+    }
   } else {  // WT_Q4_0
-    const uint32_t b = u >> 2, i = u & 3u;
+    const uint32_t b = u >> 1, h = u & 1u;
     const uint32_t off = b * 18u;
     d = h2f(ld.u16(off));
-    const uint32_t w = ld.u32_a2(off + 2u + 4u * i);
-    const uint32_t lo = w & 0x0F0F0F0Fu;
-    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+    uint32_t w[2];
+    ld.template words<2>(off + 2u + 8u * h, w);
     const float bias = -(kMagic + 8.0f);
-    v[0] = magic_pair(lo, 0x7540u, bias);
-    v[1] = magic_pair(lo, 0x7542u, bias);
-    v[2] = magic_pair(hi, 0x7540u, bias);
-    v[3] = magic_pair(hi, 0x7542u, bias);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t lo = w[i] & 0x0F0F0F0Fu;
+      const uint32_t hi = (w[i] >> 4) & 0x0F0F0F0Fu;
+      v[2 * i] = magic_pair(lo, 0x7540u, bias);
+      v[2 * i + 1] = magic_pair(lo, 0x7542u, bias);
+      v[4 + 2 * i] = magic_pair(hi, 0x7540u, bias);
+      v[4 + 2 * i + 1] = magic_pair(hi, 0x7542u, bias);
+    }
   }
 }
 
-// Element offsets (within the row / chunk) of unit u's first and second group of 4.
+// Quad rotation of a lane for the F32/F16 unit loads (0 for the block formats).
 template <int WT>
-__device__ __forceinline__ void unit_x_offsets(uint32_t u, uint32_t& e0, uint32_t& e1) {
+__device__ __forceinline__ uint32_t lane_quad_rot(int lane) {
+  return WT == WT_F32 ? ((lane >> 1) & 3u) : WT == WT_F16 ? (((lane >> 2) & 1u) << 1) : 0u;
+}
+
+// Element (within the row / chunk) of the first value of pair k of unit u.
+template <int WT>
+__device__ __forceinline__ uint32_t unit_pair_elem(uint32_t u, int k) {
   if constexpr (WT == WT_Q4_0) {
-    e0 = (u >> 2) * 32u + (u & 3u) * 4u;
-    e1 = e0 + 16u;
+    const uint32_t b = u >> 1, h = u & 1u;
+    return b * 32u + 8u * h + (k < 4 ? 2u * k : 16u + 2u * (k - 4));
   } else {
-    e0 = u * 8u;
-    e1 = e0 + 4u;
+    return u * 16u + 2u * k;
   }
 }
 
@@ -351,7 +388,8 @@ struct WarpVecReduce {
 // last multiplies by `scale` while storing.  Radix-4 passes (two butterfly stages
 // (a, b) -> (a + b, a - b) at strides h and 2h), then one radix-2 pass if log2 B is
 // odd.  `sync()` must be a barrier over the `nthr` participating threads; it is
-// called after every pass.
+// called after every pass.  Index arithmetic uses shifts and masks only, except the
+// sign index when nsigns is not a power of two dividing B.
 template <class Sync>
 __device__ __forceinline__ void fwht_smem(float* buf, int total, int B, int seg_len, int64_t koff,
                                           const float* __restrict__ signs, int nsigns, float scale,
@@ -359,9 +397,14 @@ __device__ __forceinline__ void fwht_smem(float* buf, int total, int B, int seg_
   int log2b = 0;
   while ((1 << log2b) < B) ++log2b;
   const int npass = (log2b >> 1) + (log2b & 1);
+  // nsigns a power of two dividing B: koff and seg_len are multiples of B, so the sign
+  // index of buffer position p is p & (nsigns - 1).
+  const bool sign_mask = (nsigns & (nsigns - 1)) == 0 && nsigns <= B;
+  const int koff32 = static_cast<int>(koff);
   auto sign_of = [&](int p) -> float {
     if (signs == nullptr) return 1.0f;
-    const int64_t pos = koff + (p % seg_len);
+    if (sign_mask) return __ldg(signs + (p & (nsigns - 1)));
+    const int pos = koff32 + (p % seg_len);
     return __ldg(signs + (pos % nsigns));
   };
   if (log2b == 0) {
@@ -369,16 +412,17 @@ __device__ __forceinline__ void fwht_smem(float* buf, int total, int B, int seg_
     sync();
     return;
   }
-  int h = 1;
+  int logh = 0;
   for (int pass = 0; pass < npass; ++pass) {
     const bool first = (pass == 0), last = (pass == npass - 1);
-    const bool radix4 = (h * 4 <= B);
-    if (radix4) {
-      const int per_blk = B >> 2;
+    const int h = 1 << logh;
+    if (logh + 2 <= log2b) {
+      // groups of 4 at strides h, 2h: B/4 groups per block
+      const int lpb = log2b - 2;  // log2(groups per block)
       for (int g = tid; g < (total >> 2); g += nthr) {
-        const int blk = g / per_blk, gi = g - blk * per_blk;
-        const int lo = gi & (h - 1), hi = gi / h;
-        const int p0 = blk * B + hi * (4 * h) + lo;
+        const int blk = g >> lpb, gi = g & ((1 << lpb) - 1);
+        const int lo = gi & (h - 1), hi = gi >> logh;
+        const int p0 = (blk << log2b) + (hi << (logh + 2)) + lo;
         float a0 = buf[p0], a1 = buf[p0 + h], a2 = buf[p0 + 2 * h], a3 = buf[p0 + 3 * h];
         if (first) {
           a0 *= sign_of(p0); a1 *= sign_of(p0 + h);
@@ -389,19 +433,19 @@ __device__ __forceinline__ void fwht_smem(float* buf, int total, int B, int seg_
         if (last) { c0 *= scale; c1 *= scale; c2 *= scale; c3 *= scale; }
         buf[p0] = c0; buf[p0 + h] = c1; buf[p0 + 2 * h] = c2; buf[p0 + 3 * h] = c3;
       }
-      h *= 4;
+      logh += 2;
     } else {  // final radix-2 stage, h == B / 2
-      const int per_blk = B >> 1;
+      const int lpb = log2b - 1;
       for (int g = tid; g < (total >> 1); g += nthr) {
-        const int blk = g / per_blk, lo = g - blk * per_blk;
-        const int p0 = blk * B + lo;
+        const int blk = g >> lpb, lo = g & ((1 << lpb) - 1);
+        const int p0 = (blk << log2b) + lo;
         float a0 = buf[p0], a1 = buf[p0 + h];
         if (first) { a0 *= sign_of(p0); a1 *= sign_of(p0 + h); }
         float c0 = a0 + a1, c1 = a0 - a1;
         if (last) { c0 *= scale; c1 *= scale; }
         buf[p0] = c0; buf[p0 + h] = c1;
       }
-      h *= 2;
+      logh += 1;
     }
     sync();
   }

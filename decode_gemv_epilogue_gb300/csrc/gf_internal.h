@@ -12,12 +12,21 @@ constexpr int kMaxStages = 8;
 constexpr int kBarBytes = 256;              // mbarrier area at the start of shared memory
 constexpr int kXsMaxBytes = 64 * 1024;      // x chunk (all columns) kept in shared memory
 constexpr int kSegMaxBytes = 32 * 1024;     // bytes of one row's K chunk
-constexpr int kStageTargetBytes = 32 * 1024;
+constexpr int kStageMaxBytes = 72 * 1024;
 constexpr int kRedMaxBytes = 16 * 1024;
+constexpr int kRingSlackBytes = 16;         // aligned-word decoders may read 3 bytes past a row
 constexpr int kMaxFusedFwhtBlock = 8192;
+constexpr int kUnitElems = 16;              // weights per decode unit (half a quant block)
 
-// Rows per tile and consumer warps, as functions of the column count.
-__host__ __device__ constexpr int stream_rmax(int nc) { return nc == 1 ? 16 : nc == 2 ? 8 : 4; }
+// Per (format, columns): units per thread per tile (U) and rows per thread per tile (RT).
+// A tile of R = G * RT rows is split over G row groups of consumer warps; within a
+// group every thread owns U units of 16 weights of the K chunk.
+__host__ __device__ constexpr int stream_u(int wt, int nc) {
+  return (nc == 1 && (wt == 2 || wt == 3)) ? 2 : 1;
+}
+__host__ __device__ constexpr int stream_rt(int wt, int nc) {
+  return nc == 1 ? (wt == 2 ? 2 : 4) : nc == 2 ? 4 : 2;
+}
 __host__ __device__ constexpr int stream_max_cw(int nc) { return nc <= 2 ? 16 : 8; }
 __host__ __device__ constexpr int stream_threads(int nc) { return 32 * (1 + stream_max_cw(nc)); }
 
@@ -34,11 +43,13 @@ struct StreamArgs {
   int row_bytes;     // bytes of a full row
   int kc_len;        // elements per K chunk
   int n_kc;          // K chunks
-  int R;             // rows per tile
+  int R;             // rows per tile (= G * RT)
+  int G;             // row groups of consumer warps
+  int wpg;           // warps per row group
   int NS;            // ring stages
   int stage_bytes;   // bytes reserved per stage
   int RC;            // rows per finalize chunk
-  int ncw;           // consumer warps
+  int ncw;           // consumer warps (= G * wpg)
   int rows_base;     // rows per CTA (the first rows_extra CTAs take one more)
   int rows_extra;
   int fwht_B;        // 0 = no prologue

@@ -77,25 +77,27 @@ int launch_elementwise(int op, const float* a, const float* b, int64_t nb, float
 
 // ------------------------------------------------------------------ dequantize hook
 // Same unit decoders as the streaming kernel (through a global-memory loader), one
-// thread per 8-weight unit; the product with the block scale is exact in fp32.
+// thread per 16-weight unit; the product with the block scale is exact in fp32.
 template <int WT>
 __global__ void dequantize_units_kernel(const uint8_t* W, int64_t M, int64_t K, int64_t row_bytes,
                                         float* out) {
-  const int64_t units_per_row = K / 8;
+  const int64_t units_per_row = K / kUnitElems;
   const int64_t total = M * units_per_row;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total; t += stride) {
     const int64_t row = t / units_per_row;
     const uint32_t u = static_cast<uint32_t>(t - row * units_per_row);
     const GmemLoader ld{W + row * row_bytes};
-    float2 v[4];
+    float2 v[8];
     float d;
     decode_unit<WT>(ld, u, v, d);
-    uint32_t e0, e1;
-    unit_x_offsets<WT>(u, e0, e1);
     float* o = out + row * K;
-    o[e0 + 0] = v[0].x * d; o[e0 + 1] = v[0].y * d; o[e0 + 2] = v[1].x * d; o[e0 + 3] = v[1].y * d;
-    o[e1 + 0] = v[2].x * d; o[e1 + 1] = v[2].y * d; o[e1 + 2] = v[3].x * d; o[e1 + 3] = v[3].y * d;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t e = unit_pair_elem<WT>(u, k);
+      o[e] = v[k].x * d;
+      o[e + 1] = v[k].y * d;
+    }
   }
 }
 
@@ -113,10 +115,10 @@ __global__ void dequantize_elems_kernel(const uint8_t* W, int64_t M, int64_t K, 
 
 int launch_dequantize(int wtype, const uint8_t* W, int64_t M, int64_t K, int64_t row_bytes, float* out,
                       cudaStream_t st) {
-  const bool by_unit = (K % 8 == 0) &&
+  const bool by_unit = (K % kUnitElems == 0) &&
                        ((wtype != WT_F32 && wtype != WT_F16) ||
                         (reinterpret_cast<uintptr_t>(W) % 16 == 0 && row_bytes % 16 == 0));
-  const int64_t work = by_unit ? M * (K / 8) : M * K;
+  const int64_t work = by_unit ? M * (K / kUnitElems) : M * K;
   int64_t grid = (work + 255) / 256;
   if (grid > 152 * 16) grid = 152 * 16;
   if (grid < 1) grid = 1;

@@ -27,12 +27,19 @@ def _popcount(a):
     return c
 
 
+_H_CACHE = {}
+
+
 def hadamard(n):
     """Sylvester-ordered Hadamard matrix, closed form (-1)^popcount(i & j), float64."""
     if n < 1 or n & (n - 1):
         raise ValueError("n must be a power of two")
-    i = np.arange(n, dtype=np.int64)
-    return np.where(_popcount(i[:, None] & i[None, :]) % 2 == 0, 1.0, -1.0)
+    if n not in _H_CACHE:
+        i = np.arange(n, dtype=np.int64)
+        H = np.where(_popcount(i[:, None] & i[None, :]) % 2 == 0, 1.0, -1.0)
+        H.setflags(write=False)
+        _H_CACHE[n] = H
+    return _H_CACHE[n].copy()
 
 
 def signed_input(x, signs):
@@ -53,7 +60,8 @@ def fwht_signed(x, signs, block):
     v = x if signs is None else signed_input(x, signs)
     H = hadamard(block)
     blocks = v.reshape(-1, block)
-    return (blocks @ H.T / np.sqrt(block)).reshape(-1)
+    # plain sum over t of H[j, t] * v[b, t] (numpy's own loop: one thread, no BLAS)
+    return (np.einsum("jt,bt->bj", H, blocks) / np.sqrt(block)).reshape(-1)
 
 
 def fwht_butterfly(x, signs, block):

@@ -102,7 +102,8 @@ def test_gemv_accepts_exact_in_place_and_empty(lib):
 
 @pytest.mark.parametrize("wt,K,w,expect_path", [
     (1, 4096, W, 1), (3, 4096, W, 1), (2, 4096, W, 1), (0, 512, W, 1),
-    (1, 36, W, 2), (1, 4096, W + 2, 2), (3, 96, W, 2), (2, 224, W, 2), (0, 4, W, 2),
+    (1, 36, W, 2), (1, 4096, W + 2, 2), (3, 96, W, 2), (2, 224, W, 2), (0, 4, W, 2), (0, 8, W, 2),
+    (0, 16, W, 1), (1, 24, W, 2),
 ])
 def test_plan_path_selection(lib, wt, K, w, expect_path):
     path, info = lib.plan(w, wt, X, 1000, K, 0, None, D)

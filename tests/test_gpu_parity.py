@@ -118,7 +118,8 @@ def test_formats_tiles_and_ragged_rows(G, wt, epi):
     (synth.Q4_0, 29, 96, 0, 2),      # row bytes 54, not a multiple of 16
     (synth.Q8_0, 13, 224, 0, 2),     # row bytes 238
     (synth.Q4_0, 1, 4096, 0, 1),     # a single row
-    (synth.F32, 5, 8, 0, 1),         # smallest K of the streamed kernel
+    (synth.F32, 5, 16, 0, 1),        # smallest K of the streamed kernel
+    (synth.F32, 5, 8, 0, 2),         # below one 16-weight unit
     (synth.Q4_0, 300, 32, 0, 2),     # one block per row
 ])
 def test_edge_shapes_and_paths(G, wt, M, K, w_offset, expect_path):
