@@ -12,7 +12,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/gemvfuse.h"
+#include "gemvfuse.h"
 #include "gf_device.cuh"
 #include "gf_internal.h"
 
@@ -147,14 +147,15 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
   if (rb % 16 != 0 || !aligned(c.W, 16) || !aligned(c.x, 16)) return false;
   if (rb > INT32_MAX / 2) return false;
   const int U = stream_u(c.wtype, nc), RT = stream_rt(c.wtype, nc);
-  const int max_cw = stream_max_cw(nc);
+  const int CS = stream_cs(c.wtype, nc);
+  const int max_cw = stream_max_cw(c.wtype, nc);
   auto seg_of = [&](int klen) -> int { return static_cast<int>(row_bytes_of(c.wtype, klen)); };
   // K chunk: the whole row if x, one row's bytes and the units all fit; else a multiple
   // of the granule (256 elements, or the FWHT block) that does.
   int gran = 256;
   if (c.signs) gran = std::max<int>(gran, static_cast<int>(c.fwht_block));
-  const int64_t cap_x = kXsMaxBytes / (4 * nc);
-  const int64_t cap_units = static_cast<int64_t>(kUnitElems) * U * 32 * max_cw;
+  const int64_t cap_x = c.signs ? kXsMaxBytes / (4 * nc) : INT32_MAX;  // x staged only for the prologue
+  const int64_t cap_units = static_cast<int64_t>(kUnitElems) * U * 32 * (max_cw / CS);
   const int cap_seg = std::min(kSegMaxBytes, kStageMaxBytes / RT);  // RT rows fit one stage
   int kc = K;
   if (K > cap_x || seg_of(K) > cap_seg || K > cap_units) {
@@ -173,7 +174,8 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
     if (seg_of(last) % 16 != 0 || last % kUnitElems != 0) return false;
   }
   const int units = kc / kUnitElems;
-  const int wpg = (((units + U - 1) / U) + 31) / 32;
+  const int wpc = (((units + U - 1) / U) + 31) / 32;
+  const int wpg = CS * wpc;
   if (wpg > max_cw) return false;
   const int grid = static_cast<int>(std::min<int64_t>(lim.sm_count, c.M));
   const int rows_base = static_cast<int>(c.M / grid);
@@ -183,11 +185,11 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
   while (G > 1 && G * RT * seg_full > kStageMaxBytes) --G;
   const int ncw = G * wpg;
   int R = G * RT;
-  int RC = std::min(rows_max, std::max(R, kRedMaxBytes / (wpg * nc * 4)));
+  int RC = std::min(rows_max, std::max(R, kRedMaxBytes / (wpc * nc * 4)));
   RC = std::min(RC, 512);
-  const int xs_bytes = round_up(nc * kc * 4, 128);
+  const int xs_bytes = c.signs ? round_up(nc * kc * 4, 128) : 0;
   const int aux_bytes = round_up(nc * RC * 4, 128);
-  const int red_bytes = round_up(RC * wpg * nc * 4, 128);
+  const int red_bytes = round_up(RC * wpc * nc * 4, 128);
   const int fixed = kBarBytes + xs_bytes + aux_bytes + red_bytes + kRingSlackBytes;
   const int stage_bytes = round_up(R * seg_full, 128);
   const int NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
@@ -207,6 +209,7 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
   s.R = R;
   s.G = G;
   s.wpg = wpg;
+  s.wpc = wpc;
   s.NS = NS;
   s.stage_bytes = stage_bytes;
   s.RC = RC;

@@ -27,30 +27,36 @@ __host__ __device__ constexpr int seg_bytes_of(int klen) {
   return WT == WT_F32 ? 4 * klen : WT == WT_F16 ? 2 * klen : WT == WT_Q8_0 ? (klen / 32) * 34 : (klen / 32) * 18;
 }
 
-// x values of one unit (all columns) as eight float2 pairs per column, matching the
-// pair order of decode_unit().
-template <int WT, int NC>
-__device__ __forceinline__ void load_unit_x(const float* xs, int xstride, int u, uint32_t qr,
-                                            float2 (&xv)[NC][8]) {
+// x values of one unit for the thread's NCT columns (starting at column c0; columns
+// past the batch are zero) as eight float2 pairs each, in decode_unit()'s pair order.
+// xs is either the K chunk staged in shared memory (column stride xstride) or x itself
+// in global memory (column stride K, offset to the chunk); both are read with 16-byte
+// loads.
+template <int WT, int NCT>
+__device__ __forceinline__ void load_unit_x(const float* xs, int64_t xstride, int u, uint32_t qr, int c0, int nc,
+                                            float2 (&xv)[NCT][8]) {
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
+  for (int c = 0; c < NCT; ++c) {
+    const bool live = (c0 + c) < nc;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 t = *reinterpret_cast<const float4*>(
-          xs + c * xstride + unit_pair_elem<WT>(static_cast<uint32_t>(u), 2 * static_cast<int>((q + qr) & 3u)));
+      float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (live)
+        t = *reinterpret_cast<const float4*>(
+            xs + (c0 + c) * xstride + unit_pair_elem<WT>(static_cast<uint32_t>(u), 2 * static_cast<int>((q + qr) & 3u)));
       xv[c][2 * q] = make_float2(t.x, t.y);
       xv[c][2 * q + 1] = make_float2(t.z, t.w);
     }
   }
 }
 
-// acc[c] += sum of the unit's 16 products for each column c (quant formats: the block
-// partial first, then scaled by d into the running sum).
-template <int WT, int NC>
-__device__ __forceinline__ void unit_rows_fma(const float2 (&v)[8], float d, const float2 (&xv)[NC][8],
-                                              float2 (&acc)[NC]) {
+// acc[c] += sum of the unit's 16 products for each of the thread's columns (quant
+// formats: the block partial first, then scaled by d into the running sum).
+template <int WT, int NCT>
+__device__ __forceinline__ void unit_rows_fma(const float2 (&v)[8], float d, const float2 (&xv)[NCT][8],
+                                              float2 (&acc)[NCT]) {
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
+  for (int c = 0; c < NCT; ++c) {
     if constexpr (WT == WT_F32 || WT == WT_F16) {
       float2 t = acc[c];
 #pragma unroll
@@ -68,51 +74,37 @@ __device__ __forceinline__ void unit_rows_fma(const float2 (&v)[8], float d, con
   }
 }
 
-// x held in registers for the whole K chunk when it fits (U units x NC columns x 16).
-template <int WT, int NC, int U>
-__host__ __device__ constexpr bool stream_xreg() { return U * NC * 16 <= 32; }
-
-// One thread's share of a tile: U units (16 weights each, stride tg_n within the row
-// group) times RT rows (stride G within the tile).  x comes either from registers
-// loaded once per K chunk (xr) or, for wide batches, from shared memory once per tile
-// and unit, reused for the RT rows.
-template <int WT, int NC, int U, int RT>
+// One thread's share of a tile: U units (16 weights each, stride tg_n within the
+// column group) times RT rows (stride G within the tile), against x in registers.
+template <int WT, int NCT, int U, int RT>
 __device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int units, int tg, int tg_n,
-                                             int g, int G, const float* xs, int xstride, uint32_t qr,
-                                             const float2 (&xr)[U][NC][8], float2 (&acc)[RT][NC]) {
-  constexpr bool XREG = stream_xreg<WT, NC, U>();
+                                             int g, int G, uint32_t qr, const float2 (&xr)[U][NCT][8],
+                                             float2 (&acc)[RT][NCT]) {
 #pragma unroll
   for (int i = 0; i < U; ++i) {
     const int u = tg + i * tg_n;
     if (u < units) {
-      auto rows_of_unit = [&](const float2 (&xv)[NC][8]) {
 #pragma unroll
-        for (int j = 0; j < RT; ++j) {
-          const int r = g + j * G;
-          if (r < rows) {
-            const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
-            float2 v[8];
-            float d;
-            decode_unit<WT>(ld, static_cast<uint32_t>(u), v, d, qr);
-            unit_rows_fma<WT, NC>(v, d, xv, acc[j]);
-          }
+      for (int j = 0; j < RT; ++j) {
+        const int r = g + j * G;
+        if (r < rows) {
+          const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+          float2 v[8];
+          float d;
+          decode_unit<WT>(ld, static_cast<uint32_t>(u), v, d, qr);
+          unit_rows_fma<WT, NCT>(v, d, xr[i], acc[j]);
         }
-      };
-      if constexpr (XREG) {
-        rows_of_unit(xr[i]);
-      } else {
-        float2 xt[NC][8];
-        load_unit_x<WT, NC>(xs, xstride, u, qr, xt);
-        rows_of_unit(xt);
       }
     }
   }
 }
 
 template <int WT, int NC>
-__global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(const StreamArgs a) {
+__global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(const StreamArgs a) {
   constexpr int U = stream_u(WT, NC);
   constexpr int RT = stream_rt(WT, NC);
+  constexpr int NCT = stream_nct(WT, NC);
+  static_assert(U * NCT * 16 <= 64, "x registers per thread");
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
@@ -186,8 +178,11 @@ __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(cons
     // wait gave up; after an abort the remaining work is skipped, not the barriers.
     const int cw = warp - 1, ctid = threadIdx.x - 32, nt = a.ncw * 32;
     const int g = cw / a.wpg;                  // row group of this warp
-    const int wg = cw - g * a.wpg;             // warp within the group
-    const int tg = wg * 32 + lane, tg_n = a.wpg * 32;
+    const int wr = cw - g * a.wpg;             // warp within the row group
+    const int cgi = wr / a.wpc;                // column group
+    const int wc = wr - cgi * a.wpc;           // warp within the column group
+    const int c0 = cgi * NCT;                  // first column of this thread
+    const int tg = wc * 32 + lane, tg_n = a.wpc * 32;
     const uint32_t qr = lane_quad_rot<WT>(lane);
     const bool need_aux = (a.epi == EPI_SILU_MUL || a.epi == EPI_ADD);
     pdl_wait();  // x, aux and dst may belong to the preceding grid
@@ -200,7 +195,8 @@ __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(cons
       const int nrc = min(a.RC, nrows - rc0);
       for (int kc = 0; kc < a.n_kc; ++kc) {
         const int klen = min(a.kc_len, a.K - kc * a.kc_len);
-        if (a.n_kc > 1 || !x_loaded) {
+        if (a.fwht_B > 0 && (a.n_kc > 1 || !x_loaded)) {
+          // prologue: stage the chunk of every column in shared memory, transform it there
           if (x_loaded) cbar();  // nobody still reads the previous x chunk
           if (ctid == 0 && !*abort_flag) {
             fence_proxy_async_smem();
@@ -217,9 +213,8 @@ __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(cons
             }
           ok = ok && mbar_wait_or_abort(xbar, xphase, abort_flag, a.err);
           xphase ^= 1u;
-          if (a.fwht_B > 0)
-            fwht_smem(xs, NC * klen, a.fwht_B, klen, static_cast<int64_t>(kc) * a.kc_len, a.signs,
-                      a.nsigns, a.fwht_scale, ctid, nt, cbar);
+          fwht_smem(xs, NC * klen, a.fwht_B, klen, static_cast<int64_t>(kc) * a.kc_len, a.signs, a.nsigns,
+                    a.fwht_scale, ctid, nt, cbar);
         } else if (kc == 0 && need_aux) {
           for (int i = ctid; i < nrc * NC; i += nt) {
             const int c = i / nrc, r = i - c * nrc;
@@ -228,42 +223,44 @@ __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(cons
         }
         const int units = klen / kUnitElems;
         const int seg = seg_bytes_of<WT>(klen);
-        float2 xr[U][NC][8];
-        if constexpr (stream_xreg<WT, NC, U>()) {
+        // this thread's x (its units, its columns) in registers for the whole chunk: from
+        // the transformed chunk in shared memory, or straight from global memory
+        const float* xsrc = a.fwht_B > 0 ? xs : a.x + static_cast<int64_t>(kc) * a.kc_len;
+        const int64_t xstride = a.fwht_B > 0 ? klen : a.K;
+        float2 xr[U][NCT][8];
 #pragma unroll
-          for (int i = 0; i < U; ++i) {
-            const int u = tg + i * tg_n;
-            if (u < units) load_unit_x<WT, NC>(xs, klen, u, qr, xr[i]);
-          }
+        for (int i = 0; i < U; ++i) {
+          const int u = tg + i * tg_n;
+          if (u < units && ok) load_unit_x<WT, NCT>(xsrc, xstride, u, qr, c0, NC, xr[i]);
         }
         for (int t0 = 0; t0 < nrc; t0 += a.R, ++it) {
           const int rows = min(a.R, nrc - t0);
           const int slot = it % a.NS, round = it / a.NS;
           ok = ok && mbar_wait_or_abort(full0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag,
                                         a.err);
-          float2 acc[RT][NC];
+          float2 acc[RT][NCT];
 #pragma unroll
           for (int j = 0; j < RT; ++j)
 #pragma unroll
-            for (int c = 0; c < NC; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
+            for (int c = 0; c < NCT; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
           if (ok)
-            consume_tile<WT, NC, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units,
-                                        tg, tg_n, g, a.G, xs, klen, qr, xr, acc);
+            consume_tile<WT, NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units,
+                                         tg, tg_n, g, a.G, qr, xr, acc);
           __syncwarp();
           if (lane == 0) mbar_arrive(empty0 + 8u * slot);
-          // warp reduction of the RT*NC partial sums (padded to a power of two)
-          constexpr int V = RT * NC;
+          // warp reduction of the RT*NCT partial sums (padded to a power of two)
+          constexpr int V = RT * NCT;
           constexpr int VP = V > 16 ? 32 : V > 8 ? 16 : V > 4 ? 8 : V > 2 ? 4 : V > 1 ? 2 : 1;
           float vals[VP];
 #pragma unroll
           for (int j = 0; j < VP; ++j)
-            vals[j] = j < V ? acc[j / NC][j % NC].x + acc[j / NC][j % NC].y : 0.0f;
+            vals[j] = j < V ? acc[j / NCT][j % NCT].x + acc[j / NCT][j % NCT].y : 0.0f;
           const float sum = WarpVecReduce<VP>::run(vals, lane);
           const int jv = lane >> (5 - WarpVecReduce<VP>::kLog);
           if (lane == WarpVecReduce<VP>::owner(jv) && jv < V) {
-            const int r = g + (jv / NC) * a.G, c = jv % NC;
-            if (r < rows) {
-              float* p = red + ((t0 + r) * a.wpg + wg) * NC + c;
+            const int r = g + (jv / NCT) * a.G, c = c0 + jv % NCT;
+            if (r < rows && c < NC) {
+              float* p = red + ((t0 + r) * a.wpc + wc) * NC + c;
               *p = (kc == 0) ? sum : (*p + sum);
             }
           }
@@ -274,7 +271,7 @@ __global__ void __launch_bounds__(stream_threads(NC), 1) gemv_stream_kernel(cons
         for (int i = ctid; i < nrc * NC; i += nt) {
           const int c = i / nrc, r = i - c * nrc;
           float y = 0.0f;
-          for (int w = 0; w < a.wpg; ++w) y += red[(r * a.wpg + w) * NC + c];
+          for (int w = 0; w < a.wpc; ++w) y += red[(r * a.wpc + w) * NC + c];
           const float av = need_aux ? auxs[c * a.RC + r] : 0.0f;
           a.dst[c * a.M + r0 + rc0 + r] = apply_tail(a.epi, y, av);
         }

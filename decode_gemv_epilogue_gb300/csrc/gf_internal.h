@@ -18,17 +18,26 @@ constexpr int kRingSlackBytes = 16;         // aligned-word decoders may read 3 
 constexpr int kMaxFusedFwhtBlock = 8192;
 constexpr int kUnitElems = 16;              // weights per decode unit (half a quant block)
 
-// Per (format, columns): units per thread per tile (U) and rows per thread per tile (RT).
-// A tile of R = G * RT rows is split over G row groups of consumer warps; within a
-// group every thread owns U units of 16 weights of the K chunk.
-__host__ __device__ constexpr int stream_u(int wt, int nc) {
-  return (nc == 1 && (wt == 2 || wt == 3)) ? 2 : 1;
+// Tiling of the consumer warps, per (format, columns):
+//  U   units (16 weights) per thread per K chunk, RT rows per thread per tile;
+//  NCT columns per thread, CS = ceil(NC / NCT) column groups.
+// A tile of R = G * RT rows is split over G row groups of consumer warps; a row group is
+// CS column groups of wpc warps; within a column group every thread owns U units of the
+// K chunk and keeps their x values (NCT columns) in registers for the whole chunk.
+// F32/F16 decode is cheap, so batches are split two columns per thread (more warps);
+// the block formats keep up to four columns per thread so each weight is decoded once
+// per four columns.
+__host__ __device__ constexpr bool stream_quant(int wt) { return wt == 2 || wt == 3; }
+__host__ __device__ constexpr int stream_nct(int wt, int nc) {
+  return stream_quant(wt) ? (nc <= 4 ? nc : 4) : (nc <= 2 ? nc : 2);
 }
-__host__ __device__ constexpr int stream_rt(int wt, int nc) {
-  return nc == 1 ? (wt == 2 ? 2 : 4) : nc == 2 ? 4 : 2;
+__host__ __device__ constexpr int stream_cs(int wt, int nc) {
+  return (nc + stream_nct(wt, nc) - 1) / stream_nct(wt, nc);
 }
-__host__ __device__ constexpr int stream_max_cw(int nc) { return nc <= 2 ? 16 : 8; }
-__host__ __device__ constexpr int stream_threads(int nc) { return 32 * (1 + stream_max_cw(nc)); }
+__host__ __device__ constexpr int stream_u(int wt, int nc) { return (nc == 1 && stream_quant(wt)) ? 2 : 1; }
+__host__ __device__ constexpr int stream_rt(int wt, int nc) { return (nc == 1 && wt == 2) ? 2 : 4; }
+__host__ __device__ constexpr int stream_max_cw(int wt, int nc) { return stream_nct(wt, nc) <= 2 ? 16 : 8; }
+__host__ __device__ constexpr int stream_threads(int wt, int nc) { return 32 * (1 + stream_max_cw(wt, nc)); }
 
 struct StreamArgs {
   const uint8_t* W;
@@ -45,7 +54,8 @@ struct StreamArgs {
   int n_kc;          // K chunks
   int R;             // rows per tile (= G * RT)
   int G;             // row groups of consumer warps
-  int wpg;           // warps per row group
+  int wpg;           // warps per row group (= CS * wpc)
+  int wpc;           // warps per column group
   int NS;            // ring stages
   int stage_bytes;   // bytes reserved per stage
   int RC;            // rows per finalize chunk
