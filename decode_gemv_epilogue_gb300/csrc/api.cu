@@ -99,6 +99,7 @@ struct Call {
   const float* signs;
   int64_t fwht_block, nsigns;
   uint32_t flags;
+  float* workspace;
 };
 
 static int validate(const Call& c) {
@@ -133,6 +134,13 @@ static int validate(const Call& c) {
   if (ranges_overlap(c.dst, dbytes, c.x, xbytes)) return GF_ERR_ALIAS;
   if (c.signs && ranges_overlap(c.dst, dbytes, c.signs, c.nsigns * 4)) return GF_ERR_ALIAS;
   if (need_aux && c.aux != c.dst && ranges_overlap(c.dst, dbytes, c.aux, dbytes)) return GF_ERR_ALIAS;
+  if (c.workspace && c.signs && c.M > 0 && c.K > 0) {
+    if (!aligned(c.workspace, 16)) return GF_ERR_ALIGN;
+    if (ranges_overlap(c.workspace, xbytes, c.W, wbytes) || ranges_overlap(c.workspace, xbytes, c.x, xbytes) ||
+        ranges_overlap(c.workspace, xbytes, c.dst, dbytes) || ranges_overlap(c.workspace, xbytes, c.signs, c.nsigns * 4) ||
+        (need_aux && ranges_overlap(c.workspace, xbytes, c.aux, dbytes)))
+      return GF_ERR_ALIAS;
+  }
   return GF_OK;
 }
 
@@ -280,6 +288,24 @@ static int launch_call(const Call& c, float* dst, cudaStream_t st) {
   return GF_OK;
 }
 
+// The prologue as a stand-alone transform into the workspace, then the GEMV on it.
+// The GEMV is launched with programmatic dependent launch: it streams W while the
+// transform runs and waits for it before reading x' (W is not written by the
+// transform, so this holds whatever the caller's flags).
+static int launch_via_workspace(const Call& c, float* dst, cudaStream_t st) {
+  const int e = launch_fwht(c.x, c.signs, c.workspace, c.ncols * c.K, static_cast<int>(c.fwht_block),
+                            static_cast<int>(c.nsigns), st);
+  if (e != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(e));
+  Call g = c;
+  g.x = c.workspace;
+  g.signs = nullptr;
+  g.fwht_block = 0;
+  g.nsigns = 0;
+  g.workspace = nullptr;
+  g.flags |= GF_FLAG_PDL;
+  return launch_call(g, dst, st);
+}
+
 static Call make_call(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
                       const float* aux, const float* dst, const gf_opts* opts) {
   Call c;
@@ -296,12 +322,14 @@ static Call make_call(const void* W, int wtype, const float* x, int64_t M, int64
   c.fwht_block = 0;
   c.nsigns = 0;
   c.flags = 0;
+  c.workspace = nullptr;
   if (opts) {
     c.ncols = opts->ncols == 0 ? 1 : opts->ncols;
     c.signs = opts->fwht_signs;
     c.fwht_block = opts->fwht_block;
     c.nsigns = opts->nsigns;
     c.flags = opts->flags;
+    c.workspace = opts->fwht_signs ? opts->fwht_workspace : nullptr;
   }
   return c;
 }
@@ -337,6 +365,7 @@ int gemv_fused_ex(const void* W, int wtype, const float* x, int64_t M, int64_t K
   v = check_view(opts, M);
   if (v != GF_OK) return v;
   if (M == 0) return GF_OK;
+  if (c.workspace && c.K > 0) return launch_via_workspace(c, dst, static_cast<cudaStream_t>(stream));
   return launch_call(c, dst, static_cast<cudaStream_t>(stream));
 }
 
@@ -353,9 +382,14 @@ int gf_plan(const void* W, int wtype, const float* x, int64_t M, int64_t K, int 
   v = check_view(opts, M);
   if (v != GF_OK) return v;
   if (M == 0) return 0;  // nothing would be launched
+  Call pc = c;
+  if (pc.workspace) {  // the GEMV of the workspace path reads x' without a prologue
+    pc.x = pc.workspace;
+    pc.signs = nullptr;
+  }
   Plan p;
   int gsmem = 0, ggrid = 0;
-  const int path = plan_call(c, p, &gsmem, &ggrid);
+  const int path = plan_call(pc, p, &gsmem, &ggrid);
   if (path < 0) return path;
   if (info) {
     for (int i = 0; i < 8; ++i) info[i] = 0;

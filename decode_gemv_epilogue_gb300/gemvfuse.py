@@ -29,7 +29,7 @@ _vp, _i64, _i32, _u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_
 
 class GfOpts(ctypes.Structure):
     _fields_ = [("ncols", _i64), ("fwht_signs", _vp), ("fwht_block", _i64), ("nsigns", _i64),
-                ("view_ne", _i64 * 4), ("flags", _u32)]
+                ("view_ne", _i64 * 4), ("flags", _u32), ("fwht_workspace", _vp)]
 
 
 def _sig(name, args, res=_i32):
@@ -95,7 +95,7 @@ def _check(st, what):
         raise GemvFuseError(st, what)
 
 
-def make_opts(ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, view=None, pdl=False):
+def make_opts(ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, view=None, pdl=False, fwht_workspace=None):
     o = GfOpts()
     o.ncols = ncols
     o.fwht_signs = _ptr(fwht_signs)
@@ -108,6 +108,7 @@ def make_opts(ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, view=None, pd
     for i in range(4):
         o.view_ne[i] = v[i] if i < len(v) else 0
     o.flags = FLAG_PDL if pdl else 0
+    o.fwht_workspace = _ptr(fwht_workspace)
     return o
 
 
@@ -119,8 +120,8 @@ def gemv_fused(W, wtype, x, M, K, epilogue, aux, dst, stream=None, check=True):
 
 
 def gemv_fused_ex(W, wtype, x, M, K, epilogue, aux, dst, ncols=1, fwht_signs=None, fwht_block=0,
-                  nsigns=None, view=None, pdl=False, stream=None, check=True):
-    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, view, pdl)
+                  nsigns=None, view=None, pdl=False, fwht_workspace=None, stream=None, check=True):
+    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, view, pdl, fwht_workspace)
     st = _gemv_fused_ex(_ptr(W), wtype, _ptr(x), M, K, epilogue, _ptr(aux), _ptr(dst),
                         ctypes.byref(o), _stream(stream))
     if check:

@@ -93,6 +93,11 @@ typedef struct {
                              /* contiguous memory is an index identity ([EPI] What      */
                              /* changed: result written with the matmul geometry).      */
   uint32_t flags;            /* GF_FLAG_*                                              */
+  float* fwht_workspace;     /* optional device buffer of ncols*K floats (16-byte       */
+                             /* aligned, overlapping no other argument).  Given, the    */
+                             /* prologue runs once as a stand-alone transform into it   */
+                             /* and the GEMV reads it, chained with programmatic        */
+                             /* dependent launch; NULL: every CTA transforms x on chip. */
 } gf_opts;
 
 /* y = W x with the fused tail, one column.  [EPI] Summary, What changed.
@@ -109,8 +114,10 @@ GF_API int gemv_fused(const void* W, int wtype, const float* x, int64_t M, int64
 /* gemv_fused plus the options in `opts` (may be NULL): a batch of ncols independent
  * columns sharing one pass over W; the signed-FWHT prologue
  *     x'_c[b*B + j] = (1/sqrt(B)) sum_t H_B[j][t] s[(b*B + t) % nsigns] x_c[b*B + t]
- * (Sylvester H, [FWHT] Overview) applied to each column before the product, with x'
- * kept on chip; the dst view check; and GF_FLAG_PDL.  fwht_signs must not overlap dst. */
+ * (Sylvester H, [FWHT] Overview) applied to each column before the product -- on chip
+ * in every CTA, or once into opts->fwht_workspace; the dst view check; and
+ * GF_FLAG_PDL.  fwht_signs must not overlap dst.  With a workspace two kernels are
+ * launched (the transform, then the GEMV). */
 GF_API int gemv_fused_ex(const void* W, int wtype, const float* x, int64_t M, int64_t K,
                   int epilogue, const float* aux, float* dst, const gf_opts* opts,
                   void* stream);

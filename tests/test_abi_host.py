@@ -83,6 +83,12 @@ def g(lib, *a, **k):
     ((W, 1, X, 16, 32, 0, None, D), {"fwht_signs": S, "fwht_block": 32, "nsigns": 0}, -1),
     ((W, 1, X, 16, 32, 0, None, D), {"fwht_signs": S, "fwht_block": 32, "nsigns": 5}, -1),
     ((W, 1, X, 16, 32, 0, None, S + 8), {"fwht_signs": S, "fwht_block": 32, "nsigns": 32}, -2),
+    ((W, 1, X, 16, 32, 0, None, D), {"fwht_signs": S, "fwht_block": 32, "nsigns": 32,
+                                     "fwht_workspace": (6 << 40) + 4}, -4),          # workspace misaligned
+    ((W, 1, X, 16, 32, 0, None, D), {"fwht_signs": S, "fwht_block": 32, "nsigns": 32,
+                                     "fwht_workspace": X + 64}, -2),                 # workspace over x
+    ((W, 1, X, 16, 32, 0, None, D), {"fwht_signs": S, "fwht_block": 32, "nsigns": 32,
+                                     "fwht_workspace": D}, -2),                      # workspace over dst
 ])
 def test_gemv_validation(lib, args, kw, expect):
     assert g(lib, *args, **kw) == expect
@@ -111,6 +117,13 @@ def test_plan_path_selection(lib, wt, K, w, expect_path):
     if path == lib.PATH_STREAM:
         assert info["smem"] <= 232448 and 2 <= info["stages"] <= 8
         assert info["threads"] % 32 == 0 and info["threads"] <= 544
+
+
+def test_plan_with_fwht_workspace_describes_the_plain_gemv(lib):
+    path, info = lib.plan(W, 1, X, 5120, 5120, 4, A, A, ncols=8, fwht_signs=S, fwht_block=1024, nsigns=1024,
+                          fwht_workspace=6 << 40)
+    path2, info2 = lib.plan(W, 1, 6 << 40, 5120, 5120, 4, A, A, ncols=8)
+    assert path == path2 == lib.PATH_STREAM and info == info2
 
 
 def test_plan_k_chunks_for_batches_and_long_rows(lib):

@@ -234,6 +234,33 @@ def test_fused_fwht_prologue(G, ncols):
     assert_within(got, want, gemv_bound(raw, synth.F16, Xp, M, K, x_err=E), "fwht+gemv ncols %d" % ncols)
 
 
+@pytest.mark.parametrize("ncols", [1, 3, 8])
+def test_fwht_workspace_path_matches_on_chip_prologue(G, ncols):
+    """The transform-once path (stand-alone signed FWHT into a workspace, then the GEMV,
+    chained with programmatic dependent launch) gives the same x' and therefore the same
+    outputs as the on-chip prologue, bit for bit, and passes the oracle bound."""
+    M, K, B = 700, 5120, 1024
+    raw = synth.weights(synth.F16, M, K, seed=90)
+    X = synth.normal(ncols * K, seed=91).reshape(ncols, K)
+    s = synth.rademacher(B, seed=92)
+    r = synth.normal(ncols * M, seed=93).reshape(ncols, M)
+    Wd, xd, sd = dev_tensor(raw), dev_tensor(X.reshape(-1)), dev_tensor(s)
+    ws = torch.full((ncols * K,), float("nan"), device="cuda")
+    d_chip = dev_tensor(r.reshape(-1))
+    d_ws = dev_tensor(r.reshape(-1))
+    G.gemv_fused_ex(Wd, synth.F16, xd, M, K, ogemv.EPI_ADD, d_chip, d_chip, ncols=ncols, fwht_signs=sd, fwht_block=B)
+    G.gemv_fused_ex(Wd, synth.F16, xd, M, K, ogemv.EPI_ADD, d_ws, d_ws, ncols=ncols, fwht_signs=sd, fwht_block=B,
+                    fwht_workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(d_chip.view(torch.int32), d_ws.view(torch.int32))
+    Xp = np.stack([ofwht.fwht_signed(X[c], s, B) for c in range(ncols)])
+    E = np.stack([fwht_err_bound(X[c], B) for c in range(ncols)])
+    assert_within(ws.cpu().numpy().reshape(ncols, K), Xp, E, "workspace x'")
+    want = ogemv.gemv(raw, synth.F16, Xp, M, K, ogemv.EPI_ADD, r)
+    got = d_ws.cpu().numpy().astype(np.float64).reshape(ncols, M)
+    assert_within(got, want, gemv_bound(raw, synth.F16, Xp, M, K, x_err=E), "workspace path ncols %d" % ncols)
+
+
 @pytest.mark.parametrize("wt,block,nsigns", [(synth.Q4_0, 256, 256), (synth.F32, 64, 32), (synth.F16, 8192, 8192),
                                              (synth.Q8_0, 1, 1)])
 def test_fused_fwht_other_blocks(G, wt, block, nsigns):
