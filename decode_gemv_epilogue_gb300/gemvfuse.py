@@ -43,6 +43,9 @@ _gemv_fused = _sig("gemv_fused", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, _v
 _gemv_fused_ex = _sig("gemv_fused_ex", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp,
                                         ctypes.POINTER(GfOpts), _vp])
 _fwht_signed = _sig("fwht_signed", [_vp, _vp, _vp, _i64, _i64, _i64, _vp])
+_gemv_fused_fwht_noalloc = _sig("gemv_fused_fwht_noalloc", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, _i64,
+                                                             _vp, _i64, _i64, _u32, _vp])
+NOALLOC_MAX_WORKSPACE_FLOATS = 262144
 _elementwise = _sig("gf_elementwise", [_i32, _vp, _vp, _i64, _vp, _i64, _vp])
 _dequantize = _sig("gf_dequantize", [_vp, _i32, _i64, _i64, _vp, _vp])
 _plan = _sig("gf_plan", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, ctypes.POINTER(GfOpts),
@@ -126,6 +129,19 @@ def gemv_fused_ex(W, wtype, x, M, K, epilogue, aux, dst, ncols=1, fwht_signs=Non
                         ctypes.byref(o), _stream(stream))
     if check:
         _check(st, "gemv_fused_ex")
+    return st
+
+
+def gemv_fused_fwht_noalloc(W, wtype, x, M, K, epilogue, aux, dst, ncols, fwht_signs, fwht_block, nsigns=None,
+                            pdl=False, stream=None, check=True):
+    """gemv_fused_ex with the signed-FWHT prologue, its workspace taken from the library's
+    static device array (for callers that cannot allocate one); see include/gemvfuse.h."""
+    if nsigns is None:
+        nsigns = fwht_block if isinstance(fwht_signs, int) else fwht_signs.numel()
+    st = _gemv_fused_fwht_noalloc(_ptr(W), wtype, _ptr(x), M, K, epilogue, _ptr(aux), _ptr(dst), ncols,
+                                  _ptr(fwht_signs), fwht_block, nsigns, FLAG_PDL if pdl else 0, _stream(stream))
+    if check:
+        _check(st, "gemv_fused_fwht_noalloc")
     return st
 
 

@@ -122,6 +122,28 @@ GF_API int gemv_fused_ex(const void* W, int wtype, const float* x, int64_t M, in
                   int epilogue, const float* aux, float* dst, const gf_opts* opts,
                   void* stream);
 
+/* Allocation-free variant of gemv_fused_ex with the signed-FWHT prologue.  The pages
+ * have no counterpart: this entry point exists for callers that cannot allocate a
+ * device workspace -- a C host that links only this library and has no device
+ * allocator of its own, or a serving process whose device memory is fixed at start-up
+ * and may not grow while requests run.  It computes exactly what gemv_fused_ex computes
+ * with opts = {ncols, fwht_signs, fwht_block, nsigns, flags} and a workspace, but the
+ * workspace (the transformed x', ncols*K floats) is a static device array inside the
+ * library; nothing is allocated or freed.
+ *  - Limit: ncols*K <= GF_NOALLOC_MAX_WORKSPACE_FLOATS, else GF_ERR_UNSUPPORTED with
+ *    nothing launched.  fwht_signs must be non-NULL (GF_ERR_INVALID otherwise).
+ *  - The array (1 MiB) is held on every GPU that loads the library until the process
+ *    exits.  The first call on a device looks up its address (cudaGetSymbolAddress,
+ *    with that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and overwrites it before reading it;
+ *    calls whose work overlaps on the GPU (e.g. on different streams without ordering)
+ *    race on it and give undefined results: order them, e.g. on one stream. */
+#define GF_NOALLOC_MAX_WORKSPACE_FLOATS 262144
+GF_API int gemv_fused_fwht_noalloc(const void* W, int wtype, const float* x, int64_t M, int64_t K,
+                                   int epilogue, const float* aux, float* dst, int64_t ncols,
+                                   const float* fwht_signs, int64_t fwht_block, int64_t nsigns,
+                                   uint32_t flags, void* stream);
+
 /* Signed FWHT, stand-alone ([FWHT] Overview): for every block of `block` consecutive
  * elements of x[0..n), dst_b = H_block (x_b * s) / sqrt(block), with element i using
  * signs[i % nsigns]; signs == NULL means all +1 (the plain normalised transform).
