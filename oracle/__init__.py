@@ -29,7 +29,7 @@ Parity status of every function is listed in ``PINS`` below; each one is pinned 
 ``tests/golden/``, library special cases or brute force, never to itself.
 """
 
-from . import quant, gemv, fwht, chain  # noqa: F401
+from . import quant, gemv, fwht, chain, norm  # noqa: F401
 
 PINS = {
     "quant.dequantize_f32": "pinned: bit pattern fixture, identity",
@@ -41,4 +41,7 @@ PINS = {
     "fwht.hadamard": "pinned: H2, Sylvester recursion via np.kron, scipy.linalg.hadamard, H.H=nI",
     "fwht.fwht_signed": "pinned: butterfly vs dense, e0 -> 1/sqrt(B), ones -> sqrt(B) e0, Parseval, involution",
     "chain.decode_layer": "pinned: composition on identity-like tiny weights (closed form)",
+    "gemv.gemv_glu": "pinned: hand-worked 3x2 example (golden/glu_worked.txt), zero gate/up, one-hot x",
+    "norm.rms_norm": "pinned: hand-worked example (golden/rms_norm_worked.txt), unit mean square, "
+                     "scale invariance, constant input, eps-dominated limit",
 }

@@ -76,6 +76,19 @@ def gemv(raw, wtype, x, M, K, epilogue=EPI_NONE, aux=None, rows=None):
     return apply_epilogue(y, epilogue, a)
 
 
+def gemv_glu(raw_gate, raw_up, wtype, x, M, K, rows=None):
+    """The gated dual GEMV: out[c, i] = silu(g[c, i]) * u[c, i] with g = Wg x and
+    u = Wu x, both weights in the same format and shape.  This is the SwiGLU gate and
+    the gate x up product of one FFN ("ggml-cpu: fuse element-wise epilogues (ADD, MUL,
+    SILU) into ggml_compute_forward_mul_mat", What) taken as one operation -- the
+    gated branch that "feat(cuda): fuse activations and residual add into mmv f/q
+    epilogues", Summary, leaves to its existing GLU path.  Returns float64
+    [ncols, len(rows)]."""
+    g = gemv(raw_gate, wtype, x, M, K, EPI_NONE, rows=rows)
+    u = gemv(raw_up, wtype, x, M, K, EPI_NONE, rows=rows)
+    return silu(g) * u
+
+
 def abs_dot(raw, wtype, x, M, K, rows=None):
     """sum_k |W[i,k] * x[c,k]| in fp64: the scale of the parity tolerance."""
     W = quant.dequantize(raw, wtype, M, K, rows)
