@@ -3,13 +3,15 @@
 //
 // Aliasing contract ("feat(cuda): fuse activations and residual add into mmv f/q
 // epilogues", What changed): dst may alias the mul/add operand only as the same
-// element index (dst == aux, in place), and may not overlap the product inputs W and x,
-// which are read across the whole reduction.  Every call is validated on its own; no
+// element index (dst == aux, in place), and may not overlap the product inputs (W, the
+// up matrix of the gated dual GEMV, x, the FWHT signs, the normalisation weight), which
+// are read across the whole reduction.  Every call is validated on its own; no
 // overlap-guard state is kept between calls.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <limits>
 #include <mutex>
 
 #include "gemvfuse.h"
@@ -100,11 +102,18 @@ struct Call {
   int64_t fwht_block, nsigns;
   uint32_t flags;
   float* workspace;
+  const void* W2;       // gated dual GEMV: the up matrix (epi == EPI_GLU)
+  const float* gamma;   // RMS-normalisation prologue weight [K]
+  float eps;
 };
 
 static int validate(const Call& c) {
   if (c.wtype < GF_F32 || c.wtype > GF_Q4_0) return GF_ERR_INVALID;
-  if (c.epi < GF_EPI_NONE || c.epi > GF_EPI_ADD) return GF_ERR_INVALID;
+  if (c.epi == EPI_GLU) {
+    if (!c.W2 && c.M > 0 && c.K > 0) return GF_ERR_INVALID;
+  } else if (c.epi < GF_EPI_NONE || c.epi > GF_EPI_ADD || c.W2) {
+    return GF_ERR_INVALID;
+  }
   if (c.M < 0 || c.K < 0) return GF_ERR_INVALID;
   if (c.M > INT32_MAX || c.K > INT32_MAX / 8) return GF_ERR_UNSUPPORTED;
   if (c.ncols < 1 || c.ncols > kMaxCols) return c.ncols < 1 ? GF_ERR_INVALID : GF_ERR_UNSUPPORTED;
@@ -117,6 +126,12 @@ static int validate(const Call& c) {
   }
   const uintptr_t walign = c.wtype == GF_F32 ? 4 : 2;
   if (c.W && !aligned(c.W, walign)) return GF_ERR_ALIGN;
+  if (c.W2 && !aligned(c.W2, walign)) return GF_ERR_ALIGN;
+  if (c.gamma) {
+    if (!(c.eps >= 0.0f) || !(c.eps <= std::numeric_limits<float>::max())) return GF_ERR_INVALID;
+    if (!aligned(c.gamma, 4)) return GF_ERR_ALIGN;
+    if (c.signs) return GF_ERR_UNSUPPORTED;  // one prologue per call
+  }
   if ((c.x && !aligned(c.x, 4)) || (c.dst && !aligned(c.dst, 4)) || (need_aux && c.aux && !aligned(c.aux, 4)))
     return GF_ERR_ALIGN;
   if (c.signs) {
@@ -131,12 +146,15 @@ static int validate(const Call& c) {
   const int64_t wbytes = c.M * row_bytes_of(c.wtype, c.K);
   const int64_t xbytes = c.ncols * c.K * 4;
   if (ranges_overlap(c.dst, dbytes, c.W, wbytes)) return GF_ERR_ALIAS;
+  if (ranges_overlap(c.dst, dbytes, c.W2, wbytes)) return GF_ERR_ALIAS;
+  if (c.gamma && ranges_overlap(c.dst, dbytes, c.gamma, c.K * 4)) return GF_ERR_ALIAS;
   if (ranges_overlap(c.dst, dbytes, c.x, xbytes)) return GF_ERR_ALIAS;
   if (c.signs && ranges_overlap(c.dst, dbytes, c.signs, c.nsigns * 4)) return GF_ERR_ALIAS;
   if (need_aux && c.aux != c.dst && ranges_overlap(c.dst, dbytes, c.aux, dbytes)) return GF_ERR_ALIAS;
   if (c.workspace && c.signs && c.M > 0 && c.K > 0) {
     if (!aligned(c.workspace, 16)) return GF_ERR_ALIGN;
     if (ranges_overlap(c.workspace, xbytes, c.W, wbytes) || ranges_overlap(c.workspace, xbytes, c.x, xbytes) ||
+        ranges_overlap(c.workspace, xbytes, c.W2, wbytes) ||
         ranges_overlap(c.workspace, xbytes, c.dst, dbytes) || ranges_overlap(c.workspace, xbytes, c.signs, c.nsigns * 4) ||
         (need_aux && ranges_overlap(c.workspace, xbytes, c.aux, dbytes)))
       return GF_ERR_ALIAS;
@@ -146,20 +164,26 @@ static int validate(const Call& c) {
 
 static int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Plan the TMA-streamed kernel; returns false if the shape/alignment needs the generic one.
-static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
+// Plan the TMA-streamed kernel with S CTAs per cluster splitting K (S = 1: no split);
+// returns false if the shape/alignment needs another S or the generic kernel.
+static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p) {
   const int nc = static_cast<int>(c.ncols);
   const int K = static_cast<int>(c.K);
   const int64_t rb = row_bytes_of(c.wtype, c.K);
+  const bool dual = c.W2 != nullptr;
+  const int vr = dual ? 2 : 1;  // virtual rows per output row
   if (c.K < kUnitElems || K % kUnitElems != 0) return false;
   if (rb % 16 != 0 || !aligned(c.W, 16) || !aligned(c.x, 16)) return false;
+  if (dual && !aligned(c.W2, 16)) return false;
+  if (c.gamma && !aligned(c.gamma, 16)) return false;
   if (rb > INT32_MAX / 2) return false;
   const int U = stream_u(c.wtype, nc), RT = stream_rt(c.wtype, nc);
   const int CS = stream_cs(c.wtype, nc);
   const int max_cw = stream_max_cw(c.wtype, nc);
   auto seg_of = [&](int klen) -> int { return static_cast<int>(row_bytes_of(c.wtype, klen)); };
   // K chunk: the whole row if x, one row's bytes and the units all fit; else a multiple
-  // of the granule (256 elements, or the FWHT block) that does.
+  // of the granule (256 elements, or the FWHT block) that does.  Split K caps the chunk
+  // so that every CTA of a cluster gets at least one.
   int gran = 256;
   if (c.signs) gran = std::max<int>(gran, static_cast<int>(c.fwht_block));
   const int64_t cap_x = c.signs ? kXsMaxBytes / (4 * nc) : INT32_MAX;  // x staged only for the prologue
@@ -174,7 +198,12 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
     if (gch < 1) return false;
     kc = gch * gran;
   }
+  if (S > 1) {
+    if (K % gran != 0) return false;
+    kc = std::min(kc, std::max(gran, (K / S) / gran * gran));
+  }
   const int n_kc = (K + kc - 1) / kc;
+  if (n_kc < S) return false;
   const int seg_full = seg_of(kc);
   if (seg_full % 16 != 0) return false;
   if (n_kc > 1) {
@@ -185,25 +214,29 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
   const int wpc = (((units + U - 1) / U) + 31) / 32;
   const int wpg = CS * wpc;
   if (wpg > max_cw) return false;
-  const int grid = static_cast<int>(std::min<int64_t>(lim.sm_count, c.M));
-  const int rows_base = static_cast<int>(c.M / grid);
-  const int rows_extra = static_cast<int>(c.M % grid);
+  const int nclusters = static_cast<int>(std::min<int64_t>(lim.sm_count / S, c.M));
+  if (nclusters < 1) return false;
+  const int rows_base = static_cast<int>(c.M / nclusters);
+  const int rows_extra = static_cast<int>(c.M % nclusters);
   const int rows_max = rows_base + (rows_extra ? 1 : 0);
-  int G = std::max(1, std::min(max_cw / wpg, (rows_max + RT - 1) / RT));
+  int G = std::max(1, std::min(max_cw / wpg, (vr * rows_max + RT - 1) / RT));
   while (G > 1 && G * RT * seg_full > kStageMaxBytes) --G;
   const int ncw = G * wpg;
   int R = G * RT;
-  int RC = std::min(rows_max, std::max(R, kRedMaxBytes / (wpc * nc * 4)));
+  int RC = std::min(rows_max, std::max(R, kRedMaxBytes / (vr * wpc * nc * 4)));
   RC = std::min(RC, 512);
+  if (S > 1 && RC < rows_max) return false;  // split K exchanges one row chunk per CTA
   const int xs_bytes = c.signs ? round_up(nc * kc * 4, 128) : 0;
   const int aux_bytes = round_up(nc * RC * 4, 128);
-  const int red_bytes = round_up(RC * wpc * nc * 4, 128);
-  const int fixed = kBarBytes + xs_bytes + aux_bytes + red_bytes + kRingSlackBytes;
+  const int red_bytes = round_up(vr * RC * wpc * nc * 4, 128);
+  const int norm_bytes = c.gamma ? round_up((ncw + 1) * nc * 4, 128) : 0;
+  const int xchg_bytes = S > 1 ? round_up(S * nc * vr * RC * 4, 128) : 0;
+  const int fixed = kBarBytes + xs_bytes + aux_bytes + red_bytes + norm_bytes + xchg_bytes + kRingSlackBytes;
   const int stage_bytes = round_up(R * seg_full, 128);
   const int NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
   if (NS < 2) return false;
   p.path = PATH_STREAM;
-  p.grid = grid;
+  p.grid = nclusters * S;
   p.threads = 32 * (1 + ncw);
   p.smem = fixed + NS * stage_bytes;
   StreamArgs& s = p.s;
@@ -227,17 +260,35 @@ static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
   s.fwht_B = c.signs ? static_cast<int>(c.fwht_block) : 0;
   s.nsigns = c.signs ? static_cast<int>(c.nsigns) : 1;
   s.fwht_scale = c.signs ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.fwht_block))) : 1.0f;
+  s.norm_eps = c.gamma ? c.eps : 0.0f;
+  s.S = S;
   s.off_xs = kBarBytes;
   s.off_aux = s.off_xs + xs_bytes;
   s.off_red = s.off_aux + aux_bytes;
-  s.off_ring = s.off_red + red_bytes;
+  s.off_norm = s.off_red + red_bytes;
+  s.off_xchg = s.off_norm + norm_bytes;
+  s.off_ring = s.off_xchg + xchg_bytes;
   return true;
+}
+
+// Split K when the rows alone would leave most SMs idle: S = min(8, SMs / M) CTAs per
+// cluster (at least two), each streaming a slice of every row's K chunks.
+static int split_factor(const Call& c, const DeviceLimits& lim) {
+  if (c.flags & GF_FLAG_NO_SPLIT_K) return 1;
+  if (c.M < 1 || 2 * c.M > lim.sm_count) return 1;
+  return static_cast<int>(std::min<int64_t>(kMaxSplit, lim.sm_count / c.M));
+}
+
+static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
+  for (int S = split_factor(c, lim); S > 1; --S)
+    if (plan_stream_s(c, lim, S, p)) return true;
+  return plan_stream_s(c, lim, 1, p);
 }
 
 static int plan_call(const Call& c, Plan& p, int* generic_smem, int* generic_grid) {
   const DeviceLimits lim = device_limits();
   if (plan_stream(c, lim, p)) return PATH_STREAM;
-  const int64_t smem = c.ncols * c.K * 4;
+  const int64_t smem = generic_smem_floats(c.ncols, c.K) * 4;
   if (smem > lim.smem_optin) return GF_ERR_UNSUPPORTED;
   *generic_smem = static_cast<int>(smem);
   const int64_t rows_per_cta = 8;  // one row per warp of the 256-thread generic CTA
@@ -265,6 +316,8 @@ static int launch_call(const Call& c, float* dst, cudaStream_t st) {
     s.dst = dst;
     s.signs = c.signs;
     s.err = err;
+    s.W2 = static_cast<const uint8_t*>(c.W2);
+    s.gamma = c.gamma;
     e = (c.wtype == GF_F32 || c.wtype == GF_F16) ? launch_stream_float(c.wtype, static_cast<int>(c.ncols), p, st, pdl)
                                                : launch_stream_block(c.wtype, static_cast<int>(c.ncols), p, st, pdl);
   } else {
@@ -282,6 +335,9 @@ static int launch_call(const Call& c, float* dst, cudaStream_t st) {
     g.fwht_B = c.signs ? static_cast<int>(c.fwht_block) : 0;
     g.nsigns = c.signs ? static_cast<int>(c.nsigns) : 1;
     g.fwht_scale = c.signs ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.fwht_block))) : 1.0f;
+    g.W2 = static_cast<const uint8_t*>(c.W2);
+    g.gamma = c.gamma;
+    g.norm_eps = c.gamma ? c.eps : 0.0f;
     e = launch_generic(c.wtype, static_cast<int>(c.ncols), g, ggrid, gsmem, st, pdl);
   }
   if (e != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(e));
@@ -323,6 +379,9 @@ static Call make_call(const void* W, int wtype, const float* x, int64_t M, int64
   c.nsigns = 0;
   c.flags = 0;
   c.workspace = nullptr;
+  c.W2 = nullptr;
+  c.gamma = nullptr;
+  c.eps = 0.0f;
   if (opts) {
     c.ncols = opts->ncols == 0 ? 1 : opts->ncols;
     c.signs = opts->fwht_signs;
@@ -330,6 +389,8 @@ static Call make_call(const void* W, int wtype, const float* x, int64_t M, int64
     c.nsigns = opts->nsigns;
     c.flags = opts->flags;
     c.workspace = opts->fwht_signs ? opts->fwht_workspace : nullptr;
+    c.gamma = opts->rms_norm_weight;
+    c.eps = opts->rms_norm_eps;
   }
   return c;
 }
@@ -374,14 +435,32 @@ int gemv_fused(const void* W, int wtype, const float* x, int64_t M, int64_t K, i
   return gemv_fused_ex(W, wtype, x, M, K, epilogue, aux, dst, nullptr, stream);
 }
 
-int gf_plan(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue, const float* aux,
-            const float* dst, const gf_opts* opts, int64_t info[8]) {
-  const Call c = make_call(W, wtype, x, M, K, epilogue, aux, dst, opts);
+static Call make_glu_call(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M, int64_t K,
+                          const float* dst, const gf_opts* opts) {
+  Call c = make_call(W_gate, wtype, x, M, K, GF_EPI_NONE, nullptr, dst, opts);
+  c.epi = EPI_GLU;
+  c.W2 = W_up;
+  return c;
+}
+
+int gemv_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M, int64_t K, float* dst,
+             const gf_opts* opts, void* stream) {
+  const Call c = make_glu_call(W_gate, W_up, wtype, x, M, K, dst, opts);
   int v = validate(c);
   if (v != GF_OK) return v;
   v = check_view(opts, M);
   if (v != GF_OK) return v;
-  if (M == 0) return 0;  // nothing would be launched
+  if (M == 0) return GF_OK;
+  if (c.workspace && c.K > 0) return launch_via_workspace(c, dst, static_cast<cudaStream_t>(stream));
+  return launch_call(c, dst, static_cast<cudaStream_t>(stream));
+}
+
+static int plan_info(const Call& c, const gf_opts* opts, int64_t info[8]) {
+  int v = validate(c);
+  if (v != GF_OK) return v;
+  v = check_view(opts, c.M);
+  if (v != GF_OK) return v;
+  if (c.M == 0) return 0;  // nothing would be launched
   Call pc = c;
   if (pc.workspace) {  // the GEMV of the workspace path reads x' without a prologue
     pc.x = pc.workspace;
@@ -395,12 +474,22 @@ int gf_plan(const void* W, int wtype, const float* x, int64_t M, int64_t K, int 
     for (int i = 0; i < 8; ++i) info[i] = 0;
     if (path == PATH_STREAM) {
       info[0] = p.grid; info[1] = p.threads; info[2] = p.s.R; info[3] = p.s.NS;
-      info[4] = p.s.kc_len; info[5] = p.smem; info[6] = p.s.RC;
+      info[4] = p.s.kc_len; info[5] = p.smem; info[6] = p.s.RC; info[7] = p.s.S;
     } else {
-      info[0] = ggrid; info[1] = 256; info[5] = gsmem;
+      info[0] = ggrid; info[1] = 256; info[5] = gsmem; info[7] = 1;
     }
   }
   return path;
+}
+
+int gf_plan(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue, const float* aux,
+            const float* dst, const gf_opts* opts, int64_t info[8]) {
+  return plan_info(make_call(W, wtype, x, M, K, epilogue, aux, dst, opts), opts, info);
+}
+
+int gf_plan_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M, int64_t K,
+                const float* dst, const gf_opts* opts, int64_t info[8]) {
+  return plan_info(make_glu_call(W_gate, W_up, wtype, x, M, K, dst, opts), opts, info);
 }
 
 int fwht_signed(const float* x, const float* signs, float* dst, int64_t n, int64_t block, int64_t nsigns,
@@ -484,6 +573,6 @@ const char* gf_status_string(int status) {
 
 int gf_last_cuda_error(void) { return t_last_cuda_error; }
 
-int gf_version(void) { return 1; }
+int gf_version(void) { return 2; }
 
 }  // extern "C"

@@ -3,7 +3,7 @@
 // One CTA per SM owns a contiguous range of rows.  Warp 0 is the producer: one lane
 // streams the CTA's weight bytes, tile by tile (R rows x one K chunk), into a ring of
 // shared-memory stages with 1-D bulk async copies (no multicast), signalling a "full"
-// mbarrier per stage.  Warps 1..ncw are consumers: each thread owns fixed 8-weight
+// mbarrier per stage.  Warps 1..ncw are consumers: each thread owns fixed 16-weight
 // units of the K chunk, keeps the matching x values in registers while it walks the
 // R rows of a stage, decodes the weights (F32/F16/Q8_0/Q4_0) and accumulates with
 // packed f32x2 FMAs.  Per tile, each warp reduces its per-row partial sums with
@@ -11,10 +11,22 @@
 // the consumer warps are added in a fixed order (deterministic), the fused tail is
 // applied with the prefetched aux operand, and dst is written once.
 //
-// x (all columns of one K chunk) is staged in shared memory with a bulk copy; with a
-// signed-FWHT prologue the consumers transform it in place before use, so x' never
-// leaves the chip.  Every wait is bounded; a timeout sets the device error word and
-// the kernel returns after draining its own copies.
+// Prologues: with the signed FWHT, x (all columns of one K chunk) is staged in shared
+// memory with a bulk copy and transformed in place, so x' never leaves the chip.  With
+// RMS normalisation, gamma multiplies x as it is loaded into registers and the
+// per-column 1/rms (a fixed-order sum of squares, computed while the first weight
+// tiles stream in) scales the finished dot product before the tail.
+//
+// Gated dual GEMV: every tile holds h rows of the gate matrix followed by the same h
+// rows of the up matrix ("virtual rows"), and the tail is silu(gate) * up.
+//
+// Split K: with S > 1 the grid is made of clusters of S CTAs; the CTAs of a cluster
+// share one row range and each takes a slice of its K chunks.  The per-row partial
+// sums of ranks 1..S-1 are stored into rank 0's shared memory (distributed shared
+// memory), rank 0 adds the S slices in rank order (deterministic) and applies the tail.
+//
+// Every wait is bounded; a timeout sets the device error word and the kernel returns
+// after draining its own copies.
 #pragma once
 
 #include "gf_device.cuh"
@@ -32,18 +44,23 @@ __host__ __device__ constexpr int seg_bytes_of(int klen) {
 // xs is either the K chunk staged in shared memory (column stride xstride) or x itself
 // in global memory (column stride K, offset to the chunk); both are read with 16-byte
 // loads.
+// With gsrc (the RMS-normalisation weight at the chunk's offset) each x value is
+// multiplied by its gamma as it is loaded.
 template <int WT, int NCT>
-__device__ __forceinline__ void load_unit_x(const float* xs, int64_t xstride, int u, uint32_t qr, int c0, int nc,
-                                            float2 (&xv)[NCT][8]) {
+__device__ __forceinline__ void load_unit_x(const float* xs, int64_t xstride, const float* gsrc, int u, uint32_t qr,
+                                            int c0, int nc, float2 (&xv)[NCT][8]) {
 #pragma unroll
-  for (int c = 0; c < NCT; ++c) {
-    const bool live = (c0 + c) < nc;
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t e = unit_pair_elem<WT>(static_cast<uint32_t>(u), 2 * static_cast<int>((q + qr) & 3u));
+    float4 gm = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+    if (gsrc) gm = *reinterpret_cast<const float4*>(gsrc + e);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int c = 0; c < NCT; ++c) {
       float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (live)
-        t = *reinterpret_cast<const float4*>(
-            xs + (c0 + c) * xstride + unit_pair_elem<WT>(static_cast<uint32_t>(u), 2 * static_cast<int>((q + qr) & 3u)));
+      if ((c0 + c) < nc) t = *reinterpret_cast<const float4*>(xs + (c0 + c) * xstride + e);
+      if (gsrc) {
+        t.x *= gm.x; t.y *= gm.y; t.z *= gm.z; t.w *= gm.w;
+      }
       xv[c][2 * q] = make_float2(t.x, t.y);
       xv[c][2 * q + 1] = make_float2(t.z, t.w);
     }
@@ -109,15 +126,23 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t full0 = sbase, empty0 = sbase + 8u * a.NS, xbar = sbase + 16u * a.NS;
+  const uint32_t xchbar = xbar + 8u;  // split K: arrivals of the peer CTAs (rank 0 only)
   float* xs = reinterpret_cast<float*>(smem + a.off_xs);
   float* auxs = reinterpret_cast<float*>(smem + a.off_aux);
   float* red = reinterpret_cast<float*>(smem + a.off_red);
+  float* normv = reinterpret_cast<float*>(smem + a.off_norm);  // [ncw][NC] partials, then [NC]
+  float* xch = reinterpret_cast<float*>(smem + a.off_xchg);    // split K: [S][NC][XR]
   const uint32_t ring = sbase + static_cast<uint32_t>(a.off_ring);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarBytes - 8);
 
-  const int cta = blockIdx.x;
-  const int64_t r0 = static_cast<int64_t>(cta) * a.rows_base + min(cta, a.rows_extra);
-  const int nrows = a.rows_base + (cta < a.rows_extra ? 1 : 0);
+  const int S = a.S;
+  const int crank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int rg = static_cast<int>(blockIdx.x) / S;  // row range of this CTA (its cluster's)
+  const int64_t r0 = static_cast<int64_t>(rg) * a.rows_base + min(rg, a.rows_extra);
+  const int nrows = a.rows_base + (rg < a.rows_extra ? 1 : 0);
+  const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
+  const bool dual = a.W2 != nullptr;
+  const int XR = dual ? 2 * a.RC : a.RC;  // virtual rows per row chunk
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -126,9 +151,13 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
       mbar_init(empty0 + 8u * i, static_cast<uint32_t>(a.ncw));
     }
     mbar_init(xbar, 1);
+    mbar_init(xchbar, static_cast<uint32_t>(S > 1 ? (S - 1) * a.ncw * 32 : 1));
     fence_mbar_init();
   }
-  __syncthreads();
+  if (S > 1)
+    cluster_sync_all();  // peers arrive on rank 0's barrier only after it is initialised
+  else
+    __syncthreads();
   pdl_trigger();
 
   if (warp == 0) {
@@ -139,12 +168,14 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
       bool ok = true;
       for (int rc0 = 0; rc0 < nrows && ok; rc0 += a.RC) {
         const int nrc = min(a.RC, nrows - rc0);
-        for (int kc = 0; kc < a.n_kc && ok; ++kc) {
+        const int nvr = dual ? 2 * nrc : nrc;
+        for (int kc = kc_lo; kc < kc_hi && ok; ++kc) {
           const int klen = min(a.kc_len, a.K - kc * a.kc_len);
           const int seg = seg_bytes_of<WT>(klen);
           const int64_t segoff = seg_bytes_of<WT>(kc * a.kc_len);
-          for (int t0 = 0; t0 < nrc; t0 += a.R) {
-            const int rows = min(a.R, nrc - t0);
+          for (int t0 = 0; t0 < nvr; t0 += a.R) {
+            const int rows = min(a.R, nvr - t0);
+            const int h = dual ? rows / 2 : rows;  // rows taken from each matrix
             const int slot = it % a.NS, round = it / a.NS;
             if (!mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1),
                                     abort_flag, a.err)) {
@@ -153,14 +184,19 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
             }
             const uint32_t full = full0 + 8u * slot;
             const uint32_t dst = ring + static_cast<uint32_t>(slot) * a.stage_bytes;
-            const int64_t row = r0 + rc0 + t0;
+            const int64_t row = r0 + rc0 + (dual ? t0 / 2 : t0);
             mbar_arrive_expect_tx(full, static_cast<uint32_t>(rows * seg));
             if (a.n_kc == 1) {
-              bulk_g2s(dst, a.W + row * a.row_bytes, static_cast<uint32_t>(rows * seg), full, pol);
+              bulk_g2s(dst, a.W + row * a.row_bytes, static_cast<uint32_t>(h * seg), full, pol);
+              if (dual)
+                bulk_g2s(dst + static_cast<uint32_t>(h * seg), a.W2 + row * a.row_bytes,
+                         static_cast<uint32_t>(h * seg), full, pol);
             } else {
-              for (int r = 0; r < rows; ++r)
-                bulk_g2s(dst + static_cast<uint32_t>(r * seg), a.W + (row + r) * a.row_bytes + segoff,
-                         static_cast<uint32_t>(seg), full, pol);
+              for (int r = 0; r < rows; ++r) {
+                const bool up = r >= h;
+                const uint8_t* src = (up ? a.W2 : a.W) + (row + (up ? r - h : r)) * a.row_bytes + segoff;
+                bulk_g2s(dst + static_cast<uint32_t>(r * seg), src, static_cast<uint32_t>(seg), full, pol);
+              }
             }
             ++it;
           }
@@ -185,15 +221,48 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
     const int tg = wc * 32 + lane, tg_n = a.wpc * 32;
     const uint32_t qr = lane_quad_rot<WT>(lane);
     const bool need_aux = (a.epi == EPI_SILU_MUL || a.epi == EPI_ADD);
+    const bool finalizer = (crank == 0);
     pdl_wait();  // x, aux and dst may belong to the preceding grid
     int it = 0;
     uint32_t xphase = 0;
     bool ok = true;
     bool x_loaded = false;
     auto cbar = [&]() { named_bar_sync(1, static_cast<uint32_t>(nt)); };
+    if (a.gamma && finalizer) {
+      // RMS statistics of every column over the whole K: per-thread sums in a fixed
+      // order, a shuffle butterfly, then the warps' partials in warp order.
+      const int K4 = a.K >> 2;
+      float ss[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) ss[c] = 0.0f;
+      for (int i = ctid; i < K4; i += nt) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const float4 v = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(c) * a.K)[i];
+          ss[c] = fmaf(v.x, v.x, ss[c]);
+          ss[c] = fmaf(v.y, v.y, ss[c]);
+          ss[c] = fmaf(v.z, v.z, ss[c]);
+          ss[c] = fmaf(v.w, v.w, ss[c]);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) ss[c] += __shfl_xor_sync(0xffffffffu, ss[c], off);
+        if (lane == 0) normv[cw * NC + c] = ss[c];
+      }
+      cbar();
+      if (ctid < NC) {
+        float t = 0.0f;
+        for (int w = 0; w < a.ncw; ++w) t += normv[w * NC + ctid];
+        normv[a.ncw * NC + ctid] = 1.0f / sqrtf(t / static_cast<float>(a.K) + a.norm_eps);
+      }
+      // published to the other consumers by the barriers before the finalize below
+    }
     for (int rc0 = 0; rc0 < nrows; rc0 += a.RC) {
       const int nrc = min(a.RC, nrows - rc0);
-      for (int kc = 0; kc < a.n_kc; ++kc) {
+      const int nvr = dual ? 2 * nrc : nrc;
+      for (int kc = kc_lo; kc < kc_hi; ++kc) {
         const int klen = min(a.kc_len, a.K - kc * a.kc_len);
         if (a.fwht_B > 0 && (a.n_kc > 1 || !x_loaded)) {
           // prologue: stage the chunk of every column in shared memory, transform it there
@@ -227,14 +296,15 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         // the transformed chunk in shared memory, or straight from global memory
         const float* xsrc = a.fwht_B > 0 ? xs : a.x + static_cast<int64_t>(kc) * a.kc_len;
         const int64_t xstride = a.fwht_B > 0 ? klen : a.K;
+        const float* gsrc = a.gamma ? a.gamma + static_cast<int64_t>(kc) * a.kc_len : nullptr;
         float2 xr[U][NCT][8];
 #pragma unroll
         for (int i = 0; i < U; ++i) {
           const int u = tg + i * tg_n;
-          if (u < units && ok) load_unit_x<WT, NCT>(xsrc, xstride, u, qr, c0, NC, xr[i]);
+          if (u < units && ok) load_unit_x<WT, NCT>(xsrc, xstride, gsrc, u, qr, c0, NC, xr[i]);
         }
-        for (int t0 = 0; t0 < nrc; t0 += a.R, ++it) {
-          const int rows = min(a.R, nrc - t0);
+        for (int t0 = 0; t0 < nvr; t0 += a.R, ++it) {
+          const int rows = min(a.R, nvr - t0);
           const int slot = it % a.NS, round = it / a.NS;
           ok = ok && mbar_wait_or_abort(full0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag,
                                         a.err);
@@ -261,25 +331,71 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
             const int r = g + (jv / NCT) * a.G, c = c0 + jv % NCT;
             if (r < rows && c < NC) {
               float* p = red + ((t0 + r) * a.wpc + wc) * NC + c;
-              *p = (kc == 0) ? sum : (*p + sum);
+              *p = (kc == kc_lo) ? sum : (*p + sum);
             }
           }
         }
       }
       cbar();  // all partial sums of this row chunk are in `red`
-      if (ok) {
+      if (S > 1) {
+        // split K (one row chunk per CTA): each rank's per-row sums go to slice `crank`
+        // of rank 0's exchange buffer; rank 0 waits for every peer thread's arrival
+        for (int i = ctid; i < nvr * NC; i += nt) {
+          const int c = i / nvr, v = i - c * nvr;
+          float y = 0.0f;
+          for (int w = 0; w < a.wpc; ++w) y += red[(v * a.wpc + w) * NC + c];
+          float* slot = xch + (crank * NC + c) * XR + v;
+          if (finalizer)
+            *slot = y;
+          else
+            st_cluster_f32(map_to_rank(smem_u32(slot), 0), y);
+        }
+        if (!finalizer)
+          mbar_arrive_remote(map_to_rank(xchbar, 0));
+        else
+          ok = ok && mbar_wait_cluster_or_abort(xchbar, 0, abort_flag, a.err);
+        cbar();  // rank 0: its own slice is complete too
+      }
+      if (ok && finalizer) {
+        // sum of virtual row v for column c: the consumer warps' partials (one CTA),
+        // or the S slices in rank order (split K)
+        auto vsum = [&](int v, int c) -> float {
+          float y = 0.0f;
+          if (S == 1) {
+            for (int w = 0; w < a.wpc; ++w) y += red[(v * a.wpc + w) * NC + c];
+          } else {
+            for (int sl = 0; sl < S; ++sl) y += xch[(sl * NC + c) * XR + v];
+          }
+          return y;
+        };
+        const int H = a.R / 2;
         for (int i = ctid; i < nrc * NC; i += nt) {
           const int c = i / nrc, r = i - c * nrc;
-          float y = 0.0f;
-          for (int w = 0; w < a.wpc; ++w) y += red[(r * a.wpc + w) * NC + c];
-          const float av = need_aux ? auxs[c * a.RC + r] : 0.0f;
-          a.dst[c * a.M + r0 + rc0 + r] = apply_tail(a.epi, y, av);
+          const float inv = a.gamma ? normv[a.ncw * NC + c] : 1.0f;
+          float out;
+          if (dual) {
+            // tile t holds gate rows t*H .. t*H+ht-1 then the same up rows
+            const int t = r / H, l = r - t * H, ht = min(H, nrc - t * H);
+            float yg = vsum(t * a.R + l, c), yu = vsum(t * a.R + ht + l, c);
+            if (a.gamma) {
+              yg *= inv;
+              yu *= inv;
+            }
+            out = tail_silu(yg) * yu;
+          } else {
+            float y = vsum(r, c);
+            if (a.gamma) y *= inv;
+            const float av = need_aux ? auxs[c * a.RC + r] : 0.0f;
+            out = apply_tail(a.epi, y, av);
+          }
+          a.dst[c * a.M + r0 + rc0 + r] = out;
         }
       }
       cbar();  // red / auxs may be reused by the next row chunk
     }
   }
   __syncthreads();
+  if (S > 1) cluster_sync_all();  // no CTA leaves while a peer may still store into it
 }
 
 template <int WT, int NC>
@@ -298,11 +414,22 @@ int launch_stream_t(const Plan& p, cudaStream_t st, bool pdl) {
   cfg.blockDim = dim3(p.threads);
   cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (p.s.S > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(p.s.S);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, p.s);
 }
 

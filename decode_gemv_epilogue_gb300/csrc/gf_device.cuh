@@ -10,6 +10,8 @@ namespace gf {
 
 enum { WT_F32 = 0, WT_F16 = 1, WT_Q8_0 = 2, WT_Q4_0 = 3 };
 enum { EPI_NONE = 0, EPI_SIGMOID = 1, EPI_SILU = 2, EPI_SILU_MUL = 3, EPI_ADD = 4 };
+// Internal tail of the gated dual GEMV: silu(gate row) * (up row).
+enum { EPI_GLU = 5 };
 enum { ERRBIT_TIMEOUT = 1u };
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
@@ -83,6 +85,65 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      if (err) atomicOr(err, static_cast<unsigned>(ERRBIT_TIMEOUT));
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ clusters
+// Split-K CTAs of one cluster push their partial sums into the shared memory of the
+// cluster's rank-0 CTA (remote stores, then a release-arrive on its mbarrier); rank 0
+// waits with cluster-scope acquire.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster (release, then acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address in the shared memory of CTA `rank` of this cluster matching local `addr`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kTryWaitHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait_or_abort with cluster-scope acquire (for arrivals from peer CTAs).
+__device__ __forceinline__ bool mbar_wait_cluster_or_abort(uint32_t bar, uint32_t parity,
+                                                           volatile int* abort, unsigned* err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort = 1;

@@ -17,6 +17,7 @@ constexpr int kRedMaxBytes = 16 * 1024;
 constexpr int kRingSlackBytes = 16;         // aligned-word decoders may read 3 bytes past a row
 constexpr int kMaxFusedFwhtBlock = 8192;
 constexpr int kUnitElems = 16;              // weights per decode unit (half a quant block)
+constexpr int kMaxSplit = 8;                // CTAs of a split-K cluster (portable cluster size)
 
 // Tiling of the consumer warps, per (format, columns):
 //  U   units (16 weights) per thread per K chunk, RT rows per thread per tile;
@@ -65,7 +66,11 @@ struct StreamArgs {
   int fwht_B;        // 0 = no prologue
   int nsigns;
   float fwht_scale;
-  int off_xs, off_aux, off_red, off_ring;
+  const uint8_t* W2; // up-projection rows of the gated dual GEMV (nullptr: one matrix)
+  const float* gamma;  // RMS-normalisation weight [K] (nullptr: no normalisation)
+  float norm_eps;
+  int S;             // CTAs per cluster sharing a row range, each a slice of the K chunks
+  int off_xs, off_aux, off_red, off_norm, off_xchg, off_ring;
 };
 
 struct GenericArgs {
@@ -82,7 +87,17 @@ struct GenericArgs {
   int fwht_B;
   int nsigns;
   float fwht_scale;
+  const uint8_t* W2;
+  const float* gamma;
+  float norm_eps;
 };
+
+// Generic kernel: 256 threads; shared memory x [ncols][K], 1/rms [ncols], warp
+// partials [8][ncols].
+constexpr int kGenericWarps = 8;
+__host__ __device__ constexpr int64_t generic_smem_floats(int64_t ncols, int64_t K) {
+  return ncols * K + ncols + kGenericWarps * ncols;
+}
 
 enum { PATH_STREAM = 1, PATH_GENERIC = 2 };
 
@@ -98,6 +113,7 @@ struct DeviceLimits {
 };
 
 // Launchers (return cudaError_t).  `pdl` requests programmatic stream serialization.
+// With p.s.S > 1 the launch groups the grid into clusters of S CTAs.
 int launch_stream_float(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);  // F32, F16
 int launch_stream_block(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);  // Q8_0, Q4_0
 int launch_generic(int wtype, int ncols, const GenericArgs& a, int grid, int smem,

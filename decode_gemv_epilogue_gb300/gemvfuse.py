@@ -21,7 +21,7 @@ F32, F16, Q8_0, Q4_0 = 0, 1, 2, 3
 EPI_NONE, EPI_SIGMOID, EPI_SILU, EPI_SILU_MUL, EPI_ADD = 0, 1, 2, 3, 4
 EW_SIGMOID, EW_SILU, EW_MUL, EW_ADD = 1, 2, 3, 4
 OK, ERR_INVALID, ERR_ALIAS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
-FLAG_PDL = 1
+FLAG_PDL, FLAG_NO_SPLIT_K = 1, 2
 PATH_NONE, PATH_STREAM, PATH_GENERIC = 0, 1, 2
 
 _vp, _i64, _i32, _u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
@@ -29,7 +29,8 @@ _vp, _i64, _i32, _u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_
 
 class GfOpts(ctypes.Structure):
     _fields_ = [("ncols", _i64), ("fwht_signs", _vp), ("fwht_block", _i64), ("nsigns", _i64),
-                ("view_ne", _i64 * 4), ("flags", _u32), ("fwht_workspace", _vp)]
+                ("view_ne", _i64 * 4), ("flags", _u32), ("fwht_workspace", _vp),
+                ("rms_norm_weight", _vp), ("rms_norm_eps", ctypes.c_float)]
 
 
 def _sig(name, args, res=_i32):
@@ -42,6 +43,7 @@ def _sig(name, args, res=_i32):
 _gemv_fused = _sig("gemv_fused", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, _vp])
 _gemv_fused_ex = _sig("gemv_fused_ex", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp,
                                         ctypes.POINTER(GfOpts), _vp])
+_gemv_glu = _sig("gemv_glu", [_vp, _vp, _i32, _vp, _i64, _i64, _vp, ctypes.POINTER(GfOpts), _vp])
 _fwht_signed = _sig("fwht_signed", [_vp, _vp, _vp, _i64, _i64, _i64, _vp])
 _gemv_fused_fwht_noalloc = _sig("gemv_fused_fwht_noalloc", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, _i64,
                                                              _vp, _i64, _i64, _u32, _vp])
@@ -50,6 +52,8 @@ _elementwise = _sig("gf_elementwise", [_i32, _vp, _vp, _i64, _vp, _i64, _vp])
 _dequantize = _sig("gf_dequantize", [_vp, _i32, _i64, _i64, _vp, _vp])
 _plan = _sig("gf_plan", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, ctypes.POINTER(GfOpts),
                          ctypes.POINTER(_i64 * 8)])
+_plan_glu = _sig("gf_plan_glu", [_vp, _vp, _i32, _vp, _i64, _i64, _vp, ctypes.POINTER(GfOpts),
+                                 ctypes.POINTER(_i64 * 8)])
 _device_status = _sig("gf_device_status", [_i32])
 _status_string = _sig("gf_status_string", [_i32], ctypes.c_char_p)
 _last_cuda_error = _sig("gf_last_cuda_error", [])
@@ -98,7 +102,8 @@ def _check(st, what):
         raise GemvFuseError(st, what)
 
 
-def make_opts(ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, view=None, pdl=False, fwht_workspace=None):
+def make_opts(ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, view=None, pdl=False, fwht_workspace=None,
+              rms_norm_weight=None, rms_norm_eps=0.0, split_k=True):
     o = GfOpts()
     o.ncols = ncols
     o.fwht_signs = _ptr(fwht_signs)
@@ -110,8 +115,10 @@ def make_opts(ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, view=None, pd
     v = list(view or ())
     for i in range(4):
         o.view_ne[i] = v[i] if i < len(v) else 0
-    o.flags = FLAG_PDL if pdl else 0
+    o.flags = (FLAG_PDL if pdl else 0) | (0 if split_k else FLAG_NO_SPLIT_K)
     o.fwht_workspace = _ptr(fwht_workspace)
+    o.rms_norm_weight = _ptr(rms_norm_weight)
+    o.rms_norm_eps = rms_norm_eps
     return o
 
 
@@ -123,12 +130,26 @@ def gemv_fused(W, wtype, x, M, K, epilogue, aux, dst, stream=None, check=True):
 
 
 def gemv_fused_ex(W, wtype, x, M, K, epilogue, aux, dst, ncols=1, fwht_signs=None, fwht_block=0,
-                  nsigns=None, view=None, pdl=False, fwht_workspace=None, stream=None, check=True):
-    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, view, pdl, fwht_workspace)
+                  nsigns=None, view=None, pdl=False, fwht_workspace=None, rms_norm_weight=None,
+                  rms_norm_eps=0.0, split_k=True, stream=None, check=True):
+    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, view, pdl, fwht_workspace, rms_norm_weight,
+                  rms_norm_eps, split_k)
     st = _gemv_fused_ex(_ptr(W), wtype, _ptr(x), M, K, epilogue, _ptr(aux), _ptr(dst),
                         ctypes.byref(o), _stream(stream))
     if check:
         _check(st, "gemv_fused_ex")
+    return st
+
+
+def gemv_glu(W_gate, W_up, wtype, x, M, K, dst, ncols=1, fwht_signs=None, fwht_block=0, nsigns=None,
+             view=None, pdl=False, fwht_workspace=None, rms_norm_weight=None, rms_norm_eps=0.0,
+             split_k=True, stream=None, check=True):
+    """dst = silu(W_gate x') * (W_up x') for each column (see include/gemvfuse.h)."""
+    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, view, pdl, fwht_workspace, rms_norm_weight,
+                  rms_norm_eps, split_k)
+    st = _gemv_glu(_ptr(W_gate), _ptr(W_up), wtype, _ptr(x), M, K, _ptr(dst), ctypes.byref(o), _stream(stream))
+    if check:
+        _check(st, "gemv_glu")
     return st
 
 
@@ -176,8 +197,19 @@ def plan(W, wtype, x, M, K, epilogue, aux, dst, **opts):
     info = (_i64 * 8)()
     path = _plan(_ptr(W), wtype, _ptr(x), M, K, epilogue, _ptr(aux), _ptr(dst), ctypes.byref(o),
                  ctypes.byref(info))
-    keys = ("grid", "threads", "stage_rows", "stages", "k_chunk", "smem", "row_chunk")
-    return path, dict(zip(keys, list(info)[:7]))
+    return path, dict(zip(_PLAN_KEYS, list(info)))
+
+
+_PLAN_KEYS = ("grid", "threads", "stage_rows", "stages", "k_chunk", "smem", "row_chunk", "split")
+
+
+def plan_glu(W_gate, W_up, wtype, x, M, K, dst, **opts):
+    """plan() for gemv_glu."""
+    o = make_opts(**opts)
+    info = (_i64 * 8)()
+    path = _plan_glu(_ptr(W_gate), _ptr(W_up), wtype, _ptr(x), M, K, _ptr(dst), ctypes.byref(o),
+                     ctypes.byref(info))
+    return path, dict(zip(_PLAN_KEYS, list(info)))
 
 
 def device_status(reset=False):

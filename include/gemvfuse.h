@@ -14,6 +14,9 @@
  *  [CPU]  "ggml-cpu: fuse element-wise epilogues (ADD, MUL, SILU) into
  *         ggml_compute_forward_mul_mat", Guards / Correctness: epilogue operands are F32,
  *         same shape, contiguous; F32/F16/Q8_0/Q4_0 weights; fused == unfused values.
+ *         What: the SwiGLU gate (MUL_MAT + SILU) and the gate x up product (MUL_MAT +
+ *         MUL) of one FFN -- taken together as the gated dual GEMV gemv_glu() -- and
+ *         the RMS_NORM + MUL pair ahead of a matmul (the RMS-normalisation prologue).
  *
  * Conventions for every entry point:
  *  - All array pointers are DEVICE pointers owned by the caller.  The library never
@@ -81,6 +84,12 @@ typedef enum {
                             start while the previous kernel in `stream` still runs and
                             streams W before waiting for it.  Only valid when no kernel
                             still running in `stream` writes W. */
+#define GF_FLAG_NO_SPLIT_K 2u  /* never split K over a cluster of CTAs (by default a GEMV
+                            with M <= SMs/2 rows gives each row range to a cluster of
+                            2..8 CTAs that each stream a slice of K and add their
+                            partial sums in a fixed order through distributed shared
+                            memory; the result is deterministic either way, but the
+                            summation order, hence the rounding, differs). */
 
 typedef struct {
   int64_t ncols;             /* columns in the batch, 1..8 (0 is read as 1)            */
@@ -98,6 +107,12 @@ typedef struct {
                              /* prologue runs once as a stand-alone transform into it   */
                              /* and the GEMV reads it, chained with programmatic        */
                              /* dependent launch; NULL: every CTA transforms x on chip. */
+  const float* rms_norm_weight;  /* non-NULL: RMS-normalisation prologue on every column */
+                             /* of x: x'_c = x_c / sqrt(mean_k(x_c[k]^2) + eps) * gamma, */
+                             /* gamma = rms_norm_weight [K] (device float32, overlapping */
+                             /* no output).  Not combinable with the FWHT prologue       */
+                             /* (GF_ERR_UNSUPPORTED).                                    */
+  float rms_norm_eps;        /* eps of the normalisation: finite, >= 0                 */
 } gf_opts;
 
 /* y = W x with the fused tail, one column.  [EPI] Summary, What changed.
@@ -121,6 +136,19 @@ GF_API int gemv_fused(const void* W, int wtype, const float* x, int64_t M, int64
 GF_API int gemv_fused_ex(const void* W, int wtype, const float* x, int64_t M, int64_t K,
                   int epilogue, const float* aux, float* dst, const gf_opts* opts,
                   void* stream);
+
+/* Gated dual GEMV, the gate and up projections of one FFN in a single pass:
+ *     dst_c[i] = silu(G_i . x'_c) * (U_i . x'_c),   silu(g) = g / (1 + exp(-g))
+ * ([CPU] What: MUL_MAT + SILU on the gate, then MUL by the up projection; [EPI] Summary
+ * names this gated branch, which it leaves to its own GLU path).  W_gate and W_up are
+ * two M x K matrices of the same format `wtype` (same rules as W of gemv_fused); x'
+ * is x after the prologue chosen in `opts` (none, signed FWHT, RMS normalisation).
+ * Every tile the kernel streams holds rows of both matrices, so each weight byte is
+ * read once and the gate result never leaves the chip.  opts may be NULL; its ncols,
+ * prologues, view and flags apply as in gemv_fused_ex.  dst may not overlap W_gate,
+ * W_up, x or the prologue operands. */
+GF_API int gemv_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M,
+                    int64_t K, float* dst, const gf_opts* opts, void* stream);
 
 /* Allocation-free variant of gemv_fused_ex with the signed-FWHT prologue.  The pages
  * have no counterpart: this entry point exists for callers that cannot allocate a
@@ -165,9 +193,14 @@ GF_API int gf_dequantize(const void* W, int wtype, int64_t M, int64_t K, float* 
 /* Which kernel gemv_fused_ex would launch for these arguments (host only, launches
  * nothing): 0 = none (M == 0), 1 = TMA-streamed kernel, 2 = generic kernel, <0 = the
  * gf_status the call would return.  `info` (may be NULL) receives
- *   {grid, block_threads, stage_rows, stages, k_chunk, smem_bytes, row_chunk, 0}. */
+ *   {grid, block_threads, stage_rows, stages, k_chunk, smem_bytes, row_chunk,
+ *    ctas_per_cluster (split K; 1 = no split)}. */
 GF_API int gf_plan(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
             const float* aux, const float* dst, const gf_opts* opts, int64_t info[8]);
+
+/* gf_plan for gemv_glu. */
+GF_API int gf_plan_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M,
+                       int64_t K, const float* dst, const gf_opts* opts, int64_t info[8]);
 
 /* Device error word of the current device: GF_OK, or GF_ERR_TIMEOUT if a kernel gave up
  * on a bounded wait since the last reset.  Synchronises with the device.  reset != 0

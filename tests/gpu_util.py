@@ -41,3 +41,31 @@ def assert_within(got, want, bound, what=""):
                              % (what, int(bad.sum()), bad.size, i, got.reshape(-1)[i], want.reshape(-1)[i],
                                 np.asarray(bound).reshape(-1)[i], float(np.max(err / bound))))
     return float(np.max(err / bound)) if err.size else 0.0
+
+
+# RMS-normalisation prologue: the kernel scales the finished dot product by its own
+# 1/rms (fp32 sum of squares in a fixed, mostly pairwise order, then 1/sqrt).  Its
+# relative error (a few ulp from the square root and division, plus the sum's rounding,
+# under 1e-6 for K <= 16384) adds at most this fraction of sum_k |W_ik x'_k|.
+TOL_NORM_REL = 2e-6
+
+
+def norm_bound(raw, wt, xn, M, K, rows=None):
+    """Tolerance with the RMS prologue: the literal bound on x' = oracle-normalised x,
+    plus the 1/rms term."""
+    from oracle import gemv as _g
+    return gemv_bound(raw, wt, xn, M, K, rows) + TOL_NORM_REL * _g.abs_dot(raw, wt, xn, M, K, rows)
+
+
+def glu_bound(raw_g, raw_u, wt, x, M, K, rows=None, x_err=None, extra_rel=0.0):
+    """Tolerance of silu(g) * u given the bounds Bg, Bu of the two GEMVs (each the
+    literal bound, plus extra_rel * sum|W x| for a prologue): first-order propagation with
+    |silu'| <= 1.1, the product of the two errors, and the rounding of the tail itself
+    (expf, the division and two products: under 1e-6 relative)."""
+    from oracle import gemv as _g
+    gv = _g.gemv(raw_g, wt, x, M, K, rows=rows)
+    uv = _g.gemv(raw_u, wt, x, M, K, rows=rows)
+    bg = gemv_bound(raw_g, wt, x, M, K, rows, x_err) + extra_rel * _g.abs_dot(raw_g, wt, x, M, K, rows)
+    bu = gemv_bound(raw_u, wt, x, M, K, rows, x_err) + extra_rel * _g.abs_dot(raw_u, wt, x, M, K, rows)
+    sg = _g.silu(gv)
+    return 1.1 * bg * (np.abs(uv) + bu) + np.abs(sg) * bu + 1e-6 * np.abs(sg * uv)

@@ -24,8 +24,9 @@ def declared_functions():
 
 def test_header_declares_the_abi():
     names = set(declared_functions())
-    assert {"gemv_fused", "gemv_fused_ex", "fwht_signed", "gf_elementwise", "gf_dequantize", "gf_plan",
-            "gf_device_status", "gf_status_string", "gf_last_cuda_error", "gf_version"} <= names
+    assert {"gemv_fused", "gemv_fused_ex", "gemv_glu", "fwht_signed", "gf_elementwise", "gf_dequantize",
+            "gf_plan", "gf_plan_glu", "gf_device_status", "gf_status_string", "gf_last_cuda_error",
+            "gf_version"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -48,7 +49,7 @@ def test_status_strings(lib):
     assert lib.status_string(0) == "GF_OK"
     for s in (-1, -2, -3, -4, -5, -6):
         assert lib.status_string(s).startswith("GF_ERR_")
-    assert lib.version() == 1
+    assert lib.version() == 2
 
 
 def g(lib, *a, **k):
@@ -172,3 +173,86 @@ def test_dequantize_validation(lib):
     assert lib.dequantize(W, 3, 4, 32, W + 8, stream=0, check=False) == -2
     assert lib.dequantize(W + 1, 1, 4, 32, D, stream=0, check=False) == -4
     assert lib.dequantize(W, 1, 0, 32, D, stream=0, check=False) == 0
+
+
+# ----------------------------------------------------------------------------- gated dual GEMV,
+# RMS-normalisation prologue, split K
+U2, GAM = (7 << 40), (8 << 40)
+
+
+def glu(lib, *a, **k):
+    return lib.gemv_glu(*a, check=False, stream=0, **k)
+
+
+@pytest.mark.parametrize("args,kw,expect", [
+    ((W, None, 1, X, 16, 32, D), {}, -1),                      # missing up matrix
+    ((W, U2 + 1, 1, X, 16, 32, D), {}, -4),                    # up matrix misaligned
+    ((W, U2, 1, X, 16, 32, U2 + 64), {}, -2),                  # dst inside the up matrix
+    ((W, U2, 1, X, 16, 32, W + 64), {}, -2),                   # dst inside the gate matrix
+    ((W, U2, 1, X, 16, 32, X), {}, -2),                        # dst over x
+    ((W, U2, 7, X, 16, 32, D), {}, -1),                        # bad weight type
+    ((W, U2, 1, X, 16, 32, D), {"ncols": 9}, -3),
+    ((W, U2, 1, X, 16, 32, D), {"rms_norm_weight": GAM, "fwht_signs": S, "fwht_block": 32}, -3),
+])
+def test_glu_validation(lib, args, kw, expect):
+    assert glu(lib, *args, **kw) == expect
+
+
+def test_glu_empty_and_plan(lib):
+    assert glu(lib, W, U2, 3, X, 0, 4096, D) == 0
+    path, info = lib.plan_glu(W, U2, 3, X, 14336, 4096, D)
+    assert path == lib.PATH_STREAM and info["split"] == 1
+    assert info["stage_rows"] % 2 == 0  # every tile holds equal numbers of gate and up rows
+    # unaligned up matrix (2-byte aligned f16) falls back to the generic kernel
+    path, _ = lib.plan_glu(W, U2 + 2, 1, X, 64, 4096, D)
+    assert path == lib.PATH_GENERIC
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({"rms_norm_weight": GAM + 2}, -4),                         # gamma misaligned
+    ({"rms_norm_weight": GAM, "rms_norm_eps": -1.0}, -1),       # negative eps
+    ({"rms_norm_weight": GAM, "rms_norm_eps": float("nan")}, -1),
+    ({"rms_norm_weight": GAM, "rms_norm_eps": float("inf")}, -1),
+    ({"rms_norm_weight": GAM, "fwht_signs": S, "fwht_block": 32, "nsigns": 32}, -3),  # two prologues
+])
+def test_rms_norm_validation(lib, kw, expect):
+    assert g(lib, W, 1, X, 16, 32, 0, None, D, **kw) == expect
+
+
+def test_rms_norm_dst_may_not_overlap_gamma(lib):
+    assert g(lib, W, 1, X, 16, 32, 0, None, GAM + 4, rms_norm_weight=GAM) == -2
+
+
+def test_rms_norm_plan(lib):
+    path, _ = lib.plan(W, 1, X, 4096, 4096, 0, None, D, rms_norm_weight=GAM, rms_norm_eps=1e-6)
+    assert path == lib.PATH_STREAM
+    path, _ = lib.plan(W, 1, X, 4096, 4096, 0, None, D, rms_norm_weight=GAM + 4, rms_norm_eps=1e-6)
+    assert path == lib.PATH_GENERIC  # gamma not 16-byte aligned
+
+
+@pytest.mark.parametrize("M,K,wt,expect_split", [
+    (32, 4096, 3, 4),      # the 32-row sigmoid projection: 4 CTAs per row range
+    (16, 4096, 1, 8),
+    (76, 4096, 1, 2),
+    (77, 4096, 1, 1),      # more than half the SMs' worth of rows: no split
+    (4096, 4096, 1, 1),
+    (32, 256, 3, 1),       # one K granule: nothing to split
+    (32, 512, 3, 2),
+])
+def test_split_k_selection(lib, M, K, wt, expect_split):
+    path, info = lib.plan(W, wt, X, M, K, 0, None, D)
+    assert path == lib.PATH_STREAM and info["split"] == expect_split
+    assert info["grid"] % expect_split == 0 and info["grid"] <= 152
+    if expect_split > 1:
+        assert info["k_chunk"] * (expect_split - 1) < K
+    _, off = lib.plan(W, wt, X, M, K, 0, None, D, split_k=False)
+    assert off["split"] == 1
+
+
+def test_split_k_with_glu_and_prologues(lib):
+    _, info = lib.plan_glu(W, U2, 3, X, 32, 4096, D)
+    assert info["split"] == 4
+    _, info = lib.plan(W, 1, X, 32, 5120, 0, None, D, fwht_signs=S, fwht_block=1024, nsigns=1024)
+    assert info["split"] == 4 and info["k_chunk"] % 1024 == 0
+    _, info = lib.plan(W, 1, X, 32, 4096, 0, None, D, rms_norm_weight=GAM)
+    assert info["split"] == 4
