@@ -19,6 +19,9 @@ launch) and replayed.  Also reported: per-kernel CUDA-event durations and the ro
 of the dominant kernel, microseconds per decode layer (fused and unfused chains), the
 epilogue cost against the tail-free GEMV, an end-to-end number through host buffers,
 SM clocks during the timed region, and the fp64 CPU oracle timed on the host cores.
+Under "next_rows": the layer chain with the gated dual GEMV (7 launches), the dual GEMV
+against its two separate launches, split K on and off for GEMVs with few rows, and the
+cost of the RMS-normalisation prologue.
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 (N > 1 under torch.distributed.run; every rank runs the same step on its own GPU.)
@@ -390,6 +393,8 @@ def gpu_arm(args, rank, world, local_rank):
     chain = chain_measure(G, torch, step, s, args)
     # ---------------------------------------------------------------- epilogue cost
     epi_cost = epilogue_cost(G, torch, s)
+    # ---------------------------------------------------------------- rows beyond the step
+    nxt = next_rows_measure(G, torch, step, s, args, peak)
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = e2e_measure(G, torch, step, s, args)
     assert G.device_status() == 0, "a kernel reported a bounded-wait timeout"
@@ -414,6 +419,7 @@ def gpu_arm(args, rank, world, local_rank):
         "us_per_layer": chain["fused_us"], "launches_per_layer": 8,
         "us_per_layer_unfused": chain["unfused_us"], "launches_per_layer_unfused": 13,
         "chain": chain, "epilogue_cost": epi_cost, "per_kernel": per_kernel, "per_workload": per_workload,
+        "next_rows": nxt,
         "e2e": e2e, "clocks": sampler.summary(),
     }
     if dist is not None:
@@ -530,6 +536,122 @@ def chain_measure(G, torch, step, s, args):
     res["fused_gbs"] = round(layer_bytes / (res["fused_us"] * 1e-6) / 1e9, 1)
     res["layers_timed"] = 2 * reps
     return res
+
+
+def graph_us(torch, s, issue, nsets, reps):
+    """Mean microseconds per weight set of issue(i) for i < nsets, replayed in a CUDA
+    graph on stream s (after one warm replay), CUDA events on s."""
+    with torch.cuda.stream(s):
+        for i in range(nsets):
+            issue(i)
+    s.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        for i in range(nsets):
+            issue(i)
+    with torch.cuda.stream(s):
+        gr.replay()
+    s.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(s)
+    s.synchronize()
+    del gr
+    return 1e3 * e0.elapsed_time(e1) / (reps * nsets)
+
+
+def next_rows_measure(G, torch, step, s, args, peak):
+    """The gated dual GEMV, split K and the RMS-normalisation prologue, each timed as
+    graph-replayed PDL launches cycling through enough weight copies to exceed 2x L2."""
+    from decode_gemv_epilogue_gb300 import synth
+    dev = torch.device("cuda")
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    reps = max(5, min(40, args.steps // 20))
+    out = {}
+
+    def copies_for(nbytes):
+        return int(min(32, max(2, -(-2 * L2_BYTES // nbytes))))
+
+    # 1. decode-layer chain with gate and up in one launch (7 launches per layer)
+    names = ["chain_q", "chain_k", "chain_v", "chain_o_add", "chain_up", "chain_gate_silu_mul",
+             "chain_down_add", "chain_beta_sigmoid"]
+    shapes = {n: (M, K) for (n, wt, M, K, e, nc, fw) in step_spec() if n in names}
+    layers = [{n: step.W[n] for n in names},
+              {n: up(synth.weights(3, shapes[n][0], shapes[n][1], seed=300 + i)) for i, n in enumerate(names)}]
+    x, a, r = step.cx, step.ca, step.cr
+    q, k, v, g, beta = step.cq, step.ck, step.cv, step.cg, step.cbeta
+
+    def glu_layer(i):
+        Wl = layers[i]
+        G.gemv_fused_ex(Wl["chain_q"], 3, x, 4096, 4096, 0, None, q, pdl=True)
+        G.gemv_fused_ex(Wl["chain_k"], 3, x, 4096, 4096, 0, None, k, pdl=True)
+        G.gemv_fused_ex(Wl["chain_v"], 3, x, 4096, 4096, 0, None, v, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True)
+        G.gemv_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, r, 14336, 4096, g, pdl=True)
+        G.gemv_fused_ex(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_beta_sigmoid"], 3, x, 32, 4096, 1, None, beta, pdl=True)
+
+    us = graph_us(torch, s, glu_layer, 2, max(20, min(args.steps, 500)))
+    # bytes: the 8 matrices, x/a/r reads, q/k/v/g/beta writes, r read+write twice
+    lb = sum(step.W[n].numel() for n in names) + 4 * (4096 * 3 + 4096 * 3 + 2 * 4096 * 2 + 14336 * 2 + 32)
+    out["chain_glu"] = {"us_per_layer": round(us, 3), "launches_per_layer": 7, "layer_bytes": lb,
+                        "gbs": round(lb / (us * 1e-6) / 1e9, 1)}
+
+    # 2. the FFN gate/up pair: one dual launch vs up, then gate with the silu*mul tail
+    Wg0, Wu0 = step.W["chain_gate_silu_mul"], step.W["chain_up"]
+    nset = copies_for(2 * Wg0.numel())
+    pairs = [(Wg0, Wu0)] + [(Wg0.clone(), Wu0.clone()) for _ in range(nset - 1)]
+    u_tmp = torch.empty(14336, device=dev)
+    t_glu = graph_us(torch, s, lambda i: G.gemv_glu(pairs[i][0], pairs[i][1], 3, r, 14336, 4096, g, pdl=True),
+                     nset, reps)
+
+    def two(i):
+        G.gemv_fused_ex(pairs[i][1], 3, r, 14336, 4096, 0, None, u_tmp, pdl=True)
+        G.gemv_fused_ex(pairs[i][0], 3, r, 14336, 4096, 3, u_tmp, g, pdl=True)
+
+    t_two = graph_us(torch, s, two, nset, reps)
+    gb = 2 * Wg0.numel() + 4 * (4096 + 14336)
+    out["glu_q4_0_14336x4096"] = {"dual_us": round(t_glu, 3), "two_launch_us": round(t_two, 3),
+                                  "dual_gbs": round(gb / (t_glu * 1e-6) / 1e9, 1),
+                                  "dual_frac_of_peak": round(gb / (t_glu * 1e-6) / 1e9 / peak, 4)}
+    del pairs
+
+    # 3. split K for GEMVs with few rows
+    for label, wt, M, K, epi in (("q4_0_32x4096_sigmoid", 3, 32, 4096, 1), ("f16_64x14336_none", 1, 64, 14336, 0)):
+        base = up(synth.weights(wt, M, K, seed=600))
+        nset = copies_for(base.numel())
+        Ws = [base] + [base.clone() for _ in range(nset - 1)]
+        xv = up(synth.normal(K, seed=601))
+        dst = torch.empty(M, device=dev)
+        res = {}
+        for split in (True, False):
+            _, info = G.plan(Ws[0], wt, xv, M, K, epi, None, dst, split_k=split)
+            t = graph_us(torch, s, lambda i: G.gemv_fused_ex(Ws[i], wt, xv, M, K, epi, None, dst, pdl=True,
+                                                              split_k=split), nset, reps)
+            res["split%d_us" % info["split"]] = round(t, 3)
+        b = base.numel() + 4 * (K + M)
+        res["bytes"] = b
+        out["split_k_" + label] = res
+        del Ws
+
+    # 4. RMS-normalisation prologue cost against the same GEMV without it
+    for label, wt, M, K in (("f16_4096x4096", 1, 4096, 4096), ("q4_0_14336x4096", 3, 14336, 4096)):
+        base = up(synth.weights(wt, M, K, seed=610))
+        nset = copies_for(base.numel())
+        Ws = [base] + [base.clone() for _ in range(nset - 1)]
+        xv = up(synth.normal(K, seed=611))
+        gam = up(1.0 + 0.1 * synth.normal(K, seed=612))
+        dst = torch.empty(M, device=dev)
+        t0 = graph_us(torch, s, lambda i: G.gemv_fused_ex(Ws[i], wt, xv, M, K, 0, None, dst, pdl=True), nset, reps)
+        t1 = graph_us(torch, s, lambda i: G.gemv_fused_ex(Ws[i], wt, xv, M, K, 0, None, dst, pdl=True,
+                                                           rms_norm_weight=gam, rms_norm_eps=1e-6), nset, reps)
+        out["rms_norm_" + label] = {"plain_us": round(t0, 3), "with_norm_us": round(t1, 3),
+                                    "cost": round(t1 / t0 - 1.0, 4)}
+        del Ws
+    return out
 
 
 def epilogue_cost(G, torch, s):

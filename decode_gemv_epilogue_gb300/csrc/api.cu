@@ -229,8 +229,8 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
   const int xs_bytes = c.signs ? round_up(nc * kc * 4, 128) : 0;
   const int aux_bytes = round_up(nc * RC * 4, 128);
   const int red_bytes = round_up(vr * RC * wpc * nc * 4, 128);
-  const int norm_bytes = c.gamma ? round_up((ncw + 1) * nc * 4, 128) : 0;
-  const int xchg_bytes = S > 1 ? round_up(S * nc * vr * RC * 4, 128) : 0;
+  const int norm_bytes = c.gamma ? round_up(wpc * nc * 4, 128) : 0;
+  const int xchg_bytes = S > 1 ? round_up(S * nc * (vr * RC + 1) * 4, 128) : 0;
   const int fixed = kBarBytes + xs_bytes + aux_bytes + red_bytes + norm_bytes + xchg_bytes + kRingSlackBytes;
   const int stage_bytes = round_up(R * seg_full, 128);
   const int NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
@@ -271,17 +271,35 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
   return true;
 }
 
-// Split K when the rows alone would leave most SMs idle: S = min(8, SMs / M) CTAs per
-// cluster (at least two), each streaming a slice of every row's K chunks.
+// Split K when the rows alone would leave most SMs idle and each CTA would stream a
+// long row range by itself: S = min(8, SMs / M) CTAs per cluster, each streaming a
+// slice of every row's K chunks (and of x).  Measured on GB300: with under ~128 KB of x
+// and weights per CTA the cluster launch costs more than the split saves.
+constexpr int64_t kSplitMinCtaBytes = 128 * 1024;
+
 static int split_factor(const Call& c, const DeviceLimits& lim) {
   if (c.flags & GF_FLAG_NO_SPLIT_K) return 1;
   if (c.M < 1 || 2 * c.M > lim.sm_count) return 1;
+  const int64_t vr = c.W2 ? 2 : 1;
+  const int64_t cta_bytes = c.ncols * c.K * 4 + vr * row_bytes_of(c.wtype, c.K);  // one row per CTA
+  if (cta_bytes < kSplitMinCtaBytes) return 1;
   return static_cast<int>(std::min<int64_t>(kMaxSplit, lim.sm_count / c.M));
 }
 
+static int split_max_clusters(const Call& c, const Plan& p) {
+  const int nc = static_cast<int>(c.ncols);
+  return (c.wtype == GF_F32 || c.wtype == GF_F16) ? stream_split_max_clusters_float(c.wtype, nc, p)
+                                                  : stream_split_max_clusters_block(c.wtype, nc, p);
+}
+
 static bool plan_stream(const Call& c, const DeviceLimits& lim, Plan& p) {
-  for (int S = split_factor(c, lim); S > 1; --S)
-    if (plan_stream_s(c, lim, S, p)) return true;
+  // the largest split whose clusters all fit on the device at once (when the device can
+  // be asked; without one, the largest that plans)
+  for (int S = split_factor(c, lim); S > 1; --S) {
+    if (!plan_stream_s(c, lim, S, p)) continue;
+    const int fit = split_max_clusters(c, p);
+    if (fit == 0 || p.grid / S <= fit) return true;
+  }
   return plan_stream_s(c, lim, 1, p);
 }
 
@@ -318,8 +336,14 @@ static int launch_call(const Call& c, float* dst, cudaStream_t st) {
     s.err = err;
     s.W2 = static_cast<const uint8_t*>(c.W2);
     s.gamma = c.gamma;
-    e = (c.wtype == GF_F32 || c.wtype == GF_F16) ? launch_stream_float(c.wtype, static_cast<int>(c.ncols), p, st, pdl)
-                                               : launch_stream_block(c.wtype, static_cast<int>(c.ncols), p, st, pdl);
+    const int nc = static_cast<int>(c.ncols);
+    const bool fl = (c.wtype == GF_F32 || c.wtype == GF_F16);
+    if (s.S > 1)
+      e = fl ? launch_stream_float_split(c.wtype, nc, p, st, pdl) : launch_stream_block_split(c.wtype, nc, p, st, pdl);
+    else if (c.W2 || c.gamma)
+      e = fl ? launch_stream_float_ext(c.wtype, nc, p, st, pdl) : launch_stream_block_ext(c.wtype, nc, p, st, pdl);
+    else
+      e = fl ? launch_stream_float_plain(c.wtype, nc, p, st, pdl) : launch_stream_block_plain(c.wtype, nc, p, st, pdl);
   } else {
     GenericArgs g;
     g.W = static_cast<const uint8_t*>(c.W);

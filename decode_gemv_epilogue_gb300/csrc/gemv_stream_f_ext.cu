@@ -1,0 +1,10 @@
+// TMA-streamed GEMV instantiations for the F32 and F16 formats: the gated dual GEMV / RMS-normalisation prologue.
+#include "gemv_stream_impl.cuh"
+
+namespace gf {
+
+int launch_stream_float_ext(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl) {
+  return wtype == WT_F32 ? dispatch_cols<WT_F32, FEAT_EXT>(ncols, p, st, pdl) : dispatch_cols<WT_F16, FEAT_EXT>(ncols, p, st, pdl);
+}
+
+}  // namespace gf

@@ -14,8 +14,10 @@
 // Prologues: with the signed FWHT, x (all columns of one K chunk) is staged in shared
 // memory with a bulk copy and transformed in place, so x' never leaves the chip.  With
 // RMS normalisation, gamma multiplies x as it is loaded into registers and the
-// per-column 1/rms (a fixed-order sum of squares, computed while the first weight
-// tiles stream in) scales the finished dot product before the tail.
+// per-column 1/rms scales the finished dot product before the tail; the sum of squares
+// is taken from the same register loads during the first row chunk (each column
+// group's threads together load every x value of a chunk exactly once) and reduced in
+// a fixed order with the row sums.
 //
 // Gated dual GEMV: every tile holds h rows of the gate matrix followed by the same h
 // rows of the up matrix ("virtual rows"), and the tail is silu(gate) * up.
@@ -24,6 +26,11 @@
 // share one row range and each takes a slice of its K chunks.  The per-row partial
 // sums of ranks 1..S-1 are stored into rank 0's shared memory (distributed shared
 // memory), rank 0 adds the S slices in rank order (deterministic) and applies the tail.
+//
+// Each (format, columns) pair is compiled three times (FEAT): the plain GEMV, the
+// extended one (dual GEMV, RMS prologue) and the split-K one (clusters, with the same
+// extensions).  The plain kernel carries none of the extension code: cluster
+// instructions in a kernel image alone add about a microsecond per launch on GB300.
 //
 // Every wait is bounded; a timeout sets the device error word and the kernel returns
 // after draining its own copies.
@@ -44,25 +51,46 @@ __host__ __device__ constexpr int seg_bytes_of(int klen) {
 // xs is either the K chunk staged in shared memory (column stride xstride) or x itself
 // in global memory (column stride K, offset to the chunk); both are read with 16-byte
 // loads.
-// With gsrc (the RMS-normalisation weight at the chunk's offset) each x value is
-// multiplied by its gamma as it is loaded.
-template <int WT, int NCT>
+// With GAMMA, each x value is multiplied by the RMS-normalisation weight at the same
+// element (gsrc: the weight at the chunk's offset) as it is loaded, and (with SQ) its
+// square is added to ssq[c] first.
+template <int WT, int NCT, bool GAMMA>
 __device__ __forceinline__ void load_unit_x(const float* xs, int64_t xstride, const float* gsrc, int u, uint32_t qr,
-                                            int c0, int nc, float2 (&xv)[NCT][8]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t e = unit_pair_elem<WT>(static_cast<uint32_t>(u), 2 * static_cast<int>((q + qr) & 3u));
-    float4 gm = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-    if (gsrc) gm = *reinterpret_cast<const float4*>(gsrc + e);
+                                            int c0, int nc, float2 (&xv)[NCT][8], bool sq = false,
+                                            float* ssq = nullptr) {
+  if constexpr (!GAMMA) {
 #pragma unroll
     for (int c = 0; c < NCT; ++c) {
-      float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if ((c0 + c) < nc) t = *reinterpret_cast<const float4*>(xs + (c0 + c) * xstride + e);
-      if (gsrc) {
-        t.x *= gm.x; t.y *= gm.y; t.z *= gm.z; t.w *= gm.w;
+      const bool live = (c0 + c) < nc;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (live)
+          t = *reinterpret_cast<const float4*>(
+              xs + (c0 + c) * xstride + unit_pair_elem<WT>(static_cast<uint32_t>(u), 2 * static_cast<int>((q + qr) & 3u)));
+        xv[c][2 * q] = make_float2(t.x, t.y);
+        xv[c][2 * q + 1] = make_float2(t.z, t.w);
       }
-      xv[c][2 * q] = make_float2(t.x, t.y);
-      xv[c][2 * q + 1] = make_float2(t.z, t.w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t e = unit_pair_elem<WT>(static_cast<uint32_t>(u), 2 * static_cast<int>((q + qr) & 3u));
+      const float4 gm = *reinterpret_cast<const float4*>(gsrc + e);
+#pragma unroll
+      for (int c = 0; c < NCT; ++c) {
+        float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if ((c0 + c) < nc) t = *reinterpret_cast<const float4*>(xs + (c0 + c) * xstride + e);
+        if (sq) {
+          ssq[c] = fmaf(t.x, t.x, ssq[c]);
+          ssq[c] = fmaf(t.y, t.y, ssq[c]);
+          ssq[c] = fmaf(t.z, t.z, ssq[c]);
+          ssq[c] = fmaf(t.w, t.w, ssq[c]);
+        }
+        t.x *= gm.x; t.y *= gm.y; t.z *= gm.z; t.w *= gm.w;
+        xv[c][2 * q] = make_float2(t.x, t.y);
+        xv[c][2 * q + 1] = make_float2(t.z, t.w);
+      }
     }
   }
 }
@@ -116,8 +144,10 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int
   }
 }
 
-template <int WT, int NC>
+template <int WT, int NC, int FEAT>
 __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(const StreamArgs a) {
+  constexpr bool kExt = FEAT != FEAT_PLAIN;     // dual GEMV / RMS prologue compiled in
+  constexpr bool kSplit = FEAT == FEAT_SPLIT;   // cluster split K compiled in
   constexpr int U = stream_u(WT, NC);
   constexpr int RT = stream_rt(WT, NC);
   constexpr int NCT = stream_nct(WT, NC);
@@ -130,18 +160,20 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
   float* xs = reinterpret_cast<float*>(smem + a.off_xs);
   float* auxs = reinterpret_cast<float*>(smem + a.off_aux);
   float* red = reinterpret_cast<float*>(smem + a.off_red);
-  float* normv = reinterpret_cast<float*>(smem + a.off_norm);  // [ncw][NC] partials, then [NC]
-  float* xch = reinterpret_cast<float*>(smem + a.off_xchg);    // split K: [S][NC][XR]
+  float* normv = reinterpret_cast<float*>(smem + a.off_norm);  // [wpc][NC] sums of squares
+  float* xch = reinterpret_cast<float*>(smem + a.off_xchg);    // split K: [S][NC][XR], then [S][NC]
   const uint32_t ring = sbase + static_cast<uint32_t>(a.off_ring);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarBytes - 8);
 
-  const int S = a.S;
-  const int crank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int S = kSplit ? a.S : 1;
+  int crank = 0;
+  if constexpr (kSplit) crank = static_cast<int>(cluster_ctarank());
   const int rg = static_cast<int>(blockIdx.x) / S;  // row range of this CTA (its cluster's)
   const int64_t r0 = static_cast<int64_t>(rg) * a.rows_base + min(rg, a.rows_extra);
   const int nrows = a.rows_base + (rg < a.rows_extra ? 1 : 0);
   const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
-  const bool dual = a.W2 != nullptr;
+  const bool dual = kExt && a.W2 != nullptr;
+  const bool norm = kExt && a.gamma != nullptr;
   const int XR = dual ? 2 * a.RC : a.RC;  // virtual rows per row chunk
 
   if (threadIdx.x == 0) {
@@ -154,7 +186,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
     mbar_init(xchbar, static_cast<uint32_t>(S > 1 ? (S - 1) * a.ncw * 32 : 1));
     fence_mbar_init();
   }
-  if (S > 1)
+  if constexpr (kSplit)
     cluster_sync_all();  // peers arrive on rank 0's barrier only after it is initialised
   else
     __syncthreads();
@@ -191,6 +223,10 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
               if (dual)
                 bulk_g2s(dst + static_cast<uint32_t>(h * seg), a.W2 + row * a.row_bytes,
                          static_cast<uint32_t>(h * seg), full, pol);
+            } else if (!dual) {
+              for (int r = 0; r < rows; ++r)
+                bulk_g2s(dst + static_cast<uint32_t>(r * seg), a.W + (row + r) * a.row_bytes + segoff,
+                         static_cast<uint32_t>(seg), full, pol);
             } else {
               for (int r = 0; r < rows; ++r) {
                 const bool up = r >= h;
@@ -228,37 +264,9 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
     bool ok = true;
     bool x_loaded = false;
     auto cbar = [&]() { named_bar_sync(1, static_cast<uint32_t>(nt)); };
-    if (a.gamma && finalizer) {
-      // RMS statistics of every column over the whole K: per-thread sums in a fixed
-      // order, a shuffle butterfly, then the warps' partials in warp order.
-      const int K4 = a.K >> 2;
-      float ss[NC];
+    float ssq[NCT];  // this thread's share of the sum of squares of x (first row chunk)
 #pragma unroll
-      for (int c = 0; c < NC; ++c) ss[c] = 0.0f;
-      for (int i = ctid; i < K4; i += nt) {
-#pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          const float4 v = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(c) * a.K)[i];
-          ss[c] = fmaf(v.x, v.x, ss[c]);
-          ss[c] = fmaf(v.y, v.y, ss[c]);
-          ss[c] = fmaf(v.z, v.z, ss[c]);
-          ss[c] = fmaf(v.w, v.w, ss[c]);
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) ss[c] += __shfl_xor_sync(0xffffffffu, ss[c], off);
-        if (lane == 0) normv[cw * NC + c] = ss[c];
-      }
-      cbar();
-      if (ctid < NC) {
-        float t = 0.0f;
-        for (int w = 0; w < a.ncw; ++w) t += normv[w * NC + ctid];
-        normv[a.ncw * NC + ctid] = 1.0f / sqrtf(t / static_cast<float>(a.K) + a.norm_eps);
-      }
-      // published to the other consumers by the barriers before the finalize below
-    }
+    for (int c = 0; c < NCT; ++c) ssq[c] = 0.0f;
     for (int rc0 = 0; rc0 < nrows; rc0 += a.RC) {
       const int nrc = min(a.RC, nrows - rc0);
       const int nvr = dual ? 2 * nrc : nrc;
@@ -296,12 +304,21 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         // the transformed chunk in shared memory, or straight from global memory
         const float* xsrc = a.fwht_B > 0 ? xs : a.x + static_cast<int64_t>(kc) * a.kc_len;
         const int64_t xstride = a.fwht_B > 0 ? klen : a.K;
-        const float* gsrc = a.gamma ? a.gamma + static_cast<int64_t>(kc) * a.kc_len : nullptr;
         float2 xr[U][NCT][8];
+        if (norm) {
+          const float* gsrc = a.gamma + static_cast<int64_t>(kc) * a.kc_len;
 #pragma unroll
-        for (int i = 0; i < U; ++i) {
-          const int u = tg + i * tg_n;
-          if (u < units && ok) load_unit_x<WT, NCT>(xsrc, xstride, gsrc, u, qr, c0, NC, xr[i]);
+          for (int i = 0; i < U; ++i) {
+            const int u = tg + i * tg_n;
+            if (u < units && ok)
+              load_unit_x<WT, NCT, kExt>(xsrc, xstride, gsrc, u, qr, c0, NC, xr[i], rc0 == 0, ssq);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < U; ++i) {
+            const int u = tg + i * tg_n;
+            if (u < units && ok) load_unit_x<WT, NCT, false>(xsrc, xstride, nullptr, u, qr, c0, NC, xr[i]);
+          }
         }
         for (int t0 = 0; t0 < nvr; t0 += a.R, ++it) {
           const int rows = min(a.R, nvr - t0);
@@ -336,8 +353,25 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
           }
         }
       }
-      cbar();  // all partial sums of this row chunk are in `red`
-      if (S > 1) {
+      if (norm && rc0 == 0 && g == 0) {
+        // sum of squares: row group 0's column groups saw every x value of this CTA's K
+        // range once; one slot per (warp of the column group, column)
+#pragma unroll
+        for (int c = 0; c < NCT; ++c) {
+          float v = ssq[c];
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+          if (lane == 0 && c0 + c < NC) normv[wc * NC + c0 + c] = v;
+        }
+      }
+      cbar();  // all partial sums of this row chunk are in `red` (and `normv`)
+      // sum of squares of column c over this CTA's K range, warps in order
+      auto ssum = [&](int c) -> float {
+        float t = 0.0f;
+        for (int w = 0; w < a.wpc; ++w) t += normv[w * NC + c];
+        return t;
+      };
+      if constexpr (kSplit) {
         // split K (one row chunk per CTA): each rank's per-row sums go to slice `crank`
         // of rank 0's exchange buffer; rank 0 waits for every peer thread's arrival
         for (int i = ctid; i < nvr * NC; i += nt) {
@@ -350,6 +384,14 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
           else
             st_cluster_f32(map_to_rank(smem_u32(slot), 0), y);
         }
+        if (norm && ctid < NC) {  // this rank's sum of squares, after the S row slices
+          float* slot = xch + S * NC * XR + crank * NC + ctid;
+          const float t = ssum(ctid);
+          if (finalizer)
+            *slot = t;
+          else
+            st_cluster_f32(map_to_rank(smem_u32(slot), 0), t);
+        }
         if (!finalizer)
           mbar_arrive_remote(map_to_rank(xchbar, 0));
         else
@@ -361,7 +403,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         // or the S slices in rank order (split K)
         auto vsum = [&](int v, int c) -> float {
           float y = 0.0f;
-          if (S == 1) {
+          if constexpr (!kSplit) {
             for (int w = 0; w < a.wpc; ++w) y += red[(v * a.wpc + w) * NC + c];
           } else {
             for (int sl = 0; sl < S; ++sl) y += xch[(sl * NC + c) * XR + v];
@@ -371,20 +413,29 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         const int H = a.R / 2;
         for (int i = ctid; i < nrc * NC; i += nt) {
           const int c = i / nrc, r = i - c * nrc;
-          const float inv = a.gamma ? normv[a.ncw * NC + c] : 1.0f;
+          float inv = 1.0f;
+          if (norm) {
+            float t = 0.0f;
+            if constexpr (kSplit) {
+              for (int sl = 0; sl < S; ++sl) t += xch[S * NC * XR + sl * NC + c];
+            } else {
+              t = ssum(c);
+            }
+            inv = 1.0f / sqrtf(t / static_cast<float>(a.K) + a.norm_eps);
+          }
           float out;
           if (dual) {
             // tile t holds gate rows t*H .. t*H+ht-1 then the same up rows
             const int t = r / H, l = r - t * H, ht = min(H, nrc - t * H);
             float yg = vsum(t * a.R + l, c), yu = vsum(t * a.R + ht + l, c);
-            if (a.gamma) {
+            if (norm) {
               yg *= inv;
               yu *= inv;
             }
             out = tail_silu(yg) * yu;
           } else {
             float y = vsum(r, c);
-            if (a.gamma) y *= inv;
+            if (norm) y *= inv;
             const float av = need_aux ? auxs[c * a.RC + r] : 0.0f;
             out = apply_tail(a.epi, y, av);
           }
@@ -395,12 +446,12 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
     }
   }
   __syncthreads();
-  if (S > 1) cluster_sync_all();  // no CTA leaves while a peer may still store into it
+  if constexpr (kSplit) cluster_sync_all();  // no CTA leaves while a peer may still store into it
 }
 
-template <int WT, int NC>
+template <int WT, int NC, int FEAT>
 int launch_stream_t(const Plan& p, cudaStream_t st, bool pdl) {
-  auto kern = gemv_stream_kernel<WT, NC>;
+  auto kern = gemv_stream_kernel<WT, NC, FEAT>;
   static int configured_smem[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -416,7 +467,7 @@ int launch_stream_t(const Plan& p, cudaStream_t st, bool pdl) {
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int na = 0;
-  if (p.s.S > 1) {
+  if (FEAT == FEAT_SPLIT) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = static_cast<unsigned>(p.s.S);
     attr[na].val.clusterDim.y = 1;
@@ -431,6 +482,64 @@ int launch_stream_t(const Plan& p, cudaStream_t st, bool pdl) {
   cfg.attrs = attr;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, p.s);
+}
+
+// Clusters of p.s.S CTAs of this kernel that can be resident at once (0 if the query
+// fails); p gives the threads and dynamic shared memory of the launch.
+template <int WT, int NC>
+int max_active_clusters_t(const Plan& p) {
+  auto kern = gemv_stream_kernel<WT, NC, FEAT_SPLIT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.s.S * 64);
+  cfg.blockDim = dim3(p.threads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.s.S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <int WT, int FEAT>
+int dispatch_cols(int ncols, const Plan& p, cudaStream_t st, bool pdl) {
+  switch (ncols) {
+    case 1: return launch_stream_t<WT, 1, FEAT>(p, st, pdl);
+    case 2: return launch_stream_t<WT, 2, FEAT>(p, st, pdl);
+    case 3: return launch_stream_t<WT, 3, FEAT>(p, st, pdl);
+    case 4: return launch_stream_t<WT, 4, FEAT>(p, st, pdl);
+    case 5: return launch_stream_t<WT, 5, FEAT>(p, st, pdl);
+    case 6: return launch_stream_t<WT, 6, FEAT>(p, st, pdl);
+    case 7: return launch_stream_t<WT, 7, FEAT>(p, st, pdl);
+    case 8: return launch_stream_t<WT, 8, FEAT>(p, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int WT>
+int occupancy_cols(int ncols, const Plan& p) {
+  switch (ncols) {
+    case 1: return max_active_clusters_t<WT, 1>(p);
+    case 2: return max_active_clusters_t<WT, 2>(p);
+    case 3: return max_active_clusters_t<WT, 3>(p);
+    case 4: return max_active_clusters_t<WT, 4>(p);
+    case 5: return max_active_clusters_t<WT, 5>(p);
+    case 6: return max_active_clusters_t<WT, 6>(p);
+    case 7: return max_active_clusters_t<WT, 7>(p);
+    case 8: return max_active_clusters_t<WT, 8>(p);
+    default: return 0;
+  }
 }
 
 }  // namespace gf

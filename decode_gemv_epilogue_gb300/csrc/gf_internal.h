@@ -112,10 +112,21 @@ struct DeviceLimits {
   int smem_optin;
 };
 
+// Kernel feature sets of the streamed GEMV (separate instantiations).
+enum { FEAT_PLAIN = 0, FEAT_EXT = 1, FEAT_SPLIT = 2 };
+
 // Launchers (return cudaError_t).  `pdl` requests programmatic stream serialization.
-// With p.s.S > 1 the launch groups the grid into clusters of S CTAs.
-int launch_stream_float(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);  // F32, F16
-int launch_stream_block(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);  // Q8_0, Q4_0
+// FEAT_SPLIT launches group the grid into clusters of p.s.S CTAs.  One function per
+// (format family, feature set), each in its own translation unit.
+int launch_stream_float_plain(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);  // F32, F16
+int launch_stream_float_ext(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);
+int launch_stream_float_split(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);
+int launch_stream_block_plain(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);  // Q8_0, Q4_0
+int launch_stream_block_ext(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);
+int launch_stream_block_split(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);
+// Resident clusters of the split-K kernel for this plan (0 if unknown, e.g. no device).
+int stream_split_max_clusters_float(int wtype, int ncols, const Plan& p);
+int stream_split_max_clusters_block(int wtype, int ncols, const Plan& p);
 int launch_generic(int wtype, int ncols, const GenericArgs& a, int grid, int smem,
                    cudaStream_t st, bool pdl);
 int launch_fwht(const float* x, const float* signs, float* dst, int64_t n, int B, int nsigns,

@@ -231,13 +231,14 @@ def test_rms_norm_plan(lib):
 
 
 @pytest.mark.parametrize("M,K,wt,expect_split", [
-    (32, 4096, 3, 4),      # the 32-row sigmoid projection: 4 CTAs per row range
-    (16, 4096, 1, 8),
-    (76, 4096, 1, 2),
-    (77, 4096, 1, 1),      # more than half the SMs' worth of rows: no split
+    (32, 4096, 3, 1),      # the 32-row sigmoid projection: 18 KB per CTA, not worth a cluster
+    (32, 32768, 3, 4),     # 128 KB of x + 18 KB of weights per CTA: 4 CTAs per row range
+    (16, 65536, 1, 8),
+    (8, 131072, 1, 8),
+    (76, 32768, 1, 2),
+    (77, 32768, 1, 1),     # more than half the SMs' worth of rows: no split
+    (32, 16384, 1, 1),     # 96 KB per CTA
     (4096, 4096, 1, 1),
-    (32, 256, 3, 1),       # one K granule: nothing to split
-    (32, 512, 3, 2),
 ])
 def test_split_k_selection(lib, M, K, wt, expect_split):
     path, info = lib.plan(W, wt, X, M, K, 0, None, D)
@@ -250,9 +251,12 @@ def test_split_k_selection(lib, M, K, wt, expect_split):
 
 
 def test_split_k_with_glu_and_prologues(lib):
-    _, info = lib.plan_glu(W, U2, 3, X, 32, 4096, D)
+    _, info = lib.plan_glu(W, U2, 3, X, 32, 32768, D)
     assert info["split"] == 4
-    _, info = lib.plan(W, 1, X, 32, 5120, 0, None, D, fwht_signs=S, fwht_block=1024, nsigns=1024)
+    _, info = lib.plan(W, 1, X, 32, 40960, 0, None, D, fwht_signs=S, fwht_block=1024, nsigns=1024)
     assert info["split"] == 4 and info["k_chunk"] % 1024 == 0
-    _, info = lib.plan(W, 1, X, 32, 4096, 0, None, D, rms_norm_weight=GAM)
+    _, info = lib.plan(W, 1, X, 32, 32768, 0, None, D, rms_norm_weight=GAM)
+    assert info["split"] == 4
+    # a batch multiplies the x bytes each CTA streams
+    _, info = lib.plan(W, 3, X, 32, 8192, 0, None, D, ncols=4)
     assert info["split"] == 4
