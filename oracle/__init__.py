@@ -36,6 +36,8 @@ PINS = {
     "quant.dequantize_f16": "pinned: hand-decoded binary16 fixture + numpy float16 (library)",
     "quant.dequantize_q8_0": "pinned: hand-decoded block fixture (golden/q8_0_block.txt)",
     "quant.dequantize_q4_0": "pinned: hand-decoded block fixture (golden/q4_0_block.txt)",
+    "quant.dequantize_q4_k": "pinned: hand-packed super-block (golden/q4_k_block.txt), zero codes / zero dmin, "
+                             "random fields through the generator's packer",
     "gemv.gemv": "pinned: 2x3 worked integer example, identity W, one-hot x, brute force",
     "gemv.apply_epilogue": "pinned: sigmoid(0)=1/2, silu(0)=0, symmetry, limits, W=0 cases",
     "fwht.hadamard": "pinned: H2, Sylvester recursion via np.kron, scipy.linalg.hadamard, H.H=nI",

@@ -89,14 +89,23 @@ def gemv_glu(raw_gate, raw_up, wtype, x, M, K, rows=None):
     return silu(g) * u
 
 
+def _abs_weights(raw, wtype, M, K, rows):
+    """|W| for the tolerance scale.  For Q4_K, whose weight is a difference a - b of a
+    scaled code and a sub-block min, |a| + |b|: a kernel may add the two terms'
+    products separately (the min term through a per-sub-block sum of x), and its
+    rounding then scales with both terms, not with their difference."""
+    if wtype == quant.WTYPE_Q4_K:
+        a, b = quant.q4_k_parts(raw, M, K, rows)
+        return np.abs(a) + np.abs(b)
+    return np.abs(quant.dequantize(raw, wtype, M, K, rows))
+
+
 def abs_dot(raw, wtype, x, M, K, rows=None):
     """sum_k |W[i,k] * x[c,k]| in fp64: the scale of the parity tolerance."""
-    W = quant.dequantize(raw, wtype, M, K, rows)
     X = _as_cols(x, K)
-    return np.einsum("ik,ck->ci", np.abs(W), np.abs(X))
+    return np.einsum("ik,ck->ci", _abs_weights(raw, wtype, M, K, rows), np.abs(X))
 
 
 def abs_w_dot(raw, wtype, e, M, K, rows=None):
     """sum_k |W[i,k]| * e[c,k] for a non-negative per-element error e [ncols, K]."""
-    W = quant.dequantize(raw, wtype, M, K, rows)
-    return np.einsum("ik,ck->ci", np.abs(W), _as_cols(e, K))
+    return np.einsum("ik,ck->ci", _abs_weights(raw, wtype, M, K, rows), _as_cols(e, K))
