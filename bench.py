@@ -19,9 +19,9 @@ launch) and replayed.  Also reported: per-kernel CUDA-event durations and the ro
 of the dominant kernel, microseconds per decode layer (fused and unfused chains), the
 epilogue cost against the tail-free GEMV, an end-to-end number through host buffers,
 SM clocks during the timed region, and the fp64 CPU oracle timed on the host cores.
-Under "next_rows": the layer chain with the gated dual GEMV (7 launches), the dual GEMV
-against its two separate launches, split K on and off for GEMVs with few rows, and the
-cost of the RMS-normalisation prologue.
+Under "next_rows": the layer chain with the gated dual GEMV (7 launches), the same
+layer in Q4_K, the dual GEMV against its two separate launches, split K on and off for
+GEMVs with few rows, and the cost of the RMS-normalisation prologue.
 
 Launch: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 (N > 1 under torch.distributed.run; every rank runs the same step on its own GPU.)
@@ -599,6 +599,33 @@ def next_rows_measure(G, torch, step, s, args, peak):
     lb = sum(step.W[n].numel() for n in names) + 4 * (4096 * 3 + 4096 * 3 + 2 * 4096 * 2 + 14336 * 2 + 32)
     out["chain_glu"] = {"us_per_layer": round(us, 3), "launches_per_layer": 7, "layer_bytes": lb,
                         "gbs": round(lb / (us * 1e-6) / 1e9, 1)}
+
+    # 1b. the same layer in Q4_K (a format the pages' decode-layer measurements name),
+    # 8 launches and 7 with the dual GEMV
+    layers_k = [{n: up(synth.weights(4, shapes[n][0], shapes[n][1], seed=700 + 10 * l + i))
+                 for i, n in enumerate(names)} for l in range(2)]
+
+    def k_layer(i, glu):
+        Wl = layers_k[i]
+        G.gemv_fused_ex(Wl["chain_q"], 4, x, 4096, 4096, 0, None, q, pdl=True)
+        G.gemv_fused_ex(Wl["chain_k"], 4, x, 4096, 4096, 0, None, k, pdl=True)
+        G.gemv_fused_ex(Wl["chain_v"], 4, x, 4096, 4096, 0, None, v, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 4, a, 4096, 4096, 4, r, r, pdl=True)
+        if glu:
+            G.gemv_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 4, r, 14336, 4096, g, pdl=True)
+        else:
+            G.gemv_fused_ex(Wl["chain_up"], 4, r, 14336, 4096, 0, None, step.cup, pdl=True)
+            G.gemv_fused_ex(Wl["chain_gate_silu_mul"], 4, r, 14336, 4096, 3, step.cup, g, pdl=True)
+        G.gemv_fused_ex(Wl["chain_down_add"], 4, g, 4096, 14336, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_beta_sigmoid"], 4, x, 32, 4096, 1, None, beta, pdl=True)
+
+    us8 = graph_us(torch, s, lambda i: k_layer(i, False), 2, max(20, min(args.steps, 500)))
+    us7 = graph_us(torch, s, lambda i: k_layer(i, True), 2, max(20, min(args.steps, 500)))
+    lbk = sum(layers_k[0][n].numel() for n in names) + 4 * (4096 * 3 + 4096 * 3 + 2 * 4096 * 2 + 14336 * 3 + 32)
+    out["chain_q4_k"] = {"us_per_layer": round(us8, 3), "launches_per_layer": 8,
+                         "us_per_layer_glu": round(us7, 3), "launches_per_layer_glu": 7, "layer_bytes": lbk,
+                         "gbs": round(lbk / (us8 * 1e-6) / 1e9, 1)}
+    del layers_k
 
     # 2. the FFN gate/up pair: one dual launch vs up, then gate with the silu*mul tail
     Wg0, Wu0 = step.W["chain_gate_silu_mul"], step.W["chain_up"]

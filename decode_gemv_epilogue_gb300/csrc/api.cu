@@ -75,6 +75,7 @@ static int64_t row_bytes_of(int wtype, int64_t K) {
     case GF_F32: return 4 * K;
     case GF_F16: return 2 * K;
     case GF_Q8_0: return (K / 32) * 34;
+    case GF_Q4_K: return (K / 256) * 144;
     default: return (K / 32) * 18;
   }
 }
@@ -108,7 +109,7 @@ struct Call {
 };
 
 static int validate(const Call& c) {
-  if (c.wtype < GF_F32 || c.wtype > GF_Q4_0) return GF_ERR_INVALID;
+  if (c.wtype < GF_F32 || c.wtype > GF_Q4_K) return GF_ERR_INVALID;
   if (c.epi == EPI_GLU) {
     if (!c.W2 && c.M > 0 && c.K > 0) return GF_ERR_INVALID;
   } else if (c.epi < GF_EPI_NONE || c.epi > GF_EPI_ADD || c.W2) {
@@ -118,6 +119,7 @@ static int validate(const Call& c) {
   if (c.M > INT32_MAX || c.K > INT32_MAX / 8) return GF_ERR_UNSUPPORTED;
   if (c.ncols < 1 || c.ncols > kMaxCols) return c.ncols < 1 ? GF_ERR_INVALID : GF_ERR_UNSUPPORTED;
   if ((c.wtype == GF_Q8_0 || c.wtype == GF_Q4_0) && c.K % 32 != 0) return GF_ERR_UNSUPPORTED;
+  if (c.wtype == GF_Q4_K && c.K % 256 != 0) return GF_ERR_UNSUPPORTED;
   const bool need_aux = (c.epi == GF_EPI_SILU_MUL || c.epi == GF_EPI_ADD);
   if (c.M > 0) {
     if (!c.dst) return GF_ERR_INVALID;
@@ -288,6 +290,7 @@ static int split_factor(const Call& c, const DeviceLimits& lim) {
 
 static int split_max_clusters(const Call& c, const Plan& p) {
   const int nc = static_cast<int>(c.ncols);
+  if (c.wtype == GF_Q4_K) return stream_split_max_clusters_q4k(nc, p);
   return (c.wtype == GF_F32 || c.wtype == GF_F16) ? stream_split_max_clusters_float(c.wtype, nc, p)
                                                   : stream_split_max_clusters_block(c.wtype, nc, p);
 }
@@ -338,7 +341,10 @@ static int launch_call(const Call& c, float* dst, cudaStream_t st) {
     s.gamma = c.gamma;
     const int nc = static_cast<int>(c.ncols);
     const bool fl = (c.wtype == GF_F32 || c.wtype == GF_F16);
-    if (s.S > 1)
+    if (c.wtype == GF_Q4_K)
+      e = s.S > 1 ? launch_stream_q4k_split(nc, p, st, pdl)
+          : (c.W2 || c.gamma) ? launch_stream_q4k_ext(nc, p, st, pdl) : launch_stream_q4k_plain(nc, p, st, pdl);
+    else if (s.S > 1)
       e = fl ? launch_stream_float_split(c.wtype, nc, p, st, pdl) : launch_stream_block_split(c.wtype, nc, p, st, pdl);
     else if (c.W2 || c.gamma)
       e = fl ? launch_stream_float_ext(c.wtype, nc, p, st, pdl) : launch_stream_block_ext(c.wtype, nc, p, st, pdl);
@@ -551,9 +557,10 @@ int gf_elementwise(int op, const float* a, const float* b, int64_t nb, float* ds
 }
 
 int gf_dequantize(const void* W, int wtype, int64_t M, int64_t K, float* out, void* stream) {
-  if (wtype < GF_F32 || wtype > GF_Q4_0) return GF_ERR_INVALID;
+  if (wtype < GF_F32 || wtype > GF_Q4_K) return GF_ERR_INVALID;
   if (M < 0 || K < 0) return GF_ERR_INVALID;
   if ((wtype == GF_Q8_0 || wtype == GF_Q4_0) && K % 32 != 0) return GF_ERR_UNSUPPORTED;
+  if (wtype == GF_Q4_K && K % 256 != 0) return GF_ERR_UNSUPPORTED;
   if (M == 0 || K == 0) return GF_OK;
   if (!W || !out) return GF_ERR_INVALID;
   if (!aligned(W, wtype == GF_F32 ? 4 : 2) || !aligned(out, 4)) return GF_ERR_ALIGN;

@@ -134,6 +134,7 @@ int launch_generic(int wtype, int ncols, const GenericArgs& a, int grid, int sme
     case WT_F16: return generic_cols<WT_F16>(ncols, a, grid, smem, st, pdl);
     case WT_Q8_0: return generic_cols<WT_Q8_0>(ncols, a, grid, smem, st, pdl);
     case WT_Q4_0: return generic_cols<WT_Q4_0>(ncols, a, grid, smem, st, pdl);
+    case WT_Q4_K: return generic_cols<WT_Q4_K>(ncols, a, grid, smem, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

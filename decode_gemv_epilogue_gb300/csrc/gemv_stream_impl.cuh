@@ -43,7 +43,23 @@ namespace gf {
 
 template <int WT>
 __host__ __device__ constexpr int seg_bytes_of(int klen) {
-  return WT == WT_F32 ? 4 * klen : WT == WT_F16 ? 2 * klen : WT == WT_Q8_0 ? (klen / 32) * 34 : (klen / 32) * 18;
+  return WT == WT_F32    ? 4 * klen
+         : WT == WT_F16  ? 2 * klen
+         : WT == WT_Q8_0 ? (klen / 32) * 34
+         : WT == WT_Q4_0 ? (klen / 32) * 18
+                         : (klen / 256) * 144;
+}
+
+// Unit i (< U) of the thread at position tg (of tg_n) in its column group: strided over
+// the chunk, except Q4_K, whose two units are the pair sharing one code load.
+template <int WT, int U>
+__device__ __forceinline__ int unit_index(int tg, int i, int tg_n) {
+  if constexpr (WT == WT_Q4_K) {
+    static_assert(U == 2, "Q4_K threads own one unit pair");
+    return 2 * tg + i;
+  } else {
+    return tg + i * tg_n;
+  }
 }
 
 // x values of one unit for the thread's NCT columns (starting at column c0; columns
@@ -121,6 +137,41 @@ __device__ __forceinline__ void unit_rows_fma(const float2 (&v)[8], float d, con
 
 // One thread's share of a tile: U units (16 weights each, stride tg_n within the
 // column group) times RT rows (stride G within the tile), against x in registers.
+// Q4_K: per row, one decode of the thread's unit pair; the scaled-code term through
+// packed FMAs, the min term through the units' sums of x (xsum).
+template <int NCT, int RT>
+__device__ __forceinline__ void consume_tile_q4k(uint32_t st, int seg, int rows, int units, int tg, int g, int G,
+                                                 const float2 (&xr)[2][NCT][8], const float (&xsum)[2][NCT],
+                                                 float2 (&acc)[RT][NCT]) {
+  if (2 * tg >= units) return;
+#pragma unroll
+  for (int j = 0; j < RT; ++j) {
+    const int r = g + j * G;
+    if (r < rows) {
+      const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+      float dsc[2], dmn[2];
+      const uint4 q = q4k_load_pair(ld, static_cast<uint32_t>(tg), dsc, dmn);
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        float2 v[8];
+        q4k_nibbles(q, static_cast<uint32_t>(n), v);
+#pragma unroll
+        for (int c = 0; c < NCT; ++c) {
+          float2 p0 = make_float2(0.0f, 0.0f), p1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int k = 0; k < 8; k += 2) {
+            p0 = ffma2(v[k], xr[n][c][k], p0);
+            p1 = ffma2(v[k + 1], xr[n][c][k + 1], p1);
+          }
+          float2 t = ffma2(make_float2(dsc[n], dsc[n]), fadd2(p0, p1), acc[j][c]);
+          t.x = fmaf(-dmn[n], xsum[n][c], t.x);
+          acc[j][c] = t;
+        }
+      }
+    }
+  }
+}
+
 template <int WT, int NCT, int U, int RT>
 __device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int units, int tg, int tg_n,
                                              int g, int G, uint32_t qr, const float2 (&xr)[U][NCT][8],
@@ -309,17 +360,30 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
           const float* gsrc = a.gamma + static_cast<int64_t>(kc) * a.kc_len;
 #pragma unroll
           for (int i = 0; i < U; ++i) {
-            const int u = tg + i * tg_n;
+            const int u = unit_index<WT, U>(tg, i, tg_n);
             if (u < units && ok)
               load_unit_x<WT, NCT, kExt>(xsrc, xstride, gsrc, u, qr, c0, NC, xr[i], rc0 == 0, ssq);
           }
         } else {
 #pragma unroll
           for (int i = 0; i < U; ++i) {
-            const int u = tg + i * tg_n;
+            const int u = unit_index<WT, U>(tg, i, tg_n);
             if (u < units && ok) load_unit_x<WT, NCT, false>(xsrc, xstride, nullptr, u, qr, c0, NC, xr[i]);
           }
         }
+        // Q4_K: the sum of each unit's (scaled) x, for the sub-block min term
+        float xsum[U][NCT];
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+#pragma unroll
+          for (int c = 0; c < NCT; ++c) {
+            float2 t = make_float2(0.0f, 0.0f);
+            if constexpr (WT == WT_Q4_K) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) t = fadd2(t, xr[i][c][k]);
+            }
+            xsum[i][c] = t.x + t.y;
+          }
         for (int t0 = 0; t0 < nvr; t0 += a.R, ++it) {
           const int rows = min(a.R, nvr - t0);
           const int slot = it % a.NS, round = it / a.NS;
@@ -330,9 +394,14 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
           for (int j = 0; j < RT; ++j)
 #pragma unroll
             for (int c = 0; c < NCT; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
-          if (ok)
-            consume_tile<WT, NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units,
-                                         tg, tg_n, g, a.G, qr, xr, acc);
+          if (ok) {
+            if constexpr (WT == WT_Q4_K)
+              consume_tile_q4k<NCT, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
+                                        g, a.G, xr, xsum, acc);
+            else
+              consume_tile<WT, NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units,
+                                           tg, tg_n, g, a.G, qr, xr, acc);
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(empty0 + 8u * slot);
           // warp reduction of the RT*NCT partial sums (padded to a power of two)

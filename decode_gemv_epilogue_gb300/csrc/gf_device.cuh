@@ -8,7 +8,7 @@
 
 namespace gf {
 
-enum { WT_F32 = 0, WT_F16 = 1, WT_Q8_0 = 2, WT_Q4_0 = 3 };
+enum { WT_F32 = 0, WT_F16 = 1, WT_Q8_0 = 2, WT_Q4_0 = 3, WT_Q4_K = 4 };
 enum { EPI_NONE = 0, EPI_SIGMOID = 1, EPI_SILU = 2, EPI_SILU_MUL = 3, EPI_ADD = 4 };
 // Internal tail of the gated dual GEMV: silu(gate row) * (up row).
 enum { EPI_GLU = 5 };
@@ -246,6 +246,8 @@ struct SmemLoader {
                  : "r"(base + off));
     return v;
   }
+  __device__ __forceinline__ uint32_t word(uint32_t off) const { return u32(off); }   // 4-byte aligned
+  __device__ __forceinline__ uint4 quad(uint32_t off) const { return v4(off); }       // 16-byte aligned
   template <int N>
   __device__ __forceinline__ void words(uint32_t start, uint32_t (&w)[N]) const {
     const uint32_t a = start & ~3u, sh = (start & 3u) * 8u;
@@ -269,6 +271,13 @@ struct GmemLoader {
   __device__ __forceinline__ void words(uint32_t start, uint32_t (&w)[N]) const {
 #pragma unroll
     for (int i = 0; i < N; ++i) w[i] = __byte_perm(u16(start + 4u * i), u16(start + 4u * i + 2u), 0x5410);
+  }
+  // word / quad from 16-bit loads: rows in global memory may be only 2-byte aligned
+  __device__ __forceinline__ uint32_t word(uint32_t off) const {
+    return __byte_perm(u16(off), u16(off + 2u), 0x5410);
+  }
+  __device__ __forceinline__ uint4 quad(uint32_t off) const {
+    return make_uint4(word(off), word(off + 4u), word(off + 8u), word(off + 12u));
   }
 };
 
@@ -355,6 +364,56 @@ __device__ __forceinline__ void decode_unit(const L& ld, uint32_t u, float2 (&v)
   }
 }
 
+// ---- Q4_K (super-blocks of 256 elements, 144 bytes: binary16 d and dmin, 12 bytes of
+// packed 6-bit sub-block scales sc[j] and mins m[j], 128 code bytes; value
+// d*sc[j]*q - dmin*m[j]).  Units come in pairs that share one 16-byte load of codes:
+// pair p of a row (or K chunk) is super-block b = p / 8, pair-in-block pp = p % 8
+// (group g = pp / 2, half h = pp % 2), code bytes 16 + 16*pp of the super-block.  Unit
+// 2p + n is nibble n of those bytes: sub-block j = 2g + n, elements 32j + 16h .. + 15.
+constexpr uint32_t kQ4kBytes = 144;
+
+// d*sc[j] and dmin*m[j] (both exact in fp32) of sub-blocks 2g and 2g+1 of the
+// super-block at boff.
+template <class L>
+__device__ __forceinline__ void q4k_scales(const L& ld, uint32_t boff, uint32_t g, float (&dsc)[2],
+                                           float (&dmn)[2]) {
+  const uint32_t hdr = ld.word(boff);
+  const float d = h2f(hdr & 0xFFFFu), dmin = h2f(hdr >> 16);
+  const uint32_t s0 = ld.word(boff + 4u), s1 = ld.word(boff + 8u), s2 = ld.word(boff + 12u);
+  const bool upper = g >= 2u;  // sub-blocks 4..7: low bits in bytes 8..11, high bits in 0..7
+#pragma unroll
+  for (uint32_t n = 0; n < 2; ++n) {
+    const uint32_t sh = 8u * ((2u * g + n) & 3u);
+    const uint32_t a = (s0 >> sh) & 0xFFu, b = (s1 >> sh) & 0xFFu, c = (s2 >> sh) & 0xFFu;
+    const uint32_t sc = upper ? ((c & 15u) | ((a >> 6) << 4)) : (a & 63u);
+    const uint32_t m = upper ? ((c >> 4) | ((b >> 6) << 4)) : (b & 63u);
+    dsc[n] = d * static_cast<float>(sc);
+    dmn[n] = dmin * static_cast<float>(m);
+  }
+}
+
+// The 16 code bytes of unit pair p and its two sub-blocks' scale and min.
+template <class L>
+__device__ __forceinline__ uint4 q4k_load_pair(const L& ld, uint32_t p, float (&dsc)[2], float (&dmn)[2]) {
+  const uint32_t pp = p & 7u;
+  const uint32_t boff = (p >> 3) * kQ4kBytes;
+  q4k_scales(ld, boff, pp >> 1, dsc, dmn);
+  return ld.quad(boff + 16u + 16u * pp);
+}
+
+// Nibble n of the 16 code bytes as exact floats 0..15: eight pairs of consecutive
+// elements of unit 2p + n.
+__device__ __forceinline__ void q4k_nibbles(const uint4 q, uint32_t n, float2 (&v)[8]) {
+  const float bias = -kMagic;
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t c = (w[i] >> (4u * n)) & 0x0F0F0F0Fu;
+    v[2 * i] = magic_pair(c, 0x7540u, bias);
+    v[2 * i + 1] = magic_pair(c, 0x7542u, bias);
+  }
+}
+
 // Quad rotation of a lane for the F32/F16 unit loads (0 for the block formats).
 template <int WT>
 __device__ __forceinline__ uint32_t lane_quad_rot(int lane) {
@@ -364,7 +423,11 @@ __device__ __forceinline__ uint32_t lane_quad_rot(int lane) {
 // Element (within the row / chunk) of the first value of pair k of unit u.
 template <int WT>
 __device__ __forceinline__ uint32_t unit_pair_elem(uint32_t u, int k) {
-  if constexpr (WT == WT_Q4_0) {
+  if constexpr (WT == WT_Q4_K) {
+    const uint32_t p = u >> 1, pp = p & 7u;
+    const uint32_t j = 2u * (pp >> 1) + (u & 1u);
+    return (p >> 3) * 256u + 32u * j + 16u * (pp & 1u) + 2u * k;
+  } else if constexpr (WT == WT_Q4_0) {
     const uint32_t b = u >> 1, h = u & 1u;
     return b * 32u + 8u * h + (k < 4 ? 2u * k : 16u + 2u * (k - 4));
   } else {
@@ -385,6 +448,23 @@ __device__ __forceinline__ float decode_elem(const uint8_t* row, int64_t k) {
     const uint8_t* blk = row + b * 34;
     const float d = h2f(*reinterpret_cast<const uint16_t*>(blk));
     return d * static_cast<float>(static_cast<int8_t>(blk[2 + j]));
+  } else if constexpr (WT == WT_Q4_K) {
+    const uint8_t* blk = row + (k >> 8) * kQ4kBytes;
+    const int j = static_cast<int>((k & 255) >> 5), t = static_cast<int>(k & 31);
+    const float d = h2f(*reinterpret_cast<const uint16_t*>(blk));
+    const float dmin = h2f(*reinterpret_cast<const uint16_t*>(blk + 2));
+    const uint8_t* sb = blk + 4;
+    uint32_t sc, m;
+    if (j < 4) {
+      sc = sb[j] & 63u;
+      m = sb[j + 4] & 63u;
+    } else {
+      sc = (sb[j + 4] & 15u) | ((sb[j - 4] >> 6) << 4);
+      m = (sb[j + 4] >> 4) | ((sb[j] >> 6) << 4);
+    }
+    const uint32_t byte = blk[16 + 32 * (j >> 1) + t];
+    const float q = static_cast<float>((j & 1) ? (byte >> 4) : (byte & 15u));
+    return fmaf(d * static_cast<float>(sc), q, -(dmin * static_cast<float>(m)));
   } else {
     const int64_t b = k >> 5;
     const int j = static_cast<int>(k & 31);

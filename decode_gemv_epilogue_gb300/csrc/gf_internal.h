@@ -26,16 +26,20 @@ constexpr int kMaxSplit = 8;                // CTAs of a split-K cluster (portab
 // CS column groups of wpc warps; within a column group every thread owns U units of the
 // K chunk and keeps their x values (NCT columns) in registers for the whole chunk.
 // F32/F16 decode is cheap, so batches are split two columns per thread (more warps);
-// the block formats keep up to four columns per thread so each weight is decoded once
-// per four columns.
-__host__ __device__ constexpr bool stream_quant(int wt) { return wt == 2 || wt == 3; }
+// Q8_0/Q4_0 keep up to four columns per thread so each weight is decoded once per four
+// columns.  Q4_K threads always own one unit pair (two units sharing a code load) and
+// one column: with 17 warps a thread has at most 96 registers (a quarter of the SM's
+// register file serves up to five warps), and a second column of x spills.
+__host__ __device__ constexpr bool stream_quant(int wt) { return wt == 2 || wt == 3 || wt == 4; }
 __host__ __device__ constexpr int stream_nct(int wt, int nc) {
-  return stream_quant(wt) ? (nc <= 4 ? nc : 4) : (nc <= 2 ? nc : 2);
+  return wt == 4 ? 1 : stream_quant(wt) ? (nc <= 4 ? nc : 4) : (nc <= 2 ? nc : 2);
 }
 __host__ __device__ constexpr int stream_cs(int wt, int nc) {
   return (nc + stream_nct(wt, nc) - 1) / stream_nct(wt, nc);
 }
-__host__ __device__ constexpr int stream_u(int wt, int nc) { return (nc == 1 && stream_quant(wt)) ? 2 : 1; }
+__host__ __device__ constexpr int stream_u(int wt, int nc) {
+  return wt == 4 ? 2 : (nc == 1 && stream_quant(wt)) ? 2 : 1;
+}
 __host__ __device__ constexpr int stream_rt(int wt, int nc) { return (nc == 1 && wt == 2) ? 2 : 4; }
 __host__ __device__ constexpr int stream_max_cw(int wt, int nc) { return stream_nct(wt, nc) <= 2 ? 16 : 8; }
 __host__ __device__ constexpr int stream_threads(int wt, int nc) { return 32 * (1 + stream_max_cw(wt, nc)); }
@@ -124,9 +128,13 @@ int launch_stream_float_split(int wtype, int ncols, const Plan& p, cudaStream_t 
 int launch_stream_block_plain(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);  // Q8_0, Q4_0
 int launch_stream_block_ext(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);
 int launch_stream_block_split(int wtype, int ncols, const Plan& p, cudaStream_t st, bool pdl);
+int launch_stream_q4k_plain(int ncols, const Plan& p, cudaStream_t st, bool pdl);              // Q4_K
+int launch_stream_q4k_ext(int ncols, const Plan& p, cudaStream_t st, bool pdl);
+int launch_stream_q4k_split(int ncols, const Plan& p, cudaStream_t st, bool pdl);
 // Resident clusters of the split-K kernel for this plan (0 if unknown, e.g. no device).
 int stream_split_max_clusters_float(int wtype, int ncols, const Plan& p);
 int stream_split_max_clusters_block(int wtype, int ncols, const Plan& p);
+int stream_split_max_clusters_q4k(int ncols, const Plan& p);
 int launch_generic(int wtype, int ncols, const GenericArgs& a, int grid, int smem,
                    cudaStream_t st, bool pdl);
 int launch_fwht(const float* x, const float* signs, float* dst, int64_t n, int B, int nsigns,

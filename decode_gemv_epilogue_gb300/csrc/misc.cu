@@ -101,6 +101,34 @@ __global__ void dequantize_units_kernel(const uint8_t* W, int64_t M, int64_t K, 
   }
 }
 
+// Q4_K: one thread per unit pair, through the stream kernel's pair decoder; each value
+// d*sc*q - dmin*m with one rounding (d*sc*q and dmin*m are exact in fp32).
+__global__ void dequantize_q4k_pairs_kernel(const uint8_t* W, int64_t M, int64_t K, int64_t row_bytes,
+                                            float* out) {
+  const int64_t pairs_per_row = K / (2 * kUnitElems);
+  const int64_t total = M * pairs_per_row;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total; t += stride) {
+    const int64_t row = t / pairs_per_row;
+    const uint32_t p = static_cast<uint32_t>(t - row * pairs_per_row);
+    const GmemLoader ld{W + row * row_bytes};
+    float2 v[2][8];
+    float dsc[2], dmn[2];
+    const uint4 q = q4k_load_pair(ld, p, dsc, dmn);
+    q4k_nibbles(q, 0, v[0]);
+    q4k_nibbles(q, 1, v[1]);
+    float* o = out + row * K;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t e = unit_pair_elem<WT_Q4_K>(2 * p + n, k);
+        o[e] = fmaf(dsc[n], v[n][k].x, -dmn[n]);
+        o[e + 1] = fmaf(dsc[n], v[n][k].y, -dmn[n]);
+      }
+  }
+}
+
 // Element-wise decode for F32/F16 rows whose K is not a multiple of 8.
 template <int WT>
 __global__ void dequantize_elems_kernel(const uint8_t* W, int64_t M, int64_t K, int64_t row_bytes,
@@ -134,6 +162,7 @@ int launch_dequantize(int wtype, const uint8_t* W, int64_t M, int64_t K, int64_t
       break;
     case WT_Q8_0: dequantize_units_kernel<WT_Q8_0><<<g, 256, 0, st>>>(W, M, K, row_bytes, out); break;
     case WT_Q4_0: dequantize_units_kernel<WT_Q4_0><<<g, 256, 0, st>>>(W, M, K, row_bytes, out); break;
+    case WT_Q4_K: dequantize_q4k_pairs_kernel<<<g, 256, 0, st>>>(W, M, K, row_bytes, out); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

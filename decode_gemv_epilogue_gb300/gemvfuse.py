@@ -17,7 +17,7 @@ if not os.path.exists(LIB_PATH):
 _lib = ctypes.CDLL(LIB_PATH)
 
 # enums (include/gemvfuse.h)
-F32, F16, Q8_0, Q4_0 = 0, 1, 2, 3
+F32, F16, Q8_0, Q4_0, Q4_K = 0, 1, 2, 3, 4
 EPI_NONE, EPI_SIGMOID, EPI_SILU, EPI_SILU_MUL, EPI_ADD = 0, 1, 2, 3, 4
 EW_SIGMOID, EW_SILU, EW_MUL, EW_ADD = 1, 2, 3, 4
 OK, ERR_INVALID, ERR_ALIAS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6

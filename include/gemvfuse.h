@@ -52,8 +52,15 @@ extern "C" {
  *  GF_Q8_0 : per 32 elements a 34-byte block {binary16 d; int8 q[32]}; w = d*q.
  *  GF_Q4_0 : per 32 elements an 18-byte block {binary16 d; uint8 qs[16]}; byte j holds
  *            element j (low nibble) and element j+16 (high nibble); w = d*(nibble-8).
+ *  GF_Q4_K : per 256 elements a 144-byte super-block {binary16 d; binary16 dmin;
+ *            uint8 scales[12]; uint8 qs[128]}: eight 32-element sub-blocks j with 6-bit
+ *            scale sc[j] and min m[j] (scales[j] low 6 bits = sc[j], scales[j+4] low 6
+ *            bits = m[j] for j < 4; for j >= 4 the low 4 bits are the low/high nibble of
+ *            scales[j+4] and the top 2 bits those of scales[j-4] / scales[j]); qs holds
+ *            four 32-byte groups, group g sub-block 2g in the low nibbles and 2g+1 in the
+ *            high nibbles; w = d*sc[j]*q - dmin*m[j].  K % 256 == 0.
  * (Format names from [CPU] Correctness; the layouts are the ggml block convention.) */
-typedef enum { GF_F32 = 0, GF_F16 = 1, GF_Q8_0 = 2, GF_Q4_0 = 3 } gf_wtype;
+typedef enum { GF_F32 = 0, GF_F16 = 1, GF_Q8_0 = 2, GF_Q4_0 = 3, GF_Q4_K = 4 } gf_wtype;
 
 /* Fused tails ([EPI] What changed; [CPU] What):
  *  NONE      dst = y

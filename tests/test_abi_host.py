@@ -260,3 +260,19 @@ def test_split_k_with_glu_and_prologues(lib):
     # a batch multiplies the x bytes each CTA streams
     _, info = lib.plan(W, 3, X, 32, 8192, 0, None, D, ncols=4)
     assert info["split"] == 4
+
+
+# ----------------------------------------------------------------------------- Q4_K
+
+def test_q4_k_validation_and_plan(lib):
+    assert lib.Q4_K == 4
+    assert g(lib, W, lib.Q4_K, X, 16, 4096 + 32, 0, None, D) == -3     # K % 256
+    assert g(lib, W, 5, X, 16, 4096, 0, None, D) == -1                  # past the last format
+    path, info = lib.plan(W, lib.Q4_K, X, 4096, 4096, 0, None, D)
+    assert path == lib.PATH_STREAM and info["k_chunk"] == 4096
+    path, _ = lib.plan(W + 2, lib.Q4_K, X, 4096, 4096, 0, None, D)
+    assert path == lib.PATH_GENERIC                                     # rows not 16-byte aligned
+    path, info = lib.plan(W, lib.Q4_K, X, 4096, 14336, 4, A, A, ncols=8)
+    assert path == lib.PATH_STREAM and info["k_chunk"] % 256 == 0
+    assert lib.dequantize(W, lib.Q4_K, 4, 300, D, stream=0, check=False) == -3
+    assert lib.dequantize(W, 6, 4, 256, D, stream=0, check=False) == -1
