@@ -117,7 +117,7 @@ static int validate(const Call& c) {
   }
   if (c.M < 0 || c.K < 0) return GF_ERR_INVALID;
   if (c.M > INT32_MAX || c.K > INT32_MAX / 8) return GF_ERR_UNSUPPORTED;
-  if (c.ncols < 1 || c.ncols > kMaxCols) return c.ncols < 1 ? GF_ERR_INVALID : GF_ERR_UNSUPPORTED;
+  if (c.ncols < 1 || c.ncols > kMaxBatch) return c.ncols < 1 ? GF_ERR_INVALID : GF_ERR_UNSUPPORTED;
   if ((c.wtype == GF_Q8_0 || c.wtype == GF_Q4_0) && c.K % 32 != 0) return GF_ERR_UNSUPPORTED;
   if (c.wtype == GF_Q4_K && c.K % 256 != 0) return GF_ERR_UNSUPPORTED;
   const bool need_aux = (c.epi == GF_EPI_SILU_MUL || c.epi == GF_EPI_ADD);
@@ -320,7 +320,27 @@ static int plan_call(const Call& c, Plan& p, int* generic_smem, int* generic_gri
   return PATH_GENERIC;
 }
 
+static int launch_one(const Call& c, float* dst, cudaStream_t st);
+
+// A batch wider than one launch takes runs column blocks of kMaxCols in consecutive
+// launches (each streams W again).  Later blocks may start early (programmatic
+// dependent launch): they read and write only their own columns.
 static int launch_call(const Call& c, float* dst, cudaStream_t st) {
+  if (c.ncols <= kMaxCols) return launch_one(c, dst, st);
+  for (int64_t c0 = 0; c0 < c.ncols; c0 += kMaxCols) {
+    Call b = c;
+    b.ncols = std::min<int64_t>(kMaxCols, c.ncols - c0);
+    b.x = c.x + c0 * c.K;
+    b.aux = c.aux ? c.aux + c0 * c.M : nullptr;
+    b.dst = dst + c0 * c.M;
+    if (c0 > 0) b.flags |= GF_FLAG_PDL;
+    const int e = launch_one(b, dst + c0 * c.M, st);
+    if (e != GF_OK) return e;
+  }
+  return GF_OK;
+}
+
+static int launch_one(const Call& c, float* dst, cudaStream_t st) {
   Plan p;
   int gsmem = 0, ggrid = 0;
   const int path = plan_call(c, p, &gsmem, &ggrid);
@@ -496,6 +516,7 @@ static int plan_info(const Call& c, const gf_opts* opts, int64_t info[8]) {
     pc.x = pc.workspace;
     pc.signs = nullptr;
   }
+  pc.ncols = std::min<int64_t>(pc.ncols, kMaxCols);  // wider batches: each block's launch
   Plan p;
   int gsmem = 0, ggrid = 0;
   const int path = plan_call(pc, p, &gsmem, &ggrid);

@@ -7,7 +7,8 @@
 namespace gf {
 
 // Kernel-side limits of the TMA-streamed GEMV.
-constexpr int kMaxCols = 8;
+constexpr int kMaxCols = 8;      // columns per GEMV launch
+constexpr int kMaxBatch = 256;   // columns per call (wider batches run in blocks of kMaxCols)
 constexpr int kMaxStages = 8;
 constexpr int kBarBytes = 256;              // mbarrier area at the start of shared memory
 constexpr int kXsMaxBytes = 64 * 1024;      // x chunk (all columns) kept in shared memory

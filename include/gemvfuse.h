@@ -80,7 +80,7 @@ typedef enum {
   GF_ERR_INVALID = -1,      /* bad enum, size, null pointer or view shape            */
   GF_ERR_ALIAS = -2,        /* dst overlaps an input it may not alias                */
   GF_ERR_UNSUPPORTED = -3,  /* valid but outside what is implemented (e.g. K%32 != 0 */
-                            /* for a block format, ncols > 8, FWHT block > 8192)     */
+                            /* for a block format, ncols > 256, FWHT block > 8192)   */
   GF_ERR_ALIGN = -4,        /* pointer not aligned to its element type               */
   GF_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed                  */
   GF_ERR_TIMEOUT = -6       /* a kernel gave up on a bounded wait (device status)    */
@@ -99,7 +99,8 @@ typedef enum {
                             summation order, hence the rounding, differs). */
 
 typedef struct {
-  int64_t ncols;             /* columns in the batch, 1..8 (0 is read as 1)            */
+  int64_t ncols;             /* columns in the batch, 1..256 (0 is read as 1); up to 8 */
+                             /* share one pass over W, wider batches run as blocks of 8 */
   const float* fwht_signs;   /* non-NULL: signed-FWHT prologue on every column of x     */
   int64_t fwht_block;        /* FWHT block B: power of two, 1..8192, K % B == 0         */
   int64_t nsigns;            /* length of fwht_signs; K % nsigns == 0; element k of a   */

@@ -62,7 +62,7 @@ def g(lib, *a, **k):
     ((W, 0, X, -1, 32, 0, None, D), {}, -1),                    # negative M
     ((W, 2, X, 16, 48, 0, None, D), {}, -3),                    # Q8_0 with K % 32 != 0
     ((W, 3, X, 16, 33, 0, None, D), {}, -3),                    # Q4_0 with K % 32 != 0
-    ((W, 1, X, 16, 32, 0, None, D), {"ncols": 9}, -3),          # more than 8 columns
+    ((W, 1, X, 16, 32, 0, None, D), {"ncols": 257}, -3),        # more than 256 columns
     ((W, 1, X, 16, 32, 0, None, D), {"ncols": -1}, -1),
     ((W, 1, X, 16, 32, 0, None, None), {}, -1),                 # null dst
     ((W, 1, X, 16, 32, 4, None, D), {}, -1),                    # ADD without operand
@@ -191,7 +191,7 @@ def glu(lib, *a, **k):
     ((W, U2, 1, X, 16, 32, W + 64), {}, -2),                   # dst inside the gate matrix
     ((W, U2, 1, X, 16, 32, X), {}, -2),                        # dst over x
     ((W, U2, 7, X, 16, 32, D), {}, -1),                        # bad weight type
-    ((W, U2, 1, X, 16, 32, D), {"ncols": 9}, -3),
+    ((W, U2, 1, X, 16, 32, D), {"ncols": 300}, -3),
     ((W, U2, 1, X, 16, 32, D), {"rms_norm_weight": GAM, "fwht_signs": S, "fwht_block": 32}, -3),
 ])
 def test_glu_validation(lib, args, kw, expect):
@@ -276,3 +276,11 @@ def test_q4_k_validation_and_plan(lib):
     assert path == lib.PATH_STREAM and info["k_chunk"] % 256 == 0
     assert lib.dequantize(W, lib.Q4_K, 4, 300, D, stream=0, check=False) == -3
     assert lib.dequantize(W, 6, 4, 256, D, stream=0, check=False) == -1
+
+
+def test_wide_batch_validation_covers_every_column(lib):
+    # 20 columns: dst overlapping x anywhere in the whole batch is refused
+    assert g(lib, W, 1, X, 16, 32, 0, None, X + 19 * 32 * 4, ncols=20) == -2
+    path, info = lib.plan(W, 1, X, 4096, 4096, 4, A, A, ncols=20)
+    path8, info8 = lib.plan(W, 1, X, 4096, 4096, 4, A, A, ncols=8)
+    assert path == path8 == lib.PATH_STREAM and info == info8  # each block's launch

@@ -297,3 +297,44 @@ def test_split_k_deterministic(G):
         torch.cuda.synchronize()
         outs.append(d.cpu().numpy())
     assert all(np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)) for o in outs[1:])
+
+
+# ----------------------------------------------------------------------------- batches wider than 8
+
+@pytest.mark.parametrize("wt,ncols", [(synth.F16, 9), (synth.Q4_0, 16), (synth.Q8_0, 33), (synth.Q4_K, 12)])
+def test_wide_batch_add_in_place(G, wt, ncols):
+    M, K = 300, 2048
+    raw = synth.weights(wt, M, K, seed=600 + ncols)
+    X = synth.normal(ncols * K, seed=601).reshape(ncols, K)
+    aux = synth.normal(ncols * M, seed=602).reshape(ncols, M)
+    Wd, xd, r = dev_tensor(raw), dev_tensor(X.reshape(-1)), dev_tensor(aux.reshape(-1))
+    G.gemv_fused_ex(Wd, wt, xd, M, K, ogemv.EPI_ADD, r, r, ncols=ncols, pdl=True)
+    torch.cuda.synchronize()
+    want = ogemv.gemv(raw, wt, X, M, K, ogemv.EPI_ADD, aux)
+    assert_within(_cpu(r, ncols, M), want, gemv_bound(raw, wt, X, M, K), "wide batch %d" % ncols)
+
+
+def test_wide_batch_fwht_workspace_and_glu_rms(G):
+    wt, M, K, B, ncols = synth.F16, 256, 5120, 1024, 20
+    raw = synth.weights(wt, M, K, seed=610)
+    X = synth.normal(ncols * K, seed=611).reshape(ncols, K)
+    s = synth.rademacher(B, seed=612)
+    xd, sd = dev_tensor(X.reshape(-1)), dev_tensor(s)
+    ws = torch.empty(ncols * K, device="cuda")
+    dst = _nan_out(ncols * M)
+    G.gemv_fused_ex(dev_tensor(raw), wt, xd, M, K, ogemv.EPI_SIGMOID, None, dst, ncols=ncols, fwht_signs=sd,
+                    fwht_block=B, fwht_workspace=ws)
+    torch.cuda.synchronize()
+    Xp = np.stack([ofwht.fwht_signed(X[c], s, B) for c in range(ncols)])
+    E = np.stack([fwht_err_bound(X[c], B) for c in range(ncols)])
+    want = ogemv.gemv(raw, wt, Xp, M, K, ogemv.EPI_SIGMOID)
+    assert_within(_cpu(dst, ncols, M), want, gemv_bound(raw, wt, Xp, M, K, x_err=E), "wide fwht ws")
+    # gated dual GEMV with the RMS prologue over 11 columns
+    rg, ru = synth.weights(synth.Q4_0, M, 4096, seed=613), synth.weights(synth.Q4_0, M, 4096, seed=614)
+    X2 = synth.normal(11 * 4096, seed=615).reshape(11, 4096)
+    gamma = 1.0 + 0.1 * synth.normal(4096, seed=616)
+    got, _, _ = run_glu(G, rg, ru, synth.Q4_0, X2, M, 4096, ncols=11,
+                        rms_norm_weight=dev_tensor(gamma.astype(np.float32)), rms_norm_eps=1e-6)
+    Xn = onorm.rms_norm(X2, gamma, 1e-6, 4096)
+    want = ogemv.gemv_glu(rg, ru, synth.Q4_0, Xn, M, 4096)
+    assert_within(got, want, glu_bound(rg, ru, synth.Q4_0, Xn, M, 4096, extra_rel=TOL_NORM_REL), "wide glu rms")
