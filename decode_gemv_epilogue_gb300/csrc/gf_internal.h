@@ -97,6 +97,39 @@ struct GenericArgs {
   float norm_eps;
 };
 
+struct DeviceLimits;
+
+// Tensor-core GEMV (F16 weights, batches): see gemv_tc.cu.
+struct TcArgs {
+  const float* x;
+  const float* aux;
+  float* dst;
+  unsigned* err;
+  int64_t M;
+  int K;
+  int epi;
+  int ncols;          // columns of this launch (<= kTcMaxCols)
+  int Np;             // columns rounded up to 8: B holds Np rows of hi, then Np of lo
+  int S;              // CTAs per cluster splitting K (1: none)
+  int nst;            // 64-element K stages of a row
+  int NS;             // pipeline stages
+  int tmem_cols;      // tensor-memory columns allocated (power of two >= 2 Np, >= 32)
+  int off_a, off_b;   // stage offsets from the 1024-aligned shared-memory base
+  int b_stage_bytes;  // 2 Np rows of 128 bytes
+};
+
+struct TcPlan {
+  int grid, smem;
+  TcArgs a;
+};
+
+constexpr int kTcMaxCols = 16;  // columns per tensor-core launch (one B chunk per converter thread)
+
+// Shapes only (pointers are filled by the caller); false if the kernel cannot take them.
+bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, TcPlan& p);
+// Encodes the tensor map of W ([M][K] f16, row stride 2K) and launches.
+int launch_tc(const TcPlan& p, const void* W, cudaStream_t st, bool pdl);
+
 // Generic kernel: 256 threads; shared memory x [ncols][K], 1/rms [ncols], warp
 // partials [8][ncols].
 constexpr int kGenericWarps = 8;
@@ -104,7 +137,7 @@ __host__ __device__ constexpr int64_t generic_smem_floats(int64_t ncols, int64_t
   return ncols * K + ncols + kGenericWarps * ncols;
 }
 
-enum { PATH_STREAM = 1, PATH_GENERIC = 2 };
+enum { PATH_STREAM = 1, PATH_GENERIC = 2, PATH_TC = 3 };
 
 struct Plan {
   int path;

@@ -21,8 +21,8 @@ F32, F16, Q8_0, Q4_0, Q4_K = 0, 1, 2, 3, 4
 EPI_NONE, EPI_SIGMOID, EPI_SILU, EPI_SILU_MUL, EPI_ADD = 0, 1, 2, 3, 4
 EW_SIGMOID, EW_SILU, EW_MUL, EW_ADD = 1, 2, 3, 4
 OK, ERR_INVALID, ERR_ALIAS, ERR_UNSUPPORTED, ERR_ALIGN, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
-FLAG_PDL, FLAG_NO_SPLIT_K = 1, 2
-PATH_NONE, PATH_STREAM, PATH_GENERIC = 0, 1, 2
+FLAG_PDL, FLAG_NO_SPLIT_K, FLAG_NO_TENSOR_CORES = 1, 2, 4
+PATH_NONE, PATH_STREAM, PATH_GENERIC, PATH_TC = 0, 1, 2, 3
 
 _vp, _i64, _i32, _u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
 
@@ -103,7 +103,7 @@ def _check(st, what):
 
 
 def make_opts(ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, view=None, pdl=False, fwht_workspace=None,
-              rms_norm_weight=None, rms_norm_eps=0.0, split_k=True):
+              rms_norm_weight=None, rms_norm_eps=0.0, split_k=True, tensor_cores=True):
     o = GfOpts()
     o.ncols = ncols
     o.fwht_signs = _ptr(fwht_signs)
@@ -115,7 +115,8 @@ def make_opts(ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, view=None, pd
     v = list(view or ())
     for i in range(4):
         o.view_ne[i] = v[i] if i < len(v) else 0
-    o.flags = (FLAG_PDL if pdl else 0) | (0 if split_k else FLAG_NO_SPLIT_K)
+    o.flags = (FLAG_PDL if pdl else 0) | (0 if split_k else FLAG_NO_SPLIT_K) | \
+        (0 if tensor_cores else FLAG_NO_TENSOR_CORES)
     o.fwht_workspace = _ptr(fwht_workspace)
     o.rms_norm_weight = _ptr(rms_norm_weight)
     o.rms_norm_eps = rms_norm_eps
@@ -131,9 +132,9 @@ def gemv_fused(W, wtype, x, M, K, epilogue, aux, dst, stream=None, check=True):
 
 def gemv_fused_ex(W, wtype, x, M, K, epilogue, aux, dst, ncols=1, fwht_signs=None, fwht_block=0,
                   nsigns=None, view=None, pdl=False, fwht_workspace=None, rms_norm_weight=None,
-                  rms_norm_eps=0.0, split_k=True, stream=None, check=True):
+                  rms_norm_eps=0.0, split_k=True, tensor_cores=True, stream=None, check=True):
     o = make_opts(ncols, fwht_signs, fwht_block, nsigns, view, pdl, fwht_workspace, rms_norm_weight,
-                  rms_norm_eps, split_k)
+                  rms_norm_eps, split_k, tensor_cores)
     st = _gemv_fused_ex(_ptr(W), wtype, _ptr(x), M, K, epilogue, _ptr(aux), _ptr(dst),
                         ctypes.byref(o), _stream(stream))
     if check:

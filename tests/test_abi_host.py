@@ -124,6 +124,10 @@ def test_plan_with_fwht_workspace_describes_the_plain_gemv(lib):
     path, info = lib.plan(W, 1, X, 5120, 5120, 4, A, A, ncols=8, fwht_signs=S, fwht_block=1024, nsigns=1024,
                           fwht_workspace=6 << 40)
     path2, info2 = lib.plan(W, 1, 6 << 40, 5120, 5120, 4, A, A, ncols=8)
+    assert path == path2 == lib.PATH_TC and info == info2
+    path, info = lib.plan(W, 1, X, 5120, 5120, 4, A, A, ncols=8, fwht_signs=S, fwht_block=1024, nsigns=1024,
+                          fwht_workspace=6 << 40, tensor_cores=False)
+    path2, info2 = lib.plan(W, 1, 6 << 40, 5120, 5120, 4, A, A, ncols=8, tensor_cores=False)
     assert path == path2 == lib.PATH_STREAM and info == info2
 
 
@@ -281,6 +285,41 @@ def test_q4_k_validation_and_plan(lib):
 def test_wide_batch_validation_covers_every_column(lib):
     # 20 columns: dst overlapping x anywhere in the whole batch is refused
     assert g(lib, W, 1, X, 16, 32, 0, None, X + 19 * 32 * 4, ncols=20) == -2
-    path, info = lib.plan(W, 1, X, 4096, 4096, 4, A, A, ncols=20)
-    path8, info8 = lib.plan(W, 1, X, 4096, 4096, 4, A, A, ncols=8)
+    path, info = lib.plan(W, 3, X, 4096, 4096, 4, A, A, ncols=20)
+    path8, info8 = lib.plan(W, 3, X, 4096, 4096, 4, A, A, ncols=8)
     assert path == path8 == lib.PATH_STREAM and info == info8  # each block's launch
+    # tensor cores: blocks of 16 columns
+    _, i100 = lib.plan(W, 1, X, 4096, 4096, 4, A, A, ncols=100)   # 6 blocks of 16, then 4
+    _, i16 = lib.plan(W, 1, X, 4096, 4096, 4, A, A, ncols=16)
+    assert i100 == i16
+
+
+# ----------------------------------------------------------------------------- tensor-core path
+
+@pytest.mark.parametrize("M,K,ncols,expect_split", [
+    (5120, 5120, 8, 3),     # 40 row tiles: 3 CTAs per tile
+    (4096, 4096, 8, 4),     # 32 tiles
+    (14336, 4096, 16, 1),   # 112 tiles
+    (100, 4096, 4, 8),      # one ragged tile
+    (4096, 64, 8, 1),       # one K stage
+])
+def test_tc_plan(lib, M, K, ncols, expect_split):
+    path, info = lib.plan(W, 1, X, M, K, 0, None, D, ncols=ncols)
+    assert path == lib.PATH_TC and info["split"] == expect_split
+    assert info["grid"] == -(-M // 128) * expect_split and info["grid"] <= 152
+    assert info["smem"] <= 232448 and 2 <= info["stages"] <= 12 and info["threads"] == 192
+
+
+@pytest.mark.parametrize("kw,args", [
+    ({"ncols": 1}, (W, 1, X, 4096, 4096)),                  # one column: CUDA cores
+    ({"ncols": 3}, (W, 1, X, 4096, 4096)),                  # below the tensor-core batch
+    ({"ncols": 8}, (W, 3, X, 4096, 4096)),                  # block formats: CUDA cores
+    ({"ncols": 8}, (W, 1, X, 4096, 4096 + 32)),             # K % 64
+    ({"ncols": 8}, (W + 2, 1, X, 4096, 4096)),              # W not 16-byte aligned
+    ({"ncols": 8, "tensor_cores": False}, (W, 1, X, 4096, 4096)),
+    ({"ncols": 8, "fwht_signs": S, "fwht_block": 1024, "nsigns": 1024}, (W, 1, X, 4096, 4096)),  # on-chip prologue
+    ({"ncols": 8, "rms_norm_weight": 8 << 40}, (W, 1, X, 4096, 4096)),
+])
+def test_tc_not_chosen(lib, kw, args):
+    path, _ = lib.plan(*args, 0, None, D, **kw)
+    assert path in (lib.PATH_STREAM, lib.PATH_GENERIC)

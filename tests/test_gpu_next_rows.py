@@ -104,8 +104,9 @@ def test_glu_equals_unfused_bitwise(G, wt, ncols):
     Gd, Ud = dev_tensor(rg), dev_tensor(ru)
     xd = dev_tensor(X.astype(np.float32).reshape(-1))
     u, g = _nan_out(ncols * M), _nan_out(ncols * M)
-    G.gemv_fused_ex(Ud, wt, xd, M, K, ogemv.EPI_NONE, None, u, ncols=ncols)
-    G.gemv_fused_ex(Gd, wt, xd, M, K, ogemv.EPI_SILU_MUL, u, g, ncols=ncols)
+    # the plain kernels the dual one is built from (not the tensor-core path)
+    G.gemv_fused_ex(Ud, wt, xd, M, K, ogemv.EPI_NONE, None, u, ncols=ncols, tensor_cores=False)
+    G.gemv_fused_ex(Gd, wt, xd, M, K, ogemv.EPI_SILU_MUL, u, g, ncols=ncols, tensor_cores=False)
     torch.cuda.synchronize()
     assert np.array_equal(got.astype(np.float32), _cpu(g, ncols, M).astype(np.float32))
 

@@ -31,7 +31,7 @@ def G(lib):
 
 
 def run_gemv(G, raw, wt, x, M, K, epi, aux=None, ncols=1, signs=None, block=0, view=None,
-             w_offset=0, pdl=False):
+             w_offset=0, pdl=False, tensor_cores=True):
     """Upload, call gemv_fused_ex, return dst as float64 [ncols, M] and the plan path."""
     if w_offset:
         buf = torch.zeros(raw.size + 64, dtype=torch.uint8, device="cuda")
@@ -46,9 +46,10 @@ def run_gemv(G, raw, wt, x, M, K, epi, aux=None, ncols=1, signs=None, block=0, v
     else:
         dst = torch.full((ncols * M,), float("nan"), device="cuda")
     sd = dev_tensor(signs) if signs is not None else None
-    path, _ = G.plan(Wd, wt, xd, M, K, epi, auxd, dst, ncols=ncols, fwht_signs=sd, fwht_block=block)
+    path, _ = G.plan(Wd, wt, xd, M, K, epi, auxd, dst, ncols=ncols, fwht_signs=sd, fwht_block=block,
+                     tensor_cores=tensor_cores)
     G.gemv_fused_ex(Wd, wt, xd, M, K, epi, auxd if epi in ogemv.NEEDS_AUX else None, dst,
-                    ncols=ncols, fwht_signs=sd, fwht_block=block, view=view, pdl=pdl)
+                    ncols=ncols, fwht_signs=sd, fwht_block=block, view=view, pdl=pdl, tensor_cores=tensor_cores)
     torch.cuda.synchronize()
     return dst.cpu().numpy().astype(np.float64).reshape(ncols, M), path
 
@@ -178,10 +179,11 @@ def test_ncols_batch(G, ncols, wt):
     raw = synth.weights(wt, M, K, seed=50)
     X = synth.normal(ncols * K, seed=51).reshape(ncols, K)
     aux = synth.normal(ncols * M, seed=52).reshape(ncols, M)
-    got, path = run_gemv(G, raw, wt, X, M, K, ogemv.EPI_SILU_MUL, aux, ncols=ncols)
-    assert path == G.PATH_STREAM
     want = ogemv.gemv(raw, wt, X, M, K, ogemv.EPI_SILU_MUL, aux)
-    assert_within(got, want, gemv_bound(raw, wt, X, M, K), "ncols %d" % ncols)
+    for tc in (True, False):  # F16 batches default to the tensor cores
+        got, path = run_gemv(G, raw, wt, X, M, K, ogemv.EPI_SILU_MUL, aux, ncols=ncols, tensor_cores=tc)
+        assert path == (G.PATH_TC if tc and wt == synth.F16 and ncols >= 4 else G.PATH_STREAM)
+        assert_within(got, want, gemv_bound(raw, wt, X, M, K), "ncols %d tc %s" % (ncols, tc))
 
 
 # ----------------------------------------------------------------------------- signed FWHT
@@ -237,8 +239,9 @@ def test_fused_fwht_prologue(G, ncols):
 @pytest.mark.parametrize("ncols", [1, 3, 8])
 def test_fwht_workspace_path_matches_on_chip_prologue(G, ncols):
     """The transform-once path (stand-alone signed FWHT into a workspace, then the GEMV,
-    chained with programmatic dependent launch) gives the same x' and therefore the same
-    outputs as the on-chip prologue, bit for bit, and passes the oracle bound."""
+    chained with programmatic dependent launch) gives the same x' and therefore, on the
+    same CUDA-core kernel, the same outputs as the on-chip prologue, bit for bit; with
+    the tensor cores (batches) it passes the oracle bound."""
     M, K, B = 700, 5120, 1024
     raw = synth.weights(synth.F16, M, K, seed=90)
     X = synth.normal(ncols * K, seed=91).reshape(ncols, K)
@@ -249,7 +252,10 @@ def test_fwht_workspace_path_matches_on_chip_prologue(G, ncols):
     d_chip = dev_tensor(r.reshape(-1))
     d_ws = dev_tensor(r.reshape(-1))
     G.gemv_fused_ex(Wd, synth.F16, xd, M, K, ogemv.EPI_ADD, d_chip, d_chip, ncols=ncols, fwht_signs=sd, fwht_block=B)
+    d_tc = dev_tensor(r.reshape(-1))
     G.gemv_fused_ex(Wd, synth.F16, xd, M, K, ogemv.EPI_ADD, d_ws, d_ws, ncols=ncols, fwht_signs=sd, fwht_block=B,
+                    fwht_workspace=ws, tensor_cores=False)
+    G.gemv_fused_ex(Wd, synth.F16, xd, M, K, ogemv.EPI_ADD, d_tc, d_tc, ncols=ncols, fwht_signs=sd, fwht_block=B,
                     fwht_workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(d_chip.view(torch.int32), d_ws.view(torch.int32))
@@ -257,8 +263,9 @@ def test_fwht_workspace_path_matches_on_chip_prologue(G, ncols):
     E = np.stack([fwht_err_bound(X[c], B) for c in range(ncols)])
     assert_within(ws.cpu().numpy().reshape(ncols, K), Xp, E, "workspace x'")
     want = ogemv.gemv(raw, synth.F16, Xp, M, K, ogemv.EPI_ADD, r)
-    got = d_ws.cpu().numpy().astype(np.float64).reshape(ncols, M)
-    assert_within(got, want, gemv_bound(raw, synth.F16, Xp, M, K, x_err=E), "workspace path ncols %d" % ncols)
+    for d, what in ((d_ws, "workspace path"), (d_tc, "workspace path, default kernel")):
+        got = d.cpu().numpy().astype(np.float64).reshape(ncols, M)
+        assert_within(got, want, gemv_bound(raw, synth.F16, Xp, M, K, x_err=E), "%s ncols %d" % (what, ncols))
 
 
 @pytest.mark.parametrize("wt,block,nsigns", [(synth.Q4_0, 256, 256), (synth.F32, 64, 32), (synth.F16, 8192, 8192),

@@ -1,0 +1,132 @@
+"""GPU parity of the tensor-core GEMV (F16 weights, batches of 2..16 columns per launch)
+through the C ABI against the fp64 oracle, within 2e-5 * sum_k |W_ik x_k| + 1e-6: x
+enters as scaled f16 hi + lo parts (about 2^-22 relative), f16 products are exact and
+the accumulation is fp32.  Covers ragged tiles, split K, every tail, wide dynamic
+ranges of x (the per-column power-of-two scale), determinism, the transform-once
+prologue and agreement with the CUDA-core kernels."""
+
+import numpy as np
+import pytest
+
+from decode_gemv_epilogue_gb300 import synth
+from gpu_util import assert_within, dev_tensor, fwht_err_bound, gemv_bound
+from oracle import fwht as ofwht
+from oracle import gemv as ogemv
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+F16 = synth.F16
+EPIS = [ogemv.EPI_NONE, ogemv.EPI_SIGMOID, ogemv.EPI_SILU, ogemv.EPI_SILU_MUL, ogemv.EPI_ADD]
+
+
+@pytest.fixture(scope="module")
+def G(lib):
+    assert lib.device_status(reset=True) == 0
+    yield lib
+    assert lib.device_status() == 0, "a kernel reported a bounded-wait timeout"
+
+
+def run(G, raw, X, M, K, epi, aux=None, expect_path=None, **kw):
+    ncols = X.shape[0]
+    Wd = dev_tensor(raw)
+    xd = dev_tensor(X.astype(np.float32).reshape(-1))
+    auxd = dev_tensor(aux.astype(np.float32).reshape(-1)) if aux is not None else None
+    dst = auxd if epi == ogemv.EPI_ADD else torch.full((ncols * M,), float("nan"), device="cuda")
+    path, info = G.plan(Wd, F16, xd, M, K, epi, auxd, dst, ncols=ncols, **kw)
+    if expect_path is not None:
+        assert path == expect_path, (path, info)
+    G.gemv_fused_ex(Wd, F16, xd, M, K, epi, auxd if epi in ogemv.NEEDS_AUX else None, dst, ncols=ncols, **kw)
+    torch.cuda.synchronize()
+    return dst.cpu().numpy().astype(np.float64).reshape(ncols, M), info
+
+
+@pytest.mark.parametrize("M,K,ncols", [(128, 64, 4), (100, 4096, 8), (333, 1024, 5), (1000, 2048, 16),
+                                       (4096, 512, 8), (640, 8192, 64), (257, 4096, 36)])
+def test_tc_shapes(G, M, K, ncols):
+    raw = synth.weights(F16, M, K, seed=700 + ncols)
+    X = synth.normal(ncols * K, seed=701).reshape(ncols, K)
+    got, info = run(G, raw, X, M, K, ogemv.EPI_NONE, expect_path=G.PATH_TC)
+    want = ogemv.gemv(raw, F16, X, M, K)
+    assert_within(got, want, gemv_bound(raw, F16, X, M, K), "tc %dx%d n%d split %d" % (M, K, ncols, info["split"]))
+
+
+@pytest.mark.parametrize("epi", EPIS)
+def test_tc_tails(G, epi):
+    M, K, ncols = 700, 2048, 8
+    raw = synth.weights(F16, M, K, seed=710)
+    X = synth.normal(ncols * K, seed=711).reshape(ncols, K)
+    aux = synth.normal(ncols * M, seed=712).reshape(ncols, M)
+    got, _ = run(G, raw, X, M, K, epi, aux, expect_path=G.PATH_TC, view=(7, 100) if epi == ogemv.EPI_ADD else None)
+    want = ogemv.gemv(raw, F16, X, M, K, epi, aux)
+    assert_within(got, want, gemv_bound(raw, F16, X, M, K), "tc tail %d" % epi)
+
+
+def test_tc_dynamic_range_of_x(G):
+    # per column: all zero, huge, tiny, mixed magnitudes, a single spike
+    M, K, ncols = 384, 4096, 6
+    raw = synth.weights(F16, M, K, seed=720)
+    base = synth.normal(ncols * K, seed=721).reshape(ncols, K)
+    X = np.zeros((ncols, K))
+    X[1] = base[1] * 3.0e4
+    X[2] = base[2] * 1.0e-20
+    X[3] = base[3] * np.where(np.arange(K) % 7 == 0, 1e3, 1e-3)
+    X[4, 1234] = 77.0
+    X[5] = base[5]
+    got, _ = run(G, raw, X, M, K, ogemv.EPI_NONE, expect_path=G.PATH_TC)
+    want = ogemv.gemv(raw, F16, X, M, K)
+    assert_within(got, want, gemv_bound(raw, F16, X, M, K), "tc dynamic range")
+    assert np.all(got[0] == 0.0)
+
+
+def test_tc_split_matches_unsplit_and_cuda_cores(G):
+    M, K, ncols = 512, 8192, 8
+    raw = synth.weights(F16, M, K, seed=730)
+    X = synth.normal(ncols * K, seed=731).reshape(ncols, K)
+    want = ogemv.gemv(raw, F16, X, M, K)
+    bound = gemv_bound(raw, F16, X, M, K)
+    got_split, info = run(G, raw, X, M, K, ogemv.EPI_NONE, expect_path=G.PATH_TC)
+    assert info["split"] > 1
+    got_one, info1 = run(G, raw, X, M, K, ogemv.EPI_NONE, expect_path=G.PATH_TC, split_k=False)
+    got_cc, _ = run(G, raw, X, M, K, ogemv.EPI_NONE, expect_path=G.PATH_STREAM, tensor_cores=False)
+    for got, what in ((got_split, "split"), (got_one, "one CTA per tile"), (got_cc, "cuda cores")):
+        assert_within(got, want, bound, what)
+
+
+def test_tc_deterministic(G):
+    M, K, ncols = 5120, 5120, 8
+    raw = synth.weights(F16, M, K, seed=740)
+    X = synth.normal(ncols * K, seed=741).reshape(ncols, K)
+    a, _ = run(G, raw, X, M, K, ogemv.EPI_NONE, expect_path=G.PATH_TC, pdl=True)
+    b, _ = run(G, raw, X, M, K, ogemv.EPI_NONE, expect_path=G.PATH_TC)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("ncols", [4, 8])
+def test_tc_full_fwht_f16_5120_workspace(G, ncols):
+    M, K, B = 5120, 5120, 1024
+    raw = synth.weights(F16, M, K, seed=750)
+    X = synth.normal(ncols * K, seed=751).reshape(ncols, K)
+    r = synth.normal(ncols * M, seed=752).reshape(ncols, M)
+    s = synth.rademacher(B, seed=753)
+    ws = torch.empty(ncols * K, device="cuda")
+    got, _ = run(G, raw, X, M, K, ogemv.EPI_ADD, r, expect_path=G.PATH_TC, fwht_signs=dev_tensor(s), fwht_block=B,
+                 fwht_workspace=ws, pdl=True)
+    rows = np.unique(np.concatenate([np.random.default_rng(754).choice(M, 400, replace=False), [0, M - 1]]))
+    Xp = np.stack([ofwht.fwht_signed(X[c], s, B) for c in range(ncols)])
+    E = np.stack([fwht_err_bound(X[c], B) for c in range(ncols)])
+    want = ogemv.gemv(raw, F16, Xp, M, K, ogemv.EPI_ADD, r, rows=rows)
+    assert_within(got[:, rows], want, gemv_bound(raw, F16, Xp, M, K, rows=rows, x_err=E), "tc fwht ws")
+
+
+def test_tc_wide_batch_blocks_of_16(G):
+    M, K, ncols = 256, 1024, 100
+    raw = synth.weights(F16, M, K, seed=760)
+    X = synth.normal(ncols * K, seed=761).reshape(ncols, K)
+    aux = synth.normal(ncols * M, seed=762).reshape(ncols, M)
+    got, _ = run(G, raw, X, M, K, ogemv.EPI_SILU_MUL, aux, expect_path=G.PATH_TC)
+    want = ogemv.gemv(raw, F16, X, M, K, ogemv.EPI_SILU_MUL, aux)
+    assert_within(got, want, gemv_bound(raw, F16, X, M, K), "tc 100 columns")
