@@ -135,11 +135,12 @@ class Step:
         for (n, wt, M, K, e, nc, fw) in spec:
             x_any = self.fx8 if nc > 1 else (self.fx1 if K == 5120 else self.cg if K == 14336 else self.cx)
             aux_any = self.fr8 if nc > 1 else self.gate_out
+            ws = (self.ws8 if nc > 1 else self.ws1) if fw else None
             path, _ = G.plan(self.W[n], wt, x_any, M, K, e, aux_any, aux_any, ncols=nc,
-                             fwht_signs=self.signs if fw else None, fwht_block=1024 if fw else 0)
+                             fwht_signs=self.signs if fw else None, fwht_block=1024 if fw else 0, fwht_workspace=ws)
             if path < 0:
                 raise RuntimeError("plan failed for %s: %s" % (n, G.status_string(path)))
-            kind = "gemv_stream_kernel" if path == G.PATH_STREAM else "gemv_generic_kernel"
+            kind = {G.PATH_STREAM: "gemv_stream_kernel", G.PATH_TC: "gemv_tc_kernel"}.get(path, "gemv_generic_kernel")
             self.keys[n] = ("fwht_signed_kernel+" if fw else "") + "%s<%s,%d>" % (kind, WT_NAME[wt], nc)
         # kernels launched per step (a prologue call launches the transform, then the GEMV)
         self.kernels_per_step = sum(2 if fw else 1 for (n, wt, M, K, e, nc, fw) in spec)
