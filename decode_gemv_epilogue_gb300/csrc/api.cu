@@ -547,7 +547,7 @@ static int plan_info(const Call& c, const gf_opts* opts, int64_t info[8]) {
     for (int i = 0; i < 8; ++i) info[i] = 0;
     if (path == PATH_TC) {
       info[0] = tp.grid; info[1] = 192; info[2] = 128; info[3] = tp.a.NS;
-      info[4] = 64; info[5] = tp.smem; info[6] = 0; info[7] = tp.a.S;
+      info[4] = 64 * tp.a.subs; info[5] = tp.smem; info[6] = 0; info[7] = tp.a.S;
     } else if (path == PATH_STREAM) {
       info[0] = p.grid; info[1] = p.threads; info[2] = p.s.R; info[3] = p.s.NS;
       info[4] = p.s.kc_len; info[5] = p.smem; info[6] = p.s.RC; info[7] = p.s.S;

@@ -29,88 +29,21 @@
 
 #include "gf_device.cuh"
 #include "gf_internal.h"
+#include "tc_device.cuh"
 
 namespace gf {
 
 constexpr int kTcRows = 128;                    // rows per tile (MMA M)
-constexpr int kTcK = 64;                        // K elements per stage: one 128-byte f16 row
-constexpr int kTcKSteps = kTcK / 16;            // MMAs per stage (K = 16 each)
+constexpr int kTcK = 64;                        // K elements per sub-tile: one 128-byte f16 row
+constexpr int kTcKSteps = kTcK / 16;            // MMAs per sub-tile (K = 16 each)
 constexpr int kTcThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2..5 x / epilogue
-constexpr int kTcABytes = kTcRows * kTcK * 2;   // 16 KB per stage
+constexpr int kTcABytes = kTcRows * kTcK * 2;   // 16 KB per sub-tile (a stage holds a.subs of them)
 constexpr int kTcPrefetch = 4;                  // stages of x in flight per converter thread
-constexpr int kTcMaxStages = 12;                // W tiles in flight: a 16 KB tile lands ~2.7 us after issue
-
-// ------------------------------------------------------------------ PTX wrappers
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t slot_saddr, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr), "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D[tmem] (+)= A * B^T, A and B K-major f16 in shared memory (descriptors), fp32 D.
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(da), "l"(db), "r"(idesc), "r"(accum)
-      : "memory");
-}
-
-// Arrive on `bar` once every MMA this thread has issued so far has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// Eight consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzled layout
-// (rows of 128 bytes, 8-row groups 1024 bytes apart; the tile starts 1024-aligned).
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
-  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
-  d |= static_cast<uint64_t>(1) << 16;                          // leading offset (unused when swizzled)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;                  // stride between 8-row groups
-  d |= static_cast<uint64_t>(1) << 46;                          // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                          // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 D, f16 A and B, both K-major, M x N.
-__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
-  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// Byte offset of element (row, k) of a 64-wide K-major f16 tile in the 128-byte
-// swizzle: the 16-byte chunk index is XORed with the row's position in its 8-row group.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int k) {
-  return static_cast<uint32_t>(row) * 128u + ((static_cast<uint32_t>(k >> 3) ^ (row & 7)) << 4) +
-         static_cast<uint32_t>(k & 7) * 2u;
-}
+constexpr int kTcMaxStages = 12;                // W tiles in flight
+// MMA m accumulates into accumulator m % kTcAcc: MMAs into the same TMEM columns wait
+// for each other's full latency, which a 128 x N x 16 MMA with small N does not amortise
+// (one accumulator held the kernel to ~240 cycles per MMA); the epilogue adds them.
+constexpr int kTcAcc = 8;
 
 // ------------------------------------------------------------------ kernel
 // Shared memory from a 1024-aligned base: barriers and the TMEM address slot [0, 512);
@@ -144,6 +77,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   const int st0 = crank * a.nst / S, st1 = (crank + 1) * a.nst / S;  // this CTA's K stages
   const int nmy = st1 - st0;
   const int Np = a.Np;
+  const int subs = a.subs;                  // 64-element sub-tiles per stage
+  const int b_sub_bytes = 2 * Np * 128;     // B rows of one sub-tile
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -174,9 +109,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         const int slot = i % NS, round = i / NS;
         if (!mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1), abort_flag, a.err))
           break;
-        mbar_arrive_expect_tx(fullA0 + 8u * slot, static_cast<uint32_t>(kTcABytes));
-        tma_load_2d(sA + static_cast<uint32_t>(slot * kTcABytes), &tmap, (st0 + i) * kTcK, row0,
-                    fullA0 + 8u * slot);
+        mbar_arrive_expect_tx(fullA0 + 8u * slot, static_cast<uint32_t>(subs * kTcABytes));
+        for (int sbt = 0; sbt < subs; ++sbt)
+          tma_load_2d(sA + static_cast<uint32_t>((slot * subs + sbt) * kTcABytes), &tmap,
+                      ((st0 + i) * subs + sbt) * kTcK, row0, fullA0 + 8u * slot);
         ++issued;
       }
       if (issued < nmy)  // aborted: wait (bounded) for the copies in flight
@@ -187,16 +123,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_f16(kTcRows, 2 * Np);
+      const uint32_t acc_cols = static_cast<uint32_t>(2 * Np);
       for (int i = 0; i < nmy; ++i) {
         const int slot = i % NS, round = i / NS;
         if (!mbar_wait_or_abort(fullA0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag, a.err)) break;
         if (!mbar_wait_or_abort(fullB0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag, a.err)) break;
         tc_fence_after();
-        const uint64_t da = umma_desc_sw128(sA + static_cast<uint32_t>(slot * kTcABytes));
-        const uint64_t db = umma_desc_sw128(sB + static_cast<uint32_t>(slot * a.b_stage_bytes));
+        for (int sbt = 0; sbt < subs; ++sbt) {
+          const uint64_t da = umma_desc_sw128(sA + static_cast<uint32_t>((slot * subs + sbt) * kTcABytes));
+          const uint64_t db =
+              umma_desc_sw128(sB + static_cast<uint32_t>(slot * a.b_stage_bytes + sbt * b_sub_bytes));
 #pragma unroll
-        for (int kk = 0; kk < kTcKSteps; ++kk)  // +32 bytes of K per step inside the swizzled rows
-          umma_f16(tmem, da + 2u * kk, db + 2u * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTcKSteps; ++kk) {  // +32 bytes of K per step inside the swizzled rows
+            const int m = (i * subs + sbt) * kTcKSteps + kk;
+            umma_f16(tmem + static_cast<uint32_t>(m % kTcAcc) * acc_cols, da + 2u * kk, db + 2u * kk, idesc,
+                     m >= kTcAcc ? 1u : 0u);
+          }
+        }
         umma_commit(empty0 + 8u * slot);
       }
       umma_commit(accbar);  // also after an abort: arrives once every issued MMA is done
@@ -208,7 +151,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     pdl_wait();  // x, aux and dst may belong to the preceding grid
     // scale 2^s per column with its largest |x| * 2^s in [2^14, 2^15): maxima over this
     // CTA's K slice, four columns per pass so their loads are in flight together
-    const int k0 = st0 * kTcK, klen4 = nmy * kTcK / 4;
+    const int k0 = st0 * subs * kTcK, klen4 = nmy * subs * kTcK / 4;
     for (int n0 = 0; n0 < a.ncols; n0 += 4) {
       float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 4
@@ -247,30 +190,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     const bool has_chunk = ctid < Np * 8;
     const int n_own = ctid >> 3, c8_own = ctid & 7;
     const bool live = has_chunk && n_own < a.ncols;
-    const float* xcol = a.x + static_cast<int64_t>(live ? n_own : 0) * a.K + st0 * kTcK + 8 * c8_own;
+    const float* xcol = a.x + static_cast<int64_t>(live ? n_own : 0) * a.K + st0 * subs * kTcK + 8 * c8_own;
+    const int nu = nmy * subs;  // sub-tiles of this CTA
     float4 pre[kTcPrefetch][2];
 #pragma unroll
     for (int d = 0; d < kTcPrefetch; ++d)
-      if (live && d < nmy) {
+      if (live && d < nu) {
         pre[d][0] = reinterpret_cast<const float4*>(xcol + d * kTcK)[0];
         pre[d][1] = reinterpret_cast<const float4*>(xcol + d * kTcK)[1];
       }
     const float sc_own = live ? scl[n_own] : 1.0f;
     bool ok = true;
-    for (int i0 = 0; i0 < nmy; i0 += kTcPrefetch) {
+    for (int u0 = 0; u0 < nu; u0 += kTcPrefetch) {
 #pragma unroll
-      for (int d = 0; d < kTcPrefetch; ++d) {  // register slot d holds stage i0 + d
-        const int i = i0 + d;
-        if (i >= nmy) break;
+      for (int d = 0; d < kTcPrefetch; ++d) {  // register slot d holds sub-tile u0 + d
+        const int u = u0 + d;
+        if (u >= nu) break;
         const float4 c0 = pre[d][0], c1 = pre[d][1];
-        if (live && i + kTcPrefetch < nmy) {
-          pre[d][0] = reinterpret_cast<const float4*>(xcol + (i + kTcPrefetch) * kTcK)[0];
-          pre[d][1] = reinterpret_cast<const float4*>(xcol + (i + kTcPrefetch) * kTcK)[1];
+        if (live && u + kTcPrefetch < nu) {
+          pre[d][0] = reinterpret_cast<const float4*>(xcol + (u + kTcPrefetch) * kTcK)[0];
+          pre[d][1] = reinterpret_cast<const float4*>(xcol + (u + kTcPrefetch) * kTcK)[1];
         }
+        const int i = u / subs, sbt = u - i * subs;
         const int slot = i % NS, round = i / NS;
-        ok = ok && mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1), abort_flag, a.err);
+        if (sbt == 0)
+          ok = ok && mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1), abort_flag,
+                                        a.err);
         if (ok && has_chunk) {
-          uint8_t* bt = base + a.off_b + slot * a.b_stage_bytes;
+          uint8_t* bt = base + a.off_b + slot * a.b_stage_bytes + sbt * b_sub_bytes;
           uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = make_uint4(0u, 0u, 0u, 0u);
           if (live) {
             const float v[8] = {c0.x * sc_own, c0.y * sc_own, c0.z * sc_own, c0.w * sc_own,
@@ -289,9 +236,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
           }
           *reinterpret_cast<uint4*>(bt + sw128_offset(n_own, 8 * c8_own)) = hv;
           *reinterpret_cast<uint4*>(bt + sw128_offset(Np + n_own, 8 * c8_own)) = lv;
-          fence_proxy_async_smem();  // generic-proxy writes, read by the tensor cores
         }
-        mbar_arrive(fullB0 + 8u * slot);
+        if (sbt == subs - 1) {
+          if (ok && has_chunk) fence_proxy_async_smem();  // generic-proxy writes, read by the tensor cores
+          mbar_arrive(fullB0 + 8u * slot);
+        }
       }
     }
     // epilogue: wait for every MMA (bounded, regardless of an abort: tensor memory is
@@ -305,10 +254,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     const int64_t row = static_cast<int64_t>(row0) + r;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16);
     const bool need_aux = (a.epi == EPI_SILU_MUL || a.epi == EPI_ADD);
+    const int nacc = min(kTcAcc, nmy * subs * kTcKSteps);  // accumulators written
     for (int c0 = 0; c0 < Np; c0 += 8) {
       float hv[8], lv[8];
       tmem_ld8(trow + static_cast<uint32_t>(c0), hv);
       tmem_ld8(trow + static_cast<uint32_t>(Np + c0), lv);
+      for (int ac = 1; ac < nacc; ++ac) {  // the accumulators, in order
+        float h2[8], l2[8];
+        tmem_ld8(trow + static_cast<uint32_t>(ac * 2 * Np + c0), h2);
+        tmem_ld8(trow + static_cast<uint32_t>(ac * 2 * Np + Np + c0), l2);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          hv[j] += h2[j];
+          lv[j] += l2[j];
+        }
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int c = c0 + j;
@@ -380,22 +340,32 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
   if (M < 1 || K < kTcK || K % kTcK != 0 || K > INT32_MAX / 2 || M > INT32_MAX - kTcRows) return false;
   if (ncols < 1 || ncols > kTcMaxCols) return false;
   const int Np = round_up_i(ncols, 8);
-  const int nb = 2 * Np;  // MMA N: a multiple of 16 in [16, 128]
+  const int nb = 2 * Np;  // MMA N: a multiple of 16 in [16, 32]
   int tmem_cols = 32;
-  while (tmem_cols < nb) tmem_cols *= 2;
-  const int nst = static_cast<int>(K / kTcK);
+  while (tmem_cols < kTcAcc * nb) tmem_cols *= 2;  // kTcAcc accumulators of nb columns
   const int64_t tiles = (M + kTcRows - 1) / kTcRows;
   // split K while the tiles leave SMs idle; the exchange holds S * Np * 128 floats
+  const int nsub_all = static_cast<int>(K / kTcK);
   int S = static_cast<int>(std::min<int64_t>(kMaxSplit, lim.sm_count / std::max<int64_t>(tiles, 1)));
-  S = std::min(S, nst);
+  S = std::min(S, nsub_all);
   S = std::min(S, (64 * 1024) / (Np * kTcRows * 4));
   if (S < 2) S = 1;
   const int xch_bytes = S > 1 ? S * Np * kTcRows * 4 : 0;
   const int off_a = round_up_i(2048 + xch_bytes, 1024);
-  const int b_stage = nb * 128;
-  const int stage = kTcABytes + b_stage;
   const int avail = lim.smem_optin - 1024 - off_a;  // 1024: alignment slack of the dynamic base
-  const int NS = std::min(kTcMaxStages, avail / stage);
+  // stages of `subs` sub-tiles: the MMA thread's per-stage cost (its waits and commits) is
+  // spread over more data; the widest that divides K, gives every split rank a stage and
+  // keeps at least three stages in flight
+  int subs = 1, NS = 0;
+  for (int cand = 4; cand >= 1; cand /= 2) {
+    if (nsub_all % cand != 0 || nsub_all / cand < S) continue;
+    const int ns = std::min(kTcMaxStages, avail / (cand * (kTcABytes + nb * 128)));
+    if (ns >= 3 || cand == 1) {
+      subs = cand;
+      NS = ns;
+      break;
+    }
+  }
   if (NS < 2 || 24 * NS + 24 > 512) return false;
   if (tiles * S > INT32_MAX) return false;
   TcArgs& a = p.a;
@@ -406,14 +376,15 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
   a.ncols = ncols;
   a.Np = Np;
   a.S = S;
-  a.nst = nst;
+  a.subs = subs;
+  a.nst = nsub_all / subs;
   a.NS = NS;
   a.tmem_cols = tmem_cols;
   a.off_a = off_a;
-  a.off_b = off_a + NS * kTcABytes;
-  a.b_stage_bytes = b_stage;
+  a.off_b = off_a + NS * subs * kTcABytes;
+  a.b_stage_bytes = subs * nb * 128;
   p.grid = static_cast<int>(tiles * S);
-  p.smem = 1024 + a.off_b + NS * b_stage;
+  p.smem = 1024 + a.off_b + NS * a.b_stage_bytes;
   return true;
 }
 
@@ -452,18 +423,26 @@ static int launch_tc_t(const CUtensorMap& map, const TcPlan& p, cudaStream_t st,
   return cudaLaunchKernelEx(&cfg, kern, map, p.a);
 }
 
-int launch_tc(const TcPlan& p, const void* W, cudaStream_t st, bool pdl) {
+int encode_map_2d(CUtensorMap* map, bool f16, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
-  alignas(64) CUtensorMap map;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.a.K), static_cast<cuuint64_t>(p.a.M)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.a.K) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcK), static_cast<cuuint32_t>(kTcRows)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride_bytes)};
+  const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(W), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int launch_tc(const TcPlan& p, const void* W, cudaStream_t st, bool pdl) {
+  alignas(64) CUtensorMap map;
+  const int e = encode_map_2d(&map, true, W, static_cast<uint64_t>(p.a.K), static_cast<uint64_t>(p.a.M),
+                              static_cast<uint64_t>(p.a.K) * 2, kTcK, kTcRows, true);
+  if (e != cudaSuccess) return e;
   return p.a.S > 1 ? launch_tc_t<true>(map, p, st, pdl) : launch_tc_t<false>(map, p, st, pdl);
 }
 

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+struct CUtensorMap_st;  // the driver's tensor-map descriptor (cuda.h)
+
 namespace gf {
 
 // Kernel-side limits of the TMA-streamed GEMV.
@@ -111,7 +113,8 @@ struct TcArgs {
   int ncols;          // columns of this launch (<= kTcMaxCols)
   int Np;             // columns rounded up to 8: B holds Np rows of hi, then Np of lo
   int S;              // CTAs per cluster splitting K (1: none)
-  int nst;            // 64-element K stages of a row
+  int subs;           // 64-element sub-tiles per stage
+  int nst;            // stages of a row (K / (64 subs))
   int NS;             // pipeline stages
   int tmem_cols;      // tensor-memory columns allocated (power of two >= 2 Np, >= 32)
   int off_a, off_b;   // stage offsets from the 1024-aligned shared-memory base
@@ -129,6 +132,13 @@ constexpr int kTcMaxCols = 16;  // columns per tensor-core launch (one B chunk p
 bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, TcPlan& p);
 // Encodes the tensor map of W ([M][K] f16, row stride 2K) and launches.
 int launch_tc(const TcPlan& p, const void* W, cudaStream_t st, bool pdl);
+
+// A 2-D tensor map (f16 or bytes) over rows of `inner` elements, `stride_bytes` apart,
+// with boxes of box_inner x box_rows (128-byte swizzle or none).  `map` points to a
+// 64-byte aligned CUtensorMap.  Returns a cudaError_t.
+int encode_map_2d(::CUtensorMap_st* map, bool f16, const void* base, uint64_t inner, uint64_t rows,
+                  uint64_t stride_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+
 
 // Generic kernel: 256 threads; shared memory x [ncols][K], 1/rms [ncols], warp
 // partials [8][ncols].

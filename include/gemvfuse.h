@@ -91,10 +91,10 @@ typedef enum {
                             start while the previous kernel in `stream` still runs and
                             streams W before waiting for it.  Only valid when no kernel
                             still running in `stream` writes W. */
-#define GF_FLAG_NO_TENSOR_CORES 4u  /* keep F16 batches on the CUDA-core kernels (by default
-                            F16 weights with 4 or more columns, K % 64 == 0 and 16-byte
-                            aligned W and x run on the tensor cores: tcgen05 MMAs with x
-                            split into scaled f16 hi + lo parts, fp32 accumulation). */
+#define GF_FLAG_NO_TENSOR_CORES 4u  /* use the CUDA-core kernels only.  By default F16 weights
+                            with 4..16 columns, K % 64 == 0 and 16-byte aligned W and x
+                            run on the tensor cores: tcgen05 MMAs of the f16 weights with
+                            x split into scaled f16 hi + lo parts, fp32 accumulation. */
 #define GF_FLAG_NO_SPLIT_K 2u  /* never split K over a cluster of CTAs (by default a GEMV
                             with M <= SMs/2 rows gives each row range to a cluster of
                             2..8 CTAs that each stream a slice of K and add their
@@ -204,7 +204,7 @@ GF_API int gf_dequantize(const void* W, int wtype, int64_t M, int64_t K, float* 
 
 /* Which kernel gemv_fused_ex would launch for these arguments (host only, launches
  * nothing): 0 = none (M == 0), 1 = TMA-streamed kernel, 2 = generic kernel, 3 = tensor-core
- * kernel, <0 = the gf_status the call would return.  `info` (may be NULL) receives
+ * kernel (F16 batches), <0 = the gf_status the call would return.  `info` (may be NULL) receives
  *   {grid, block_threads, stage_rows, stages, k_chunk, smem_bytes, row_chunk,
  *    ctas_per_cluster (split K; 1 = no split)}. */
 GF_API int gf_plan(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
