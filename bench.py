@@ -601,6 +601,25 @@ def next_rows_measure(G, torch, step, s, args, peak):
     out["chain_glu"] = {"us_per_layer": round(us, 3), "launches_per_layer": 7, "layer_bytes": lb,
                         "gbs": round(lb / (us * 1e-6) / 1e9, 1)}
 
+    # 1a. q, k and v stored as one 12288 x 4096 matrix (a layout choice of the caller:
+    # one launch reads all three), with the gated dual GEMV: 5 launches per layer
+    qkv = [torch.cat([layers[l]["chain_q"], layers[l]["chain_k"], layers[l]["chain_v"]]) for l in range(2)]
+    qkv_out = torch.empty(3 * 4096, device=dev)
+
+    def qkv_layer(i):
+        Wl = layers[i]
+        G.gemv_fused_ex(qkv[i], 3, x, 3 * 4096, 4096, 0, None, qkv_out, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True)
+        G.gemv_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, r, 14336, 4096, g, pdl=True)
+        G.gemv_fused_ex(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_beta_sigmoid"], 3, x, 32, 4096, 1, None, beta, pdl=True)
+
+    us5 = graph_us(torch, s, qkv_layer, 2, max(20, min(args.steps, 500)))
+    out["chain_qkv_glu"] = {"us_per_layer": round(us5, 3), "launches_per_layer": 5, "layer_bytes": lb,
+                            "gbs": round(lb / (us5 * 1e-6) / 1e9, 1),
+                            "note": "q, k, v weights concatenated into one matrix by the caller"}
+    del qkv
+
     # 1b. the same layer in Q4_K (a format the pages' decode-layer measurements name),
     # 8 launches and 7 with the dual GEMV
     layers_k = [{n: up(synth.weights(4, shapes[n][0], shapes[n][1], seed=700 + 10 * l + i))
@@ -794,12 +813,16 @@ def oracle_step(frac, seed0=0):
     return total_b, total_t
 
 
-def cpu_baseline(frac=2):
-    b, t = oracle_step(frac)
+def cpu_baseline(reps=3):
+    """The oracle over every row of every launch of the step, `reps` times (~10 s)."""
+    b, t = 0, 0.0
+    for _ in range(reps):
+        bi, ti = oracle_step(1)
+        b += bi
+        t += ti
     return {"value": round(b / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "every %d%s row of every launch of one decode step (%.0f MB of the step's "
-                      "algorithmic bytes), numpy fp64 oracle, one thread" % (frac, "nd" if frac == 2 else "th",
-                                                                           b / 1e6),
+            "sample": "%d full decode steps (every row of every launch, %.0f MB of algorithmic bytes each), "
+                      "numpy fp64 oracle, one thread" % (reps, b / reps / 1e6),
             "seconds": round(t, 2)}
 
 
