@@ -618,6 +618,18 @@ int gf_dequantize(const void* W, int wtype, int64_t M, int64_t K, float* out, vo
   return GF_OK;
 }
 
+int gf_selftest_wait_timeout(int64_t limit_us, int* out, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return GF_ERR_INVALID;
+  if (!out) return GF_ERR_INVALID;
+  if (!aligned(out, 4)) return GF_ERR_ALIGN;
+  unsigned* err = device_error_word();
+  if (!err) return cuda_fail(cudaGetLastError());
+  const int e = launch_selftest_wait(err, static_cast<uint64_t>(limit_us) * 1000ull, out,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(e));
+  return GF_OK;
+}
+
 int gf_device_status(int reset) {
   unsigned* err = device_error_word();
   if (!err) return cuda_fail(cudaGetLastError());

@@ -438,10 +438,46 @@ int encode_map_2d(CUtensorMap* map, bool f16, const void* base, uint64_t inner, 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Encoded tensor maps of recent weight matrices: a map holds only the address, shape
+// and stride, so an entry with the same (W, M, K) is always the right one.
+namespace {
+struct MapEntry {
+  const void* W;
+  int64_t M;
+  int K;
+  alignas(64) CUtensorMap map;
+};
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+}  // namespace
+
+static int w_map(const void* W, int64_t M, int K, CUtensorMap* out) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (int i = 0; i < g_map_used; ++i)
+    if (g_maps[i].W == W && g_maps[i].M == M && g_maps[i].K == K) {
+      *out = g_maps[i].map;
+      return cudaSuccess;
+    }
+  alignas(64) CUtensorMap fresh;
+  const int r = encode_map_2d(&fresh, true, W, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                              static_cast<uint64_t>(K) * 2, kTcK, kTcRows, true);
+  if (r != cudaSuccess) return r;
+  MapEntry& e = g_maps[g_map_next];
+  e.map = fresh;
+  e.W = W;
+  e.M = M;
+  e.K = K;
+  *out = e.map;
+  g_map_next = (g_map_next + 1) % kMapCache;
+  if (g_map_used < kMapCache) ++g_map_used;
+  return cudaSuccess;
+}
+
 int launch_tc(const TcPlan& p, const void* W, cudaStream_t st, bool pdl) {
   alignas(64) CUtensorMap map;
-  const int e = encode_map_2d(&map, true, W, static_cast<uint64_t>(p.a.K), static_cast<uint64_t>(p.a.M),
-                              static_cast<uint64_t>(p.a.K) * 2, kTcK, kTcRows, true);
+  const int e = w_map(W, p.a.M, p.a.K, &map);
   if (e != cudaSuccess) return e;
   return p.a.S > 1 ? launch_tc_t<true>(map, p, st, pdl) : launch_tc_t<false>(map, p, st, pdl);
 }

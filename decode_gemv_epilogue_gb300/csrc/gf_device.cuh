@@ -79,14 +79,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // As mbar_wait, but also gives up as soon as *abort is set, and sets *abort (and the
 // error word) when its own time limit runs out, so the rest of the CTA stops waiting.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
-                                                   volatile int* abort, unsigned* err) {
+                                                   volatile int* abort, unsigned* err,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
   if (*abort) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       if (err) atomicOr(err, static_cast<unsigned>(ERRBIT_TIMEOUT));
       return false;

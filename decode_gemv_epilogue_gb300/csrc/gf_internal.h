@@ -189,5 +189,6 @@ int launch_dequantize(int wtype, const uint8_t* W, int64_t M, int64_t K, int64_t
                       float* out, cudaStream_t st);
 
 unsigned* device_error_word();  // this device's error word (nullptr on failure)
+int launch_selftest_wait(unsigned* err, uint64_t limit_ns, int* out, cudaStream_t st);
 
 }  // namespace gf

@@ -75,6 +75,36 @@ int launch_elementwise(int op, const float* a, const float* b, int64_t nb, float
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ failure-path self-test
+// One thread waits, through the kernels' bounded wait, on a barrier phase that nothing
+// completes (a fresh barrier's phase 0 with no arrivals expected).  The wait gives up after
+// limit_ns, sets the abort flag and the device error word; a second wait then returns at
+// once because of the abort flag.  out = {first wait succeeded, second wait succeeded,
+// microseconds of the first wait, microseconds of the second}.
+__global__ void selftest_wait_kernel(unsigned* err, uint64_t limit_ns, int* out) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  const uint64_t t0 = global_timer_ns();
+  const bool first = mbar_wait_or_abort(b, 0, &abort_flag, err, limit_ns);
+  const uint64_t t1 = global_timer_ns();
+  const bool second = mbar_wait_or_abort(b, 0, &abort_flag, err, limit_ns);
+  const uint64_t t2 = global_timer_ns();
+  out[0] = first ? 1 : 0;
+  out[1] = second ? 1 : 0;
+  out[2] = static_cast<int>(min((t1 - t0) / 1000ull, 2000000000ull));
+  out[3] = static_cast<int>(min((t2 - t1) / 1000ull, 2000000000ull));
+}
+
+int launch_selftest_wait(unsigned* err, uint64_t limit_ns, int* out, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(err, limit_ns, out);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ dequantize hook
 // Same unit decoders as the streaming kernel (through a global-memory loader), one
 // thread per 16-weight unit; the product with the block scale is exact in fp32.

@@ -55,6 +55,7 @@ _plan = _sig("gf_plan", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, ctypes.POIN
 _plan_glu = _sig("gf_plan_glu", [_vp, _vp, _i32, _vp, _i64, _i64, _vp, ctypes.POINTER(GfOpts),
                                  ctypes.POINTER(_i64 * 8)])
 _device_status = _sig("gf_device_status", [_i32])
+_selftest_wait = _sig("gf_selftest_wait_timeout", [_i64, _vp, _vp])
 _status_string = _sig("gf_status_string", [_i32], ctypes.c_char_p)
 _last_cuda_error = _sig("gf_last_cuda_error", [])
 _version = _sig("gf_version", [])
@@ -211,6 +212,14 @@ def plan_glu(W_gate, W_up, wtype, x, M, K, dst, **opts):
     path = _plan_glu(_ptr(W_gate), _ptr(W_up), wtype, _ptr(x), M, K, _ptr(dst), ctypes.byref(o),
                      ctypes.byref(info))
     return path, dict(zip(_PLAN_KEYS, list(info)))
+
+
+def selftest_wait_timeout(limit_us, out, stream=None, check=True):
+    """Run the bounded-wait failure self-test (see include/gemvfuse.h); out: device int32[4]."""
+    st = _selftest_wait(int(limit_us), _ptr(out), _stream(stream))
+    if check:
+        _check(st, "gf_selftest_wait_timeout")
+    return st
 
 
 def device_status(reset=False):

@@ -214,6 +214,14 @@ GF_API int gf_plan(const void* W, int wtype, const float* x, int64_t M, int64_t 
 GF_API int gf_plan_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M,
                        int64_t K, const float* dst, const gf_opts* opts, int64_t info[8]);
 
+/* Failure-path self-test (no GEMV): one GPU thread waits, through the same bounded wait
+ * every kernel uses, on a barrier that nothing completes.  After limit_us microseconds
+ * (1..1000000) the wait gives up, sets the device error word (gf_device_status then
+ * reports GF_ERR_TIMEOUT) and the kernel returns; the context stays usable.  out: device
+ * int[4] = {first wait succeeded (0), second wait succeeded (0: it returns at once on the
+ * abort flag), microseconds spent in the first wait, microseconds in the second}. */
+GF_API int gf_selftest_wait_timeout(int64_t limit_us, int* out, void* stream);
+
 /* Device error word of the current device: GF_OK, or GF_ERR_TIMEOUT if a kernel gave up
  * on a bounded wait since the last reset.  Synchronises with the device.  reset != 0
  * clears it. */

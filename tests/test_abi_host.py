@@ -323,3 +323,10 @@ def test_tc_plan(lib, M, K, ncols, expect_split):
 def test_tc_not_chosen(lib, kw, args):
     path, _ = lib.plan(*args, 0, None, D, **kw)
     assert path in (lib.PATH_STREAM, lib.PATH_GENERIC)
+
+
+def test_selftest_wait_validation(lib):
+    assert lib.selftest_wait_timeout(0, D, stream=0, check=False) == -1
+    assert lib.selftest_wait_timeout(2000000, D, stream=0, check=False) == -1
+    assert lib.selftest_wait_timeout(1000, None, stream=0, check=False) == -1
+    assert lib.selftest_wait_timeout(1000, D + 2, stream=0, check=False) == -4
