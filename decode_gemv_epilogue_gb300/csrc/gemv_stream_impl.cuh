@@ -172,6 +172,30 @@ __device__ __forceinline__ void consume_tile_q4k(uint32_t st, int seg, int rows,
   }
 }
 
+// Q4_0 through integer dot products: per row, the unit's codes against each column's
+// XInt; the block scale d times 2^-s scales the exact integer sum.
+template <int NCT, int U, int RT>
+__device__ __forceinline__ void consume_tile_int(uint32_t st, int seg, int rows, int units, int tg, int tg_n,
+                                                 int g, int G, const XInt (&xq)[U][NCT], float2 (&acc)[RT][NCT]) {
+#pragma unroll
+  for (int i = 0; i < U; ++i) {
+    const int u = tg + i * tg_n;
+    if (u < units) {
+#pragma unroll
+      for (int j = 0; j < RT; ++j) {
+        const int r = g + j * G;
+        if (r < rows) {
+          const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+          int t[NCT];
+          const float d = q4_0_unit_int<NCT>(ld, static_cast<uint32_t>(u), xq[i], t);
+#pragma unroll
+          for (int c = 0; c < NCT; ++c) acc[j][c].x = fmaf(d * xq[i][c].sc, static_cast<float>(t[c]), acc[j][c].x);
+        }
+      }
+    }
+  }
+}
+
 template <int WT, int NCT, int U, int RT>
 __device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int units, int tg, int tg_n,
                                              int g, int G, uint32_t qr, const float2 (&xr)[U][NCT][8],
@@ -202,6 +226,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
   constexpr int U = stream_u(WT, NC);
   constexpr int RT = stream_rt(WT, NC);
   constexpr int NCT = stream_nct(WT, NC);
+  constexpr bool kInt = stream_int(WT, NC);
   static_assert(U * NCT * 16 <= 64, "x registers per thread");
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -355,20 +380,23 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         // the transformed chunk in shared memory, or straight from global memory
         const float* xsrc = a.fwht_B > 0 ? xs : a.x + static_cast<int64_t>(kc) * a.kc_len;
         const int64_t xstride = a.fwht_B > 0 ? klen : a.K;
-        float2 xr[U][NCT][8];
-        if (norm) {
-          const float* gsrc = a.gamma + static_cast<int64_t>(kc) * a.kc_len;
+        // (integer path: each unit's x is converted as soon as it is loaded)
+        float2 xr[kInt ? 1 : U][NCT][8];
+        XInt xq[kInt ? U : 1][kInt ? NCT : 1];
+        const float* gsrc = norm ? a.gamma + static_cast<int64_t>(kc) * a.kc_len : nullptr;
 #pragma unroll
-          for (int i = 0; i < U; ++i) {
-            const int u = unit_index<WT, U>(tg, i, tg_n);
-            if (u < units && ok)
-              load_unit_x<WT, NCT, kExt>(xsrc, xstride, gsrc, u, qr, c0, NC, xr[i], rc0 == 0, ssq);
-          }
-        } else {
+        for (int i = 0; i < U; ++i) {
+          const int u = unit_index<WT, U>(tg, i, tg_n);
+          if (u < units && ok) {
+            float2 (&xv)[NCT][8] = xr[kInt ? 0 : i];
+            if (norm)
+              load_unit_x<WT, NCT, kExt>(xsrc, xstride, gsrc, u, qr, c0, NC, xv, rc0 == 0, ssq);
+            else
+              load_unit_x<WT, NCT, false>(xsrc, xstride, nullptr, u, qr, c0, NC, xv);
+            if constexpr (kInt) {
 #pragma unroll
-          for (int i = 0; i < U; ++i) {
-            const int u = unit_index<WT, U>(tg, i, tg_n);
-            if (u < units && ok) load_unit_x<WT, NCT, false>(xsrc, xstride, nullptr, u, qr, c0, NC, xr[i]);
+              for (int c = 0; c < NCT; ++c) x_to_int(xv[c], xq[i][c]);
+            }
           }
         }
         // Q4_K: the sum of each unit's (scaled) x, for the sub-block min term
@@ -398,6 +426,9 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
             if constexpr (WT == WT_Q4_K)
               consume_tile_q4k<NCT, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
                                         g, a.G, xr, xsum, acc);
+            else if constexpr (kInt)
+              consume_tile_int<NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
+                                           tg_n, g, a.G, xq, acc);
             else
               consume_tile<WT, NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units,
                                            tg, tg_n, g, a.G, qr, xr, acc);

@@ -415,6 +415,91 @@ __device__ __forceinline__ void q4k_nibbles(const uint4 q, uint32_t n, float2 (&
   }
 }
 
+// ---- integer dot products (Q4_0, single columns)
+// A unit's 16 x values become integers X_j = trunc(x_j * 2^s) that share the exponent s
+// (chosen so that max |x_j| * 2^s lies in [2^22, 2^23), hence |X_j| <= 2^23 - 1).  Each
+// X_j is split into three bytes X = D2 * 2^16 + D1 * 2^8 + D0 (D2 signed, D1 and D0
+// unsigned), packed four elements to a register in the order of the unit's code bytes:
+// group g holds the elements of the low nibbles (g = 0, 1) or high nibbles (g = 2, 3) of
+// code word g % 2.  sum_j (q_j - 8) X_j is then exact in 32-bit integers (|.| < 2^30):
+// three chains of four dp4a (one per digit) on the unpacked nibbles, combined at the end
+// with -8 sum_j X_j (modulo 2^32; the result fits).  The block's d times 2^-s scales the
+// converted sum.  Truncating x * 2^s changes each product by less than
+// |w_j| * 2^-s <= |w_j| * 2^-22 * max_unit |x|.
+struct XInt {
+  uint32_t d2[4], d1[4], d0[4];  // digit bytes of the four element groups
+  uint32_t c;                    // -8 * sum_j X_j (two's complement)
+  float sc;                      // 2^-s
+};
+
+__device__ __forceinline__ uint32_t dp4a_us(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Digit registers of four integers a..d (byte k of each register is element k).
+__device__ __forceinline__ void pack_digits(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t& d2,
+                                            uint32_t& d1, uint32_t& d0) {
+  const uint32_t ab = __byte_perm(a, b, 0x5140u), cd = __byte_perm(c, d, 0x5140u);  // bytes 0, 1 interleaved
+  d0 = __byte_perm(ab, cd, 0x5410u);
+  d1 = __byte_perm(ab, cd, 0x7632u);
+  d2 = __byte_perm(__byte_perm(a, b, 0x0062u), __byte_perm(c, d, 0x6200u), 0x7610u);
+}
+
+// x of one unit (eight pairs in decode_unit()'s pair order: pairs 2g and 2g+1 form group
+// g) -> XInt.  The exponent is kept in [-126, 126] so that 2^s and 2^-s are normal
+// floats; below |x| = 2^-103 the integers get shorter (absolute error under 2^-126).
+__device__ __forceinline__ void x_to_int(const float2 (&xv)[8], XInt& xi) {
+  float m = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m = fmaxf(m, fmaxf(fabsf(xv[k].x), fabsf(xv[k].y)));
+  // m = f * 2^E with f in [0.5, 1): E = biased exponent - 126 (m = 0: any s works)
+  const int E = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 126;
+  const int s = max(-126, min(126, 23 - E));
+  const float up = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
+  xi.sc = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  int sum = 0;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int X0 = __float2int_rz(xv[2 * g].x * up), X1 = __float2int_rz(xv[2 * g].y * up);
+    const int X2 = __float2int_rz(xv[2 * g + 1].x * up), X3 = __float2int_rz(xv[2 * g + 1].y * up);
+    sum += (X0 + X1) + (X2 + X3);
+    pack_digits(static_cast<uint32_t>(X0), static_cast<uint32_t>(X1), static_cast<uint32_t>(X2),
+                static_cast<uint32_t>(X3), xi.d2[g], xi.d1[g], xi.d0[g]);
+  }
+  xi.c = static_cast<uint32_t>(-8 * sum);
+}
+
+// Q4_0 unit u of a row (its half block: code bytes 8h .. 8h+7 of block u/2) against the
+// XInt of each of NCT columns: returns the block scale d, t[c] = sum_j (q_j - 8) X_j.
+template <int NCT, class L>
+__device__ __forceinline__ float q4_0_unit_int(const L& ld, uint32_t u, const XInt (&xq)[NCT], int (&t)[NCT]) {
+  const uint32_t off = (u >> 1) * 18u;
+  const float d = h2f(ld.u16(off));
+  uint32_t w[2];
+  ld.template words<2>(off + 2u + 8u * (u & 1u), w);
+  const uint32_t n[4] = {w[0] & 0x0F0F0F0Fu, w[1] & 0x0F0F0F0Fu, (w[0] >> 4) & 0x0F0F0F0Fu,
+                         (w[1] >> 4) & 0x0F0F0F0Fu};
+#pragma unroll
+  for (int c = 0; c < NCT; ++c) {
+    uint32_t s2 = 0u, s1 = 0u, s0 = xq[c].c;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      s2 = dp4a_us(n[g], xq[c].d2[g], s2);
+      s1 = dp4a_uu(n[g], xq[c].d1[g], s1);
+      s0 = dp4a_uu(n[g], xq[c].d0[g], s0);
+    }
+    t[c] = static_cast<int>((s2 * 256u + s1) * 256u + s0);
+  }
+  return d;
+}
+
 // Quad rotation of a lane for the F32/F16 unit loads (0 for the block formats).
 template <int WT>
 __device__ __forceinline__ uint32_t lane_quad_rot(int lane) {

@@ -32,7 +32,9 @@ constexpr int kMaxSplit = 8;                // CTAs of a split-K cluster (portab
 // Q8_0/Q4_0 keep up to four columns per thread so each weight is decoded once per four
 // columns.  Q4_K threads always own one unit pair (two units sharing a code load) and
 // one column: with 17 warps a thread has at most 96 registers (a quarter of the SM's
-// register file serves up to five warps), and a second column of x spills.
+// register file serves up to five warps), and a second column of x spills.  Single-
+// column Q4_0 (integer dot products, below) keeps one unit and eight rows per thread: its
+// x conversion per unit is the costly part of a chunk's start, and eight rows share it.
 __host__ __device__ constexpr bool stream_quant(int wt) { return wt == 2 || wt == 3 || wt == 4; }
 __host__ __device__ constexpr int stream_nct(int wt, int nc) {
   return wt == 4 ? 1 : stream_quant(wt) ? (nc <= 4 ? nc : 4) : (nc <= 2 ? nc : 2);
@@ -41,11 +43,19 @@ __host__ __device__ constexpr int stream_cs(int wt, int nc) {
   return (nc + stream_nct(wt, nc) - 1) / stream_nct(wt, nc);
 }
 __host__ __device__ constexpr int stream_u(int wt, int nc) {
-  return wt == 4 ? 2 : (nc == 1 && stream_quant(wt)) ? 2 : 1;
+  return wt == 4 ? 2 : (wt == 3 && nc == 1) ? 1 : (nc == 1 && stream_quant(wt)) ? 2 : 1;
 }
-__host__ __device__ constexpr int stream_rt(int wt, int nc) { return (nc == 1 && wt == 2) ? 2 : 4; }
+__host__ __device__ constexpr int stream_rt(int wt, int nc) {
+  return (nc == 1 && wt == 2) ? 2 : (nc == 1 && wt == 3) ? 8 : 4;
+}
 __host__ __device__ constexpr int stream_max_cw(int wt, int nc) { return stream_nct(wt, nc) <= 2 ? 16 : 8; }
 __host__ __device__ constexpr int stream_threads(int wt, int nc) { return 32 * (1 + stream_max_cw(wt, nc)); }
+// Q4_0 with up to kIntMaxCols columns takes integer dot products (x as shared-exponent
+// 24-bit integers, dp4a on the unpacked codes): a third of the instructions per weight of
+// the float decode.  With more columns per thread the float decode, done once for all of
+// them, is cheaper.
+constexpr int kIntMaxCols = 1;
+__host__ __device__ constexpr bool stream_int(int wt, int nc) { return wt == 3 && nc <= kIntMaxCols; }
 
 struct StreamArgs {
   const uint8_t* W;

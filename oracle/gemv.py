@@ -106,6 +106,19 @@ def abs_dot(raw, wtype, x, M, K, rows=None):
     return np.einsum("ik,ck->ci", _abs_weights(raw, wtype, M, K, rows), np.abs(X))
 
 
+def block_max_dot(raw, wtype, x, M, K, rows=None, block=32):
+    """sum over blocks b of max_{k in b} |x[c,k]| * sum_{k in b} |W[i,k]|, blocks of
+    `block` consecutive elements: the scale of the error of a product that rounds x
+    relative to the largest |x| of each block (a parity-tolerance term)."""
+    X = np.abs(_as_cols(x, K))
+    if K % block:
+        raise ValueError("K must be a multiple of the block")
+    mx = X.reshape(X.shape[0], K // block, block).max(axis=2)                 # [C, nb]
+    Wa = _abs_weights(raw, wtype, M, K, rows)
+    wb = Wa.reshape(Wa.shape[0], K // block, block).sum(axis=2)              # [R, nb]
+    return np.einsum("cb,ib->ci", mx, wb)
+
+
 def abs_w_dot(raw, wtype, e, M, K, rows=None):
     """sum_k |W[i,k]| * e[c,k] for a non-negative per-element error e [ncols, K]."""
     return np.einsum("ik,ck->ci", _abs_weights(raw, wtype, M, K, rows), _as_cols(e, K))
