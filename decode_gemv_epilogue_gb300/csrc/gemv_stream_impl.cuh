@@ -173,24 +173,36 @@ __device__ __forceinline__ void consume_tile_q4k(uint32_t st, int seg, int rows,
 }
 
 // Q4_0 through integer dot products: per row, the unit's codes against each column's
-// XInt; the block scale d times 2^-s scales the exact integer sum.
+// XInt; the block scale d times 2^-s scales the exact integer sum.  All rows' shared-
+// memory words are loaded before any arithmetic (the loads are ordered asm, so this
+// leaves the scheduler every row's dp4a chains to interleave); rows past the tile's end
+// read its last row and their sums are never stored.
 template <int NCT, int U, int RT>
 __device__ __forceinline__ void consume_tile_int(uint32_t st, int seg, int rows, int units, int tg, int tg_n,
                                                  int g, int G, const XInt (&xq)[U][NCT], float2 (&acc)[RT][NCT]) {
 #pragma unroll
   for (int i = 0; i < U; ++i) {
-    const int u = tg + i * tg_n;
-    if (u < units) {
+    const uint32_t u = static_cast<uint32_t>(tg + i * tg_n);
+    if (u < static_cast<uint32_t>(units)) {
+      const uint32_t off = (u >> 1) * 18u, start = off + 2u + 8u * (u & 1u);
+      const uint32_t wa = start & ~3u, sh = (start & 3u) * 8u;
+      uint32_t dr[RT], wr[RT][3];
 #pragma unroll
       for (int j = 0; j < RT; ++j) {
-        const int r = g + j * G;
-        if (r < rows) {
-          const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
-          int t[NCT];
-          const float d = q4_0_unit_int<NCT>(ld, static_cast<uint32_t>(u), xq[i], t);
+        const int r = min(g + j * G, rows - 1);
+        const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+        dr[j] = ld.u16(off);
 #pragma unroll
-          for (int c = 0; c < NCT; ++c) acc[j][c].x = fmaf(d * xq[i][c].sc, static_cast<float>(t[c]), acc[j][c].x);
-        }
+        for (int k = 0; k < 3; ++k) wr[j][k] = ld.u32(wa + 4u * k);
+      }
+#pragma unroll
+      for (int j = 0; j < RT; ++j) {
+        const uint32_t w0 = __funnelshift_r(wr[j][0], wr[j][1], sh), w1 = __funnelshift_r(wr[j][1], wr[j][2], sh);
+        int t[NCT];
+        q4_0_words_int<NCT>(w0, w1, xq[i], t);
+        const float d = h2f(dr[j]);
+#pragma unroll
+        for (int c = 0; c < NCT; ++c) acc[j][c].x = fmaf(d * xq[i][c].sc, static_cast<float>(t[c]), acc[j][c].x);
       }
     }
   }
@@ -272,7 +284,8 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      int it = 0;
+      int it = 0, slot = 0;  // tiles issued; ring slot of the next one
+      uint32_t ephase = 1u;   // parity of the empty-barrier phase that frees `slot`
       bool ok = true;
       for (int rc0 = 0; rc0 < nrows && ok; rc0 += a.RC) {
         const int nrc = min(a.RC, nrows - rc0);
@@ -284,9 +297,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
           for (int t0 = 0; t0 < nvr; t0 += a.R) {
             const int rows = min(a.R, nvr - t0);
             const int h = dual ? rows / 2 : rows;  // rows taken from each matrix
-            const int slot = it % a.NS, round = it / a.NS;
-            if (!mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1),
-                                    abort_flag, a.err)) {
+            if (!mbar_wait_or_abort(empty0 + 8u * slot, ephase, abort_flag, a.err)) {
               ok = false;
               break;
             }
@@ -311,6 +322,10 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
               }
             }
             ++it;
+            if (++slot == a.NS) {
+              slot = 0;
+              ephase ^= 1u;
+            }
           }
         }
       }
@@ -335,7 +350,8 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
     const bool need_aux = (a.epi == EPI_SILU_MUL || a.epi == EPI_ADD);
     const bool finalizer = (crank == 0);
     pdl_wait();  // x, aux and dst may belong to the preceding grid
-    int it = 0;
+    int slot = 0;            // ring slot of the next tile
+    uint32_t fphase = 0;     // parity of its full-barrier phase
     uint32_t xphase = 0;
     bool ok = true;
     bool x_loaded = false;
@@ -412,11 +428,9 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
             }
             xsum[i][c] = t.x + t.y;
           }
-        for (int t0 = 0; t0 < nvr; t0 += a.R, ++it) {
+        for (int t0 = 0; t0 < nvr; t0 += a.R) {
           const int rows = min(a.R, nvr - t0);
-          const int slot = it % a.NS, round = it / a.NS;
-          ok = ok && mbar_wait_or_abort(full0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag,
-                                        a.err);
+          ok = ok && mbar_wait_or_abort(full0 + 8u * slot, fphase, abort_flag, a.err);
           float2 acc[RT][NCT];
 #pragma unroll
           for (int j = 0; j < RT; ++j)
@@ -435,6 +449,10 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+          if (++slot == a.NS) {
+            slot = 0;
+            fphase ^= 1u;
+          }
           // warp reduction of the RT*NCT partial sums (padded to a power of two)
           constexpr int V = RT * NCT;
           constexpr int VP = V > 16 ? 32 : V > 8 ? 16 : V > 4 ? 8 : V > 2 ? 4 : V > 1 ? 2 : 1;

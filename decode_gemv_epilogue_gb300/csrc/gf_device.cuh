@@ -476,16 +476,11 @@ __device__ __forceinline__ void x_to_int(const float2 (&xv)[8], XInt& xi) {
   xi.c = static_cast<uint32_t>(-8 * sum);
 }
 
-// Q4_0 unit u of a row (its half block: code bytes 8h .. 8h+7 of block u/2) against the
-// XInt of each of NCT columns: returns the block scale d, t[c] = sum_j (q_j - 8) X_j.
-template <int NCT, class L>
-__device__ __forceinline__ float q4_0_unit_int(const L& ld, uint32_t u, const XInt (&xq)[NCT], int (&t)[NCT]) {
-  const uint32_t off = (u >> 1) * 18u;
-  const float d = h2f(ld.u16(off));
-  uint32_t w[2];
-  ld.template words<2>(off + 2u + 8u * (u & 1u), w);
-  const uint32_t n[4] = {w[0] & 0x0F0F0F0Fu, w[1] & 0x0F0F0F0Fu, (w[0] >> 4) & 0x0F0F0F0Fu,
-                         (w[1] >> 4) & 0x0F0F0F0Fu};
+// A Q4_0 unit's two code words (code bytes 8h .. 8h+7 of its block) against the XInt of
+// each of NCT columns: t[c] = sum_j (q_j - 8) X_j.
+template <int NCT>
+__device__ __forceinline__ void q4_0_words_int(uint32_t w0, uint32_t w1, const XInt (&xq)[NCT], int (&t)[NCT]) {
+  const uint32_t n[4] = {w0 & 0x0F0F0F0Fu, w1 & 0x0F0F0F0Fu, (w0 >> 4) & 0x0F0F0F0Fu, (w1 >> 4) & 0x0F0F0F0Fu};
 #pragma unroll
   for (int c = 0; c < NCT; ++c) {
     uint32_t s2 = 0u, s1 = 0u, s0 = xq[c].c;
@@ -497,7 +492,6 @@ __device__ __forceinline__ float q4_0_unit_int(const L& ld, uint32_t u, const XI
     }
     t[c] = static_cast<int>((s2 * 256u + s1) * 256u + s0);
   }
-  return d;
 }
 
 // Quad rotation of a lane for the F32/F16 unit loads (0 for the block formats).
