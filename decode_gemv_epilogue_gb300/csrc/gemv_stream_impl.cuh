@@ -208,7 +208,9 @@ __device__ __forceinline__ void consume_tile_int(uint32_t st, int seg, int rows,
   }
 }
 
-template <int WT, int NCT, int U, int RT>
+// BATCH: load every row's raw unit before any arithmetic (else row by row; F32 always
+// goes row by row).
+template <int WT, int NCT, int U, int RT, bool BATCH>
 __device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int units, int tg, int tg_n,
                                              int g, int G, uint32_t qr, const float2 (&xr)[U][NCT][8],
                                              float2 (&acc)[RT][NCT]) {
@@ -216,14 +218,32 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int
   for (int i = 0; i < U; ++i) {
     const int u = tg + i * tg_n;
     if (u < units) {
+      if constexpr (WT == WT_F32 || !BATCH) {
 #pragma unroll
-      for (int j = 0; j < RT; ++j) {
-        const int r = g + j * G;
-        if (r < rows) {
-          const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+        for (int j = 0; j < RT; ++j) {
+          const int r = g + j * G;
+          if (r < rows) {
+            const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+            float2 v[8];
+            float d;
+            decode_unit<WT>(ld, static_cast<uint32_t>(u), v, d, qr);
+            unit_rows_fma<WT, NCT>(v, d, xr[i], acc[j]);
+          }
+        }
+      } else {
+        // every row's loads first (rows past the tile's end read its last row; their
+        // sums are never stored), then the arithmetic
+        RawUnit<WT> raw[RT];
+#pragma unroll
+        for (int j = 0; j < RT; ++j) {
+          const int r = min(g + j * G, rows - 1);
+          load_raw<WT>(SmemLoader{st + static_cast<uint32_t>(r * seg)}, static_cast<uint32_t>(u), qr, raw[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < RT; ++j) {
           float2 v[8];
           float d;
-          decode_unit<WT>(ld, static_cast<uint32_t>(u), v, d, qr);
+          decode_raw<WT>(raw[j], static_cast<uint32_t>(u), v, d);
           unit_rows_fma<WT, NCT>(v, d, xr[i], acc[j]);
         }
       }
@@ -239,6 +259,9 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
   constexpr int RT = stream_rt(WT, NC);
   constexpr int NCT = stream_nct(WT, NC);
   constexpr bool kInt = stream_int(WT, NC);
+  // batched tile loads, except where they would spill (two F16 columns per thread with
+  // the extension code)
+  constexpr bool kBatch = !(kExt && WT == WT_F16 && NCT > 1);
   static_assert(U * NCT * 16 <= 64, "x registers per thread");
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -444,8 +467,8 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
               consume_tile_int<NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
                                            tg_n, g, a.G, xq, acc);
             else
-              consume_tile<WT, NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units,
-                                           tg, tg_n, g, a.G, qr, xr, acc);
+              consume_tile<WT, NCT, U, RT, kBatch>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows,
+                                                   units, tg, tg_n, g, a.G, qr, xr, acc);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(empty0 + 8u * slot);

@@ -365,6 +365,64 @@ __device__ __forceinline__ void decode_unit(const L& ld, uint32_t u, float2 (&v)
   }
 }
 
+// The same decode for a shared-memory stage, split into the loads (RawUnit, so a
+// thread can issue the loads of all its rows before any arithmetic) and the arithmetic
+// (decode_raw).  F32 (16 registers per unit) keeps decode_unit.
+template <int WT> struct RawUnit;
+template <> struct RawUnit<WT_F16> { uint4 a, b; };
+template <> struct RawUnit<WT_Q8_0> { uint32_t d, w[5]; };
+template <> struct RawUnit<WT_Q4_0> { uint32_t d, w[3]; };
+
+template <int WT>
+__device__ __forceinline__ void load_raw(const SmemLoader& ld, uint32_t u, uint32_t qr, RawUnit<WT>& r) {
+  if constexpr (WT == WT_F16) {
+    const uint32_t h0 = (qr >> 1) & 1u;
+    r.a = ld.v4(u * 32u + 16u * h0);
+    r.b = ld.v4(u * 32u + 16u * (h0 ^ 1u));
+  } else {
+    constexpr uint32_t kBlk = WT == WT_Q8_0 ? 34u : 18u, kHalf = WT == WT_Q8_0 ? 16u : 8u;
+    constexpr int kW = WT == WT_Q8_0 ? 5 : 3;
+    const uint32_t off = (u >> 1) * kBlk;
+    r.d = ld.u16(off);
+    const uint32_t a = (off + 2u + kHalf * (u & 1u)) & ~3u;
+#pragma unroll
+    for (int i = 0; i < kW; ++i) r.w[i] = ld.u32(a + 4u * i);
+  }
+}
+
+template <int WT>
+__device__ __forceinline__ void decode_raw(const RawUnit<WT>& r, uint32_t u, float2 (&v)[8], float& d) {
+  if constexpr (WT == WT_F16) {
+    v[0] = h2pair(r.a.x); v[1] = h2pair(r.a.y); v[2] = h2pair(r.a.z); v[3] = h2pair(r.a.w);
+    v[4] = h2pair(r.b.x); v[5] = h2pair(r.b.y); v[6] = h2pair(r.b.z); v[7] = h2pair(r.b.w);
+    d = 1.0f;
+  } else {
+    constexpr uint32_t kBlk = WT == WT_Q8_0 ? 34u : 18u, kHalf = WT == WT_Q8_0 ? 16u : 8u;
+    const uint32_t sh = (((u >> 1) * kBlk + 2u + kHalf * (u & 1u)) & 3u) * 8u;
+    d = h2f(r.d);
+    if constexpr (WT == WT_Q8_0) {
+      const float bias = -(kMagic + 128.0f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t t = __funnelshift_r(r.w[i], r.w[i + 1], sh) ^ 0x80808080u;  // bytes q + 128
+        v[2 * i] = magic_pair(t, 0x7540u, bias);
+        v[2 * i + 1] = magic_pair(t, 0x7542u, bias);
+      }
+    } else {
+      const float bias = -(kMagic + 8.0f);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint32_t w = __funnelshift_r(r.w[i], r.w[i + 1], sh);
+        const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+        v[2 * i] = magic_pair(lo, 0x7540u, bias);
+        v[2 * i + 1] = magic_pair(lo, 0x7542u, bias);
+        v[4 + 2 * i] = magic_pair(hi, 0x7540u, bias);
+        v[4 + 2 * i + 1] = magic_pair(hi, 0x7542u, bias);
+      }
+    }
+  }
+}
+
 // ---- Q4_K (super-blocks of 256 elements, 144 bytes: binary16 d and dmin, 12 bytes of
 // packed 6-bit sub-block scales sc[j] and mins m[j], 128 code bytes; value
 // d*sc[j]*q - dmin*m[j]).  Units come in pairs that share one 16-byte load of codes:
