@@ -239,14 +239,26 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
   int RC = std::min(rows_max, std::max(R, kRedMaxBytes / (vr * wpc * nc * 4)));
   RC = std::min(RC, 512);
   if (S > 1 && RC < rows_max) return false;  // split K exchanges one row chunk per CTA
-  const int xs_bytes = c.signs ? round_up(nc * kc * 4, 128) : 0;
+  // x is staged in shared memory by the producer when the row is one chunk and the
+  // staging costs at most one ring stage of a ring that keeps four or more
+  bool stage_x = !c.signs && n_kc == 1 && nc * kc * 4 <= kXStageMaxBytes;
+  int xs_bytes = (c.signs || stage_x) ? round_up(nc * kc * 4, 128) : 0;
   const int aux_bytes = round_up(nc * RC * 4, 128);
   const int red_bytes = round_up(vr * RC * wpc * nc * 4, 128);
   const int norm_bytes = c.gamma ? round_up(wpc * nc * 4, 128) : 0;
   const int xchg_bytes = S > 1 ? round_up(S * nc * (vr * RC + 1) * 4, 128) : 0;
-  const int fixed = kBarBytes + xs_bytes + aux_bytes + red_bytes + norm_bytes + xchg_bytes + kRingSlackBytes;
+  int fixed = kBarBytes + xs_bytes + aux_bytes + red_bytes + norm_bytes + xchg_bytes + kRingSlackBytes;
   const int stage_bytes = round_up(R * seg_full, 128);
-  const int NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
+  int NS = std::min(kMaxStages, (lim.smem_optin - fixed) / stage_bytes);
+  if (stage_x) {
+    const int ns_plain = std::min(kMaxStages, (lim.smem_optin - (fixed - xs_bytes)) / stage_bytes);
+    if (NS < std::min(ns_plain, 4) || NS < ns_plain - 1) {  // not worth the stages: load x directly
+      stage_x = false;
+      fixed -= xs_bytes;
+      xs_bytes = 0;
+      NS = ns_plain;
+    }
+  }
   if (NS < 2) return false;
   p.path = PATH_STREAM;
   p.grid = nclusters * S;
@@ -275,6 +287,7 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
   s.fwht_scale = c.signs ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.fwht_block))) : 1.0f;
   s.norm_eps = c.gamma ? c.eps : 0.0f;
   s.S = S;
+  s.stage_x = stage_x ? 1 : 0;
   s.off_xs = kBarBytes;
   s.off_aux = s.off_xs + xs_bytes;
   s.off_red = s.off_aux + aux_bytes;

@@ -11,6 +11,10 @@
 // the consumer warps are added in a fixed order (deterministic), the fused tail is
 // applied with the prefetched aux operand, and dst is written once.
 //
+// x: when a row fits one K chunk, the producer stages x (all columns) in shared memory
+// with a bulk copy issued right behind the first weight tile; otherwise each consumer
+// loads its x values from global memory.
+//
 // Prologues: with the signed FWHT, x (all columns of one K chunk) is staged in shared
 // memory with a bulk copy and transformed in place, so x' never leaves the chip.  With
 // RMS normalisation, gamma multiplies x as it is loaded into registers and the
@@ -310,6 +314,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
       int it = 0, slot = 0;  // tiles issued; ring slot of the next one
       uint32_t ephase = 1u;   // parity of the empty-barrier phase that frees `slot`
       bool ok = true;
+      bool x_issued = false;
       for (int rc0 = 0; rc0 < nrows && ok; rc0 += a.RC) {
         const int nrc = min(a.RC, nrows - rc0);
         const int nvr = dual ? 2 * nrc : nrc;
@@ -320,7 +325,9 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
           for (int t0 = 0; t0 < nvr; t0 += a.R) {
             const int rows = min(a.R, nvr - t0);
             const int h = dual ? rows / 2 : rows;  // rows taken from each matrix
-            if (!mbar_wait_or_abort(empty0 + 8u * slot, ephase, abort_flag, a.err)) {
+            // the first NS tiles go to empty slots: no wait (a wait on the phase before a
+            // fresh barrier's first one took ~0.9 us on GB300)
+            if (it >= a.NS && !mbar_wait_or_abort(empty0 + 8u * slot, ephase, abort_flag, a.err)) {
               ok = false;
               break;
             }
@@ -349,6 +356,17 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
               slot = 0;
               ephase ^= 1u;
             }
+            if (a.stage_x && !x_issued) {
+              // x staged by bulk copy right behind the first weight tile, once the
+              // preceding grid (which may write x) has finished: later in the queue it
+              // waits behind the whole ring of weight tiles
+              pdl_wait();
+              mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(NC * a.K * 4));
+              for (int c = 0; c < NC; ++c)
+                bulk_g2s(smem_u32(xs + c * a.K), a.x + static_cast<int64_t>(c) * a.K,
+                         static_cast<uint32_t>(a.K * 4), xbar);
+              x_issued = true;
+            }
           }
         }
       }
@@ -356,6 +374,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         // Drain: wait (bounded) until every copy this thread issued has landed.
         for (int i = max(0, it - a.NS); i < it; ++i)
           (void)mbar_wait(full0 + 8u * (i % a.NS), static_cast<uint32_t>((i / a.NS) & 1));
+        if (x_issued) (void)mbar_wait(xbar, 0u);
       }
     }
   } else {
@@ -417,8 +436,10 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         const int seg = seg_bytes_of<WT>(klen);
         // this thread's x (its units, its columns) in registers for the whole chunk: from
         // the transformed chunk in shared memory, or straight from global memory
-        const float* xsrc = a.fwht_B > 0 ? xs : a.x + static_cast<int64_t>(kc) * a.kc_len;
-        const int64_t xstride = a.fwht_B > 0 ? klen : a.K;
+        if (a.stage_x && kc == kc_lo && rc0 == 0) ok = ok && mbar_wait_or_abort(xbar, 0u, abort_flag, a.err);
+        const bool x_smem = a.fwht_B > 0 || a.stage_x;
+        const float* xsrc = x_smem ? xs : a.x + static_cast<int64_t>(kc) * a.kc_len;
+        const int64_t xstride = x_smem ? klen : a.K;
         // (integer path: each unit's x is converted as soon as it is loaded)
         float2 xr[kInt ? 1 : U][NCT][8];
         XInt xq[kInt ? U : 1][kInt ? NCT : 1];

@@ -107,7 +107,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       int issued = 0;
       for (int i = 0; i < nmy; ++i) {
         const int slot = i % NS, round = i / NS;
-        if (!mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1), abort_flag, a.err))
+        // the first NS stages are empty: no wait (see the stream kernel)
+        if (i >= NS && !mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1), abort_flag,
+                                            a.err))
           break;
         mbar_arrive_expect_tx(fullA0 + 8u * slot, static_cast<uint32_t>(subs * kTcABytes));
         for (int sbt = 0; sbt < subs; ++sbt)
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         }
         const int i = u / subs, sbt = u - i * subs;
         const int slot = i % NS, round = i / NS;
-        if (sbt == 0)
+        if (sbt == 0 && i >= NS)
           ok = ok && mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1), abort_flag,
                                         a.err);
         if (ok && has_chunk) {

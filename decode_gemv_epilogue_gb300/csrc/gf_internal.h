@@ -14,6 +14,7 @@ constexpr int kMaxBatch = 256;   // columns per call (wider batches run in block
 constexpr int kMaxStages = 8;
 constexpr int kBarBytes = 256;              // mbarrier area at the start of shared memory
 constexpr int kXsMaxBytes = 64 * 1024;      // x chunk (all columns) kept in shared memory
+constexpr int kXStageMaxBytes = 32 * 1024;  // x staged without a prologue (whole rows only)
 constexpr int kSegMaxBytes = 32 * 1024;     // bytes of one row's K chunk
 constexpr int kStageMaxBytes = 72 * 1024;
 constexpr int kRedMaxBytes = 16 * 1024;
@@ -87,6 +88,7 @@ struct StreamArgs {
   const float* gamma;  // RMS-normalisation weight [K] (nullptr: no normalisation)
   float norm_eps;
   int S;             // CTAs per cluster sharing a row range, each a slice of the K chunks
+  int stage_x;       // 1: the producer bulk-copies x (one K chunk, every column) into xs
   int off_xs, off_aux, off_red, off_norm, off_xchg, off_ring;
 };
 
