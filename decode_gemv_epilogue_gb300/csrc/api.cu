@@ -229,13 +229,25 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
   if (wpg > max_cw) return false;
   const int nclusters = static_cast<int>(std::min<int64_t>(lim.sm_count / S, c.M));
   if (nclusters < 1) return false;
-  const int rows_base = static_cast<int>(c.M / nclusters);
-  const int rows_extra = static_cast<int>(c.M % nclusters);
-  const int rows_max = rows_base + (rows_extra ? 1 : 0);
+  int rows_base = static_cast<int>(c.M / nclusters);
+  int rows_extra = static_cast<int>(c.M % nclusters);
+  int rows_max = rows_base + (rows_extra ? 1 : 0);
   int G = std::max(1, std::min(max_cw / wpg, (vr * rows_max + RT - 1) / RT));
   while (G > 1 && G * RT * seg_full > kStageMaxBytes) --G;
   const int ncw = G * wpg;
   int R = G * RT;
+  // With at least one full tile per CTA, hand out whole tiles: the CTAs with the highest
+  // indices, which a launch behind another (PDL) starts last, take one tile fewer, and
+  // no CTA decodes a part-filled tile of a full tile's cost.  Fewer rows than that: rows.
+  int row_gran = 1;
+  const int64_t tile_rows = R / vr;  // real rows of a full tile
+  if (S == 1 && c.M >= tile_rows * nclusters) {
+    const int64_t ntile = (c.M + tile_rows - 1) / tile_rows;
+    row_gran = static_cast<int>(tile_rows);
+    rows_base = static_cast<int>(ntile / nclusters);
+    rows_extra = static_cast<int>(ntile % nclusters);
+    rows_max = (rows_base + (rows_extra ? 1 : 0)) * row_gran;
+  }
   int RC = std::min(rows_max, std::max(R, kRedMaxBytes / (vr * wpc * nc * 4)));
   RC = std::min(RC, 512);
   if (S > 1 && RC < rows_max) return false;  // split K exchanges one row chunk per CTA
@@ -282,6 +294,7 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
   s.ncw = ncw;
   s.rows_base = rows_base;
   s.rows_extra = rows_extra;
+  s.gran = row_gran;
   s.fwht_B = c.signs ? static_cast<int>(c.fwht_block) : 0;
   s.nsigns = c.signs ? static_cast<int>(c.nsigns) : 1;
   s.fwht_scale = c.signs ? static_cast<float>(1.0 / std::sqrt(static_cast<double>(c.fwht_block))) : 1.0f;

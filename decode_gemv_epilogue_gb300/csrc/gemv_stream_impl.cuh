@@ -284,8 +284,9 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
   int crank = 0;
   if constexpr (kSplit) crank = static_cast<int>(cluster_ctarank());
   const int rg = static_cast<int>(blockIdx.x) / S;  // row range of this CTA (its cluster's)
-  const int64_t r0 = static_cast<int64_t>(rg) * a.rows_base + min(rg, a.rows_extra);
-  const int nrows = a.rows_base + (rg < a.rows_extra ? 1 : 0);
+  const int64_t r0 = (static_cast<int64_t>(rg) * a.rows_base + min(rg, a.rows_extra)) * a.gran;
+  const int nrows = static_cast<int>(
+      min(static_cast<int64_t>((a.rows_base + (rg < a.rows_extra ? 1 : 0)) * a.gran), a.M - r0));
   const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
   const bool dual = kExt && a.W2 != nullptr;
   const bool norm = kExt && a.gamma != nullptr;

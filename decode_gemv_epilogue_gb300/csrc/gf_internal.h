@@ -79,8 +79,9 @@ struct StreamArgs {
   int stage_bytes;   // bytes reserved per stage
   int RC;            // rows per finalize chunk
   int ncw;           // consumer warps (= G * wpg)
-  int rows_base;     // rows per CTA (the first rows_extra CTAs take one more)
+  int rows_base;     // granules of rows per CTA (the first rows_extra CTAs take one more)
   int rows_extra;
+  int gran;          // rows per granule: 1, or a full tile's real rows
   int fwht_B;        // 0 = no prologue
   int nsigns;
   float fwht_scale;
