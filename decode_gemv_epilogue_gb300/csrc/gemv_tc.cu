@@ -3,9 +3,10 @@
 //
 // A CTA owns one tile of 128 rows of W and a slice of its K range.  Per 64-element K
 // stage, warp 0 loads the 128 x 64 f16 tile of W with one 2-D TMA copy (128-byte
-// swizzle, K-major: the tensor cores read it straight from shared memory); warps 2..5
-// write the batch's x for the same 64 elements next to it as f16 rows in the same
-// swizzled layout.  x is fp32, so each column is scaled by an exact power of two
+// swizzle, K-major: the tensor cores read it straight from shared memory) and the
+// batch's x for the same elements with one bulk copy per column (issued once the
+// preceding grid, which may write x, has finished; the first W stage goes out before
+// that); warps 2..5 turn the staged x into f16 rows of B in the same swizzled layout.  x is fp32, so each column is scaled by an exact power of two
 // (its largest |x| over the CTA's K slice lands in [2^14, 2^15)) and split into
 // hi = f16(x) and lo = f16(x - hi): B holds Np rows of hi followed by Np rows of lo
 // (Np = columns rounded up to 8).  One thread of warp 1 issues four
@@ -38,7 +39,6 @@ constexpr int kTcK = 64;                        // K elements per sub-tile: one 
 constexpr int kTcKSteps = kTcK / 16;            // MMAs per sub-tile (K = 16 each)
 constexpr int kTcThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2..5 x / epilogue
 constexpr int kTcABytes = kTcRows * kTcK * 2;   // 16 KB per sub-tile (a stage holds a.subs of them)
-constexpr int kTcPrefetch = 4;                  // stages of x in flight per converter thread
 constexpr int kTcMaxStages = 12;                // W tiles in flight
 // MMA m accumulates into accumulator m % kTcAcc: MMAs into the same TMEM columns wait
 // for each other's full latency, which a 128 x N x 16 MMA with small N does not amortise
@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   float* iscl = scl + 64;                               // [64]
   float* xch = reinterpret_cast<float*>(base + 2048);   // [S][Np][128]
   const uint32_t sA = sb + static_cast<uint32_t>(a.off_a), sB = sb + static_cast<uint32_t>(a.off_b);
+  const uint32_t sX = sb + static_cast<uint32_t>(a.off_x);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int crank = 0;
@@ -102,24 +103,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   pdl_trigger();
 
   if (warp == 0) {
-    // ------------------------------------------------------------ W tiles (TMA)
+    // ------------------------------------------------------------ W tiles and x (TMA)
     if (lane == 0) {
-      int issued = 0;
+      const int xrow = subs * kTcK;  // floats of one column per stage
+      auto issue_x = [&](int i) {
+        const int slot = i % NS;
+        for (int c = 0; c < a.ncols; ++c)
+          bulk_g2s(sX + static_cast<uint32_t>(slot * a.x_stage_bytes + c * xrow * 4),
+                   a.x + static_cast<int64_t>(c) * a.K + static_cast<int64_t>(st0 + i) * xrow,
+                   static_cast<uint32_t>(xrow * 4), fullA0 + 8u * slot);
+      };
+      int issued = 0, x_done = 0;  // stages whose W / x copies are out
+      bool waited = false;
       for (int i = 0; i < nmy; ++i) {
         const int slot = i % NS, round = i / NS;
         // the first NS stages are empty: no wait (see the stream kernel)
         if (i >= NS && !mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1), abort_flag,
                                             a.err))
           break;
-        mbar_arrive_expect_tx(fullA0 + 8u * slot, static_cast<uint32_t>(subs * kTcABytes));
+        mbar_arrive_expect_tx(fullA0 + 8u * slot,
+                              static_cast<uint32_t>(subs * kTcABytes + a.ncols * xrow * 4));
         for (int sbt = 0; sbt < subs; ++sbt)
           tma_load_2d(sA + static_cast<uint32_t>((slot * subs + sbt) * kTcABytes), &tmap,
                       ((st0 + i) * subs + sbt) * kTcK, row0, fullA0 + 8u * slot);
         ++issued;
+        if (!waited) {  // first W stage out: now x, once the preceding grid has finished
+          pdl_wait();
+          waited = true;
+        }
+        if (waited)
+          for (; x_done < issued; ++x_done) issue_x(x_done);
       }
-      if (issued < nmy)  // aborted: wait (bounded) for the copies in flight
+      if (issued < nmy) {  // aborted: complete the stages' x, then wait (bounded) for the copies in flight
+        if (!waited) pdl_wait();
+        for (; x_done < issued; ++x_done) issue_x(x_done);
         for (int i = max(0, issued - NS); i < issued; ++i)
           (void)mbar_wait(fullA0 + 8u * (i % NS), static_cast<uint32_t>((i / NS) & 1));
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
@@ -152,14 +172,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     auto xbar = [&]() { named_bar_sync(1, 128); };
     pdl_wait();  // x, aux and dst may belong to the preceding grid
     // scale 2^s per column with its largest |x| * 2^s in [2^14, 2^15): maxima over this
-    // CTA's K slice, four columns per pass so their loads are in flight together
+    // CTA's K slice, eight columns per pass so their loads are in flight together (under
+    // the weight stream an L2 round trip takes ~1-2 us)
     const int k0 = st0 * subs * kTcK, klen4 = nmy * subs * kTcK / 4;
-    for (int n0 = 0; n0 < a.ncols; n0 += 4) {
-      float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int n0 = 0; n0 < a.ncols; n0 += 8) {
+      float m[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 4
       for (int i = ctid; i < klen4; i += 128) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           if (n0 + u < a.ncols) {
             const float4 v = reinterpret_cast<const float4*>(a.x + static_cast<int64_t>(n0 + u) * a.K + k0)[i];
             m[u] = fmaxf(m[u], fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
@@ -167,7 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], off));
         if (lane == 0 && n0 + u < a.ncols) smax[cw * 64 + n0 + u] = m[u];
@@ -187,51 +208,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     }
     xbar();
     // B rows per stage: chunk ch = (column n, 8 elements c8) with Np * 8 <= 128 chunks, so
-    // thread ctid owns chunk ctid of every stage; the x of the next kTcPrefetch stages
-    // is in flight in registers while this stage waits for its slot and converts
+    // thread ctid owns chunk ctid of every sub-tile; a stage's x lands with its W tile
+    // (same barrier), by which time the MMAs that read the slot's previous B are done
     const bool has_chunk = ctid < Np * 8;
     const int n_own = ctid >> 3, c8_own = ctid & 7;
     const bool live = has_chunk && n_own < a.ncols;
-    const float* xcol = a.x + static_cast<int64_t>(live ? n_own : 0) * a.K + st0 * subs * kTcK + 8 * c8_own;
     const int nu = nmy * subs;  // sub-tiles of this CTA
-    float4 pre[kTcPrefetch][2];
-#pragma unroll
-    for (int d = 0; d < kTcPrefetch; ++d)
-      if (live && d < nu) {
-        pre[d][0] = reinterpret_cast<const float4*>(xcol + d * kTcK)[0];
-        pre[d][1] = reinterpret_cast<const float4*>(xcol + d * kTcK)[1];
-      }
     const float sc_own = live ? scl[n_own] : 1.0f;
     bool ok = true;
-    for (int u0 = 0; u0 < nu; u0 += kTcPrefetch) {
-#pragma unroll
-      for (int d = 0; d < kTcPrefetch; ++d) {  // register slot d holds sub-tile u0 + d
-        const int u = u0 + d;
-        if (u >= nu) break;
-        const float4 c0 = pre[d][0], c1 = pre[d][1];
-        if (live && u + kTcPrefetch < nu) {
-          pre[d][0] = reinterpret_cast<const float4*>(xcol + (u + kTcPrefetch) * kTcK)[0];
-          pre[d][1] = reinterpret_cast<const float4*>(xcol + (u + kTcPrefetch) * kTcK)[1];
-        }
+    for (int u = 0; u < nu; ++u) {
+      {
         const int i = u / subs, sbt = u - i * subs;
         const int slot = i % NS, round = i / NS;
-        if (sbt == 0 && i >= NS)
-          ok = ok && mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1), abort_flag,
-                                        a.err);
+        if (sbt == 0)
+          ok = ok && mbar_wait_or_abort(fullA0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag, a.err);
+        float4 c0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), c1 = c0;
+        if (ok && live) {
+          const float* xs = reinterpret_cast<const float*>(base + a.off_x + slot * a.x_stage_bytes) +
+                            n_own * subs * kTcK + sbt * kTcK + 8 * c8_own;
+          c0 = reinterpret_cast<const float4*>(xs)[0];
+          c1 = reinterpret_cast<const float4*>(xs)[1];
+        }
         if (ok && has_chunk) {
           uint8_t* bt = base + a.off_b + slot * a.b_stage_bytes + sbt * b_sub_bytes;
           uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = make_uint4(0u, 0u, 0u, 0u);
           if (live) {
-            const float v[8] = {c0.x * sc_own, c0.y * sc_own, c0.z * sc_own, c0.w * sc_own,
-                                c1.x * sc_own, c1.y * sc_own, c1.z * sc_own, c1.w * sc_own};
+            // hi = f16(x * 2^s), lo = f16(x * 2^s - hi), two elements per conversion
+            const float2 sc2 = make_float2(sc_own, sc_own);
+            const float2 v[4] = {fmul2(make_float2(c0.x, c0.y), sc2), fmul2(make_float2(c0.z, c0.w), sc2),
+                                 fmul2(make_float2(c1.x, c1.y), sc2), fmul2(make_float2(c1.z, c1.w), sc2)};
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-              const __half h0 = __float2half_rn(v[2 * t]), h1 = __float2half_rn(v[2 * t + 1]);
-              const __half l0 = __float2half_rn(v[2 * t] - __half2float(h0));
-              const __half l1 = __float2half_rn(v[2 * t + 1] - __half2float(h1));
-              hw[t] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-              lw[t] = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+              const __half2 h = __floats2half2_rn(v[t].x, v[t].y);
+              const float2 r = fsub2(v[t], __half22float2(h));
+              const __half2 l = __floats2half2_rn(r.x, r.y);
+              hw[t] = *reinterpret_cast<const uint32_t*>(&h);
+              lw[t] = *reinterpret_cast<const uint32_t*>(&l);
             }
             hv = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             lv = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -361,7 +374,7 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
   int subs = 1, NS = 0;
   for (int cand = 4; cand >= 1; cand /= 2) {
     if (nsub_all % cand != 0 || nsub_all / cand < S) continue;
-    const int ns = std::min(kTcMaxStages, avail / (cand * (kTcABytes + nb * 128)));
+    const int ns = std::min(kTcMaxStages, avail / (cand * (kTcABytes + nb * 128 + ncols * kTcK * 4)));
     if (ns >= 3 || cand == 1) {
       subs = cand;
       NS = ns;
@@ -385,8 +398,10 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
   a.off_a = off_a;
   a.off_b = off_a + NS * subs * kTcABytes;
   a.b_stage_bytes = subs * nb * 128;
+  a.off_x = a.off_b + NS * a.b_stage_bytes;
+  a.x_stage_bytes = subs * ncols * kTcK * 4;
   p.grid = static_cast<int>(tiles * S);
-  p.smem = 1024 + a.off_b + NS * a.b_stage_bytes;
+  p.smem = 1024 + a.off_x + NS * a.x_stage_bytes;
   return true;
 }
 

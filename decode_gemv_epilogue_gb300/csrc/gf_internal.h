@@ -132,6 +132,8 @@ struct TcArgs {
   int tmem_cols;      // tensor-memory columns allocated (power of two >= 2 Np, >= 32)
   int off_a, off_b;   // stage offsets from the 1024-aligned shared-memory base
   int b_stage_bytes;  // 2 Np rows of 128 bytes
+  int off_x;          // x stages: ncols rows of 64 * subs floats per stage
+  int x_stage_bytes;
 };
 
 struct TcPlan {
