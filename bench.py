@@ -145,42 +145,37 @@ class Step:
         # kernels launched per step (a prologue call launches the transform, then the GEMV)
         self.kernels_per_step = sum(2 if fw else 1 for (n, wt, M, K, e, nc, fw) in spec)
 
+    def call_specs(self):
+        """(name, arguments, keyword arguments) of the step's gemv_fused_ex calls, on the
+        buffers the step holds now."""
+        W = self.W
+        return [
+            ("f16_add_view", (W["f16_add_view"], 1, self.x4096, 4096, 4096, 4, self.r4096, self.r4096),
+             {"view": (32, 128)}),
+            ("f16_sigmoid", (W["f16_sigmoid"], 1, self.xsig, 4096, 4096, 1, None, self.sig_out), {}),
+            ("q8_0_silu_mul", (W["q8_0_silu_mul"], 2, self.xq8, 11008, 4096, 3, self.m, self.gate_out), {}),
+            ("chain_q", (W["chain_q"], 3, self.cx, 4096, 4096, 0, None, self.cq), {}),
+            ("chain_k", (W["chain_k"], 3, self.cx, 4096, 4096, 0, None, self.ck), {}),
+            ("chain_v", (W["chain_v"], 3, self.cx, 4096, 4096, 0, None, self.cv), {}),
+            ("chain_o_add", (W["chain_o_add"], 3, self.ca, 4096, 4096, 4, self.cr, self.cr), {}),
+            ("chain_up", (W["chain_up"], 3, self.cr, 14336, 4096, 0, None, self.cup), {}),
+            ("chain_gate_silu_mul", (W["chain_gate_silu_mul"], 3, self.cr, 14336, 4096, 3, self.cup, self.cg), {}),
+            ("chain_down_add", (W["chain_down_add"], 3, self.cg, 4096, 14336, 4, self.cr, self.cr), {}),
+            ("chain_beta_sigmoid", (W["chain_beta_sigmoid"], 3, self.cx, 32, 4096, 1, None, self.cbeta), {}),
+            ("fwht_f16_add_n1", (W["fwht_f16_add_n1"], 1, self.fx1, 5120, 5120, 4, self.fr1, self.fr1),
+             {"fwht_signs": self.signs, "fwht_block": 1024, "fwht_workspace": self.ws1}),
+            ("fwht_f16_add_n8", (W["fwht_f16_add_n8"], 1, self.fx8, 5120, 5120, 4, self.fr8, self.fr8),
+             {"ncols": 8, "fwht_signs": self.signs, "fwht_block": 1024, "fwht_workspace": self.ws8}),
+        ]
+
     def calls(self, pdl=True, stream=None):
-        G, W = self.G, self.W
-        c = []
-        add = lambda name, fn: c.append((name, fn))
-        st = stream
-        add("f16_add_view", lambda: G.gemv_fused_ex(W["f16_add_view"], 1, self.x4096, 4096, 4096, 4,
-                                                    self.r4096, self.r4096, view=(32, 128), pdl=pdl, stream=st))
-        add("f16_sigmoid", lambda: G.gemv_fused_ex(W["f16_sigmoid"], 1, self.xsig, 4096, 4096, 1, None,
-                                                   self.sig_out, pdl=pdl, stream=st))
-        add("q8_0_silu_mul", lambda: G.gemv_fused_ex(W["q8_0_silu_mul"], 2, self.xq8, 11008, 4096, 3, self.m,
-                                                     self.gate_out, pdl=pdl, stream=st))
-        add("chain_q", lambda: G.gemv_fused_ex(W["chain_q"], 3, self.cx, 4096, 4096, 0, None, self.cq, pdl=pdl,
-                                               stream=st))
-        add("chain_k", lambda: G.gemv_fused_ex(W["chain_k"], 3, self.cx, 4096, 4096, 0, None, self.ck, pdl=pdl,
-                                               stream=st))
-        add("chain_v", lambda: G.gemv_fused_ex(W["chain_v"], 3, self.cx, 4096, 4096, 0, None, self.cv, pdl=pdl,
-                                               stream=st))
-        add("chain_o_add", lambda: G.gemv_fused_ex(W["chain_o_add"], 3, self.ca, 4096, 4096, 4, self.cr,
-                                                   self.cr, pdl=pdl, stream=st))
-        add("chain_up", lambda: G.gemv_fused_ex(W["chain_up"], 3, self.cr, 14336, 4096, 0, None, self.cup,
-                                                pdl=pdl, stream=st))
-        add("chain_gate_silu_mul", lambda: G.gemv_fused_ex(W["chain_gate_silu_mul"], 3, self.cr, 14336, 4096,
-                                                           3, self.cup, self.cg, pdl=pdl, stream=st))
-        add("chain_down_add", lambda: G.gemv_fused_ex(W["chain_down_add"], 3, self.cg, 4096, 14336, 4,
-                                                      self.cr, self.cr, pdl=pdl, stream=st))
-        add("chain_beta_sigmoid", lambda: G.gemv_fused_ex(W["chain_beta_sigmoid"], 3, self.cx, 32, 4096, 1,
-                                                          None, self.cbeta, pdl=pdl, stream=st))
-        add("fwht_f16_add_n1", lambda: G.gemv_fused_ex(W["fwht_f16_add_n1"], 1, self.fx1, 5120, 5120, 4,
-                                                       self.fr1, self.fr1, fwht_signs=self.signs,
-                                                       fwht_block=1024, pdl=pdl, fwht_workspace=self.ws1,
-                                                       stream=st))
-        add("fwht_f16_add_n8", lambda: G.gemv_fused_ex(W["fwht_f16_add_n8"], 1, self.fx8, 5120, 5120, 4,
-                                                       self.fr8, self.fr8, ncols=8, fwht_signs=self.signs,
-                                                       fwht_block=1024, pdl=pdl, fwht_workspace=self.ws8,
-                                                       stream=st))
-        return c
+        G = self.G
+        return [(name, (lambda a=a, kw=kw: G.gemv_fused_ex(*a, pdl=pdl, stream=stream, **kw)))
+                for (name, a, kw) in self.call_specs()]
+
+    def prepared(self, pdl=True):
+        """The step's calls planned once (gf_prepare), in order."""
+        return [(name, self.G.prepare(*a, pdl=pdl, **kw)) for (name, a, kw) in self.call_specs()]
 
     # the end-to-end leg: every per-step activation in one device arena laid out as
     # [results only | residuals (read and written in place) | inputs only], mirrored by a
@@ -763,18 +758,21 @@ def epilogue_cost(G, torch, s):
 
 def e2e_measure(G, torch, step, s, args):
     """The same step through the public API from pinned host memory: every step copies its
-    activations host->device (one copy), runs the 13 ABI calls and copies every result
-    back (one copy)."""
+    activations host->device (one copy), launches the step's graph of the 13 prepared
+    calls and copies every result back (one copy)."""
     arena, host, (i0, i1), (o0, o1) = step.pack_for_e2e()
-    calls = step.calls(pdl=True, stream=s.cuda_stream)
+    # the decode loop's calls, planned once on the step's buffers (gf_prepare) and
+    # recorded as one graph (gf_graph_create); each step is one gf_graph_launch
+    prepared = [h for _, h in step.prepared(pdl=True)]
+    graph = G.Graph(prepared)
     reps = max(5, min(args.steps, 200))
     d_in, h_in = arena[i0:i1], host[i0:i1]
     d_out, h_out = arena[o0:o1], host[o0:o1]
+    st = s.cuda_stream
 
     def one():
         d_in.copy_(h_in, non_blocking=True)
-        for _, fn in calls:
-            fn()
+        graph.launch(stream=st)
         h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(s):
@@ -795,8 +793,9 @@ def e2e_measure(G, torch, step, s, args):
     bo = h_out.numel() * h_out.element_size()
     return {"value": round(step.step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 6), "wall_ms_per_step": round(1e3 * wall / reps, 6),
-            "steps": reps, "launch_mode": "eager ABI calls with programmatic dependent launch, one H2D and one "
-                                          "D2H copy per step from pinned host memory"}
+            "steps": reps, "launch_mode": "the step's 13 calls prepared once (gf_prepare) and recorded as one graph "
+                                          "(gf_graph_create, programmatic dependent launch inside); per step one "
+                                          "gf_graph_launch, one H2D and one D2H copy from pinned host memory"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle

@@ -9,6 +9,7 @@
 // overlap-guard state is kept between calls.
 #include <algorithm>
 #include <cmath>
+#include <new>
 #include <cstdint>
 #include <cstring>
 #include <limits>
@@ -358,46 +359,46 @@ static int plan_call(const Call& c, Plan& p, int* generic_smem, int* generic_gri
   return PATH_GENERIC;
 }
 
-static int launch_one(const Call& c, float* dst, cudaStream_t st);
-
-// A batch wider than one launch takes runs in column blocks (kMaxCols columns on the
-// CUDA-core kernels, kTcMaxCols on the tensor cores) in consecutive launches (each
-// streams W again).  Later blocks may start early (programmatic dependent launch): they
-// read and write only their own columns.
-static int launch_call(const Call& c, float* dst, cudaStream_t st) {
-  const int64_t width = tc_eligible(c) ? kTcMaxCols : kMaxCols;
-  if (c.ncols <= width) return launch_one(c, dst, st);
-  for (int64_t c0 = 0; c0 < c.ncols; c0 += width) {
-    Call b = c;
-    b.ncols = std::min<int64_t>(width, c.ncols - c0);
-    b.x = c.x + c0 * c.K;
-    b.aux = c.aux ? c.aux + c0 * c.M : nullptr;
-    b.dst = dst + c0 * c.M;
-    if (c0 > 0) b.flags |= GF_FLAG_PDL;
-    const int e = launch_one(b, dst + c0 * c.M, st);
-    if (e != GF_OK) return e;
-  }
-  return GF_OK;
-}
-
-static int launch_one(const Call& c, float* dst, cudaStream_t st) {
-  Plan p;
+// One kernel launch with every argument resolved: what a call plans, and what a
+// prepared call keeps (gf_prepare) so that launching it does no planning at all.
+enum { REC_FWHT = 0, REC_TC = 1, REC_STREAM = 2, REC_GENERIC = 3 };
+struct LaunchRec {
+  int kind;
+  bool pdl;
+  int wtype, ncols;
+  const void* W;  // tensor-core path: the matrix of the tensor map
+  const float* fx;  // stand-alone FWHT
+  const float* fsigns;
+  float* fdst;
+  int64_t fn;
+  int fB, fnsigns;
   TcPlan tp;
+  Plan p;
+  GenericArgs g;
+  int ggrid, gsmem;
+};
+constexpr int kMaxRecs = 1 + kMaxBatch / kMaxCols;  // transform + column blocks
+
+// Plans one launch of at most one column block into r.
+static int plan_one(const Call& c, float* dst, LaunchRec& r) {
   int gsmem = 0, ggrid = 0;
-  const int path = plan_call(c, p, &gsmem, &ggrid, &tp);
+  const int path = plan_call(c, r.p, &gsmem, &ggrid, &r.tp);
   if (path < 0) return path;
   unsigned* err = device_error_word();
   if (!err) return cuda_fail(cudaGetLastError());
-  const bool pdl = (c.flags & GF_FLAG_PDL) != 0;
-  int e;
+  r.pdl = (c.flags & GF_FLAG_PDL) != 0;
+  r.wtype = c.wtype;
+  r.ncols = static_cast<int>(c.ncols);
+  r.W = c.W;
   if (path == PATH_TC) {
-    tp.a.x = c.x;
-    tp.a.aux = c.aux;
-    tp.a.dst = dst;
-    tp.a.err = err;
-    e = launch_tc(tp, c.W, st, pdl);
+    r.kind = REC_TC;
+    r.tp.a.x = c.x;
+    r.tp.a.aux = c.aux;
+    r.tp.a.dst = dst;
+    r.tp.a.err = err;
   } else if (path == PATH_STREAM) {
-    StreamArgs& s = p.s;
+    r.kind = REC_STREAM;
+    StreamArgs& s = r.p.s;
     s.W = static_cast<const uint8_t*>(c.W);
     s.x = c.x;
     s.aux = c.aux;
@@ -406,19 +407,9 @@ static int launch_one(const Call& c, float* dst, cudaStream_t st) {
     s.err = err;
     s.W2 = static_cast<const uint8_t*>(c.W2);
     s.gamma = c.gamma;
-    const int nc = static_cast<int>(c.ncols);
-    const bool fl = (c.wtype == GF_F32 || c.wtype == GF_F16);
-    if (c.wtype == GF_Q4_K)
-      e = s.S > 1 ? launch_stream_q4k_split(nc, p, st, pdl)
-          : (c.W2 || c.gamma) ? launch_stream_q4k_ext(nc, p, st, pdl) : launch_stream_q4k_plain(nc, p, st, pdl);
-    else if (s.S > 1)
-      e = fl ? launch_stream_float_split(c.wtype, nc, p, st, pdl) : launch_stream_block_split(c.wtype, nc, p, st, pdl);
-    else if (c.W2 || c.gamma)
-      e = fl ? launch_stream_float_ext(c.wtype, nc, p, st, pdl) : launch_stream_block_ext(c.wtype, nc, p, st, pdl);
-    else
-      e = fl ? launch_stream_float_plain(c.wtype, nc, p, st, pdl) : launch_stream_block_plain(c.wtype, nc, p, st, pdl);
   } else {
-    GenericArgs g;
+    r.kind = REC_GENERIC;
+    GenericArgs& g = r.g;
     g.W = static_cast<const uint8_t*>(c.W);
     g.x = c.x;
     g.aux = c.aux;
@@ -435,28 +426,97 @@ static int launch_one(const Call& c, float* dst, cudaStream_t st) {
     g.W2 = static_cast<const uint8_t*>(c.W2);
     g.gamma = c.gamma;
     g.norm_eps = c.gamma ? c.eps : 0.0f;
-    e = launch_generic(c.wtype, static_cast<int>(c.ncols), g, ggrid, gsmem, st, pdl);
+    r.ggrid = ggrid;
+    r.gsmem = gsmem;
   }
-  if (e != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(e));
   return GF_OK;
 }
 
-// The prologue as a stand-alone transform into the workspace, then the GEMV on it.
-// The GEMV is launched with programmatic dependent launch: it streams W while the
-// transform runs and waits for it before reading x' (W is not written by the
-// transform, so this holds whatever the caller's flags).
-static int launch_via_workspace(const Call& c, float* dst, cudaStream_t st) {
-  const int e = launch_fwht(c.x, c.signs, c.workspace, c.ncols * c.K, static_cast<int>(c.fwht_block),
-                            static_cast<int>(c.nsigns), st);
-  if (e != cudaSuccess) return cuda_fail(static_cast<cudaError_t>(e));
-  Call g = c;
-  g.x = c.workspace;
-  g.signs = nullptr;
-  g.fwht_block = 0;
-  g.nsigns = 0;
-  g.workspace = nullptr;
-  g.flags |= GF_FLAG_PDL;
-  return launch_call(g, dst, st);
+static int issue(const LaunchRec& r, cudaStream_t st) {
+  int e;
+  if (r.kind == REC_FWHT) {
+    e = launch_fwht(r.fx, r.fsigns, r.fdst, r.fn, r.fB, r.fnsigns, st);
+  } else if (r.kind == REC_TC) {
+    e = launch_tc(r.tp, r.W, st, r.pdl);
+  } else if (r.kind == REC_STREAM) {
+    const StreamArgs& s = r.p.s;
+    const int nc = r.ncols;
+    const bool fl = (r.wtype == GF_F32 || r.wtype == GF_F16);
+    const bool ext = s.W2 != nullptr || s.gamma != nullptr;
+    if (r.wtype == GF_Q4_K)
+      e = s.S > 1 ? launch_stream_q4k_split(nc, r.p, st, r.pdl)
+          : ext   ? launch_stream_q4k_ext(nc, r.p, st, r.pdl)
+                  : launch_stream_q4k_plain(nc, r.p, st, r.pdl);
+    else if (s.S > 1)
+      e = fl ? launch_stream_float_split(r.wtype, nc, r.p, st, r.pdl)
+             : launch_stream_block_split(r.wtype, nc, r.p, st, r.pdl);
+    else if (ext)
+      e = fl ? launch_stream_float_ext(r.wtype, nc, r.p, st, r.pdl)
+             : launch_stream_block_ext(r.wtype, nc, r.p, st, r.pdl);
+    else
+      e = fl ? launch_stream_float_plain(r.wtype, nc, r.p, st, r.pdl)
+             : launch_stream_block_plain(r.wtype, nc, r.p, st, r.pdl);
+  } else {
+    e = launch_generic(r.wtype, r.ncols, r.g, r.ggrid, r.gsmem, st, r.pdl);
+  }
+  return e != cudaSuccess ? cuda_fail(static_cast<cudaError_t>(e)) : GF_OK;
+}
+
+// The launches of a validated call, in order, into recs[0 .. *n).  A batch wider than
+// one launch takes runs in column blocks (kMaxCols columns on the CUDA-core kernels,
+// kTcMaxCols on the tensor cores) in consecutive launches (each streams W again); later
+// blocks may start early (programmatic dependent launch): they read and write only
+// their own columns.  With a workspace the prologue runs first as a stand-alone
+// transform into it, and the GEMV on it is launched with programmatic dependent launch:
+// it streams W while the transform runs and waits for it before reading x' (W is not
+// written by the transform, so this holds whatever the caller's flags).
+static int plan_launches(const Call& c0, float* dst, LaunchRec* recs, int* n) {
+  *n = 0;
+  if (c0.M == 0) return GF_OK;
+  Call c = c0;
+  if (c0.workspace && c0.K > 0) {
+    LaunchRec& f = recs[(*n)++];
+    f.kind = REC_FWHT;
+    f.pdl = false;
+    f.fx = c0.x;
+    f.fsigns = c0.signs;
+    f.fdst = c0.workspace;
+    f.fn = c0.ncols * c0.K;
+    f.fB = static_cast<int>(c0.fwht_block);
+    f.fnsigns = static_cast<int>(c0.nsigns);
+    c.x = c0.workspace;
+    c.signs = nullptr;
+    c.fwht_block = 0;
+    c.nsigns = 0;
+    c.workspace = nullptr;
+    c.flags |= GF_FLAG_PDL;
+  }
+  const int64_t width = tc_eligible(c) ? kTcMaxCols : kMaxCols;
+  for (int64_t col = 0; col < c.ncols; col += width) {
+    Call b = c;
+    b.ncols = std::min<int64_t>(width, c.ncols - col);
+    b.x = c.x + col * c.K;
+    b.aux = c.aux ? c.aux + col * c.M : nullptr;
+    b.dst = dst + col * c.M;
+    if (col > 0) b.flags |= GF_FLAG_PDL;
+    if (*n >= kMaxRecs) return GF_ERR_UNSUPPORTED;
+    const int e = plan_one(b, dst + col * c.M, recs[*n]);
+    if (e != GF_OK) return e;
+    ++*n;
+  }
+  return GF_OK;
+}
+
+static int run_call(const Call& c, float* dst, cudaStream_t st) {
+  LaunchRec recs[kMaxRecs];
+  int n = 0;
+  const int e = plan_launches(c, dst, recs, &n);
+  if (e != GF_OK) return e;
+  for (int i = 0; i < n; ++i) {
+    const int r = issue(recs[i], st);
+    if (r != GF_OK) return r;
+  }
+  return GF_OK;
 }
 
 static Call make_call(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
@@ -522,9 +582,7 @@ int gemv_fused_ex(const void* W, int wtype, const float* x, int64_t M, int64_t K
   if (v != GF_OK) return v;
   v = check_view(opts, M);
   if (v != GF_OK) return v;
-  if (M == 0) return GF_OK;
-  if (c.workspace && c.K > 0) return launch_via_workspace(c, dst, static_cast<cudaStream_t>(stream));
-  return launch_call(c, dst, static_cast<cudaStream_t>(stream));
+  return run_call(c, dst, static_cast<cudaStream_t>(stream));
 }
 
 int gemv_fused(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
@@ -547,9 +605,7 @@ int gemv_glu(const void* W_gate, const void* W_up, int wtype, const float* x, in
   if (v != GF_OK) return v;
   v = check_view(opts, M);
   if (v != GF_OK) return v;
-  if (M == 0) return GF_OK;
-  if (c.workspace && c.K > 0) return launch_via_workspace(c, dst, static_cast<cudaStream_t>(stream));
-  return launch_call(c, dst, static_cast<cudaStream_t>(stream));
+  return run_call(c, dst, static_cast<cudaStream_t>(stream));
 }
 
 static int plan_info(const Call& c, const gf_opts* opts, int64_t info[8]) {
@@ -688,6 +744,131 @@ const char* gf_status_string(int status) {
 
 int gf_last_cuda_error(void) { return t_last_cuda_error; }
 
-int gf_version(void) { return 2; }
+int gf_version(void) { return 3; }
+
+// ------------------------------------------------------------------ prepared calls
+struct gf_prepared {
+  int device;
+  int n;
+  gf::LaunchRec recs[gf::kMaxRecs];
+};
+
+static int prepare(const Call& c, const gf_opts* opts, gf_prepared** out) {
+  if (!out) return GF_ERR_INVALID;
+  *out = nullptr;
+  int v = validate(c);
+  if (v != GF_OK) return v;
+  v = check_view(opts, c.M);
+  if (v != GF_OK) return v;
+  gf_prepared* p = new (std::nothrow) gf_prepared;
+  if (!p) return GF_ERR_INVALID;
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return cuda_fail(cudaGetLastError());
+  }
+  v = plan_launches(c, const_cast<float*>(c.dst), p->recs, &p->n);  // dst came in as float*
+  if (v != GF_OK) {
+    delete p;
+    return v;
+  }
+  *out = p;
+  return GF_OK;
+}
+
+int gf_prepare(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue, const float* aux,
+               float* dst, const gf_opts* opts, gf_prepared** out) {
+  return prepare(make_call(W, wtype, x, M, K, epilogue, aux, dst, opts), opts, out);
+}
+
+int gf_prepare_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M, int64_t K, float* dst,
+                   const gf_opts* opts, gf_prepared** out) {
+  return prepare(make_glu_call(W_gate, W_up, wtype, x, M, K, dst, opts), opts, out);
+}
+
+int gf_launch_prepared(const gf_prepared* const* calls, int n, void* stream) {
+  if (n < 0 || (n > 0 && !calls)) return GF_ERR_INVALID;
+  for (int i = 0; i < n; ++i)
+    if (!calls[i]) return GF_ERR_INVALID;
+  int dev = -1;
+  if (n > 0 && cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError());
+  for (int i = 0; i < n; ++i)
+    if (calls[i]->device != dev) return GF_ERR_INVALID;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < n; ++i)
+    for (int k = 0; k < calls[i]->n; ++k) {
+      const int e = gf::issue(calls[i]->recs[k], st);
+      if (e != GF_OK) return e;
+    }
+  return GF_OK;
+}
+
+void gf_free_prepared(gf_prepared* p) { delete p; }
+
+// ------------------------------------------------------------------ step graphs
+struct gf_graph {
+  int device;
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+int gf_graph_create(const gf_prepared* const* calls, int n, gf_graph** out) {
+  if (!out) return GF_ERR_INVALID;
+  *out = nullptr;
+  if (n < 1 || !calls) return GF_ERR_INVALID;
+  for (int i = 0; i < n; ++i)
+    if (!calls[i]) return GF_ERR_INVALID;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError());
+  for (int i = 0; i < n; ++i)
+    if (calls[i]->device != dev) return GF_ERR_INVALID;
+  cudaStream_t s = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+  int st = GF_OK;
+  if (e == cudaSuccess) {
+    st = gf_launch_prepared(calls, n, s);
+    e = cudaStreamEndCapture(s, &g);  // ends the capture whatever the launches returned
+  }
+  cudaStreamDestroy(s);
+  if (e != cudaSuccess || st != GF_OK) {
+    if (g) cudaGraphDestroy(g);
+    return st != GF_OK ? st : cuda_fail(e);
+  }
+  cudaGraphExec_t x = nullptr;
+  e = cudaGraphInstantiate(&x, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return cuda_fail(e);
+  }
+  gf_graph* r = new (std::nothrow) gf_graph;
+  if (!r) {
+    cudaGraphExecDestroy(x);
+    cudaGraphDestroy(g);
+    return GF_ERR_INVALID;
+  }
+  r->device = dev;
+  r->graph = g;
+  r->exec = x;
+  *out = r;
+  return GF_OK;
+}
+
+int gf_graph_launch(const gf_graph* g, void* stream) {
+  if (!g) return GF_ERR_INVALID;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError());
+  if (dev != g->device) return GF_ERR_INVALID;
+  const cudaError_t e = cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? GF_OK : cuda_fail(e);
+}
+
+void gf_graph_free(gf_graph* g) {
+  if (!g) return;
+  cudaGraphExecDestroy(g->exec);
+  cudaGraphDestroy(g->graph);
+  delete g;
+}
 
 }  // extern "C"

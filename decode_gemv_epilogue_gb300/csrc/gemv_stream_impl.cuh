@@ -652,7 +652,12 @@ int launch_stream_t(const Plan& p, cudaStream_t st, bool pdl) {
 template <int WT, int NC>
 int max_active_clusters_t(const Plan& p) {
   auto kern = gemv_stream_kernel<WT, NC, FEAT_SPLIT>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem) != cudaSuccess) {
+  // raise the limit to the device maximum, never below what a launch of this kernel set
+  int dev = 0, smem_max = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      smem_max < p.smem ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }

@@ -351,6 +351,44 @@ static EncodeTiledFn encode_tiled() {
 
 static int round_up_i(int v, int a) { return (v + a - 1) / a * a; }
 
+// Clusters of S CTAs of the split kernel that can be resident at once (0 if the device
+// cannot be asked): a cluster's CTAs share a GPC, so clusters of S may fit fewer times
+// than SMs / S.  Every plan holds one CTA per SM; the answer is kept per device and S.
+// The query raises the kernel's shared-memory limit to the device maximum, which keeps
+// every later launch's own (smaller) setting valid.
+static int tc_max_clusters(int S, int smem_max) {
+  static int cache[64][kMaxSplit + 1];
+  static bool init[64][kMaxSplit + 1];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || S < 2 || S > kMaxSplit) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (init[dev][S]) return cache[dev][S];
+  int n = 0;
+  auto kern = gemv_tc_kernel<true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S * 64);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = 160 * 1024;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cache[dev][S] = n;
+  init[dev][S] = true;
+  return n;
+}
+
 bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, TcPlan& p) {
   if (M < 1 || K < kTcK || K % kTcK != 0 || K > INT32_MAX / 2 || M > INT32_MAX - kTcRows) return false;
   if (ncols < 1 || ncols > kTcMaxCols) return false;
@@ -364,6 +402,11 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
   int S = static_cast<int>(std::min<int64_t>(kMaxSplit, lim.sm_count / std::max<int64_t>(tiles, 1)));
   S = std::min(S, nsub_all);
   S = std::min(S, (64 * 1024) / (Np * kTcRows * 4));
+  while (S >= 2) {  // every cluster resident at once (when the device can say)
+    const int fit = tc_max_clusters(S, lim.smem_optin);
+    if (fit == 0 || tiles <= fit) break;
+    --S;
+  }
   if (S < 2) S = 1;
   const int xch_bytes = S > 1 ? S * Np * kTcRows * 4 : 0;
   const int off_a = round_up_i(2048 + xch_bytes, 1024);

@@ -59,6 +59,15 @@ _selftest_wait = _sig("gf_selftest_wait_timeout", [_i64, _vp, _vp])
 _status_string = _sig("gf_status_string", [_i32], ctypes.c_char_p)
 _last_cuda_error = _sig("gf_last_cuda_error", [])
 _version = _sig("gf_version", [])
+_prepare = _sig("gf_prepare", [_vp, _i32, _vp, _i64, _i64, _i32, _vp, _vp, ctypes.POINTER(GfOpts),
+                               ctypes.POINTER(_vp)])
+_prepare_glu = _sig("gf_prepare_glu", [_vp, _vp, _i32, _vp, _i64, _i64, _vp, ctypes.POINTER(GfOpts),
+                                       ctypes.POINTER(_vp)])
+_launch_prepared = _sig("gf_launch_prepared", [ctypes.POINTER(_vp), _i32, _vp])
+_free_prepared = _sig("gf_free_prepared", [_vp], None)
+_graph_create = _sig("gf_graph_create", [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp)])
+_graph_launch = _sig("gf_graph_launch", [_vp, _vp])
+_graph_free = _sig("gf_graph_free", [_vp], None)
 
 #: the raw C functions, for callers that want the status codes themselves
 raw = _lib
@@ -153,6 +162,101 @@ def gemv_glu(W_gate, W_up, wtype, x, M, K, dst, ncols=1, fwht_signs=None, fwht_b
     if check:
         _check(st, "gemv_glu")
     return st
+
+
+class Prepared:
+    """A planned call (gf_prepare / gf_prepare_glu): launch() issues its kernels with no
+    planning.  The buffers it was prepared with must stay allocated while it is used;
+    the handle is released when the object is garbage-collected (or by close())."""
+
+    def __init__(self, handle, keep):
+        self._h = _vp(handle)
+        self._keep = keep  # the options struct and tensors the handle points into
+
+    @property
+    def handle(self):
+        return self._h
+
+    def launch(self, stream=None, check=True):
+        return launch_prepared([self], stream=stream, check=check)
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            _free_prepared(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def prepare(W, wtype, x, M, K, epilogue, aux, dst, ncols=1, fwht_signs=None, fwht_block=0, nsigns=None,
+            view=None, pdl=False, fwht_workspace=None, rms_norm_weight=None, rms_norm_eps=0.0, split_k=True,
+            tensor_cores=True, check=True):
+    """gf_prepare: the call gemv_fused_ex(...) would make, planned once (see Prepared)."""
+    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, view, pdl, fwht_workspace, rms_norm_weight,
+                  rms_norm_eps, split_k, tensor_cores)
+    h = _vp()
+    st = _prepare(_ptr(W), wtype, _ptr(x), M, K, epilogue, _ptr(aux), _ptr(dst), ctypes.byref(o), ctypes.byref(h))
+    if check:
+        _check(st, "gf_prepare")
+    return Prepared(h.value, (W, x, aux, dst, fwht_signs, fwht_workspace, rms_norm_weight)) if st == OK else st
+
+
+def prepare_glu(W_gate, W_up, wtype, x, M, K, dst, ncols=1, fwht_signs=None, fwht_block=0, nsigns=None,
+                view=None, pdl=False, fwht_workspace=None, rms_norm_weight=None, rms_norm_eps=0.0, split_k=True,
+                check=True):
+    """gf_prepare_glu: the call gemv_glu(...) would make, planned once (see Prepared)."""
+    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, view, pdl, fwht_workspace, rms_norm_weight,
+                  rms_norm_eps, split_k)
+    h = _vp()
+    st = _prepare_glu(_ptr(W_gate), _ptr(W_up), wtype, _ptr(x), M, K, _ptr(dst), ctypes.byref(o), ctypes.byref(h))
+    if check:
+        _check(st, "gf_prepare_glu")
+    return Prepared(h.value, (W_gate, W_up, x, dst, fwht_signs, fwht_workspace, rms_norm_weight)) \
+        if st == OK else st
+
+
+def launch_prepared(calls, stream=None, check=True):
+    """gf_launch_prepared: issue the prepared calls' kernels in order on `stream`."""
+    arr = (_vp * max(1, len(calls)))(*[c.handle.value if isinstance(c, Prepared) else c for c in calls])
+    st = _launch_prepared(arr, len(calls), _stream(stream))
+    if check:
+        _check(st, "gf_launch_prepared")
+    return st
+
+
+class Graph:
+    """gf_graph_create: prepared calls recorded as one CUDA graph; launch() replays it."""
+
+    def __init__(self, calls, check=True):
+        arr = (_vp * max(1, len(calls)))(*[c.handle.value if isinstance(c, Prepared) else c for c in calls])
+        h = _vp()
+        st = _graph_create(arr, len(calls), ctypes.byref(h))
+        if check:
+            _check(st, "gf_graph_create")
+        self.status = st
+        self._h = h if st == OK else None
+        self._keep = list(calls)
+
+    def launch(self, stream=None, check=True):
+        st = _graph_launch(self._h, _stream(stream))
+        if check:
+            _check(st, "gf_graph_launch")
+        return st
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            _graph_free(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def gemv_fused_fwht_noalloc(W, wtype, x, M, K, epilogue, aux, dst, ncols, fwht_signs, fwht_block, nsigns=None,

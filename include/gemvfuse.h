@@ -162,6 +162,45 @@ GF_API int gemv_fused_ex(const void* W, int wtype, const float* x, int64_t M, in
 GF_API int gemv_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M,
                     int64_t K, float* dst, const gf_opts* opts, void* stream);
 
+/* Prepared calls: plan once, launch many times.  A decode loop issues the same GEMVs
+ * with the same buffers every step; gf_prepare / gf_prepare_glu validate and plan a
+ * call exactly as gemv_fused_ex / gemv_glu would (same arguments, same rules, same
+ * status codes) and keep every launch argument, so gf_launch_prepared only issues the
+ * kernels: no validation, planning or allocation per step.  The results are the ones
+ * the direct call gives (the same kernels with the same arguments).
+ *  out      : receives a handle owned by the caller, released with gf_free_prepared;
+ *             NULL on failure.  A call with M == 0 gives a handle that launches nothing.
+ *  Buffers  : the handle holds the device pointers given here (W, x, aux, dst, opts'
+ *             signs, workspace and RMS weight); their contents may change between
+ *             launches, the allocations must stay valid while the handle is used.
+ *  Device   : the handle belongs to the device current at gf_prepare; launching it
+ *             with another device current returns GF_ERR_INVALID. */
+typedef struct gf_prepared gf_prepared;
+GF_API int gf_prepare(const void* W, int wtype, const float* x, int64_t M, int64_t K, int epilogue,
+                      const float* aux, float* dst, const gf_opts* opts, gf_prepared** out);
+GF_API int gf_prepare_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M,
+                          int64_t K, float* dst, const gf_opts* opts, gf_prepared** out);
+/* Issues the launches of calls[0], ..., calls[n-1] in order on `stream` (n >= 0; the
+ * calls' GF_FLAG_PDL settings apply as given to gf_prepare).  Stops at the first
+ * failing launch and returns its status; GF_ERR_INVALID (nothing launched) for a NULL
+ * handle or one prepared on another device. */
+GF_API int gf_launch_prepared(const gf_prepared* const* calls, int n, void* stream);
+/* Releases a handle (NULL is ignored).  Launches already issued are not affected. */
+GF_API void gf_free_prepared(gf_prepared* p);
+
+/* A decode step as one launch: gf_graph_create records the launches of calls[0..n)
+ * (n >= 1, in order, as gf_launch_prepared would issue them, programmatic dependent
+ * launches included) into a CUDA graph and instantiates it; gf_graph_launch replays it
+ * on `stream` -- one host call for the whole sequence, and the launch overhead of a
+ * graph instead of one per kernel.  The graph keeps the prepared calls' arguments
+ * (the handles may be freed afterwards; their buffers must stay allocated).  It belongs
+ * to the device current at creation (another one: GF_ERR_INVALID).  Errors: NULL or
+ * foreign handles GF_ERR_INVALID; a failing capture or instantiation GF_ERR_CUDA. */
+typedef struct gf_graph gf_graph;
+GF_API int gf_graph_create(const gf_prepared* const* calls, int n, gf_graph** out);
+GF_API int gf_graph_launch(const gf_graph* g, void* stream);
+GF_API void gf_graph_free(gf_graph* g);
+
 /* Allocation-free variant of gemv_fused_ex with the signed-FWHT prologue.  The pages
  * have no counterpart: this entry point exists for callers that cannot allocate a
  * device workspace -- a C host that links only this library and has no device

@@ -26,7 +26,8 @@ def test_header_declares_the_abi():
     names = set(declared_functions())
     assert {"gemv_fused", "gemv_fused_ex", "gemv_glu", "fwht_signed", "gf_elementwise", "gf_dequantize",
             "gf_plan", "gf_plan_glu", "gf_device_status", "gf_status_string", "gf_last_cuda_error",
-            "gf_version"} <= names
+            "gf_version", "gf_prepare", "gf_prepare_glu", "gf_launch_prepared", "gf_free_prepared",
+            "gf_graph_create", "gf_graph_launch", "gf_graph_free"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -49,7 +50,7 @@ def test_status_strings(lib):
     assert lib.status_string(0) == "GF_OK"
     for s in (-1, -2, -3, -4, -5, -6):
         assert lib.status_string(s).startswith("GF_ERR_")
-    assert lib.version() == 2
+    assert lib.version() == 3
 
 
 def g(lib, *a, **k):
@@ -330,3 +331,43 @@ def test_selftest_wait_validation(lib):
     assert lib.selftest_wait_timeout(2000000, D, stream=0, check=False) == -1
     assert lib.selftest_wait_timeout(1000, None, stream=0, check=False) == -1
     assert lib.selftest_wait_timeout(1000, D + 2, stream=0, check=False) == -4
+
+
+# ----------------------------------------------------------------------------- prepared calls
+
+def test_prepare_validates_like_the_direct_call(lib):
+    # the same status as gemv_fused_ex, before anything is planned; no handle is returned
+    h = ctypes.c_void_p(123)
+    st = lib.raw.gf_prepare(ctypes.c_void_p(W), 9, ctypes.c_void_p(X), 64, 256, 0, None, ctypes.c_void_p(D),
+                            None, ctypes.byref(h))
+    assert st == lib.ERR_INVALID and not h.value
+    st = lib.raw.gf_prepare(ctypes.c_void_p(W), 1, ctypes.c_void_p(X), 64, 256, 0, None, ctypes.c_void_p(W + 64),
+                            None, ctypes.byref(h))  # dst inside W
+    assert st == lib.ERR_ALIAS and not h.value
+    st = lib.raw.gf_prepare(ctypes.c_void_p(W), 1, ctypes.c_void_p(X), 64, 256, 4, None, ctypes.c_void_p(D),
+                            None, ctypes.byref(h))  # ADD without its operand
+    assert st == lib.ERR_INVALID and not h.value
+    st = lib.raw.gf_prepare_glu(ctypes.c_void_p(W), ctypes.c_void_p(A), 1, ctypes.c_void_p(X), 64, 256,
+                                ctypes.c_void_p(W + 64), None, ctypes.byref(h))
+    assert st == lib.ERR_ALIAS and not h.value
+    # no place for the handle
+    assert lib.raw.gf_prepare(ctypes.c_void_p(W), 1, ctypes.c_void_p(X), 64, 256, 0, None, ctypes.c_void_p(D),
+                              None, None) == lib.ERR_INVALID
+
+
+def test_launch_prepared_arguments(lib):
+    arr = (ctypes.c_void_p * 2)(None, None)
+    assert lib.raw.gf_launch_prepared(arr, 0, None) == lib.OK  # nothing to launch
+    assert lib.raw.gf_launch_prepared(None, 1, None) == lib.ERR_INVALID
+    assert lib.raw.gf_launch_prepared(arr, -1, None) == lib.ERR_INVALID
+    lib.raw.gf_free_prepared(None)  # ignored
+
+
+def test_graph_arguments(lib):
+    h = ctypes.c_void_p(7)
+    arr = (ctypes.c_void_p * 1)(None)
+    assert lib.raw.gf_graph_create(arr, 0, ctypes.byref(h)) == lib.ERR_INVALID and not h.value
+    assert lib.raw.gf_graph_create(arr, 1, ctypes.byref(h)) == lib.ERR_INVALID and not h.value  # NULL handle
+    assert lib.raw.gf_graph_create(arr, 1, None) == lib.ERR_INVALID
+    assert lib.raw.gf_graph_launch(None, None) == lib.ERR_INVALID
+    lib.raw.gf_graph_free(None)  # ignored
