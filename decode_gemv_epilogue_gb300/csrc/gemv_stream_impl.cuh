@@ -176,37 +176,50 @@ __device__ __forceinline__ void consume_tile_q4k(uint32_t st, int seg, int rows,
   }
 }
 
-// Q4_0 through integer dot products: per row, the unit's codes against each column's
-// XInt; the block scale d times 2^-s scales the exact integer sum.  All rows' shared-
-// memory words are loaded before any arithmetic (the loads are ordered asm, so this
-// leaves the scheduler every row's dp4a chains to interleave); rows past the tile's end
-// read its last row and their sums are never stored.
-template <int NCT, int U, int RT>
+// Q4_0 / Q8_0 through integer dot products: per row, the unit's codes against each
+// column's XInt; the block scale d times 2^-s scales the exact integer sum.  All rows'
+// shared-memory words are loaded before any arithmetic (the loads are ordered asm, so
+// this leaves the scheduler every row's dp4a chains to interleave); rows past the tile's
+// end read its last row and their sums are never stored.
+template <int WT, int NCT, int U, int RT>
 __device__ __forceinline__ void consume_tile_int(uint32_t st, int seg, int rows, int units, int tg, int tg_n,
                                                  int g, int G, const XInt (&xq)[U][NCT], float2 (&acc)[RT][NCT]) {
+  constexpr bool kQ8 = WT == WT_Q8_0;
+  constexpr uint32_t kBlk = kQ8 ? 34u : 18u, kHalf = kQ8 ? 16u : 8u;
+  constexpr int kW = kQ8 ? 5 : 3;  // aligned words covering the unit's code bytes
 #pragma unroll
   for (int i = 0; i < U; ++i) {
     const uint32_t u = static_cast<uint32_t>(tg + i * tg_n);
     if (u < static_cast<uint32_t>(units)) {
-      const uint32_t off = (u >> 1) * 18u, start = off + 2u + 8u * (u & 1u);
+      const uint32_t off = (u >> 1) * kBlk, start = off + 2u + kHalf * (u & 1u);
       const uint32_t wa = start & ~3u, sh = (start & 3u) * 8u;
-      uint32_t dr[RT], wr[RT][3];
+      uint32_t dr[RT], wr[RT][kW];
 #pragma unroll
       for (int j = 0; j < RT; ++j) {
         const int r = min(g + j * G, rows - 1);
         const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
         dr[j] = ld.u16(off);
 #pragma unroll
-        for (int k = 0; k < 3; ++k) wr[j][k] = ld.u32(wa + 4u * k);
+        for (int k = 0; k < kW; ++k) wr[j][k] = ld.u32(wa + 4u * k);
       }
 #pragma unroll
       for (int j = 0; j < RT; ++j) {
-        const uint32_t w0 = __funnelshift_r(wr[j][0], wr[j][1], sh), w1 = __funnelshift_r(wr[j][1], wr[j][2], sh);
-        int t[NCT];
-        q4_0_words_int<NCT>(w0, w1, xq[i], t);
+        float t[NCT];
+        if constexpr (kQ8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(wr[j][k], wr[j][k + 1], sh);
+          q8_0_words_int<NCT>(w, xq[i], t);
+        } else {
+          int ti[NCT];
+          q4_0_words_int<NCT>(__funnelshift_r(wr[j][0], wr[j][1], sh), __funnelshift_r(wr[j][1], wr[j][2], sh),
+                              xq[i], ti);
+#pragma unroll
+          for (int c = 0; c < NCT; ++c) t[c] = static_cast<float>(ti[c]);
+        }
         const float d = h2f(dr[j]);
 #pragma unroll
-        for (int c = 0; c < NCT; ++c) acc[j][c].x = fmaf(d * xq[i][c].sc, static_cast<float>(t[c]), acc[j][c].x);
+        for (int c = 0; c < NCT; ++c) acc[j][c].x = fmaf(d * xq[i][c].sc, t[c], acc[j][c].x);
       }
     }
   }
@@ -486,7 +499,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
               consume_tile_q4k<NCT, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
                                         g, a.G, xr, xsum, acc);
             else if constexpr (kInt)
-              consume_tile_int<NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
+              consume_tile_int<WT, NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
                                            tg_n, g, a.G, xq, acc);
             else
               consume_tile<WT, NCT, U, RT, kBatch>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows,

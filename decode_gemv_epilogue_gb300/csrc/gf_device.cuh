@@ -497,7 +497,7 @@ __device__ __forceinline__ void q4k_nibbles(const uint4 q, uint32_t n, float2 (&
   }
 }
 
-// ---- integer dot products (Q4_0, single columns)
+// ---- integer dot products (Q4_0 and Q8_0, single columns)
 // A unit's 16 x values become integers X_j = trunc(x_j * 2^s) that share the exponent s
 // (chosen so that max |x_j| * 2^s lies in [2^22, 2^23), hence |X_j| <= 2^23 - 1).  Each
 // X_j is split into three bytes X = D2 * 2^16 + D1 * 2^8 + D0 (D2 signed, D1 and D0
@@ -522,6 +522,17 @@ __device__ __forceinline__ uint32_t dp4a_us(uint32_t a, uint32_t b, uint32_t c) 
 __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t dp4a_ss(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t dp4a_su(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 
@@ -573,6 +584,27 @@ __device__ __forceinline__ void q4_0_words_int(uint32_t w0, uint32_t w1, const X
       s0 = dp4a_uu(n[g], xq[c].d0[g], s0);
     }
     t[c] = static_cast<int>((s2 * 256u + s1) * 256u + s0);
+  }
+}
+
+// A Q8_0 unit's four code words (16 signed codes, group g = word g) against the XInt of
+// each of NCT columns: t[c] = sum_j q_j X_j.  |q_j| <= 128 and 24-bit X_j overflow 32
+// bits in one sum, so the three digit sums (each exact, |.| < 2^19 * 2) are combined in
+// float: t = S2 * 2^16 + S1 * 2^8 + S0, rounded once or twice to 24 bits.  (XInt.c, the
+// Q4_0 offset term, is not used.)
+template <int NCT>
+__device__ __forceinline__ void q8_0_words_int(const uint32_t (&w)[4], const XInt (&xq)[NCT], float (&t)[NCT]) {
+#pragma unroll
+  for (int c = 0; c < NCT; ++c) {
+    uint32_t s2 = 0u, s1 = 0u, s0 = 0u;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      s2 = dp4a_ss(w[g], xq[c].d2[g], s2);
+      s1 = dp4a_su(w[g], xq[c].d1[g], s1);
+      s0 = dp4a_su(w[g], xq[c].d0[g], s0);
+    }
+    t[c] = fmaf(static_cast<float>(static_cast<int>(s2)), 65536.0f,
+                fmaf(static_cast<float>(static_cast<int>(s1)), 256.0f, static_cast<float>(static_cast<int>(s0))));
   }
 }
 

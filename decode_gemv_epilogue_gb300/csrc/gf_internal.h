@@ -44,19 +44,19 @@ __host__ __device__ constexpr int stream_cs(int wt, int nc) {
   return (nc + stream_nct(wt, nc) - 1) / stream_nct(wt, nc);
 }
 __host__ __device__ constexpr int stream_u(int wt, int nc) {
-  return wt == 4 ? 2 : (wt == 3 && nc == 1) ? 1 : (nc == 1 && stream_quant(wt)) ? 2 : 1;
+  return wt == 4 ? 2 : ((wt == 3 || wt == 2) && nc == 1) ? 1 : (nc == 1 && stream_quant(wt)) ? 2 : 1;
 }
 __host__ __device__ constexpr int stream_rt(int wt, int nc) {
-  return (nc == 1 && wt == 2) ? 2 : (nc == 1 && wt == 3) ? 8 : 4;
+  return (nc == 1 && wt == 3) ? 8 : 4;
 }
 __host__ __device__ constexpr int stream_max_cw(int wt, int nc) { return stream_nct(wt, nc) <= 2 ? 16 : 8; }
 __host__ __device__ constexpr int stream_threads(int wt, int nc) { return 32 * (1 + stream_max_cw(wt, nc)); }
-// Q4_0 with up to kIntMaxCols columns takes integer dot products (x as shared-exponent
-// 24-bit integers, dp4a on the unpacked codes): a third of the instructions per weight of
-// the float decode.  With more columns per thread the float decode, done once for all of
-// them, is cheaper.
+// Q4_0 and Q8_0 with up to kIntMaxCols columns take integer dot products (x as shared-
+// exponent 24-bit integers, dp4a on the codes): a third (Q4_0) to a half (Q8_0) of the
+// instructions per weight of the float decode.  With more columns per thread the float
+// decode, done once for all of them, is cheaper.
 constexpr int kIntMaxCols = 1;
-__host__ __device__ constexpr bool stream_int(int wt, int nc) { return wt == 3 && nc <= kIntMaxCols; }
+__host__ __device__ constexpr bool stream_int(int wt, int nc) { return (wt == 3 || wt == 2) && nc <= kIntMaxCols; }
 
 struct StreamArgs {
   const uint8_t* W;
