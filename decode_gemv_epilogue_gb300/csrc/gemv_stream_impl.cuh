@@ -176,6 +176,47 @@ __device__ __forceinline__ void consume_tile_q4k(uint32_t st, int seg, int rows,
   }
 }
 
+// Q4_K through integer dot products: per row, one 16-byte code load and one unpack of the
+// scales for the thread's unit pair; each unit's nibbles against its XInt, scaled by
+// d * sc[j] * 2^-s, and the min term through the unit's sum of x.  Every row's loads
+// come first, as in consume_tile_int.
+template <int RT>
+__device__ __forceinline__ void consume_tile_q4k_int(uint32_t st, int seg, int rows, int units, int tg, int g,
+                                                     int G, const XInt (&xq)[2][1], const float (&xsum)[2][1],
+                                                     float2 (&acc)[RT][1]) {
+  if (2 * tg >= units) return;
+  const uint32_t p = static_cast<uint32_t>(tg), pp = p & 7u, gq = pp >> 1;
+  const uint32_t boff = (p >> 3) * kQ4kBytes;
+  uint32_t hdr[RT], sw[RT][3];
+  uint4 q[RT];
+#pragma unroll
+  for (int j = 0; j < RT; ++j) {
+    const int r = min(g + j * G, rows - 1);
+    const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+    hdr[j] = ld.word(boff);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) sw[j][k] = ld.word(boff + 4u + 4u * k);
+    q[j] = ld.quad(boff + 16u + 16u * pp);
+  }
+#pragma unroll
+  for (int j = 0; j < RT; ++j) {
+    float dsc[2], dmn[2];
+    q4k_scales_from(hdr[j], sw[j][0], sw[j][1], sw[j][2], gq, dsc, dmn);
+    const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+      uint32_t nb[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) nb[k] = (w[k] >> (4u * n)) & 0x0F0F0F0Fu;
+      const XInt (&xn)[1] = xq[n];
+      int t[1];
+      nibble_words_int<1, false>(nb, xn, t);
+      float a = fmaf(dsc[n] * xq[n][0].sc, static_cast<float>(t[0]), acc[j][0].x);
+      acc[j][0].x = fmaf(-dmn[n], xsum[n][0], a);
+    }
+  }
+}
+
 // Q4_0 / Q8_0 through integer dot products: per row, the unit's codes against each
 // column's XInt; the block scale d times 2^-s scales the exact integer sum.  All rows'
 // shared-memory words are loaded before any arithmetic (the loads are ordered asm, so
@@ -457,6 +498,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         // (integer path: each unit's x is converted as soon as it is loaded)
         float2 xr[kInt ? 1 : U][NCT][8];
         XInt xq[kInt ? U : 1][kInt ? NCT : 1];
+        float xsum[U][NCT];
         const float* gsrc = norm ? a.gamma + static_cast<int64_t>(kc) * a.kc_len : nullptr;
 #pragma unroll
         for (int i = 0; i < U; ++i) {
@@ -467,25 +509,21 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
               load_unit_x<WT, NCT, kExt>(xsrc, xstride, gsrc, u, qr, c0, NC, xv, rc0 == 0, ssq);
             else
               load_unit_x<WT, NCT, false>(xsrc, xstride, nullptr, u, qr, c0, NC, xv);
+            if constexpr (WT == WT_Q4_K) {  // the unit's sum of (scaled) x, for the sub-block min term
+#pragma unroll
+              for (int c = 0; c < NCT; ++c) {
+                float2 t = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) t = fadd2(t, xv[c][k]);
+                xsum[i][c] = t.x + t.y;
+              }
+            }
             if constexpr (kInt) {
 #pragma unroll
               for (int c = 0; c < NCT; ++c) x_to_int(xv[c], xq[i][c]);
             }
           }
         }
-        // Q4_K: the sum of each unit's (scaled) x, for the sub-block min term
-        float xsum[U][NCT];
-#pragma unroll
-        for (int i = 0; i < U; ++i)
-#pragma unroll
-          for (int c = 0; c < NCT; ++c) {
-            float2 t = make_float2(0.0f, 0.0f);
-            if constexpr (WT == WT_Q4_K) {
-#pragma unroll
-              for (int k = 0; k < 8; ++k) t = fadd2(t, xr[i][c][k]);
-            }
-            xsum[i][c] = t.x + t.y;
-          }
         for (int t0 = 0; t0 < nvr; t0 += a.R) {
           const int rows = min(a.R, nvr - t0);
           ok = ok && mbar_wait_or_abort(full0 + 8u * slot, fphase, abort_flag, a.err);
@@ -495,7 +533,10 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
 #pragma unroll
             for (int c = 0; c < NCT; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
           if (ok) {
-            if constexpr (WT == WT_Q4_K)
+            if constexpr (WT == WT_Q4_K && kInt)
+              consume_tile_q4k_int<RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg, g,
+                                       a.G, xq, xsum, acc);
+            else if constexpr (WT == WT_Q4_K)
               consume_tile_q4k<NCT, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
                                         g, a.G, xr, xsum, acc);
             else if constexpr (kInt)

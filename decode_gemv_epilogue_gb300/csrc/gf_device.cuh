@@ -455,14 +455,11 @@ __device__ __forceinline__ void decode_raw(const RawUnit<WT>& r, uint32_t u, flo
 // 2p + n is nibble n of those bytes: sub-block j = 2g + n, elements 32j + 16h .. + 15.
 constexpr uint32_t kQ4kBytes = 144;
 
-// d*sc[j] and dmin*m[j] (both exact in fp32) of sub-blocks 2g and 2g+1 of the
-// super-block at boff.
-template <class L>
-__device__ __forceinline__ void q4k_scales(const L& ld, uint32_t boff, uint32_t g, float (&dsc)[2],
-                                           float (&dmn)[2]) {
-  const uint32_t hdr = ld.word(boff);
+// d*sc[j] and dmin*m[j] (both exact in fp32) of sub-blocks 2g and 2g+1 of a super-block,
+// from its first four words (hdr = d | dmin << 16, then the 12 packed scale bytes).
+__device__ __forceinline__ void q4k_scales_from(uint32_t hdr, uint32_t s0, uint32_t s1, uint32_t s2, uint32_t g,
+                                                float (&dsc)[2], float (&dmn)[2]) {
   const float d = h2f(hdr & 0xFFFFu), dmin = h2f(hdr >> 16);
-  const uint32_t s0 = ld.word(boff + 4u), s1 = ld.word(boff + 8u), s2 = ld.word(boff + 12u);
   const bool upper = g >= 2u;  // sub-blocks 4..7: low bits in bytes 8..11, high bits in 0..7
 #pragma unroll
   for (uint32_t n = 0; n < 2; ++n) {
@@ -473,6 +470,13 @@ __device__ __forceinline__ void q4k_scales(const L& ld, uint32_t boff, uint32_t 
     dsc[n] = d * static_cast<float>(sc);
     dmn[n] = dmin * static_cast<float>(m);
   }
+}
+
+// The same for the super-block at boff.
+template <class L>
+__device__ __forceinline__ void q4k_scales(const L& ld, uint32_t boff, uint32_t g, float (&dsc)[2],
+                                           float (&dmn)[2]) {
+  q4k_scales_from(ld.word(boff), ld.word(boff + 4u), ld.word(boff + 8u), ld.word(boff + 12u), g, dsc, dmn);
 }
 
 // The 16 code bytes of unit pair p and its two sub-blocks' scale and min.
@@ -497,7 +501,7 @@ __device__ __forceinline__ void q4k_nibbles(const uint4 q, uint32_t n, float2 (&
   }
 }
 
-// ---- integer dot products (Q4_0 and Q8_0, single columns)
+// ---- integer dot products (Q4_0, Q8_0 and Q4_K, single columns)
 // A unit's 16 x values become integers X_j = trunc(x_j * 2^s) that share the exponent s
 // (chosen so that max |x_j| * 2^s lies in [2^22, 2^23), hence |X_j| <= 2^23 - 1).  Each
 // X_j is split into three bytes X = D2 * 2^16 + D1 * 2^8 + D0 (D2 signed, D1 and D0
@@ -569,14 +573,14 @@ __device__ __forceinline__ void x_to_int(const float2 (&xv)[8], XInt& xi) {
   xi.c = static_cast<uint32_t>(-8 * sum);
 }
 
-// A Q4_0 unit's two code words (code bytes 8h .. 8h+7 of its block) against the XInt of
-// each of NCT columns: t[c] = sum_j (q_j - 8) X_j.
-template <int NCT>
-__device__ __forceinline__ void q4_0_words_int(uint32_t w0, uint32_t w1, const XInt (&xq)[NCT], int (&t)[NCT]) {
-  const uint32_t n[4] = {w0 & 0x0F0F0F0Fu, w1 & 0x0F0F0F0Fu, (w0 >> 4) & 0x0F0F0F0Fu, (w1 >> 4) & 0x0F0F0F0Fu};
+// Four registers of unsigned codes (byte k of n[g] is element 4g + k) against the XInt of
+// each of NCT columns: t[c] = sum_j q_j X_j, minus 8 sum_j X_j with OFFSET (Q4_0's
+// q - 8; |t| < 2^31 for codes below 16).
+template <int NCT, bool OFFSET>
+__device__ __forceinline__ void nibble_words_int(const uint32_t (&n)[4], const XInt (&xq)[NCT], int (&t)[NCT]) {
 #pragma unroll
   for (int c = 0; c < NCT; ++c) {
-    uint32_t s2 = 0u, s1 = 0u, s0 = xq[c].c;
+    uint32_t s2 = 0u, s1 = 0u, s0 = OFFSET ? xq[c].c : 0u;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       s2 = dp4a_us(n[g], xq[c].d2[g], s2);
@@ -585,6 +589,14 @@ __device__ __forceinline__ void q4_0_words_int(uint32_t w0, uint32_t w1, const X
     }
     t[c] = static_cast<int>((s2 * 256u + s1) * 256u + s0);
   }
+}
+
+// A Q4_0 unit's two code words (code bytes 8h .. 8h+7 of its block) against the XInt of
+// each of NCT columns: t[c] = sum_j (q_j - 8) X_j.
+template <int NCT>
+__device__ __forceinline__ void q4_0_words_int(uint32_t w0, uint32_t w1, const XInt (&xq)[NCT], int (&t)[NCT]) {
+  const uint32_t n[4] = {w0 & 0x0F0F0F0Fu, w1 & 0x0F0F0F0Fu, (w0 >> 4) & 0x0F0F0F0Fu, (w1 >> 4) & 0x0F0F0F0Fu};
+  nibble_words_int<NCT, true>(n, xq, t);
 }
 
 // A Q8_0 unit's four code words (16 signed codes, group g = word g) against the XInt of

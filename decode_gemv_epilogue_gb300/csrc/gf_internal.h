@@ -51,12 +51,12 @@ __host__ __device__ constexpr int stream_rt(int wt, int nc) {
 }
 __host__ __device__ constexpr int stream_max_cw(int wt, int nc) { return stream_nct(wt, nc) <= 2 ? 16 : 8; }
 __host__ __device__ constexpr int stream_threads(int wt, int nc) { return 32 * (1 + stream_max_cw(wt, nc)); }
-// Q4_0 and Q8_0 with up to kIntMaxCols columns take integer dot products (x as shared-
-// exponent 24-bit integers, dp4a on the codes): a third (Q4_0) to a half (Q8_0) of the
+// Q4_0, Q8_0 and Q4_K with up to kIntMaxCols columns take integer dot products (x as
+// shared-exponent 24-bit integers, dp4a on the codes): a third to a half of the
 // instructions per weight of the float decode.  With more columns per thread the float
 // decode, done once for all of them, is cheaper.
 constexpr int kIntMaxCols = 1;
-__host__ __device__ constexpr bool stream_int(int wt, int nc) { return (wt == 3 || wt == 2) && nc <= kIntMaxCols; }
+__host__ __device__ constexpr bool stream_int(int wt, int nc) { return (wt >= 2 && wt <= 4) && nc <= kIntMaxCols; }
 
 struct StreamArgs {
   const uint8_t* W;

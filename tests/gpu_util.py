@@ -8,9 +8,9 @@ from oracle import gemv as ogemv
 
 TOL_REL = 2e-5   # |gpu - oracle| <= 2e-5 * sum_k |W_ik x_k| + 1e-6 (fp32 accumulation)
 TOL_ABS = 1e-6
-# Q4_0 and Q8_0 integer dot products truncate each x to 24 bits relative to the largest
-# |x| of its 16-element unit (a subset of its 32-element block): less than
-# 2^-22 * max_block |x| per weight magnitude.
+# Q4_0, Q8_0 and Q4_K integer dot products truncate each x to 24 bits relative to the
+# largest |x| of its 16-element unit (a subset of its 32-element block): less than
+# 2^-22 * max_block |x| per weight magnitude (for Q4_K, per |d sc q| <= |d sc q| + |dmin m|).
 INT_DOT_REL = 2.0 ** -22
 
 
@@ -25,7 +25,7 @@ def gemv_bound(raw, wt, x, M, K, rows=None, x_err=None):
     b = TOL_REL * ogemv.abs_dot(raw, wt, x, M, K, rows) + TOL_ABS
     if x_err is not None:
         b = b + ogemv.abs_w_dot(raw, wt, x_err, M, K, rows)
-    if wt in (2, 3):  # Q8_0, Q4_0
+    if wt in (2, 3, 4):  # Q8_0, Q4_0, Q4_K
         xa = np.abs(np.asarray(x, dtype=np.float64))
         if x_err is not None:
             xa = xa + np.asarray(x_err, dtype=np.float64).reshape(xa.shape)
