@@ -254,8 +254,10 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
   if (S > 1 && RC < rows_max) return false;  // split K exchanges one row chunk per CTA
   // x is staged in shared memory by the producer when the row is one chunk and the
   // staging costs at most one ring stage of a ring that keeps four or more
-  bool stage_x = !c.signs && n_kc == 1 && nc * kc * 4 <= kXStageMaxBytes;
-  int xs_bytes = (c.signs || stage_x) ? round_up(nc * kc * 4, 128) : 0;
+  // (with the RMS prologue gamma is staged after x)
+  const int xcols = nc + (c.gamma ? 1 : 0);
+  bool stage_x = !c.signs && n_kc == 1 && xcols * kc * 4 <= kXStageMaxBytes;
+  int xs_bytes = c.signs ? round_up(nc * kc * 4, 128) : stage_x ? round_up(xcols * kc * 4, 128) : 0;
   const int aux_bytes = round_up(nc * RC * 4, 128);
   const int red_bytes = round_up(vr * RC * wpc * nc * 4, 128);
   const int norm_bytes = c.gamma ? round_up(wpc * nc * 4, 128) : 0;

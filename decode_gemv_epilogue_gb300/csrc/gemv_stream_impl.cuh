@@ -415,11 +415,13 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
               // x staged by bulk copy right behind the first weight tile, once the
               // preceding grid (which may write x) has finished: later in the queue it
               // waits behind the whole ring of weight tiles
+              // (with the RMS prologue, gamma follows x on the same barrier)
               pdl_wait();
-              mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(NC * a.K * 4));
+              mbar_arrive_expect_tx(xbar, static_cast<uint32_t>((NC + (norm ? 1 : 0)) * a.K * 4));
               for (int c = 0; c < NC; ++c)
                 bulk_g2s(smem_u32(xs + c * a.K), a.x + static_cast<int64_t>(c) * a.K,
                          static_cast<uint32_t>(a.K * 4), xbar);
+              if (norm) bulk_g2s(smem_u32(xs + NC * a.K), a.gamma, static_cast<uint32_t>(a.K * 4), xbar);
               x_issued = true;
             }
           }
@@ -499,7 +501,9 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         float2 xr[kInt ? 1 : U][NCT][8];
         XInt xq[kInt ? U : 1][kInt ? NCT : 1];
         float xsum[U][NCT];
-        const float* gsrc = norm ? a.gamma + static_cast<int64_t>(kc) * a.kc_len : nullptr;
+        const float* gsrc = !norm ? nullptr
+                            : a.stage_x ? xs + NC * a.K  // staged after x
+                                        : a.gamma + static_cast<int64_t>(kc) * a.kc_len;
 #pragma unroll
         for (int i = 0; i < U; ++i) {
           const int u = unit_index<WT, U>(tg, i, tg_n);
