@@ -637,6 +637,22 @@ def next_rows_measure(G, torch, step, s, args, peak):
                             "note": "q, k, v weights concatenated into one matrix by the caller"}
     del qkv
 
+    # 1a'. q, k, v and the sigmoid head in one gemv_multi launch (the matrices stay separate
+    # buffers), o, the gated dual GEMV and down: 4 launches per layer
+    def multi_layer(i):
+        Wl = layers[i]
+        G.gemv_multi([(Wl["chain_q"], 4096, 0, None, q), (Wl["chain_k"], 4096, 0, None, k),
+                      (Wl["chain_v"], 4096, 0, None, v), (Wl["chain_beta_sigmoid"], 32, 1, None, beta)],
+                     3, x, 4096, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True)
+        G.gemv_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, r, 14336, 4096, g, pdl=True)
+        G.gemv_fused_ex(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True)
+
+    us4 = graph_us(torch, s, multi_layer, 2, max(20, min(args.steps, 500)))
+    out["chain_multi_glu"] = {"us_per_layer": round(us4, 3), "launches_per_layer": 4, "layer_bytes": lb,
+                              "gbs": round(lb / (us4 * 1e-6) / 1e9, 1),
+                              "note": "q, k, v and the sigmoid head in one gemv_multi launch (separate buffers)"}
+
     # 1b. the same layer in Q4_K (a format the pages' decode-layer measurements name),
     # 8 launches and 7 with the dual GEMV
     layers_k = [{n: up(synth.weights(4, shapes[n][0], shapes[n][1], seed=700 + 10 * l + i))

@@ -107,6 +107,8 @@ struct Call {
   const void* W2;       // gated dual GEMV: the up matrix (epi == EPI_GLU)
   const float* gamma;   // RMS-normalisation prologue weight [K]
   float eps;
+  int nseg = 0;         // several matrices sharing x (gemv_multi): M is their rows' sum
+  gf_multi_item segs[kMaxSeg];
 };
 
 static int validate(const Call& c) {
@@ -172,7 +174,7 @@ static int validate(const Call& c) {
 constexpr int kTcMinCols = 4;
 
 static bool tc_eligible(const Call& c) {
-  return c.wtype == GF_F16 && !c.W2 && !c.gamma && !c.signs && !(c.flags & GF_FLAG_NO_TENSOR_CORES) &&
+  return c.wtype == GF_F16 && !c.W2 && !c.gamma && !c.signs && c.nseg == 0 && !(c.flags & GF_FLAG_NO_TENSOR_CORES) &&
          c.ncols >= kTcMinCols && c.K >= 64 && c.K % 64 == 0 && aligned(c.W, 16) && aligned(c.x, 16);
 }
 
@@ -189,6 +191,8 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
   if (c.K < kUnitElems || K % kUnitElems != 0) return false;
   if (rb % 16 != 0 || !aligned(c.W, 16) || !aligned(c.x, 16)) return false;
   if (dual && !aligned(c.W2, 16)) return false;
+  for (int i = 0; i < c.nseg; ++i)
+    if (!aligned(c.segs[i].W, 16)) return false;
   if (c.gamma && !aligned(c.gamma, 16)) return false;
   if (rb > INT32_MAX / 2) return false;
   const int U = stream_u(c.wtype, nc), RT = stream_rt(c.wtype, nc);
@@ -320,7 +324,7 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
 constexpr int64_t kSplitMinCtaBytes = 128 * 1024;
 
 static int split_factor(const Call& c, const DeviceLimits& lim) {
-  if (c.flags & GF_FLAG_NO_SPLIT_K) return 1;
+  if ((c.flags & GF_FLAG_NO_SPLIT_K) || c.nseg > 0) return 1;
   if (c.M < 1 || 2 * c.M > lim.sm_count) return 1;
   const int64_t vr = c.W2 ? 2 : 1;
   const int64_t cta_bytes = c.ncols * c.K * 4 + vr * row_bytes_of(c.wtype, c.K);  // one row per CTA
@@ -379,7 +383,7 @@ struct LaunchRec {
   GenericArgs g;
   int ggrid, gsmem;
 };
-constexpr int kMaxRecs = 1 + kMaxBatch / kMaxCols;  // transform + column blocks
+constexpr int kMaxRecs = 1 + kMaxSeg * (kMaxBatch / kMaxCols);  // transform + column blocks (per matrix)
 
 // Plans one launch of at most one column block into r.
 static int plan_one(const Call& c, float* dst, LaunchRec& r) {
@@ -409,6 +413,16 @@ static int plan_one(const Call& c, float* dst, LaunchRec& r) {
     s.err = err;
     s.W2 = static_cast<const uint8_t*>(c.W2);
     s.gamma = c.gamma;
+    s.nseg = c.nseg;
+    int64_t end = 0;
+    for (int i = 0; i < c.nseg; ++i) {
+      end += c.segs[i].M;
+      s.seg_W[i] = static_cast<const uint8_t*>(c.segs[i].W);
+      s.seg_end[i] = end;
+      s.seg_epi[i] = c.segs[i].epilogue;
+      s.seg_aux[i] = c.segs[i].aux;
+      s.seg_dst[i] = c.segs[i].dst;
+    }
   } else {
     r.kind = REC_GENERIC;
     GenericArgs& g = r.g;
@@ -444,7 +458,7 @@ static int issue(const LaunchRec& r, cudaStream_t st) {
     const StreamArgs& s = r.p.s;
     const int nc = r.ncols;
     const bool fl = (r.wtype == GF_F32 || r.wtype == GF_F16);
-    const bool ext = s.W2 != nullptr || s.gamma != nullptr;
+    const bool ext = s.W2 != nullptr || s.gamma != nullptr || s.nseg > 0;
     if (r.wtype == GF_Q4_K)
       e = s.S > 1 ? launch_stream_q4k_split(nc, r.p, st, r.pdl)
           : ext   ? launch_stream_q4k_ext(nc, r.p, st, r.pdl)
@@ -472,11 +486,12 @@ static int issue(const LaunchRec& r, cudaStream_t st) {
 // transform into it, and the GEMV on it is launched with programmatic dependent launch:
 // it streams W while the transform runs and waits for it before reading x' (W is not
 // written by the transform, so this holds whatever the caller's flags).
-static int plan_launches(const Call& c0, float* dst, LaunchRec* recs, int* n) {
+static int plan_launches(const Call& c0, float* dst, LaunchRec* recs, int cap, int* n) {
   *n = 0;
   if (c0.M == 0) return GF_OK;
   Call c = c0;
   if (c0.workspace && c0.K > 0) {
+    if (cap < 1) return GF_ERR_UNSUPPORTED;
     LaunchRec& f = recs[(*n)++];
     f.kind = REC_FWHT;
     f.pdl = false;
@@ -494,15 +509,43 @@ static int plan_launches(const Call& c0, float* dst, LaunchRec* recs, int* n) {
     c.flags |= GF_FLAG_PDL;
   }
   const int64_t width = tc_eligible(c) ? kTcMaxCols : kMaxCols;
+  if (c.nseg > 0) {
+    // one pass over every matrix when the streamed kernel takes the block shape, else one
+    // launch per matrix
+    Call probe = c;
+    probe.ncols = std::min<int64_t>(width, c.ncols);
+    Plan pp;
+    if (!plan_stream(probe, device_limits(), pp)) {
+      for (int i = 0; i < c.nseg; ++i) {
+        Call one = c;
+        one.nseg = 0;
+        one.W = c.segs[i].W;
+        one.M = c.segs[i].M;
+        one.epi = c.segs[i].epilogue;
+        one.aux = c.segs[i].aux;
+        one.dst = c.segs[i].dst;
+        if (*n > 0) one.flags |= GF_FLAG_PDL;  // after the transform or the previous matrix
+        int m = 0;
+        const int e = plan_launches(one, c.segs[i].dst, recs + *n, cap - *n, &m);
+        if (e != GF_OK) return e;
+        *n += m;
+      }
+      return GF_OK;
+    }
+  }
   for (int64_t col = 0; col < c.ncols; col += width) {
     Call b = c;
     b.ncols = std::min<int64_t>(width, c.ncols - col);
     b.x = c.x + col * c.K;
     b.aux = c.aux ? c.aux + col * c.M : nullptr;
     b.dst = dst + col * c.M;
+    for (int i = 0; i < c.nseg; ++i) {
+      b.segs[i].aux = c.segs[i].aux ? c.segs[i].aux + col * c.segs[i].M : nullptr;
+      b.segs[i].dst = c.segs[i].dst + col * c.segs[i].M;
+    }
     if (col > 0) b.flags |= GF_FLAG_PDL;
-    if (*n >= kMaxRecs) return GF_ERR_UNSUPPORTED;
-    const int e = plan_one(b, dst + col * c.M, recs[*n]);
+    if (*n >= cap) return GF_ERR_UNSUPPORTED;
+    const int e = plan_one(b, const_cast<float*>(b.dst), recs[*n]);
     if (e != GF_OK) return e;
     ++*n;
   }
@@ -512,7 +555,7 @@ static int plan_launches(const Call& c0, float* dst, LaunchRec* recs, int* n) {
 static int run_call(const Call& c, float* dst, cudaStream_t st) {
   LaunchRec recs[kMaxRecs];
   int n = 0;
-  const int e = plan_launches(c, dst, recs, &n);
+  const int e = plan_launches(c, dst, recs, kMaxRecs, &n);
   if (e != GF_OK) return e;
   for (int i = 0; i < n; ++i) {
     const int r = issue(recs[i], st);
@@ -552,6 +595,47 @@ static Call make_call(const void* W, int wtype, const float* x, int64_t M, int64
     c.eps = opts->rms_norm_eps;
   }
   return c;
+}
+
+// gemv_multi: each matrix is checked as the call gemv_fused_ex(W_i, ...) would be, then
+// against the other matrices' operands.
+static int make_multi_call(const gf_multi_item* items, int n, int wtype, const float* x, int64_t K,
+                           const gf_opts* opts, Call* out) {
+  if (!items || n < 1) return GF_ERR_INVALID;
+  if (n > kMaxSeg) return GF_ERR_UNSUPPORTED;
+  if (opts)
+    for (int i = 0; i < 4; ++i)
+      if (opts->view_ne[i] != 0) return GF_ERR_INVALID;
+  int64_t rows = 0;
+  for (int i = 0; i < n; ++i) {
+    const gf_multi_item& it = items[i];
+    const Call one = make_call(it.W, wtype, x, it.M, K, it.epilogue, it.aux, it.dst, opts);
+    const int v = validate(one);
+    if (v != GF_OK) return v;
+    if (it.M > INT32_MAX - rows) return GF_ERR_UNSUPPORTED;
+    rows += it.M;
+  }
+  Call c = make_call(items[0].W, wtype, x, rows, K, GF_EPI_NONE, nullptr, items[0].dst, opts);
+  const int64_t nc = c.ncols;
+  for (int i = 0; i < n; ++i) {
+    const gf_multi_item& a = items[i];
+    const bool aux_a = a.epilogue == GF_EPI_SILU_MUL || a.epilogue == GF_EPI_ADD;
+    for (int j = 0; j < n; ++j) {
+      if (j == i) continue;
+      const gf_multi_item& b = items[j];
+      const bool aux_b = b.epilogue == GF_EPI_SILU_MUL || b.epilogue == GF_EPI_ADD;
+      const int64_t da = nc * a.M * 4;
+      if (ranges_overlap(a.dst, da, b.W, b.M * row_bytes_of(wtype, K)) ||
+          ranges_overlap(a.dst, da, b.dst, nc * b.M * 4) || (aux_b && ranges_overlap(a.dst, da, b.aux, nc * b.M * 4)))
+        return GF_ERR_ALIAS;
+      (void)aux_a;
+    }
+    c.segs[i] = items[i];
+    if (!aux_a) c.segs[i].aux = nullptr;
+  }
+  c.nseg = n;
+  *out = c;
+  return GF_OK;
 }
 
 static int check_view(const gf_opts* opts, int64_t M) {
@@ -608,6 +692,14 @@ int gemv_glu(const void* W_gate, const void* W_up, int wtype, const float* x, in
   v = check_view(opts, M);
   if (v != GF_OK) return v;
   return run_call(c, dst, static_cast<cudaStream_t>(stream));
+}
+
+int gemv_multi(const gf_multi_item* items, int n, int wtype, const float* x, int64_t K, const gf_opts* opts,
+               void* stream) {
+  Call c;
+  const int v = make_multi_call(items, n, wtype, x, K, opts, &c);
+  if (v != GF_OK) return v;
+  return run_call(c, const_cast<float*>(c.dst), static_cast<cudaStream_t>(stream));
 }
 
 static int plan_info(const Call& c, const gf_opts* opts, int64_t info[8]) {
@@ -758,9 +850,9 @@ struct gf_prepared {
 static int prepare(const Call& c, const gf_opts* opts, gf_prepared** out) {
   if (!out) return GF_ERR_INVALID;
   *out = nullptr;
-  int v = validate(c);
+  int v = c.nseg > 0 ? GF_OK : validate(c);  // a multi-matrix call was checked per matrix
   if (v != GF_OK) return v;
-  v = check_view(opts, c.M);
+  v = c.nseg > 0 ? GF_OK : check_view(opts, c.M);
   if (v != GF_OK) return v;
   gf_prepared* p = new (std::nothrow) gf_prepared;
   if (!p) return GF_ERR_INVALID;
@@ -768,7 +860,7 @@ static int prepare(const Call& c, const gf_opts* opts, gf_prepared** out) {
     delete p;
     return cuda_fail(cudaGetLastError());
   }
-  v = plan_launches(c, const_cast<float*>(c.dst), p->recs, &p->n);  // dst came in as float*
+  v = plan_launches(c, const_cast<float*>(c.dst), p->recs, kMaxRecs, &p->n);  // dst came in as float*
   if (v != GF_OK) {
     delete p;
     return v;
@@ -785,6 +877,16 @@ int gf_prepare(const void* W, int wtype, const float* x, int64_t M, int64_t K, i
 int gf_prepare_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M, int64_t K, float* dst,
                    const gf_opts* opts, gf_prepared** out) {
   return prepare(make_glu_call(W_gate, W_up, wtype, x, M, K, dst, opts), opts, out);
+}
+
+int gf_prepare_multi(const gf_multi_item* items, int n, int wtype, const float* x, int64_t K, const gf_opts* opts,
+                     gf_prepared** out) {
+  if (!out) return GF_ERR_INVALID;
+  *out = nullptr;
+  Call c;
+  const int v = make_multi_call(items, n, wtype, x, K, opts, &c);
+  if (v != GF_OK) return v;
+  return prepare(c, opts, out);
 }
 
 int gf_launch_prepared(const gf_prepared* const* calls, int n, void* stream) {

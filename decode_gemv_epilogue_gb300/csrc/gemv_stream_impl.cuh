@@ -45,6 +45,16 @@
 
 namespace gf {
 
+// Segment of virtual row r of a multi-matrix launch (a.nseg > 0) and the row's index in it.
+__device__ __forceinline__ int seg_of(const StreamArgs& a, int64_t r, int64_t& local) {
+  int i = 0;
+#pragma unroll
+  for (int k = 0; k < kMaxSeg - 1; ++k)
+    if (k < a.nseg - 1 && r >= a.seg_end[i]) ++i;
+  local = r - (i ? a.seg_end[i - 1] : 0);
+  return i;
+}
+
 template <int WT>
 __host__ __device__ constexpr int seg_bytes_of(int klen) {
   return WT == WT_F32    ? 4 * klen
@@ -343,6 +353,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
       min(static_cast<int64_t>((a.rows_base + (rg < a.rows_extra ? 1 : 0)) * a.gran), a.M - r0));
   const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
   const bool dual = kExt && a.W2 != nullptr;
+  const bool multi = kExt && a.nseg > 0;  // several matrices sharing x (never with dual)
   const bool norm = kExt && a.gamma != nullptr;
   const int XR = dual ? 2 * a.RC : a.RC;  // virtual rows per row chunk
 
@@ -390,7 +401,23 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
             const uint32_t dst = ring + static_cast<uint32_t>(slot) * a.stage_bytes;
             const int64_t row = r0 + rc0 + (dual ? t0 / 2 : t0);
             mbar_arrive_expect_tx(full, static_cast<uint32_t>(rows * seg));
-            if (a.n_kc == 1) {
+            if (multi) {
+              // the tile's rows, cut at segment boundaries (rows are contiguous within one)
+              for (int r = 0; r < rows;) {
+                int64_t local;
+                const int i = seg_of(a, row + r, local);
+                const int n = static_cast<int>(min(static_cast<int64_t>(rows - r), a.seg_end[i] - (row + r)));
+                if (a.n_kc == 1) {
+                  bulk_g2s(dst + static_cast<uint32_t>(r * seg), a.seg_W[i] + local * a.row_bytes,
+                           static_cast<uint32_t>(n * seg), full, pol);
+                } else {
+                  for (int q = 0; q < n; ++q)
+                    bulk_g2s(dst + static_cast<uint32_t>((r + q) * seg), a.seg_W[i] + (local + q) * a.row_bytes + segoff,
+                             static_cast<uint32_t>(seg), full, pol);
+                }
+                r += n;
+              }
+            } else if (a.n_kc == 1) {
               bulk_g2s(dst, a.W + row * a.row_bytes, static_cast<uint32_t>(h * seg), full, pol);
               if (dual)
                 bulk_g2s(dst + static_cast<uint32_t>(h * seg), a.W2 + row * a.row_bytes,
@@ -446,7 +473,19 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
     const int c0 = cgi * NCT;                  // first column of this thread
     const int tg = wc * 32 + lane, tg_n = a.wpc * 32;
     const uint32_t qr = lane_quad_rot<WT>(lane);
-    const bool need_aux = (a.epi == EPI_SILU_MUL || a.epi == EPI_ADD);
+    auto epi_aux = [](int e) { return e == EPI_SILU_MUL || e == EPI_ADD; };
+    bool need_aux = epi_aux(a.epi);
+    if (multi)
+      for (int i = 0; i < a.nseg; ++i) need_aux = need_aux || epi_aux(a.seg_epi[i]);
+    // aux of column c at virtual row gr (0 for a segment whose tail takes none)
+    auto aux_at = [&](int c, int64_t gr) -> float {
+      if (!multi) return a.aux[c * a.M + gr];
+      int64_t local;
+      const int i = seg_of(a, gr, local);
+      if (!epi_aux(a.seg_epi[i])) return 0.0f;
+      const int64_t mi = a.seg_end[i] - (i ? a.seg_end[i - 1] : 0);
+      return a.seg_aux[i][c * mi + local];
+    };
     const bool finalizer = (crank == 0);
     pdl_wait();  // x, aux and dst may belong to the preceding grid
     int slot = 0;            // ring slot of the next tile
@@ -477,7 +516,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
           if (kc == 0 && need_aux)  // aux loads overlap the x copy
             for (int i = ctid; i < nrc * NC; i += nt) {
               const int c = i / nrc, r = i - c * nrc;
-              auxs[c * a.RC + r] = a.aux[c * a.M + r0 + rc0 + r];  // plain load: aux may alias dst
+              auxs[c * a.RC + r] = aux_at(c, r0 + rc0 + r);  // plain load: aux may alias dst
             }
           ok = ok && mbar_wait_or_abort(xbar, xphase, abort_flag, a.err);
           xphase ^= 1u;
@@ -486,7 +525,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         } else if (kc == 0 && need_aux) {
           for (int i = ctid; i < nrc * NC; i += nt) {
             const int c = i / nrc, r = i - c * nrc;
-            auxs[c * a.RC + r] = a.aux[c * a.M + r0 + rc0 + r];
+            auxs[c * a.RC + r] = aux_at(c, r0 + rc0 + r);
           }
         }
         const int units = klen / kUnitElems;
@@ -654,6 +693,14 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
               yu *= inv;
             }
             out = tail_silu(yg) * yu;
+          } else if (multi) {
+            float y = vsum(r, c);
+            if (norm) y *= inv;
+            int64_t local;
+            const int si = seg_of(a, r0 + rc0 + r, local);
+            const int64_t mi = a.seg_end[si] - (si ? a.seg_end[si - 1] : 0);
+            a.seg_dst[si][c * mi + local] = apply_tail(a.seg_epi[si], y, need_aux ? auxs[c * a.RC + r] : 0.0f);
+            continue;
           } else {
             float y = vsum(r, c);
             if (norm) y *= inv;

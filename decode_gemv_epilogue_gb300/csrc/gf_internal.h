@@ -22,6 +22,7 @@ constexpr int kRingSlackBytes = 16;         // aligned-word decoders may read 3 
 constexpr int kMaxFusedFwhtBlock = 8192;
 constexpr int kUnitElems = 16;              // weights per decode unit (half a quant block)
 constexpr int kMaxSplit = 8;                // CTAs of a split-K cluster (portable cluster size)
+constexpr int kMaxSeg = 4;                  // matrices sharing x in one multi-matrix launch
 
 // Tiling of the consumer warps, per (format, columns):
 //  U   units (16 weights) per thread per K chunk, RT rows per thread per tile;
@@ -88,6 +89,16 @@ struct StreamArgs {
   const uint8_t* W2; // up-projection rows of the gated dual GEMV (nullptr: one matrix)
   const float* gamma;  // RMS-normalisation weight [K] (nullptr: no normalisation)
   float norm_eps;
+  // Several matrices sharing x in one pass (nseg > 0): virtual row r belongs to segment
+  // i = the first with r < seg_end[i]; its rows are seg_W[i], its tail seg_epi[i] with
+  // seg_aux[i], its output seg_dst[i] ([ncols][rows of the segment]).  W, epi, aux and dst
+  // above are then unused.
+  int nseg;
+  const uint8_t* seg_W[kMaxSeg];
+  int64_t seg_end[kMaxSeg];
+  int seg_epi[kMaxSeg];
+  const float* seg_aux[kMaxSeg];
+  float* seg_dst[kMaxSeg];
   int S;             // CTAs per cluster sharing a row range, each a slice of the K chunks
   int stage_x;       // 1: the producer bulk-copies x (one K chunk, every column) into xs
   int off_xs, off_aux, off_red, off_norm, off_xchg, off_ring;

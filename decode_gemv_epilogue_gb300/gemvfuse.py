@@ -65,6 +65,16 @@ _prepare_glu = _sig("gf_prepare_glu", [_vp, _vp, _i32, _vp, _i64, _i64, _vp, cty
                                        ctypes.POINTER(_vp)])
 _launch_prepared = _sig("gf_launch_prepared", [ctypes.POINTER(_vp), _i32, _vp])
 _free_prepared = _sig("gf_free_prepared", [_vp], None)
+
+
+class MultiItem(ctypes.Structure):
+    _fields_ = [("W", _vp), ("M", _i64), ("epilogue", _i32), ("aux", _vp), ("dst", _vp)]
+
+
+MULTI_MAX = 4
+_gemv_multi = _sig("gemv_multi", [ctypes.POINTER(MultiItem), _i32, _i32, _vp, _i64, ctypes.POINTER(GfOpts), _vp])
+_prepare_multi = _sig("gf_prepare_multi", [ctypes.POINTER(MultiItem), _i32, _i32, _vp, _i64,
+                                           ctypes.POINTER(GfOpts), ctypes.POINTER(_vp)])
 _graph_create = _sig("gf_graph_create", [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp)])
 _graph_launch = _sig("gf_graph_launch", [_vp, _vp])
 _graph_free = _sig("gf_graph_free", [_vp], None)
@@ -257,6 +267,35 @@ class Graph:
             self.close()
         except Exception:
             pass
+
+
+def _multi_items(items):
+    arr = (MultiItem * max(1, len(items)))()
+    for i, (W, M, epi, aux, dst) in enumerate(items):
+        arr[i].W, arr[i].M, arr[i].epilogue, arr[i].aux, arr[i].dst = _ptr(W), M, epi, _ptr(aux), _ptr(dst)
+    return arr
+
+
+def gemv_multi(items, wtype, x, K, ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, pdl=False,
+               fwht_workspace=None, rms_norm_weight=None, rms_norm_eps=0.0, stream=None, check=True):
+    """dst_i = epilogue_i(W_i x') for items [(W, M, epilogue, aux, dst), ...] sharing x, in one
+    pass (see include/gemvfuse.h)."""
+    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, None, pdl, fwht_workspace, rms_norm_weight, rms_norm_eps)
+    st = _gemv_multi(_multi_items(items), len(items), wtype, _ptr(x), K, ctypes.byref(o), _stream(stream))
+    if check:
+        _check(st, "gemv_multi")
+    return st
+
+
+def prepare_multi(items, wtype, x, K, ncols=1, fwht_signs=None, fwht_block=0, nsigns=None, pdl=False,
+                  fwht_workspace=None, rms_norm_weight=None, rms_norm_eps=0.0, check=True):
+    """gf_prepare_multi: the call gemv_multi(...) would make, planned once (see Prepared)."""
+    o = make_opts(ncols, fwht_signs, fwht_block, nsigns, None, pdl, fwht_workspace, rms_norm_weight, rms_norm_eps)
+    h = _vp()
+    st = _prepare_multi(_multi_items(items), len(items), wtype, _ptr(x), K, ctypes.byref(o), ctypes.byref(h))
+    if check:
+        _check(st, "gf_prepare_multi")
+    return Prepared(h.value, (items, x, fwht_signs, fwht_workspace, rms_norm_weight)) if st == OK else st
 
 
 def gemv_fused_fwht_noalloc(W, wtype, x, M, K, epilogue, aux, dst, ncols, fwht_signs, fwht_block, nsigns=None,

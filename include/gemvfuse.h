@@ -162,6 +162,33 @@ GF_API int gemv_fused_ex(const void* W, int wtype, const float* x, int64_t M, in
 GF_API int gemv_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M,
                     int64_t K, float* dst, const gf_opts* opts, void* stream);
 
+/* Several matrices that share x, in one pass (no counterpart on the pages; it carries
+ * their fusion one step further): for each item i,
+ *     dst_i = epilogue_i(W_i x')          (x' = x after the prologue in `opts`)
+ * e.g. a layer's q, k and v projections (and a small gate such as a sigmoid head) on the
+ * same activations, without concatenating their weights.  One launch streams every
+ * matrix once, as one matrix of sum_i M_i rows: the fixed cost of a launch is paid once.
+ *  items : n items (1 <= n <= GF_MULTI_MAX, else GF_ERR_INVALID / GF_ERR_UNSUPPORTED),
+ *          each a matrix W (M rows of format `wtype`, K columns; the rules of W in
+ *          gemv_fused) with its own epilogue, aux ([ncols][M], required iff SILU_MUL or
+ *          ADD) and dst ([ncols][M]).
+ *  x, K, wtype, opts : shared; opts as in gemv_fused_ex (ncols, either prologue,
+ *          flags) except `view_ne`, which must be all zero.
+ *  Aliasing: each dst as in gemv_fused against its own operands, and it may not overlap
+ *  any other item's W, aux or dst (GF_ERR_ALIAS).  The results equal those of the n
+ *  separate calls bit for bit (the same per-row arithmetic).  Shapes the streamed kernel
+ *  cannot take in one pass run as one launch per matrix. */
+#define GF_MULTI_MAX 4
+typedef struct {
+  const void* W;
+  int64_t M;
+  int epilogue;
+  const float* aux;
+  float* dst;
+} gf_multi_item;
+GF_API int gemv_multi(const gf_multi_item* items, int n, int wtype, const float* x, int64_t K,
+                      const gf_opts* opts, void* stream);
+
 /* Prepared calls: plan once, launch many times.  A decode loop issues the same GEMVs
  * with the same buffers every step; gf_prepare / gf_prepare_glu validate and plan a
  * call exactly as gemv_fused_ex / gemv_glu would (same arguments, same rules, same
@@ -170,6 +197,7 @@ GF_API int gemv_glu(const void* W_gate, const void* W_up, int wtype, const float
  * the direct call gives (the same kernels with the same arguments).
  *  out      : receives a handle owned by the caller, released with gf_free_prepared;
  *             NULL on failure.  A call with M == 0 gives a handle that launches nothing.
+ *  (gf_prepare_multi plans gemv_multi the same way.)
  *  Buffers  : the handle holds the device pointers given here (W, x, aux, dst, opts'
  *             signs, workspace and RMS weight); their contents may change between
  *             launches, the allocations must stay valid while the handle is used.
@@ -180,6 +208,8 @@ GF_API int gf_prepare(const void* W, int wtype, const float* x, int64_t M, int64
                       const float* aux, float* dst, const gf_opts* opts, gf_prepared** out);
 GF_API int gf_prepare_glu(const void* W_gate, const void* W_up, int wtype, const float* x, int64_t M,
                           int64_t K, float* dst, const gf_opts* opts, gf_prepared** out);
+GF_API int gf_prepare_multi(const gf_multi_item* items, int n, int wtype, const float* x, int64_t K,
+                            const gf_opts* opts, gf_prepared** out);
 /* Issues the launches of calls[0], ..., calls[n-1] in order on `stream` (n >= 0; the
  * calls' GF_FLAG_PDL settings apply as given to gf_prepare).  Stops at the first
  * failing launch and returns its status; GF_ERR_INVALID (nothing launched) for a NULL

@@ -27,7 +27,7 @@ def test_header_declares_the_abi():
     assert {"gemv_fused", "gemv_fused_ex", "gemv_glu", "fwht_signed", "gf_elementwise", "gf_dequantize",
             "gf_plan", "gf_plan_glu", "gf_device_status", "gf_status_string", "gf_last_cuda_error",
             "gf_version", "gf_prepare", "gf_prepare_glu", "gf_launch_prepared", "gf_free_prepared",
-            "gf_graph_create", "gf_graph_launch", "gf_graph_free"} <= names
+            "gf_graph_create", "gf_graph_launch", "gf_graph_free", "gemv_multi", "gf_prepare_multi"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -371,3 +371,36 @@ def test_graph_arguments(lib):
     assert lib.raw.gf_graph_create(arr, 1, None) == lib.ERR_INVALID
     assert lib.raw.gf_graph_launch(None, None) == lib.ERR_INVALID
     lib.raw.gf_graph_free(None)  # ignored
+
+
+# ----------------------------------------------------------------------------- several matrices, one x
+
+def _items(lib, *specs):
+    arr = (lib.MultiItem * len(specs))()
+    for i, (w, m, e, a, d) in enumerate(specs):
+        arr[i].W, arr[i].M, arr[i].epilogue, arr[i].aux, arr[i].dst = w, m, e, a, d
+    return arr
+
+
+def test_gemv_multi_validation(lib):
+    f = lib.raw.gemv_multi
+    K, M = 256, 64
+    ok_items = _items(lib, (W, M, 0, None, D), (W + (1 << 30), M, 1, None, D + (1 << 30)))
+    assert f(None, 1, 1, ctypes.c_void_p(X), K, None, None) == lib.ERR_INVALID
+    assert f(ok_items, 0, 1, ctypes.c_void_p(X), K, None, None) == lib.ERR_INVALID
+    five = _items(lib, *[(W + (i << 30), M, 0, None, D + (i << 30)) for i in range(5)])
+    assert f(five, 5, 1, ctypes.c_void_p(X), K, None, None) == lib.ERR_UNSUPPORTED
+    # a matrix that is invalid alone (ADD without its operand)
+    bad = _items(lib, (W, M, 0, None, D), (W + (1 << 30), M, 4, None, D + (1 << 30)))
+    assert f(bad, 2, 1, ctypes.c_void_p(X), K, None, None) == lib.ERR_INVALID
+    # one item's dst over another item's W, or over another item's dst
+    cross = _items(lib, (W, M, 0, None, D), (W + (1 << 30), M, 0, None, W + 64))
+    assert f(cross, 2, 1, ctypes.c_void_p(X), K, None, None) == lib.ERR_ALIAS
+    same = _items(lib, (W, M, 0, None, D), (W + (1 << 30), M, 0, None, D + 4 * (M // 2)))
+    assert f(same, 2, 1, ctypes.c_void_p(X), K, None, None) == lib.ERR_ALIAS
+    # a dst view has no meaning for several outputs
+    o = lib.make_opts(view=(8, 8))
+    assert f(ok_items, 2, 1, ctypes.c_void_p(X), K, ctypes.byref(o), None) == lib.ERR_INVALID
+    h = ctypes.c_void_p(5)
+    assert lib.raw.gf_prepare_multi(cross, 2, 1, ctypes.c_void_p(X), K, None, ctypes.byref(h)) == lib.ERR_ALIAS
+    assert not h.value
