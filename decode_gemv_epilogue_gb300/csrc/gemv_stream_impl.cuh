@@ -1,12 +1,16 @@
 // TMA-streamed persistent GEMV with fused prologue/epilogue.
 //
-// One CTA per SM owns a contiguous range of rows.  Warp 0 is the producer: one lane
-// streams the CTA's weight bytes, tile by tile (R rows x one K chunk), into a ring of
-// shared-memory stages with 1-D bulk async copies (no multicast), signalling a "full"
-// mbarrier per stage.  Warps 1..ncw are consumers: each thread owns fixed 16-weight
-// units of the K chunk, keeps the matching x values in registers while it walks the
-// R rows of a stage, decodes the weights (F32/F16/Q8_0/Q4_0) and accumulates with
-// packed f32x2 FMAs.  Per tile, each warp reduces its per-row partial sums with
+// One CTA per SM owns a contiguous range of rows (whole tiles when every CTA gets one,
+// the remainder to the lowest block indices, which a launch behind another starts
+// first).  Warp 0 is the producer: one lane streams the CTA's weight bytes, tile by
+// tile (R rows x one K chunk), into a ring of shared-memory stages with 1-D bulk async
+// copies (no multicast), signalling a "full" mbarrier per stage.  Warps 1..ncw are
+// consumers: each thread owns fixed 16-weight units of the K chunk and keeps the
+// matching x in registers while it walks the R rows of a stage, issuing every row's
+// shared-memory loads before the arithmetic.  F32/F16 (and batched block formats)
+// decode to floats and accumulate with packed f32x2 FMAs; single-column Q8_0, Q4_0 and
+// Q4_K take exact integer dot products (dp4a) against x held as 24-bit integers with a
+// shared exponent per unit.  Per tile, each warp reduces its per-row partial sums with
 // shuffles and stores them to shared memory; after the last K chunk the partials of
 // the consumer warps are added in a fixed order (deterministic), the fused tail is
 // applied with the prefetched aux operand, and dst is written once.
@@ -26,14 +30,17 @@
 // Gated dual GEMV: every tile holds h rows of the gate matrix followed by the same h
 // rows of the up matrix ("virtual rows"), and the tail is silu(gate) * up.
 //
+// Several matrices sharing x (nseg > 0): their rows are streamed as one matrix; tile
+// copies are cut at matrix boundaries and each row's tail, aux and dst are its matrix's.
+//
 // Split K: with S > 1 the grid is made of clusters of S CTAs; the CTAs of a cluster
 // share one row range and each takes a slice of its K chunks.  The per-row partial
 // sums of ranks 1..S-1 are stored into rank 0's shared memory (distributed shared
 // memory), rank 0 adds the S slices in rank order (deterministic) and applies the tail.
 //
 // Each (format, columns) pair is compiled three times (FEAT): the plain GEMV, the
-// extended one (dual GEMV, RMS prologue) and the split-K one (clusters, with the same
-// extensions).  The plain kernel carries none of the extension code: cluster
+// extended one (dual GEMV, several matrices, RMS prologue) and the split-K one
+// (clusters, with the same extensions).  The plain kernel carries none of the extension code: cluster
 // instructions in a kernel image alone add about a microsecond per launch on GB300.
 //
 // Every wait is bounded; a timeout sets the device error word and the kernel returns

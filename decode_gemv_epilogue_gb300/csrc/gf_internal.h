@@ -35,8 +35,9 @@ constexpr int kMaxSeg = 4;                  // matrices sharing x in one multi-m
 // columns.  Q4_K threads always own one unit pair (two units sharing a code load) and
 // one column: with 17 warps a thread has at most 96 registers (a quarter of the SM's
 // register file serves up to five warps), and a second column of x spills.  Single-
-// column Q4_0 (integer dot products, below) keeps one unit and eight rows per thread: its
-// x conversion per unit is the costly part of a chunk's start, and eight rows share it.
+// column Q4_0 and Q8_0 (integer dot products, below) keep one unit per thread and eight
+// (Q4_0) or four (Q8_0, twice the bytes per row) rows per tile: the x conversion per unit
+// is the costly part of a chunk's start, and the rows share it.
 __host__ __device__ constexpr bool stream_quant(int wt) { return wt == 2 || wt == 3 || wt == 4; }
 __host__ __device__ constexpr int stream_nct(int wt, int nc) {
   return wt == 4 ? 1 : stream_quant(wt) ? (nc <= 4 ? nc : 4) : (nc <= 2 ? nc : 2);
