@@ -9,14 +9,16 @@ every launch streams its weights from HBM):
   f16 4096x4096  sigmoid tail                                        (1)
   Q8_0 11008x4096  silu(y) * m                                      (1)
   Q4_0 decode-layer chain, d_model 4096, ffn 14336: q, k, v, o+add,
-       up, gate silu*up, down+add, beta sigmoid (M=32)               (8)
+       up, gate silu*up, down+add, beta sigmoid (M=32): the 8 calls
+       prepared and run as one persistent chain (gf_prepare_chain)    (1)
   signed FWHT(1024) prologue + f16 5120x5120 + add in place, 1 column (1)
   the same with a batch of 8 columns                                 (1)
 
 value = algorithmic bytes of the step (W + x + aux + dst, each once) / step time, GB/s,
 with the step captured in a CUDA graph (launches chained with programmatic dependent
 launch) and replayed.  Also reported: per-kernel CUDA-event durations and the roofline
-of the dominant kernel, microseconds per decode layer (fused and unfused chains), the
+of the dominant kernel, microseconds per decode layer (the persistent chain, the 8
+fused launches, the 13 unfused ones), the
 epilogue cost against the tail-free GEMV, an end-to-end number through host buffers,
 SM clocks during the timed region, and the fp64 CPU oracle timed on the host cores.
 Under "next_rows": the layer chain with the gated dual GEMV (7 launches), the same
@@ -43,7 +45,8 @@ sys.path.insert(0, ROOT)
 METRIC = "fused GEMV HBM GB/s & % of GB300 peak; µs per decode layer chain"
 UNIT = "GB/s"
 WORKLOAD = ("decode_step: f16 4096x4096 add-in-place via [32,128] view + sigmoid; "
-            "Q8_0 11008x4096 silu*m; Q4_0 decode-layer chain (d_model 4096, ffn 14336, 8 GEMVs); "
+            "Q8_0 11008x4096 silu*m; Q4_0 decode-layer chain (d_model 4096, ffn 14336, 8 GEMVs in one "
+            "persistent launch); "
             "signed FWHT(1024) + f16 5120x5120 add-in-place, ncols 1 and 8")
 L2_BYTES = 129 * 1024 * 1024
 
@@ -87,6 +90,10 @@ def algo_bytes(wt, M, K, epi, ncols, fwht):
 
 
 WT_NAME = {0: "f32", 1: "f16", 2: "q8_0", 3: "q4_0"}
+CHAIN_NAMES = ["chain_q", "chain_k", "chain_v", "chain_o_add", "chain_up", "chain_gate_silu_mul",
+               "chain_down_add", "chain_beta_sigmoid"]
+CHAIN_UNIT = "decode_layer_chain"
+CHAIN_KEY = "gemv_stream_kernel<q4_0,1,chain>"
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -142,8 +149,14 @@ class Step:
                 raise RuntimeError("plan failed for %s: %s" % (n, G.status_string(path)))
             kind = {G.PATH_STREAM: "gemv_stream_kernel", G.PATH_TC: "gemv_tc_kernel"}.get(path, "gemv_generic_kernel")
             self.keys[n] = ("fwht_signed_kernel+" if fw else "") + "%s<%s,%d>" % (kind, WT_NAME[wt], nc)
+        # the step's launch units: every call on its own, except the layer's eight calls,
+        # which run as one persistent chain
+        self.unit_names = [n for (n, *_r) in spec if n not in CHAIN_NAMES]
+        self.unit_names.insert(3, CHAIN_UNIT)
+        self.bytes[CHAIN_UNIT] = sum(self.bytes[n] for n in CHAIN_NAMES)
+        self.keys[CHAIN_UNIT] = CHAIN_KEY
         # kernels launched per step (a prologue call launches the transform, then the GEMV)
-        self.kernels_per_step = sum(2 if fw else 1 for (n, wt, M, K, e, nc, fw) in spec)
+        self.kernels_per_step = sum(2 if fw else 1 for (n, wt, M, K, e, nc, fw) in spec if n not in CHAIN_NAMES) + 1
 
     def call_specs(self):
         """(name, arguments, keyword arguments) of the step's gemv_fused_ex calls, on the
@@ -174,8 +187,17 @@ class Step:
                 for (name, a, kw) in self.call_specs()]
 
     def prepared(self, pdl=True):
-        """The step's calls planned once (gf_prepare), in order."""
-        return [(name, self.G.prepare(*a, pdl=pdl, **kw)) for (name, a, kw) in self.call_specs()]
+        """The step's launch units planned once, in order: gf_prepare for each call, and the
+        layer's eight prepared calls as one chain (gf_prepare_chain)."""
+        G = self.G
+        one = {name: G.prepare(*a, pdl=pdl, split_k=False, **kw) for (name, a, kw) in self.call_specs()}
+        chain = G.prepare_chain([one[n] for n in CHAIN_NAMES])
+        return [(n, chain if n == CHAIN_UNIT else one[n]) for n in self.unit_names]
+
+    def unit_calls(self, pdl=True):
+        """(name, fn) per launch unit: fn issues it on the current stream."""
+        G = self.G
+        return [(n, (lambda h=h: G.launch_prepared([h]))) for n, h in self.prepared(pdl)]
 
     # the end-to-end leg: every per-step activation in one device arena laid out as
     # [results only | residuals (read and written in place) | inputs only], mirrored by a
@@ -321,7 +343,7 @@ def gpu_arm(args, rank, world, local_rank):
     step = Step(G, torch)
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
-    calls = step.calls(pdl=True)
+    calls = step.unit_calls(pdl=True)
     sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
 
     with torch.cuda.stream(s):
@@ -434,7 +456,8 @@ def gpu_arm(args, rank, world, local_rank):
         "roofline": roofline,
         "pct_of_peak": round(100 * value / world / peak, 2),
         "gpu_launches": launches,
-        "us_per_layer": chain["fused_us"], "launches_per_layer": 8,
+        "us_per_layer": chain["persistent_us"], "launches_per_layer": 1,
+        "us_per_layer_8_launches": chain["fused_us"],
         "us_per_layer_unfused": chain["unfused_us"], "launches_per_layer_unfused": 13,
         "chain": chain, "epilogue_cost": epi_cost, "per_kernel": per_kernel, "per_workload": per_workload,
         "next_rows": nxt,
@@ -450,9 +473,11 @@ def launch_durations(G, torch, step, s, args):
     of back-to-back launches (chained with programmatic dependent launch, as in the step)
     cycling through copies of its weights -- enough copies to exceed 2x L2 when the
     weights allow, at most 32 -- timed with CUDA events on the launch stream."""
-    out = {}
+    out = {CHAIN_UNIT: chain_unit_us(G, torch, step, s, args)}
     calls = dict(step.calls(pdl=True))
     for name, wt, M, K, epi, nc, fw in step_spec():
+        if name in CHAIN_NAMES:
+            continue
         W0 = step.W[name]
         ncopy = int(min(32, max(2, -(-2 * L2_BYTES // W0.numel()))))
         copies = [W0] + [W0.clone() for _ in range(ncopy - 1)]
@@ -486,18 +511,47 @@ def launch_durations(G, torch, step, s, args):
     return out
 
 
-def chain_measure(G, torch, step, s, args):
-    """Microseconds per decode layer: the 8 fused launches vs the 13-launch unfused
-    chain (separate GEMV, add, silu, mul, sigmoid kernels), each captured in a CUDA
-    graph, two layers' weights alternating so nothing stays in L2."""
+def second_layer(torch, step):
+    """A second set of the layer's weights (seeded apart from the step's), so that timed
+    layers alternate between two sets and nothing stays in L2."""
     from decode_gemv_epilogue_gb300 import synth
+    if not hasattr(step, "_layer2"):
+        shapes = {n: (M, K) for (n, wt, M, K, e, nc, fw) in step_spec() if n in CHAIN_NAMES}
+        dev = torch.device("cuda")
+        step._layer2 = {n: torch.from_numpy(synth.weights(3, shapes[n][0], shapes[n][1], seed=300 + i)).to(dev)
+                        for i, n in enumerate(CHAIN_NAMES)}
+    return step._layer2
+
+
+def layer_chains(G, step, layers, pdl=True):
+    """One persistent chain of the layer's eight calls per weight set."""
+    specs = dict((n, (a, kw)) for (n, a, kw) in step.call_specs())
+    out = []
+    for Wl in layers:
+        calls = []
+        for n in CHAIN_NAMES:
+            a, kw = specs[n]
+            calls.append(G.prepare(Wl[n], *a[1:], pdl=pdl, split_k=False, **kw))
+        out.append(G.prepare_chain(calls))
+    return out
+
+
+def chain_unit_us(G, torch, step, s, args):
+    """Per-launch device time of the step's persistent layer chain: a CUDA graph of
+    back-to-back chain launches alternating between two weight sets."""
+    chains = layer_chains(G, step, [{n: step.W[n] for n in CHAIN_NAMES}, second_layer(torch, step)])
+    return graph_us(torch, s, lambda i: chains[i].launch(), 2, max(10, min(args.steps, 200))) * 1e-3
+
+
+def chain_measure(G, torch, step, s, args):
+    """Microseconds per decode layer: the persistent chain (one launch), the 8 fused
+    launches and the 13-launch unfused chain (separate GEMV, add, silu, mul, sigmoid
+    kernels), each captured in a CUDA graph, two layers' weights alternating so nothing
+    stays in L2."""
     dev = torch.device("cuda")
-    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     names = ["chain_q", "chain_k", "chain_v", "chain_o_add", "chain_up", "chain_gate_silu_mul",
              "chain_down_add", "chain_beta_sigmoid"]
-    shapes = {n: (M, K) for (n, wt, M, K, e, nc, fw) in step_spec() if n in names}
-    layers = [{n: step.W[n] for n in names},
-              {n: up(synth.weights(3, shapes[n][0], shapes[n][1], seed=300 + i)) for i, n in enumerate(names)}]
+    layers = [{n: step.W[n] for n in names}, second_layer(torch, step)]
     x, a, r = step.cx, step.ca, step.cr
     q, k, v, u, g, beta = step.cq, step.ck, step.cv, step.cup, step.cg, step.cbeta
     y4 = torch.empty(4096, device=dev)
@@ -549,9 +603,13 @@ def chain_measure(G, torch, step, s, args):
             e1.record(s)
         s.synchronize()
         res[label + "_us"] = round(1e3 * e0.elapsed_time(e1) / (2 * reps), 3)
+    chains = layer_chains(G, step, layers)
+    res["persistent_us"] = round(graph_us(torch, s, lambda i: chains[i].launch(), 2, reps), 3)
+    res["persistent_info"] = G.chain_info(chains[0])
     layer_bytes = sum(step.bytes[n] for n in names)
     res["layer_bytes"] = layer_bytes
     res["fused_gbs"] = round(layer_bytes / (res["fused_us"] * 1e-6) / 1e9, 1)
+    res["persistent_gbs"] = round(layer_bytes / (res["persistent_us"] * 1e-6) / 1e9, 1)
     res["layers_timed"] = 2 * reps
     return res
 
@@ -597,8 +655,7 @@ def next_rows_measure(G, torch, step, s, args, peak):
     names = ["chain_q", "chain_k", "chain_v", "chain_o_add", "chain_up", "chain_gate_silu_mul",
              "chain_down_add", "chain_beta_sigmoid"]
     shapes = {n: (M, K) for (n, wt, M, K, e, nc, fw) in step_spec() if n in names}
-    layers = [{n: step.W[n] for n in names},
-              {n: up(synth.weights(3, shapes[n][0], shapes[n][1], seed=300 + i)) for i, n in enumerate(names)}]
+    layers = [{n: step.W[n] for n in names}, second_layer(torch, step)]
     x, a, r = step.cx, step.ca, step.cr
     q, k, v, g, beta = step.cq, step.ck, step.cv, step.cg, step.cbeta
 
@@ -652,6 +709,24 @@ def next_rows_measure(G, torch, step, s, args, peak):
     out["chain_multi_glu"] = {"us_per_layer": round(us4, 3), "launches_per_layer": 4, "layer_bytes": lb,
                               "gbs": round(lb / (us4 * 1e-6) / 1e9, 1),
                               "note": "q, k, v and the sigmoid head in one gemv_multi launch (separate buffers)"}
+
+    # 1a''. the same four calls prepared and run as one persistent chain
+    def fused_chain(Wl):
+        return G.prepare_chain([
+            G.prepare_multi([(Wl["chain_q"], 4096, 0, None, q), (Wl["chain_k"], 4096, 0, None, k),
+                             (Wl["chain_v"], 4096, 0, None, v), (Wl["chain_beta_sigmoid"], 32, 1, None, beta)],
+                            3, x, 4096, pdl=True),
+            G.prepare(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True, split_k=False),
+            G.prepare_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, r, 14336, 4096, g, pdl=True, split_k=False),
+            G.prepare(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True, split_k=False)])
+
+    fchains = [fused_chain(layers[0]), fused_chain(layers[1])]
+    us1 = graph_us(torch, s, lambda i: fchains[i].launch(), 2, max(20, min(args.steps, 500)))
+    out["chain_persistent_multi_glu"] = {"us_per_layer": round(us1, 3), "launches_per_layer": 1, "layer_bytes": lb,
+                                         "gbs": round(lb / (us1 * 1e-6) / 1e9, 1),
+                                         "info": G.chain_info(fchains[0]),
+                                         "note": "the four calls above as one gf_prepare_chain launch"}
+    del fchains
 
     # 1b. the same layer in Q4_K (a format the pages' decode-layer measurements name),
     # 8 launches and 7 with the dual GEMV
@@ -774,8 +849,8 @@ def epilogue_cost(G, torch, s):
 
 def e2e_measure(G, torch, step, s, args):
     """The same step through the public API from pinned host memory: every step copies its
-    activations host->device (one copy), launches the step's graph of the 13 prepared
-    calls and copies every result back (one copy)."""
+    activations host->device (one copy), launches the step's graph of the prepared calls
+    (the layer's eight as one chain) and copies every result back (one copy)."""
     arena, host, (i0, i1), (o0, o1) = step.pack_for_e2e()
     # the decode loop's calls, planned once on the step's buffers (gf_prepare) and
     # recorded as one graph (gf_graph_create); each step is one gf_graph_launch
@@ -809,7 +884,8 @@ def e2e_measure(G, torch, step, s, args):
     bo = h_out.numel() * h_out.element_size()
     return {"value": round(step.step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 6), "wall_ms_per_step": round(1e3 * wall / reps, 6),
-            "steps": reps, "launch_mode": "the step's 13 calls prepared once (gf_prepare) and recorded as one graph "
+            "steps": reps, "launch_mode": "the step's 13 calls prepared once (gf_prepare; the layer's 8 as one "
+                                          "gf_prepare_chain) and recorded as one graph "
                                           "(gf_graph_create, programmatic dependent launch inside); per step one "
                                           "gf_graph_launch, one H2D and one D2H copy from pinned host memory"}
 

@@ -326,9 +326,61 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int
   }
 }
 
+// Kernel argument block: one call, or a chain of calls (FEAT_CHAIN).
+template <int FEAT>
+struct KernelArgsOf {
+  using type = StreamArgs;
+};
+template <>
+struct KernelArgsOf<FEAT_CHAIN> {
+  using type = ChainArgs;
+};
+__device__ __forceinline__ const StreamArgs& stage_args(const StreamArgs& p, int) { return p; }
+__device__ __forceinline__ const StreamArgs& stage_args(const ChainArgs& p, int s) { return p.st[s]; }
+
+// Rows [r0, r0 + nrows) of call a owned by the CTA (cluster) with row-range index rg; none
+// for an index past the call's CTAs (a chain stage with fewer rows than the grid).
+__device__ __forceinline__ void cta_rows(const StreamArgs& a, int rg, int64_t& r0, int& nrows) {
+  r0 = (static_cast<int64_t>(rg) * a.rows_base + min(rg, a.rows_extra)) * a.gran;
+  const int64_t n = min(static_cast<int64_t>((a.rows_base + (rg < a.rows_extra ? 1 : 0)) * a.gran), a.M - r0);
+  nrows = static_cast<int>(max(n, static_cast<int64_t>(0)));
+}
+
+// Grid barrier of a chain.  Arrival: the caller's CTA has passed a barrier after all of
+// its consumers' stores; the release (fence, then the add) publishes them, and the proxy
+// fence orders them before later bulk copies that read the same bytes.
+__device__ __forceinline__ void grid_arrive(unsigned long long* ctr) {
+  __threadfence();
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  atomicAdd(ctr, 1ull);
+}
+
+// Wait (acquire, bounded) until the counter reaches target; then later bulk copies read
+// what the other CTAs published.  On timeout: error word, abort flag, false.
+__device__ __forceinline__ bool grid_wait(const unsigned long long* ctr, unsigned long long target,
+                                          volatile int* abort, unsigned* err) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+    if (v >= target) break;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      set_error(err, ERRBIT_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 template <int WT, int NC, int FEAT>
-__global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(const StreamArgs a) {
-  constexpr bool kExt = FEAT != FEAT_PLAIN;     // dual GEMV / RMS prologue compiled in
+__global__ void __launch_bounds__(stream_threads(WT, NC), 1)
+    gemv_stream_kernel(const __grid_constant__ typename KernelArgsOf<FEAT>::type prm) {
+  constexpr bool kChain = FEAT == FEAT_CHAIN;   // several calls, grid barriers between dependent ones
+  constexpr bool kExt = FEAT != FEAT_PLAIN;     // dual GEMV / several matrices / RMS prologue compiled in
   constexpr bool kSplit = FEAT == FEAT_SPLIT;   // cluster split K compiled in
   constexpr int U = stream_u(WT, NC);
   constexpr int RT = stream_rt(WT, NC);
@@ -338,47 +390,59 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
   // the extension code)
   constexpr bool kBatch = !(kExt && WT == WT_F16 && NCT > 1);
   static_assert(U * NCT * 16 <= 64, "x registers per thread");
+  // launch-wide values (equal in every stage of a chain): ring, consumer warps, layout
+  const StreamArgs& a0 = stage_args(prm, 0);
+  int nst = 1, nbar = 0;
+  if constexpr (kChain) {
+    nst = prm.nst;
+    nbar = prm.nbar;
+  }
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t full0 = sbase, empty0 = sbase + 8u * a.NS, xbar = sbase + 16u * a.NS;
+  const uint32_t full0 = sbase, empty0 = sbase + 8u * a0.NS, xbar = sbase + 16u * a0.NS;
   const uint32_t xchbar = xbar + 8u;  // split K: arrivals of the peer CTAs (rank 0 only)
-  float* xs = reinterpret_cast<float*>(smem + a.off_xs);
-  float* auxs = reinterpret_cast<float*>(smem + a.off_aux);
-  float* red = reinterpret_cast<float*>(smem + a.off_red);
-  float* normv = reinterpret_cast<float*>(smem + a.off_norm);  // [wpc][NC] sums of squares
-  float* xch = reinterpret_cast<float*>(smem + a.off_xchg);    // split K: [S][NC][XR], then [S][NC]
-  const uint32_t ring = sbase + static_cast<uint32_t>(a.off_ring);
+  const uint32_t xfree = xbar + 16u;  // chain: the consumers are done with the staged x
+  float* xs = reinterpret_cast<float*>(smem + a0.off_xs);
+  float* auxs = reinterpret_cast<float*>(smem + a0.off_aux);
+  float* red = reinterpret_cast<float*>(smem + a0.off_red);
+  float* normv = reinterpret_cast<float*>(smem + a0.off_norm);  // [wpc][NC] sums of squares
+  float* xch = reinterpret_cast<float*>(smem + a0.off_xchg);    // split K: [S][NC][XR], then [S][NC]
+  const uint32_t ring = sbase + static_cast<uint32_t>(a0.off_ring);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarBytes - 8);
+  // chain: the barrier counter when the launch began (a multiple of the grid)
+  volatile unsigned long long* gbase_s = reinterpret_cast<volatile unsigned long long*>(smem + kBarBytes - 16);
 
-  const int S = kSplit ? a.S : 1;
+  const int S = kSplit ? a0.S : 1;
   int crank = 0;
   if constexpr (kSplit) crank = static_cast<int>(cluster_ctarank());
   const int rg = static_cast<int>(blockIdx.x) / S;  // row range of this CTA (its cluster's)
-  const int64_t r0 = (static_cast<int64_t>(rg) * a.rows_base + min(rg, a.rows_extra)) * a.gran;
-  const int nrows = static_cast<int>(
-      min(static_cast<int64_t>((a.rows_base + (rg < a.rows_extra ? 1 : 0)) * a.gran), a.M - r0));
-  const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
-  const bool dual = kExt && a.W2 != nullptr;
-  const bool multi = kExt && a.nseg > 0;  // several matrices sharing x (never with dual)
-  const bool norm = kExt && a.gamma != nullptr;
-  const int XR = dual ? 2 * a.RC : a.RC;  // virtual rows per row chunk
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < a.NS; ++i) {
+    for (int i = 0; i < a0.NS; ++i) {
       mbar_init(full0 + 8u * i, 1);
-      mbar_init(empty0 + 8u * i, static_cast<uint32_t>(a.ncw));
+      mbar_init(empty0 + 8u * i, static_cast<uint32_t>(a0.ncw));
     }
     mbar_init(xbar, 1);
-    mbar_init(xchbar, static_cast<uint32_t>(S > 1 ? (S - 1) * a.ncw * 32 : 1));
+    mbar_init(xchbar, static_cast<uint32_t>(S > 1 ? (S - 1) * a0.ncw * 32 : 1));
+    if constexpr (kChain) {
+      mbar_init(xfree, 1);
+      // no CTA can have completed the first barrier before this one arrives, and the
+      // previous launch on this counter finished all of its arrivals before this one began
+      const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(prm.gbar);
+      *gbase_s = v - v % gridDim.x;
+    }
     fence_mbar_init();
   }
   if constexpr (kSplit)
     cluster_sync_all();  // peers arrive on rank 0's barrier only after it is initialised
   else
     __syncthreads();
-  pdl_trigger();
+  // A chain lets the next grid in only after its last grid barrier: that grid may be this
+  // chain again, which reads the counter when it starts.
+  if (nbar == 0) pdl_trigger();
+  const unsigned long long gbase = kChain ? *gbase_s : 0ull;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -387,7 +451,33 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
       int it = 0, slot = 0;  // tiles issued; ring slot of the next one
       uint32_t ephase = 1u;   // parity of the empty-barrier phase that frees `slot`
       bool ok = true;
-      bool x_issued = false;
+      int nx = 0;             // x copies issued
+      bool waited = false;    // preceding grid waited for
+      int bars = 0, bars_seen = 0;  // chain: grid barriers up to this stage; the last waited for
+      for (int s = 0; s < nst && ok; ++s) {
+      const StreamArgs& a = stage_args(prm, s);
+      if constexpr (kChain) bars += (s > 0 && prm.bar_before[s]) ? 1 : 0;
+      int64_t r0;
+      int nrows;
+      cta_rows(a, rg, r0, nrows);
+      const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
+      const bool dual = kExt && a.W2 != nullptr;
+      const bool multi = kExt && a.nseg > 0;
+      const bool norm = kExt && a.gamma != nullptr;
+      bool xnew = a.stage_x && nrows > 0;  // this stage copies x (and gamma) into xs
+      if constexpr (kChain) xnew = xnew && !prm.x_reuse[s];
+      // x goes right behind the launch's first weight tile; in a later stage of a chain,
+      // behind as many of the stage's tiles as the ring holds (their slots free up as the
+      // previous stage ends, and x is not needed earlier)
+      int x_after = 1, its = 0;
+      if (kChain && s > 0) {
+        int ntl = 0;
+        for (int rc0 = 0; rc0 < nrows; rc0 += a.RC) {
+          const int nvr = (dual ? 2 : 1) * min(a.RC, nrows - rc0);
+          ntl += (kc_hi - kc_lo) * ((nvr + a.R - 1) / a.R);
+        }
+        x_after = max(1, min(a.NS, ntl));
+      }
       for (int rc0 = 0; rc0 < nrows && ok; rc0 += a.RC) {
         const int nrc = min(a.RC, nrows - rc0);
         const int nvr = dual ? 2 * nrc : nrc;
@@ -445,42 +535,93 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
               slot = 0;
               ephase ^= 1u;
             }
-            if (a.stage_x && !x_issued) {
-              // x staged by bulk copy right behind the first weight tile, once the
-              // preceding grid (which may write x) has finished: later in the queue it
-              // waits behind the whole ring of weight tiles
-              // (with the RMS prologue, gamma follows x on the same barrier)
-              pdl_wait();
+            if (xnew && ++its == x_after) {
+              // x staged by bulk copy behind the weight tiles above, once the preceding
+              // grid (which may write x) has finished: later in the queue it waits behind
+              // the whole ring of weight tiles (with the RMS prologue, gamma follows x on
+              // the same barrier).  In a chain, also once the consumers are done with the
+              // previous x and, after a grid barrier, once every CTA has passed it.
+              if (!waited) {
+                pdl_wait();
+                waited = true;
+              }
+              if constexpr (kChain) {
+                if (nx > 0 && !mbar_wait_or_abort(xfree, static_cast<uint32_t>((nx - 1) & 1), abort_flag, a.err)) {
+                  ok = false;
+                  break;
+                }
+                if (bars > bars_seen) {
+                  if (!grid_wait(prm.gbar, gbase + static_cast<unsigned long long>(bars) * gridDim.x, abort_flag,
+                                 a.err)) {
+                    ok = false;
+                    break;
+                  }
+                  bars_seen = bars;
+                }
+              }
               mbar_arrive_expect_tx(xbar, static_cast<uint32_t>((NC + (norm ? 1 : 0)) * a.K * 4));
               for (int c = 0; c < NC; ++c)
                 bulk_g2s(smem_u32(xs + c * a.K), a.x + static_cast<int64_t>(c) * a.K,
                          static_cast<uint32_t>(a.K * 4), xbar);
               if (norm) bulk_g2s(smem_u32(xs + NC * a.K), a.gamma, static_cast<uint32_t>(a.K * 4), xbar);
-              x_issued = true;
+              ++nx;
             }
           }
         }
       }
+      }  // stages
       if (!ok) {
         // Drain: wait (bounded) until every copy this thread issued has landed.
-        for (int i = max(0, it - a.NS); i < it; ++i)
-          (void)mbar_wait(full0 + 8u * (i % a.NS), static_cast<uint32_t>((i / a.NS) & 1));
-        if (x_issued) (void)mbar_wait(xbar, 0u);
+        for (int i = max(0, it - a0.NS); i < it; ++i)
+          (void)mbar_wait(full0 + 8u * (i % a0.NS), static_cast<uint32_t>((i / a0.NS) & 1));
+        if (nx > 0) (void)mbar_wait(xbar, static_cast<uint32_t>((nx - 1) & 1));
       }
     }
   } else {
     // ------------------------------------------------------------ consumers
     // Every consumer thread runs the same sequence of named barriers whether or not a
     // wait gave up; after an abort the remaining work is skipped, not the barriers.
-    const int cw = warp - 1, ctid = threadIdx.x - 32, nt = a.ncw * 32;
+    const int cw = warp - 1, ctid = threadIdx.x - 32, nt = a0.ncw * 32;
+    const uint32_t qr = lane_quad_rot<WT>(lane);
+    auto epi_aux = [](int e) { return e == EPI_SILU_MUL || e == EPI_ADD; };
+    const bool finalizer = (crank == 0);
+    pdl_wait();  // x, aux and dst may belong to the preceding grid
+    int slot = 0;            // ring slot of the next tile
+    uint32_t fphase = 0;     // parity of its full-barrier phase
+    uint32_t xphase = 0;
+    bool ok = true;
+    auto cbar = [&]() { named_bar_sync(1, static_cast<uint32_t>(nt)); };
+    int bars = 0;  // chain: grid barriers passed
+    for (int s = 0; s < nst; ++s) {
+    const StreamArgs& a = stage_args(prm, s);
+    if constexpr (kChain) {
+      if (s > 0 && prm.bar_before[s]) {
+        // this CTA arrived at the end of the previous stage; wait for every other one
+        ++bars;
+        if (ctid == 0 && ok)
+          (void)grid_wait(prm.gbar, gbase + static_cast<unsigned long long>(bars) * gridDim.x, abort_flag, a.err);
+        cbar();
+        ok = ok && !*abort_flag;
+        if (bars == nbar) pdl_trigger();
+      }
+    }
+    int64_t r0;
+    int nrows;
+    cta_rows(a, rg, r0, nrows);
+    const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
+    const bool dual = kExt && a.W2 != nullptr;
+    const bool multi = kExt && a.nseg > 0;  // several matrices sharing x (never with dual)
+    const bool norm = kExt && a.gamma != nullptr;
+    const int XR = dual ? 2 * a.RC : a.RC;  // virtual rows per row chunk
+    bool xnew = a.stage_x && nrows > 0;     // x (and gamma) copied into xs for this stage
+    if constexpr (kChain) xnew = xnew && !prm.x_reuse[s];
     const int g = cw / a.wpg;                  // row group of this warp
+    const bool live = !kChain || g < a.G;      // chain: warps past the stage's row groups idle
     const int wr = cw - g * a.wpg;             // warp within the row group
     const int cgi = wr / a.wpc;                // column group
     const int wc = wr - cgi * a.wpc;           // warp within the column group
     const int c0 = cgi * NCT;                  // first column of this thread
     const int tg = wc * 32 + lane, tg_n = a.wpc * 32;
-    const uint32_t qr = lane_quad_rot<WT>(lane);
-    auto epi_aux = [](int e) { return e == EPI_SILU_MUL || e == EPI_ADD; };
     bool need_aux = epi_aux(a.epi);
     if (multi)
       for (int i = 0; i < a.nseg; ++i) need_aux = need_aux || epi_aux(a.seg_epi[i]);
@@ -493,14 +634,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
       const int64_t mi = a.seg_end[i] - (i ? a.seg_end[i - 1] : 0);
       return a.seg_aux[i][c * mi + local];
     };
-    const bool finalizer = (crank == 0);
-    pdl_wait();  // x, aux and dst may belong to the preceding grid
-    int slot = 0;            // ring slot of the next tile
-    uint32_t fphase = 0;     // parity of its full-barrier phase
-    uint32_t xphase = 0;
-    bool ok = true;
     bool x_loaded = false;
-    auto cbar = [&]() { named_bar_sync(1, static_cast<uint32_t>(nt)); };
     float ssq[NCT];  // this thread's share of the sum of squares of x (first row chunk)
 #pragma unroll
     for (int c = 0; c < NCT; ++c) ssq[c] = 0.0f;
@@ -539,7 +673,10 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
         const int seg = seg_bytes_of<WT>(klen);
         // this thread's x (its units, its columns) in registers for the whole chunk: from
         // the transformed chunk in shared memory, or straight from global memory
-        if (a.stage_x && kc == kc_lo && rc0 == 0) ok = ok && mbar_wait_or_abort(xbar, 0u, abort_flag, a.err);
+        if (xnew && kc == kc_lo && rc0 == 0) {
+          ok = ok && mbar_wait_or_abort(xbar, xphase, abort_flag, a.err);
+          xphase ^= 1u;
+        }
         const bool x_smem = a.fwht_B > 0 || a.stage_x;
         const float* xsrc = x_smem ? xs : a.x + static_cast<int64_t>(kc) * a.kc_len;
         const int64_t xstride = x_smem ? klen : a.K;
@@ -582,7 +719,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
           for (int j = 0; j < RT; ++j)
 #pragma unroll
             for (int c = 0; c < NCT; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
-          if (ok) {
+          if (ok && live) {
             if constexpr (WT == WT_Q4_K && kInt)
               consume_tile_q4k_int<RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg, g,
                                        a.G, xq, xsum, acc);
@@ -611,7 +748,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
             vals[j] = j < V ? acc[j / NCT][j % NCT].x + acc[j / NCT][j % NCT].y : 0.0f;
           const float sum = WarpVecReduce<VP>::run(vals, lane);
           const int jv = lane >> (5 - WarpVecReduce<VP>::kLog);
-          if (lane == WarpVecReduce<VP>::owner(jv) && jv < V) {
+          if (live && lane == WarpVecReduce<VP>::owner(jv) && jv < V) {
             const int r = g + (jv / NCT) * a.G, c = c0 + jv % NCT;
             if (r < rows && c < NC) {
               float* p = red + ((t0 + r) * a.wpc + wc) * NC + c;
@@ -719,6 +856,22 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1) gemv_stream_kernel(
       }
       cbar();  // red / auxs may be reused by the next row chunk
     }
+    if constexpr (kChain) {
+      // The staged x is free once no later stage reuses it (the barrier above ended every
+      // read of it); the grid barrier's arrival publishes this CTA's outputs.
+      if (a.stage_x && nrows > 0 && ctid == 0) {
+        bool keep = false;
+        if (s + 1 < nst && prm.x_reuse[s + 1]) {
+          int64_t r0n;
+          int nrn;
+          cta_rows(stage_args(prm, s + 1), rg, r0n, nrn);
+          keep = nrn > 0;
+        }
+        if (!keep) mbar_arrive(xfree);
+      }
+      if (s + 1 < nst && prm.bar_before[s + 1] && ctid == 0) grid_arrive(prm.gbar);
+    }
+    }  // stages
   }
   __syncthreads();
   if constexpr (kSplit) cluster_sync_all();  // no CTA leaves while a peer may still store into it
@@ -786,6 +939,51 @@ int max_active_clusters_t(const Plan& p) {
   cfg.numAttrs = 1;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Persistent chain of one-column calls (one instantiation per format).
+template <int WT>
+int launch_chain_t(int grid, int threads, int smem, const ChainArgs& a, cudaStream_t st, bool pdl) {
+  auto kern = gemv_stream_kernel<WT, 1, FEAT_CHAIN>;
+  static int configured_smem[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && configured_smem[dev] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured_smem[dev] = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// CTAs of the chain kernel resident per SM (0 if the query fails).
+template <int WT>
+int chain_ctas_per_sm_t(int threads, int smem) {
+  auto kern = gemv_stream_kernel<WT, 1, FEAT_CHAIN>;
+  int dev = 0, smem_max = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      smem_max < smem ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, static_cast<size_t>(smem)) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }

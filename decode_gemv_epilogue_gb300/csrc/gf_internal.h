@@ -23,6 +23,7 @@ constexpr int kMaxFusedFwhtBlock = 8192;
 constexpr int kUnitElems = 16;              // weights per decode unit (half a quant block)
 constexpr int kMaxSplit = 8;                // CTAs of a split-K cluster (portable cluster size)
 constexpr int kMaxSeg = 4;                  // matrices sharing x in one multi-matrix launch
+constexpr int kMaxChain = 8;                // calls run by one persistent chain launch
 
 // Tiling of the consumer warps, per (format, columns):
 //  U   units (16 weights) per thread per K chunk, RT rows per thread per tile;
@@ -103,6 +104,21 @@ struct StreamArgs {
   int S;             // CTAs per cluster sharing a row range, each a slice of the K chunks
   int stage_x;       // 1: the producer bulk-copies x (one K chunk, every column) into xs
   int off_xs, off_aux, off_red, off_norm, off_xchg, off_ring;
+};
+
+// Several single-column streamed calls run by one persistent launch (FEAT_CHAIN).  Stage s
+// is the call st[s], planned with the launch's common consumer warps, ring stages and
+// shared-memory layout; the producer streams the stages' weight tiles back to back.
+// Before a stage with bar_before[s] set, every CTA's consumers have finished and published
+// the stages before it: a grid barrier on *gbar, a counter that only grows (each CTA adds
+// one per barrier, so it is a multiple of the grid whenever no launch is in flight).
+struct ChainArgs {
+  StreamArgs st[kMaxChain];
+  unsigned long long* gbar;
+  int nst;   // stages
+  int nbar;  // grid barriers (stages with bar_before set)
+  unsigned char bar_before[kMaxChain];
+  unsigned char x_reuse[kMaxChain];  // 1: x staged for stage s-1 is stage s's x (no copy)
 };
 
 struct GenericArgs {
@@ -188,7 +204,7 @@ struct DeviceLimits {
 };
 
 // Kernel feature sets of the streamed GEMV (separate instantiations).
-enum { FEAT_PLAIN = 0, FEAT_EXT = 1, FEAT_SPLIT = 2 };
+enum { FEAT_PLAIN = 0, FEAT_EXT = 1, FEAT_SPLIT = 2, FEAT_CHAIN = 3 };
 
 // Launchers (return cudaError_t).  `pdl` requests programmatic stream serialization.
 // FEAT_SPLIT launches group the grid into clusters of p.s.S CTAs.  One function per
@@ -206,6 +222,11 @@ int launch_stream_q4k_split(int ncols, const Plan& p, cudaStream_t st, bool pdl)
 int stream_split_max_clusters_float(int wtype, int ncols, const Plan& p);
 int stream_split_max_clusters_block(int wtype, int ncols, const Plan& p);
 int stream_split_max_clusters_q4k(int ncols, const Plan& p);
+// Persistent chain (one column, the extended kernel's features): launch, and CTAs of
+// `threads` threads and `smem` bytes resident per SM (0 if unknown).
+int launch_stream_chain(int wtype, int grid, int threads, int smem, const ChainArgs& a, cudaStream_t st,
+                        bool pdl);
+int stream_chain_ctas_per_sm(int wtype, int threads, int smem);
 int launch_generic(int wtype, int ncols, const GenericArgs& a, int grid, int smem,
                    cudaStream_t st, bool pdl);
 int launch_fwht(const float* x, const float* signs, float* dst, int64_t n, int B, int nsigns,
