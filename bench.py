@@ -9,16 +9,17 @@ every launch streams its weights from HBM):
   f16 4096x4096  sigmoid tail                                        (1)
   Q8_0 11008x4096  silu(y) * m                                      (1)
   Q4_0 decode-layer chain, d_model 4096, ffn 14336: q, k, v, o+add,
-       up, gate silu*up, down+add, beta sigmoid (M=32): the 8 calls
-       prepared and run as one persistent chain (gf_prepare_chain)    (1)
+       up, gate silu*up, down+add, beta sigmoid (M=32): q, k, v and beta
+       sharing x in one gemv_multi, o+add, gate and up in one gemv_glu,
+       down+add                                                         (4)
   signed FWHT(1024) prologue + f16 5120x5120 + add in place, 1 column (1)
   the same with a batch of 8 columns                                 (1)
 
 value = algorithmic bytes of the step (W + x + aux + dst, each once) / step time, GB/s,
 with the step captured in a CUDA graph (launches chained with programmatic dependent
 launch) and replayed.  Also reported: per-kernel CUDA-event durations and the roofline
-of the dominant kernel, microseconds per decode layer (the persistent chain, the 8
-fused launches, the 13 unfused ones), the
+of the dominant kernel, microseconds per decode layer (the step's 4 launches, the 8
+fused launches, the 13 unfused ones, the persistent chain), the
 epilogue cost against the tail-free GEMV, an end-to-end number through host buffers,
 SM clocks during the timed region, and the fp64 CPU oracle timed on the host cores.
 Under "next_rows": the layer chain with the gated dual GEMV (7 launches), the same
@@ -45,8 +46,8 @@ sys.path.insert(0, ROOT)
 METRIC = "fused GEMV HBM GB/s & % of GB300 peak; µs per decode layer chain"
 UNIT = "GB/s"
 WORKLOAD = ("decode_step: f16 4096x4096 add-in-place via [32,128] view + sigmoid; "
-            "Q8_0 11008x4096 silu*m; Q4_0 decode-layer chain (d_model 4096, ffn 14336, 8 GEMVs in one "
-            "persistent launch); "
+            "Q8_0 11008x4096 silu*m; Q4_0 decode-layer chain (d_model 4096, ffn 14336, 8 GEMVs in 4 "
+            "launches: multi q/k/v/beta, o+add, glu gate*up, down+add); "
             "signed FWHT(1024) + f16 5120x5120 add-in-place, ncols 1 and 8")
 L2_BYTES = 129 * 1024 * 1024
 
@@ -92,8 +93,19 @@ def algo_bytes(wt, M, K, epi, ncols, fwht):
 WT_NAME = {0: "f32", 1: "f16", 2: "q8_0", 3: "q4_0"}
 CHAIN_NAMES = ["chain_q", "chain_k", "chain_v", "chain_o_add", "chain_up", "chain_gate_silu_mul",
                "chain_down_add", "chain_beta_sigmoid"]
-CHAIN_UNIT = "decode_layer_chain"
-CHAIN_KEY = "gemv_stream_kernel<q4_0,1,chain>"
+# The step runs the layer's eight GEMVs as four launches: q, k, v and the sigmoid head
+# sharing x (gemv_multi), o + residual add, gate and up in one pass with silu(gate) * up
+# (gemv_glu), down + residual add.  Measured on GB300 (us per layer, two weight sets
+# alternating): 42.1 for these four, 53.3 for the eight calls as separate launches and
+# 46.3 / 54.3 for the four / eight as one persistent chain (gf_prepare_chain).
+LAYER_UNITS = {
+    "layer_qkv_beta": ["chain_q", "chain_k", "chain_v", "chain_beta_sigmoid"],
+    "layer_o_add": ["chain_o_add"],
+    "layer_gate_up": ["chain_gate_silu_mul", "chain_up"],
+    "layer_down_add": ["chain_down_add"],
+}
+LAYER_KEYS = {"layer_qkv_beta": "gemv_stream_kernel<q4_0,1,ext>", "layer_o_add": "gemv_stream_kernel<q4_0,1>",
+              "layer_gate_up": "gemv_stream_kernel<q4_0,1,ext>", "layer_down_add": "gemv_stream_kernel<q4_0,1>"}
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -149,14 +161,21 @@ class Step:
                 raise RuntimeError("plan failed for %s: %s" % (n, G.status_string(path)))
             kind = {G.PATH_STREAM: "gemv_stream_kernel", G.PATH_TC: "gemv_tc_kernel"}.get(path, "gemv_generic_kernel")
             self.keys[n] = ("fwht_signed_kernel+" if fw else "") + "%s<%s,%d>" % (kind, WT_NAME[wt], nc)
-        # the step's launch units: every call on its own, except the layer's eight calls,
-        # which run as one persistent chain
+        # the step's launch units: every call on its own, except the layer's eight GEMVs,
+        # which run as four launches (LAYER_UNITS)
         self.unit_names = [n for (n, *_r) in spec if n not in CHAIN_NAMES]
-        self.unit_names.insert(3, CHAIN_UNIT)
-        self.bytes[CHAIN_UNIT] = sum(self.bytes[n] for n in CHAIN_NAMES)
-        self.keys[CHAIN_UNIT] = CHAIN_KEY
+        self.unit_names[3:3] = list(LAYER_UNITS)
+        wb = lambda n: self.W[n].numel()
+        d, f = 4096, 14336
+        self.bytes["layer_qkv_beta"] = sum(wb(n) for n in LAYER_UNITS["layer_qkv_beta"]) + 4 * d + 4 * (3 * d + 32)
+        self.bytes["layer_o_add"] = wb("chain_o_add") + 4 * d + 2 * 4 * d
+        self.bytes["layer_gate_up"] = wb("chain_gate_silu_mul") + wb("chain_up") + 4 * d + 4 * f
+        self.bytes["layer_down_add"] = wb("chain_down_add") + 4 * f + 2 * 4 * d
+        self.keys.update(LAYER_KEYS)
+        self.step_bytes = sum(self.bytes[n] for n in self.unit_names)
         # kernels launched per step (a prologue call launches the transform, then the GEMV)
-        self.kernels_per_step = sum(2 if fw else 1 for (n, wt, M, K, e, nc, fw) in spec if n not in CHAIN_NAMES) + 1
+        self.kernels_per_step = (sum(2 if fw else 1 for (n, wt, M, K, e, nc, fw) in spec if n not in CHAIN_NAMES)
+                                 + len(LAYER_UNITS))
 
     def call_specs(self):
         """(name, arguments, keyword arguments) of the step's gemv_fused_ex calls, on the
@@ -186,13 +205,29 @@ class Step:
         return [(name, (lambda a=a, kw=kw: G.gemv_fused_ex(*a, pdl=pdl, stream=stream, **kw)))
                 for (name, a, kw) in self.call_specs()]
 
+    def layer_call(self, unit, Wl, prepare=False, pdl=True):
+        """One of the layer's four launches on weight set Wl: issued now, or (prepare) planned
+        once and returned (gf_prepare*)."""
+        G, d, f = self.G, 4096, 14336
+        if unit == "layer_qkv_beta":
+            items = [(Wl["chain_q"], d, 0, None, self.cq), (Wl["chain_k"], d, 0, None, self.ck),
+                     (Wl["chain_v"], d, 0, None, self.cv), (Wl["chain_beta_sigmoid"], 32, 1, None, self.cbeta)]
+            return (G.prepare_multi if prepare else G.gemv_multi)(items, 3, self.cx, d, pdl=pdl)
+        if unit == "layer_gate_up":
+            fn = G.prepare_glu if prepare else G.gemv_glu
+            return fn(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, self.cr, f, d, self.cg, pdl=pdl, split_k=False)
+        fn = G.prepare if prepare else G.gemv_fused_ex
+        if unit == "layer_o_add":
+            return fn(Wl["chain_o_add"], 3, self.ca, d, d, 4, self.cr, self.cr, pdl=pdl, split_k=False)
+        return fn(Wl["chain_down_add"], 3, self.cg, d, f, 4, self.cr, self.cr, pdl=pdl, split_k=False)
+
     def prepared(self, pdl=True):
-        """The step's launch units planned once, in order: gf_prepare for each call, and the
-        layer's eight prepared calls as one chain (gf_prepare_chain)."""
+        """The step's launch units planned once (gf_prepare*), in order."""
         G = self.G
-        one = {name: G.prepare(*a, pdl=pdl, split_k=False, **kw) for (name, a, kw) in self.call_specs()}
-        chain = G.prepare_chain([one[n] for n in CHAIN_NAMES])
-        return [(n, chain if n == CHAIN_UNIT else one[n]) for n in self.unit_names]
+        one = {name: G.prepare(*a, pdl=pdl, **kw) for (name, a, kw) in self.call_specs() if name not in CHAIN_NAMES}
+        for u in LAYER_UNITS:
+            one[u] = self.layer_call(u, self.W, prepare=True, pdl=pdl)
+        return [(n, one[n]) for n in self.unit_names]
 
     def unit_calls(self, pdl=True):
         """(name, fn) per launch unit: fn issues it on the current stream."""
@@ -456,8 +491,8 @@ def gpu_arm(args, rank, world, local_rank):
         "roofline": roofline,
         "pct_of_peak": round(100 * value / world / peak, 2),
         "gpu_launches": launches,
-        "us_per_layer": chain["persistent_us"], "launches_per_layer": 1,
-        "us_per_layer_8_launches": chain["fused_us"],
+        "us_per_layer": chain["step_form_us"], "launches_per_layer": len(LAYER_UNITS),
+        "us_per_layer_8_launches": chain["fused_us"], "us_per_layer_persistent_chain": chain["persistent_us"],
         "us_per_layer_unfused": chain["unfused_us"], "launches_per_layer_unfused": 13,
         "chain": chain, "epilogue_cost": epi_cost, "per_kernel": per_kernel, "per_workload": per_workload,
         "next_rows": nxt,
@@ -473,21 +508,23 @@ def launch_durations(G, torch, step, s, args):
     of back-to-back launches (chained with programmatic dependent launch, as in the step)
     cycling through copies of its weights -- enough copies to exceed 2x L2 when the
     weights allow, at most 32 -- timed with CUDA events on the launch stream."""
-    out = {CHAIN_UNIT: chain_unit_us(G, torch, step, s, args)}
-    calls = dict(step.calls(pdl=True))
-    for name, wt, M, K, epi, nc, fw in step_spec():
-        if name in CHAIN_NAMES:
-            continue
-        W0 = step.W[name]
-        ncopy = int(min(32, max(2, -(-2 * L2_BYTES // W0.numel()))))
-        copies = [W0] + [W0.clone() for _ in range(ncopy - 1)]
-        fn = calls[name]
+    out = {}
+    specs = {n: (a, kw) for (n, a, kw) in step.call_specs()}
+    for name in step.unit_names:
+        mats = LAYER_UNITS.get(name, [name])
+        nbytes = sum(step.W[n].numel() for n in mats)
+        ncopy = int(min(32, max(2, -(-2 * L2_BYTES // nbytes))))
+        W0 = {n: step.W[n] for n in mats}
+        copies = [W0] + [{n: W0[n].clone() for n in mats} for _ in range(ncopy - 1)]
+        if name in LAYER_UNITS:
+            fn = lambda Wl, name=name: step.layer_call(name, Wl)
+        else:
+            a, kw = specs[name]
+            fn = lambda Wl, name=name, a=a, kw=kw: G.gemv_fused_ex(Wl[name], *a[1:], pdl=True, **kw)
 
         def run_all():
             for Wc in copies:
-                step.W[name] = Wc
-                fn()
-            step.W[name] = W0
+                fn(Wc)
 
         with torch.cuda.stream(s):
             run_all()
@@ -524,7 +561,7 @@ def second_layer(torch, step):
 
 
 def layer_chains(G, step, layers, pdl=True):
-    """One persistent chain of the layer's eight calls per weight set."""
+    """One persistent chain of the layer's eight calls per weight set (gf_prepare_chain)."""
     specs = dict((n, (a, kw)) for (n, a, kw) in step.call_specs())
     out = []
     for Wl in layers:
@@ -534,13 +571,6 @@ def layer_chains(G, step, layers, pdl=True):
             calls.append(G.prepare(Wl[n], *a[1:], pdl=pdl, split_k=False, **kw))
         out.append(G.prepare_chain(calls))
     return out
-
-
-def chain_unit_us(G, torch, step, s, args):
-    """Per-launch device time of the step's persistent layer chain: a CUDA graph of
-    back-to-back chain launches alternating between two weight sets."""
-    chains = layer_chains(G, step, [{n: step.W[n] for n in CHAIN_NAMES}, second_layer(torch, step)])
-    return graph_us(torch, s, lambda i: chains[i].launch(), 2, max(10, min(args.steps, 200))) * 1e-3
 
 
 def chain_measure(G, torch, step, s, args):
@@ -606,10 +636,16 @@ def chain_measure(G, torch, step, s, args):
     chains = layer_chains(G, step, layers)
     res["persistent_us"] = round(graph_us(torch, s, lambda i: chains[i].launch(), 2, reps), 3)
     res["persistent_info"] = G.chain_info(chains[0])
+    del chains
+    # the step's form: four launches
+    res["step_form_us"] = round(graph_us(torch, s, lambda i: [step.layer_call(u, layers[i]) for u in LAYER_UNITS],
+                                         2, reps), 3)
     layer_bytes = sum(step.bytes[n] for n in names)
     res["layer_bytes"] = layer_bytes
+    res["step_form_bytes"] = sum(step.bytes[u] for u in LAYER_UNITS)
     res["fused_gbs"] = round(layer_bytes / (res["fused_us"] * 1e-6) / 1e9, 1)
     res["persistent_gbs"] = round(layer_bytes / (res["persistent_us"] * 1e-6) / 1e9, 1)
+    res["step_form_gbs"] = round(res["step_form_bytes"] / (res["step_form_us"] * 1e-6) / 1e9, 1)
     res["layers_timed"] = 2 * reps
     return res
 
@@ -884,8 +920,8 @@ def e2e_measure(G, torch, step, s, args):
     bo = h_out.numel() * h_out.element_size()
     return {"value": round(step.step_bytes / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 6), "wall_ms_per_step": round(1e3 * wall / reps, 6),
-            "steps": reps, "launch_mode": "the step's 13 calls prepared once (gf_prepare; the layer's 8 as one "
-                                          "gf_prepare_chain) and recorded as one graph "
+            "steps": reps, "launch_mode": "the step's calls prepared once (gf_prepare, gf_prepare_multi, "
+                                          "gf_prepare_glu) and recorded as one graph "
                                           "(gf_graph_create, programmatic dependent launch inside); per step one "
                                           "gf_graph_launch, one H2D and one D2H copy from pinned host memory"}
 

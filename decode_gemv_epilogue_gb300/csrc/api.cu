@@ -707,6 +707,8 @@ static bool any_overlap(const void* const* a, const int64_t* an, int na, const v
 // of its group writes, or writes what one reads, starts a new group behind a grid
 // barrier.  No stage may write another's weights: the weights of later stages are
 // streamed before the barriers.
+static_assert(sizeof(StreamArgs) % 8 == 0, "stage arguments are copied to 8-byte aligned shared memory");
+
 static int plan_chain(const Call* calls, int n, ChainArgs& ca, int& grid, int& threads, int& smem) {
   const DeviceLimits lim = device_limits();
   std::memset(&ca, 0, sizeof(ca));
@@ -736,11 +738,14 @@ static int plan_chain(const Call* calls, int n, ChainArgs& ca, int& grid, int& t
     stage_bytes = std::max(stage_bytes, a.stage_bytes);
     grid = std::max(grid, pl[i].grid);
   }
-  const int off_ring = kBarBytes + xs + aux + red + nrm;
-  const int NS = std::min(kMaxStages, (lim.smem_optin - off_ring - kRingSlackBytes) / stage_bytes);
+  // aux and partial-sum buffers twice: even and odd stages alternate
+  const int off_ring = kBarBytes + xs + 2 * aux + 2 * red + nrm;
+  const int args_bytes = n * static_cast<int>(sizeof(StreamArgs));
+  const int NS = std::min(kMaxStages, (lim.smem_optin - off_ring - kRingSlackBytes - 16 - args_bytes) / stage_bytes);
   if (NS < 2) return GF_ERR_UNSUPPORTED;
   threads = 32 * (1 + ncw);
-  smem = off_ring + NS * stage_bytes + kRingSlackBytes;
+  ca.off_args = round_up(off_ring + NS * stage_bytes + kRingSlackBytes, 16);
+  smem = ca.off_args + args_bytes;
   const int per_sm = stream_chain_ctas_per_sm(calls[0].wtype, threads, smem);
   if (per_sm < 1 || grid > per_sm * lim.sm_count) return GF_ERR_UNSUPPORTED;  // every CTA resident at once
   unsigned* err = device_error_word();
@@ -750,17 +755,20 @@ static int plan_chain(const Call* calls, int n, ChainArgs& ca, int& grid, int& t
   for (int i = 0; i < n; ++i)
     for (int j = 0; j < n; ++j)
       if (any_overlap(rg[i].w, rg[i].wn, rg[i].nw, rg[j].m, rg[j].mn, rg[j].nm)) return GF_ERR_ALIAS;
-  int g0 = 0;  // first stage of the current group
+  int g0 = 0;   // first stage of the current group
+  int rot = 0;  // the CTAs with a granule more than the others move on from stage to stage
   for (int i = 0; i < n; ++i) {
     StreamArgs& a = ca.st[i];
     a = pl[i].s;
     fill_stream_ptrs(cs[i], const_cast<float*>(cs[i].dst), err, a);
+    a.rot = rot;
+    rot = (rot + (pl[i].grid < grid ? pl[i].grid : a.rows_extra)) % grid;
     a.NS = NS;
     a.stage_bytes = stage_bytes;
     a.off_xs = kBarBytes;
     a.off_aux = a.off_xs + xs;
-    a.off_red = a.off_aux + aux;
-    a.off_norm = a.off_red + red;
+    a.off_red = a.off_aux + 2 * aux;
+    a.off_norm = a.off_red + 2 * red;
     a.off_xchg = a.off_norm + nrm;
     a.off_ring = off_ring;
     bool hazard = false;
@@ -769,17 +777,22 @@ static int plan_chain(const Call* calls, int n, ChainArgs& ca, int& grid, int& t
                any_overlap(rg[t].w, rg[t].wn, rg[t].nw, rg[i].w, rg[i].wn, rg[i].nw) ||
                any_overlap(rg[t].r, rg[t].rn, rg[t].nr, rg[i].w, rg[i].wn, rg[i].nw);
     if (hazard) {
-      ca.bar_before[i] = 1;
+      a.cflags |= CHAIN_BAR;
       ++ca.nbar;
       g0 = i;
     }
-    // the previous stage's staged x (and gamma) serve again when every CTA with rows
-    // here had rows there (x is never a stage's own output)
+    // the previous stage's staged x (and gamma) serve again when every CTA had rows there
+    // (x is never a stage's own output); each thread's converted x, too, when the
+    // threads own the same units of one K chunk (and no RMS prologue scales x)
     const StreamArgs& b = ca.st[i > 0 ? i - 1 : 0];
-    ca.x_reuse[i] = i > 0 && a.stage_x && b.stage_x && a.x == b.x && a.K == b.K && a.gamma == b.gamma &&
-                    pl[i - 1].grid >= pl[i].grid;
+    const bool reuse = i > 0 && a.stage_x && b.stage_x && a.x == b.x && a.K == b.K && a.gamma == b.gamma &&
+                       pl[i - 1].grid == grid;
+    if (reuse) a.cflags |= CHAIN_REUSE;
+    if (reuse && a.n_kc == 1 && b.n_kc == 1 && a.wpg == b.wpg && a.wpc == b.wpc && !a.gamma) a.cflags |= CHAIN_KEEP;
   }
   ca.nst = n;
+  ca.off_aux2 = kBarBytes + xs + aux;
+  ca.off_red2 = kBarBytes + xs + 2 * aux + red;
   return GF_OK;
 }
 
@@ -1122,8 +1135,8 @@ int gf_chain_info(const gf_prepared* chain, int64_t info[8]) {
   info[0] = ca.nst;
   info[1] = ca.nbar;
   for (int s = 0; s < ca.nst; ++s) {
-    if (ca.bar_before[s]) info[2] |= int64_t{1} << s;
-    if (ca.x_reuse[s]) info[3] |= int64_t{1} << s;
+    if (ca.st[s].cflags & CHAIN_BAR) info[2] |= int64_t{1} << s;
+    if (ca.st[s].cflags & CHAIN_REUSE) info[3] |= int64_t{1} << s;
   }
   info[4] = r.cgrid;
   info[5] = r.cthreads;

@@ -335,42 +335,68 @@ template <>
 struct KernelArgsOf<FEAT_CHAIN> {
   using type = ChainArgs;
 };
-__device__ __forceinline__ const StreamArgs& stage_args(const StreamArgs& p, int) { return p; }
-__device__ __forceinline__ const StreamArgs& stage_args(const ChainArgs& p, int s) { return p.st[s]; }
+__device__ __forceinline__ const StreamArgs& first_args(const StreamArgs& p) { return p; }
+__device__ __forceinline__ const StreamArgs& first_args(const ChainArgs& p) { return p.st[0]; }
 
-// Rows [r0, r0 + nrows) of call a owned by the CTA (cluster) with row-range index rg; none
-// for an index past the call's CTAs (a chain stage with fewer rows than the grid).
-__device__ __forceinline__ void cta_rows(const StreamArgs& a, int rg, int64_t& r0, int& nrows) {
+// Rows [r0, r0 + nrows) of call a owned by the CTA (cluster) with row-range index rg of
+// nrg; none for an index past the call's CTAs (a chain stage with fewer rows than the
+// grid).  A chain stage rotates the indices (a.rot) so that the CTAs given one granule
+// more than the others differ from stage to stage.
+__device__ __forceinline__ void cta_rows(const StreamArgs& a, int rg, int nrg, int64_t& r0, int& nrows) {
+  if (a.rot) rg = (rg + nrg - a.rot) % nrg;
   r0 = (static_cast<int64_t>(rg) * a.rows_base + min(rg, a.rows_extra)) * a.gran;
   const int64_t n = min(static_cast<int64_t>((a.rows_base + (rg < a.rows_extra ? 1 : 0)) * a.gran), a.M - r0);
   nrows = static_cast<int>(max(n, static_cast<int64_t>(0)));
 }
 
 // Grid barrier of a chain.  Arrival: the caller's CTA has passed a barrier after all of
-// its consumers' stores; the release (fence, then the add) publishes them, and the proxy
-// fence orders them before later bulk copies that read the same bytes.
-__device__ __forceinline__ void grid_arrive(unsigned long long* ctr) {
-  __threadfence();
+// its consumers' stores; the release add publishes them (cumulatively), and the proxy
+// fence orders them before later bulk copies that read the same bytes.  Returns the
+// counter's value before the add.
+__device__ __forceinline__ unsigned long long grid_arrive(unsigned long long* ctr) {
+  unsigned long long old;
   asm volatile("fence.proxy.async.global;" ::: "memory");
-  atomicAdd(ctr, 1ull);
+  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
+  return old;
 }
 
-// Wait (acquire, bounded) until the counter reaches target; then later bulk copies read
-// what the other CTAs published.  On timeout: error word, abort flag, false.
+// Wait (acquire, bounded) until the counter reaches target.  On timeout: error word,
+// abort flag, false.
 __device__ __forceinline__ bool grid_wait(const unsigned long long* ctr, unsigned long long target,
                                           volatile int* abort, unsigned* err) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
-    if (v >= target) break;
+    if (v >= target) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort = 1;
       set_error(err, ERRBIT_TIMEOUT);
       return false;
     }
-    __nanosleep(64);
+  }
+}
+
+// The chain's producer learns of passed grid barriers from the consumer thread that
+// waited for them (a count in shared memory, release / acquire at CTA scope); its bulk
+// copies after that read what the other CTAs published (the proxy fence).
+__device__ __forceinline__ void publish_count(volatile unsigned* p, unsigned v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(const_cast<unsigned*>(p))), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ bool wait_count(volatile unsigned* p, unsigned v, volatile int* abort, unsigned* err) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    unsigned c;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(c) : "r"(smem_u32(const_cast<unsigned*>(p))) : "memory");
+    if (c >= v) break;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      set_error(err, ERRBIT_TIMEOUT);
+      return false;
+    }
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");
   return true;
@@ -391,7 +417,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
   constexpr bool kBatch = !(kExt && WT == WT_F16 && NCT > 1);
   static_assert(U * NCT * 16 <= 64, "x registers per thread");
   // launch-wide values (equal in every stage of a chain): ring, consumer warps, layout
-  const StreamArgs& a0 = stage_args(prm, 0);
+  const StreamArgs& a0 = first_args(prm);
   int nst = 1, nbar = 0;
   if constexpr (kChain) {
     nst = prm.nst;
@@ -404,19 +430,26 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
   const uint32_t xchbar = xbar + 8u;  // split K: arrivals of the peer CTAs (rank 0 only)
   const uint32_t xfree = xbar + 16u;  // chain: the consumers are done with the staged x
   float* xs = reinterpret_cast<float*>(smem + a0.off_xs);
-  float* auxs = reinterpret_cast<float*>(smem + a0.off_aux);
-  float* red = reinterpret_cast<float*>(smem + a0.off_red);
+  float* auxs0 = reinterpret_cast<float*>(smem + a0.off_aux);
+  float* red0 = reinterpret_cast<float*>(smem + a0.off_red);
+  float* auxs_alt = auxs0;
+  float* red_alt = red0;
+  if constexpr (kChain) {
+    auxs_alt = reinterpret_cast<float*>(smem + prm.off_aux2);
+    red_alt = reinterpret_cast<float*>(smem + prm.off_red2);
+  }
   float* normv = reinterpret_cast<float*>(smem + a0.off_norm);  // [wpc][NC] sums of squares
   float* xch = reinterpret_cast<float*>(smem + a0.off_xchg);    // split K: [S][NC][XR], then [S][NC]
   const uint32_t ring = sbase + static_cast<uint32_t>(a0.off_ring);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarBytes - 8);
-  // chain: the barrier counter when the launch began (a multiple of the grid)
-  volatile unsigned long long* gbase_s = reinterpret_cast<volatile unsigned long long*>(smem + kBarBytes - 16);
+  // chain: grid barriers the consumers have passed (for the producer)
+  volatile unsigned* bars_passed = reinterpret_cast<volatile unsigned*>(smem + kBarBytes - 16);
 
   const int S = kSplit ? a0.S : 1;
   int crank = 0;
   if constexpr (kSplit) crank = static_cast<int>(cluster_ctarank());
   const int rg = static_cast<int>(blockIdx.x) / S;  // row range of this CTA (its cluster's)
+  const int nrg = static_cast<int>(gridDim.x) / S;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -428,13 +461,26 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
     mbar_init(xchbar, static_cast<uint32_t>(S > 1 ? (S - 1) * a0.ncw * 32 : 1));
     if constexpr (kChain) {
       mbar_init(xfree, 1);
-      // no CTA can have completed the first barrier before this one arrives, and the
-      // previous launch on this counter finished all of its arrivals before this one began
-      const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(prm.gbar);
-      *gbase_s = v - v % gridDim.x;
+      *bars_passed = 0u;
     }
     fence_mbar_init();
   }
+  // chain: every stage's arguments copied to shared memory (indexed parameter loads of a
+  // later stage each miss the constant cache at that stage's start)
+  const StreamArgs* sargs = nullptr;
+  if constexpr (kChain) {
+    sargs = reinterpret_cast<const StreamArgs*>(smem + prm.off_args);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&prm.st[0]);
+    uint32_t* dstw = reinterpret_cast<uint32_t*>(smem + prm.off_args);
+    const int nw = nst * static_cast<int>(sizeof(StreamArgs) / 4);
+    for (int i = threadIdx.x; i < nw; i += blockDim.x) dstw[i] = src[i];
+  }
+  auto stage = [&](int s) -> const StreamArgs& {
+    if constexpr (kChain)
+      return sargs[s];
+    else
+      return prm;
+  };
   if constexpr (kSplit)
     cluster_sync_all();  // peers arrive on rank 0's barrier only after it is initialised
   else
@@ -442,7 +488,6 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
   // A chain lets the next grid in only after its last grid barrier: that grid may be this
   // chain again, which reads the counter when it starts.
   if (nbar == 0) pdl_trigger();
-  const unsigned long long gbase = kChain ? *gbase_s : 0ull;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -455,17 +500,17 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
       bool waited = false;    // preceding grid waited for
       int bars = 0, bars_seen = 0;  // chain: grid barriers up to this stage; the last waited for
       for (int s = 0; s < nst && ok; ++s) {
-      const StreamArgs& a = stage_args(prm, s);
-      if constexpr (kChain) bars += (s > 0 && prm.bar_before[s]) ? 1 : 0;
+      const StreamArgs& a = stage(s);
+      if constexpr (kChain) bars += (a.cflags & CHAIN_BAR) ? 1 : 0;
       int64_t r0;
       int nrows;
-      cta_rows(a, rg, r0, nrows);
+      cta_rows(a, rg, nrg, r0, nrows);
       const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
       const bool dual = kExt && a.W2 != nullptr;
       const bool multi = kExt && a.nseg > 0;
       const bool norm = kExt && a.gamma != nullptr;
       bool xnew = a.stage_x && nrows > 0;  // this stage copies x (and gamma) into xs
-      if constexpr (kChain) xnew = xnew && !prm.x_reuse[s];
+      if constexpr (kChain) xnew = xnew && !(a.cflags & CHAIN_REUSE);
       // x goes right behind the launch's first weight tile; in a later stage of a chain,
       // behind as many of the stage's tiles as the ring holds (their slots free up as the
       // previous stage ends, and x is not needed earlier)
@@ -551,8 +596,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
                   break;
                 }
                 if (bars > bars_seen) {
-                  if (!grid_wait(prm.gbar, gbase + static_cast<unsigned long long>(bars) * gridDim.x, abort_flag,
-                                 a.err)) {
+                  if (!wait_count(bars_passed, static_cast<unsigned>(bars), abort_flag, a.err)) {
                     ok = false;
                     break;
                   }
@@ -591,15 +635,25 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
     uint32_t xphase = 0;
     bool ok = true;
     auto cbar = [&]() { named_bar_sync(1, static_cast<uint32_t>(nt)); };
-    int bars = 0;  // chain: grid barriers passed
+    int bars = 0;                  // chain: grid barriers passed
+    unsigned long long gbase = 0;  // chain (thread ctid 0): the counter when the launch began
+    // this thread's x for the current K chunk (a chain keeps it from stage to stage)
+    struct XRegs {
+      float2 xr[kInt ? 1 : U][NCT][8];
+      XInt xq[kInt ? U : 1][kInt ? NCT : 1];
+      float xsum[U][NCT];
+    };
+    XRegs x_chain;
     for (int s = 0; s < nst; ++s) {
-    const StreamArgs& a = stage_args(prm, s);
+    const StreamArgs& a = stage(s);
     if constexpr (kChain) {
-      if (s > 0 && prm.bar_before[s]) {
+      if (a.cflags & CHAIN_BAR) {
         // this CTA arrived at the end of the previous stage; wait for every other one
         ++bars;
-        if (ctid == 0 && ok)
-          (void)grid_wait(prm.gbar, gbase + static_cast<unsigned long long>(bars) * gridDim.x, abort_flag, a.err);
+        if (ctid == 0) {
+          if (ok) (void)grid_wait(prm.gbar, gbase + static_cast<unsigned long long>(bars) * gridDim.x, abort_flag, a.err);
+          publish_count(bars_passed, static_cast<unsigned>(bars));
+        }
         cbar();
         ok = ok && !*abort_flag;
         if (bars == nbar) pdl_trigger();
@@ -607,14 +661,14 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
     }
     int64_t r0;
     int nrows;
-    cta_rows(a, rg, r0, nrows);
+    cta_rows(a, rg, nrg, r0, nrows);
     const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
     const bool dual = kExt && a.W2 != nullptr;
     const bool multi = kExt && a.nseg > 0;  // several matrices sharing x (never with dual)
     const bool norm = kExt && a.gamma != nullptr;
     const int XR = dual ? 2 * a.RC : a.RC;  // virtual rows per row chunk
     bool xnew = a.stage_x && nrows > 0;     // x (and gamma) copied into xs for this stage
-    if constexpr (kChain) xnew = xnew && !prm.x_reuse[s];
+    if constexpr (kChain) xnew = xnew && !(a.cflags & CHAIN_REUSE);
     const int g = cw / a.wpg;                  // row group of this warp
     const bool live = !kChain || g < a.G;      // chain: warps past the stage's row groups idle
     const int wr = cw - g * a.wpg;             // warp within the row group
@@ -635,6 +689,12 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
       return a.seg_aux[i][c * mi + local];
     };
     bool x_loaded = false;
+    // chain: this thread's x (converted) survives the stage when the next one keeps it
+    const bool keep_x = kChain && (a.cflags & CHAIN_KEEP);
+    // chain: odd stages use the second aux / partial-sum buffers, so that a stage's
+    // finalisation may overlap the next stage's start (no CTA barrier between them)
+    float* const auxs = (kChain && (s & 1)) ? auxs_alt : auxs0;
+    float* const red = (kChain && (s & 1)) ? red_alt : red0;
     float ssq[NCT];  // this thread's share of the sum of squares of x (first row chunk)
 #pragma unroll
     for (int c = 0; c < NCT; ++c) ssq[c] = 0.0f;
@@ -681,16 +741,21 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
         const float* xsrc = x_smem ? xs : a.x + static_cast<int64_t>(kc) * a.kc_len;
         const int64_t xstride = x_smem ? klen : a.K;
         // (integer path: each unit's x is converted as soon as it is loaded)
-        float2 xr[kInt ? 1 : U][NCT][8];
-        XInt xq[kInt ? U : 1][kInt ? NCT : 1];
-        float xsum[U][NCT];
+        XRegs x_chunk;
+        XRegs& xreg = kChain ? x_chain : x_chunk;
+        auto& xr = xreg.xr;
+        auto& xq = xreg.xq;
+        auto& xsum = xreg.xsum;
         const float* gsrc = !norm ? nullptr
                             : a.stage_x ? xs + NC * a.K  // staged after x
                                         : a.gamma + static_cast<int64_t>(kc) * a.kc_len;
+        // a chain reloads x only for a new K chunk: not for a later row chunk of a one-chunk
+        // row, nor for a stage that keeps the previous stage's x
+        const bool load_x = !kChain || !(a.n_kc == 1 && (rc0 > 0 || keep_x));
 #pragma unroll
         for (int i = 0; i < U; ++i) {
           const int u = unit_index<WT, U>(tg, i, tg_n);
-          if (u < units && ok) {
+          if (u < units && ok && load_x) {
             float2 (&xv)[NCT][8] = xr[kInt ? 0 : i];
             if (norm)
               load_unit_x<WT, NCT, kExt>(xsrc, xstride, gsrc, u, qr, c0, NC, xv, rc0 == 0, ssq);
@@ -854,22 +919,34 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
           a.dst[c * a.M + r0 + rc0 + r] = out;
         }
       }
-      cbar();  // red / auxs may be reused by the next row chunk
+      // red / auxs may be reused by the next row chunk; a chain's next stage uses the other
+      // buffers and may start at once, unless it waits at a grid barrier (which publishes
+      // this stage's outputs) or writes the sums of squares read above
+      bool sync_end = true;
+      if constexpr (kChain)
+        sync_end = rc0 + a.RC < nrows || s + 1 == nst || (stage(s + 1).cflags & CHAIN_BAR) ||
+                   stage(s + 1).gamma != nullptr;
+      if (sync_end) cbar();
     }
     if constexpr (kChain) {
       // The staged x is free once no later stage reuses it (the barrier above ended every
       // read of it); the grid barrier's arrival publishes this CTA's outputs.
       if (a.stage_x && nrows > 0 && ctid == 0) {
         bool keep = false;
-        if (s + 1 < nst && prm.x_reuse[s + 1]) {
+        if (s + 1 < nst && (stage(s + 1).cflags & CHAIN_REUSE)) {
           int64_t r0n;
           int nrn;
-          cta_rows(stage_args(prm, s + 1), rg, r0n, nrn);
+          cta_rows(stage(s + 1), rg, nrg, r0n, nrn);
           keep = nrn > 0;
         }
         if (!keep) mbar_arrive(xfree);
       }
-      if (s + 1 < nst && prm.bar_before[s + 1] && ctid == 0) grid_arrive(prm.gbar);
+      if (s + 1 < nst && (stage(s + 1).cflags & CHAIN_BAR) && ctid == 0) {
+        // no CTA completes the launch's first barrier before this one arrives, and the
+        // previous launch on this counter made all of its arrivals before this one began
+        const unsigned long long old = grid_arrive(prm.gbar);
+        if (bars == 0) gbase = old - old % gridDim.x;
+      }
     }
     }  // stages
   }

@@ -103,22 +103,30 @@ struct StreamArgs {
   float* seg_dst[kMaxSeg];
   int S;             // CTAs per cluster sharing a row range, each a slice of the K chunks
   int stage_x;       // 1: the producer bulk-copies x (one K chunk, every column) into xs
+  int rot;           // chain stage: row range of CTA rg is that of index (rg - rot) mod CTAs
+  int cflags;        // chain stage: CHAIN_* bits
   int off_xs, off_aux, off_red, off_norm, off_xchg, off_ring;
 };
 
 // Several single-column streamed calls run by one persistent launch (FEAT_CHAIN).  Stage s
 // is the call st[s], planned with the launch's common consumer warps, ring stages and
 // shared-memory layout; the producer streams the stages' weight tiles back to back.
-// Before a stage with bar_before[s] set, every CTA's consumers have finished and published
-// the stages before it: a grid barrier on *gbar, a counter that only grows (each CTA adds
-// one per barrier, so it is a multiple of the grid whenever no launch is in flight).
+// Before a stage flagged CHAIN_BAR, every CTA's consumers have finished and published the
+// stages before it: a grid barrier on *gbar, a counter that only grows (each CTA adds one
+// per barrier, so it is a multiple of the grid whenever no launch is in flight).
+// Chain stage flags (StreamArgs.cflags):
+enum {
+  CHAIN_BAR = 1,     // a grid barrier before the stage
+  CHAIN_REUSE = 2,   // x staged for the previous stage is this stage's x (no copy)
+  CHAIN_KEEP = 4,    // and each thread keeps its converted x of the previous stage
+};
 struct ChainArgs {
   StreamArgs st[kMaxChain];
   unsigned long long* gbar;
-  int nst;   // stages
-  int nbar;  // grid barriers (stages with bar_before set)
-  unsigned char bar_before[kMaxChain];
-  unsigned char x_reuse[kMaxChain];  // 1: x staged for stage s-1 is stage s's x (no copy)
+  int nst;       // stages
+  int nbar;      // grid barriers
+  int off_args;  // shared-memory copy of st[0 .. nst) (8-byte aligned)
+  int off_aux2, off_red2;  // odd stages' aux and partial-sum buffers (even ones: off_aux, off_red)
 };
 
 struct GenericArgs {
