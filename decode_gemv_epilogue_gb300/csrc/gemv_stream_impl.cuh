@@ -40,7 +40,8 @@
 //
 // Each (format, columns) pair is compiled three times (FEAT): the plain GEMV, the
 // extended one (dual GEMV, several matrices, RMS prologue) and the split-K one
-// (clusters, with the same extensions).  The plain kernel carries none of the extension code: cluster
+// (clusters, with the same extensions); each format once more with one column for
+// persistent chains (several calls in one launch, grid barriers between dependent ones).  The plain kernel carries none of the extension code: cluster
 // instructions in a kernel image alone add about a microsecond per launch on GB300.
 //
 // Every wait is bounded; a timeout sets the device error word and the kernel returns
