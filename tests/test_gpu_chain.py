@@ -263,3 +263,46 @@ def test_chain_refusals(G, q4_layer):
     nothing.launch()
     torch.cuda.synchronize()
     assert G.device_status() == 0
+
+
+def test_chain_hazards_and_prologues(G):
+    """Barriers for every kind of hazard between stages, and stages with the RMS prologue:
+    stage 1 writes what stage 0 reads (write after read), stage 2 writes what stage 1
+    writes (write after write), stage 3 reads nothing earlier stages write but shares their
+    x with the RMS prologue, stage 4 reads stage 3's output as its aux."""
+    wt, K, M = synth.Q4_0, 2048, 1024
+    raw = [synth.weights(wt, M, K, seed=900 + i) for i in range(5)]
+    W = [dev_tensor(r) for r in raw]
+    xa = dev_tensor(synth.normal(K, seed=910))
+    b = dev_tensor(synth.normal(K, seed=911))  # stage 0's x; its first M elements are stage 1's and 2's output
+    gamma = dev_tensor(synth.normal(K, seed=912))
+    y0, y3, y4 = (torch.empty(M, device="cuda") for _ in range(3))
+    y1 = b[:M]
+    def calls():
+        return [G.prepare(W[0], wt, b, M, K, NONE, None, y0, pdl=True),                 # reads b
+                G.prepare(W[1], wt, xa, M, K, NONE, None, y1, pdl=True),                # writes b: WAR
+                G.prepare(W[2], wt, xa, M, K, SIG, None, y1, pdl=True),                 # writes b again: WAW
+                G.prepare(W[3], wt, xa, M, K, NONE, None, y3, pdl=True, rms_norm_weight=gamma, rms_norm_eps=1e-5),
+                G.prepare(W[4], wt, xa, M, K, ADD, y3, y4, pdl=True)]                   # reads y3: RAW
+    b0 = b.clone()
+
+    def run(fn):
+        b.copy_(b0)
+        for t in (y0, y3, y4):
+            t.fill_(float("nan"))
+        fn()
+        torch.cuda.synchronize()
+        return {n: t.cpu().numpy().view(np.uint32).copy() for n, t in (("y0", y0), ("b", b), ("y3", y3), ("y4", y4))}
+
+    cs = calls()
+    want = run(lambda: G.launch_prepared(cs))
+    chain = G.prepare_chain(cs)
+    info = G.chain_info(chain)
+    # barriers before stages 1 (WAR on b), 2 (WAW on b) and 4 (RAW on y3), none before 3;
+    # stage 2 reuses stage 1's staged x
+    assert (info["barrier_mask"], info["reuse_mask"]) == (0b10110, 0b00100), info
+    got = run(lambda: chain.launch())
+    _equal(want, got, "hazards")
+    # stage 0 against the oracle on the original b
+    want0 = ogemv.gemv(raw[0], wt, b0.cpu().numpy(), M, K, NONE, None)
+    assert_within(got["y0"].view(np.float32), want0[0], gemv_bound(raw[0], wt, b0.cpu().numpy(), M, K)[0], "y0")
