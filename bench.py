@@ -338,19 +338,30 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def kernel_source_hash():
+    """Hash of the library's sources with comments and blank lines left out (a change to a
+    comment leaves the kernels, and so their counters, as they were)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_gemv_epilogue_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = [re.sub(r"//.*$", "", l).rstrip() for l in text.splitlines()]
+        h.update(fn.encode())
+        h.update("\n".join(l for l in lines if l.strip()).encode())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic(kernel_key):
     """dram read+write bytes per launch from the committed ncu summary, if it still
     matches the kernel source (profiles/traffic.txt: key, bytes, source hash)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    import hashlib
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "decode_gemv_epilogue_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(f.read())
-    src = h.hexdigest()[:16]
+    src = kernel_source_hash()
     with open(path) as f:
         for line in f:
             parts = line.split()

@@ -466,8 +466,8 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
     }
     fence_mbar_init();
   }
-  // chain: every stage's arguments copied to shared memory (indexed parameter loads of a
-  // later stage each miss the constant cache at that stage's start)
+  // chain: every stage's arguments copied to shared memory, where any stage's are read
+  // with plain shared loads
   const StreamArgs* sargs = nullptr;
   if constexpr (kChain) {
     sargs = reinterpret_cast<const StreamArgs*>(smem + prm.off_args);
@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
   else
     __syncthreads();
   // A chain lets the next grid in only after its last grid barrier: that grid may be this
-  // chain again, which reads the counter when it starts.
+  // chain again, whose first arrival takes its base from the counter.
   if (nbar == 0) pdl_trigger();
 
   if (warp == 0) {
