@@ -36,9 +36,10 @@ constexpr int kMaxChain = 8;                // calls run by one persistent chain
 // columns.  Q4_K threads always own one unit pair (two units sharing a code load) and
 // one column: with 17 warps a thread has at most 96 registers (a quarter of the SM's
 // register file serves up to five warps), and a second column of x spills.  Single-
-// column Q4_0 and Q8_0 (integer dot products, below) keep one unit per thread and eight
-// (Q4_0) or four (Q8_0, twice the bytes per row) rows per tile: the x conversion per unit
-// is the costly part of a chunk's start, and the rows share it.
+// column Q4_0 and Q8_0 (integer dot products, below) keep one unit and eight rows per
+// thread per tile: the x conversion per unit is the costly part of a chunk's start, the
+// rows share it, and the per-tile reduction is spread over more rows (Q8_0 with four
+// rows per thread: 5-8% slower at 4096..14336 rows).
 __host__ __device__ constexpr bool stream_quant(int wt) { return wt == 2 || wt == 3 || wt == 4; }
 __host__ __device__ constexpr int stream_nct(int wt, int nc) {
   return wt == 4 ? 1 : stream_quant(wt) ? (nc <= 4 ? nc : 4) : (nc <= 2 ? nc : 2);
@@ -50,7 +51,7 @@ __host__ __device__ constexpr int stream_u(int wt, int nc) {
   return wt == 4 ? 2 : ((wt == 3 || wt == 2) && nc == 1) ? 1 : (nc == 1 && stream_quant(wt)) ? 2 : 1;
 }
 __host__ __device__ constexpr int stream_rt(int wt, int nc) {
-  return (nc == 1 && wt == 3) ? 8 : 4;
+  return (nc == 1 && (wt == 3 || wt == 2)) ? 8 : 4;
 }
 __host__ __device__ constexpr int stream_max_cw(int wt, int nc) { return stream_nct(wt, nc) <= 2 ? 16 : 8; }
 __host__ __device__ constexpr int stream_threads(int wt, int nc) { return 32 * (1 + stream_max_cw(wt, nc)); }
