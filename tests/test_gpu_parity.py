@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 from decode_gemv_epilogue_gb300 import synth
-from gpu_util import assert_within, dev_tensor, fwht_err_bound, gemv_bound
+from gpu_util import assert_within, dev_tensor, fwht_err_bound, gemv_bound, glu_bound
 from oracle import chain as ochain
 from oracle import fwht as ofwht
 from oracle import gemv as ogemv
@@ -424,6 +424,49 @@ def _chain_weights():
 
 CHAIN_SHAPES = {"q": (4096, 4096), "k": (4096, 4096), "v": (4096, 4096), "o": (4096, 4096),
                 "up": (14336, 4096), "gate": (14336, 4096), "down": (4096, 14336), "beta": (32, 4096)}
+
+
+def test_full_q4_0_decode_layer_four_launches(G):
+    """The same layer as the bench step runs it: q, k, v and the sigmoid head sharing x in
+    one gemv_multi, o + residual add, gate and up in one gemv_glu, down + residual add.
+    Each launch's outputs against the oracle on the inputs it saw (sampled rows)."""
+    w = _chain_weights()
+    dev = {name: dev_tensor(w[name][0]) for name in ochain.LAYER_ORDER}
+    x = synth.normal(4096, seed=210)
+    a = synth.normal(4096, seed=211)
+    r = synth.normal(4096, seed=212)
+    xd, ad, rd = dev_tensor(x), dev_tensor(a), dev_tensor(r)
+    outs = {n: torch.full((CHAIN_SHAPES[n][0],), float("nan"), device="cuda") for n in ("q", "k", "v", "gate", "beta")}
+    G.gemv_multi([(dev["q"], 4096, 0, None, outs["q"]), (dev["k"], 4096, 0, None, outs["k"]),
+                  (dev["v"], 4096, 0, None, outs["v"]), (dev["beta"], 32, ogemv.EPI_SIGMOID, None, outs["beta"])],
+                 synth.Q4_0, xd, 4096, pdl=True)
+    G.gemv_fused_ex(dev["o"], synth.Q4_0, ad, 4096, 4096, ogemv.EPI_ADD, rd, rd, pdl=True)
+    torch.cuda.synchronize()
+    r1 = rd.cpu().numpy().astype(np.float64)
+    G.gemv_glu(dev["gate"], dev["up"], synth.Q4_0, rd, 14336, 4096, outs["gate"], pdl=True)
+    G.gemv_fused_ex(dev["down"], synth.Q4_0, outs["gate"], 4096, 14336, ogemv.EPI_ADD, rd, rd, pdl=True)
+    torch.cuda.synchronize()
+    h = {k: v.cpu().numpy().astype(np.float64) for k, v in outs.items()}
+    r2 = rd.cpu().numpy().astype(np.float64)
+
+    def check(name, vec_in, epi, aux, got):
+        raw, wt, M, K = w[name]
+        rows = _sample_rows(M, 256, 11)
+        want = ogemv.gemv(raw, wt, vec_in, M, K, epi, aux, rows=rows)
+        assert_within(got[rows], want[0], gemv_bound(raw, wt, vec_in, M, K, rows)[0], name)
+
+    for n in ("q", "k", "v"):
+        check(n, x, 0, None, h[n])
+    check("beta", x, ogemv.EPI_SIGMOID, None, h["beta"])
+    check("o", a, ogemv.EPI_ADD, r, r1)
+    # silu(gate r1) * (up r1): the oracle's gated dual GEMV on the same rows
+    rows = _sample_rows(14336, 256, 12)
+    rg, _, M, K = w["gate"]
+    ru = w["up"][0]
+    r1f = r1.astype(np.float32)
+    want = ogemv.gemv_glu(rg, ru, synth.Q4_0, r1f, M, K, rows=rows)
+    assert_within(h["gate"][rows], want[0], glu_bound(rg, ru, synth.Q4_0, r1f, M, K, rows)[0], "gate*up")
+    check("down", h["gate"].astype(np.float32), ogemv.EPI_ADD, r1, r2)
 
 
 @pytest.mark.parametrize("pdl", [False, True])
