@@ -19,8 +19,7 @@ value = algorithmic bytes of the step (W + x + aux + dst, each once) / step time
 with the step captured in a CUDA graph (launches chained with programmatic dependent
 launch) and replayed.  Also reported: per-kernel CUDA-event durations and the roofline
 of the dominant kernel, microseconds per decode layer (the step's 4 launches, the 8
-fused launches, the 13 unfused ones, the persistent chain), the
-epilogue cost against the tail-free GEMV, an end-to-end number through host buffers,
+fused launches, the 13 unfused ones), the epilogue cost against the tail-free GEMV, an end-to-end number through host buffers,
 SM clocks during the timed region, and the fp64 CPU oracle timed on the host cores.
 Under "next_rows": the layer chain with the gated dual GEMV (7 launches), the same
 layer in Q4_K, the dual GEMV against its two separate launches, split K on and off for
@@ -96,8 +95,7 @@ CHAIN_NAMES = ["chain_q", "chain_k", "chain_v", "chain_o_add", "chain_up", "chai
 # The step runs the layer's eight GEMVs as four launches: q, k, v and the sigmoid head
 # sharing x (gemv_multi), o + residual add, gate and up in one pass with silu(gate) * up
 # (gemv_glu), down + residual add.  Measured on GB300 (us per layer, two weight sets
-# alternating): 42.1 for these four, 53.3 for the eight calls as separate launches and
-# 46.3 / 54.3 for the four / eight as one persistent chain (gf_prepare_chain).
+# alternating): 42.1 for these four and 53.3 for the eight calls as separate launches.
 LAYER_UNITS = {
     "layer_qkv_beta": ["chain_q", "chain_k", "chain_v", "chain_beta_sigmoid"],
     "layer_o_add": ["chain_o_add"],
@@ -474,6 +472,8 @@ def gpu_arm(args, rank, world, local_rank):
                         "gbs": round(step.bytes[n] / (per_call[n] * 1e-3) / 1e9, 1),
                         "frac_of_peak": round(step.bytes[n] / (per_call[n] * 1e-3) / 1e9 / peak, 4)}
                     for n in per_call}
+    # the FWHT + f16 5120x5120 call at every batch width 1..8
+    per_workload["fwht_f16_add_ncols_1_to_8"] = fwht_ncols_measure(G, torch, step, s, args, peak)
 
     # ---------------------------------------------------------------- decode-layer chain
     chain = chain_measure(G, torch, step, s, args)
@@ -503,7 +503,7 @@ def gpu_arm(args, rank, world, local_rank):
         "pct_of_peak": round(100 * value / world / peak, 2),
         "gpu_launches": launches,
         "us_per_layer": chain["step_form_us"], "launches_per_layer": len(LAYER_UNITS),
-        "us_per_layer_8_launches": chain["fused_us"], "us_per_layer_persistent_chain": chain["persistent_us"],
+        "us_per_layer_8_launches": chain["fused_us"],
         "us_per_layer_unfused": chain["unfused_us"], "launches_per_layer_unfused": 13,
         "chain": chain, "epilogue_cost": epi_cost, "per_kernel": per_kernel, "per_workload": per_workload,
         "next_rows": nxt,
@@ -559,6 +559,56 @@ def launch_durations(G, torch, step, s, args):
     return out
 
 
+def fwht_ncols_measure(G, torch, step, s, args, peak):
+    """The signed-FWHT(1024) + f16 5120x5120 + in-place residual call for every batch width
+    1..8 (the workload's ncols = 1..8), as the step issues it (transform once into the
+    workspace, then the GEMV, PDL-chained): per width the mean device time over a CUDA graph
+    of back-to-back calls cycling through weight copies (> 2x L2), the algorithmic bytes,
+    GB/s and the fraction of the measured HBM peak."""
+    M = K = 5120
+    W0 = step.W["fwht_f16_add_n8"]
+    ncopy = int(min(32, max(2, -(-2 * L2_BYTES // W0.numel()))))
+    copies = [W0] + [W0.clone() for _ in range(ncopy - 1)]
+    reps = max(3, min(20, args.steps // 20))
+    out = {}
+    for nc in range(1, 9):
+        x, r, ws = step.fx8[:nc * K], step.fr8[:nc * M], step.ws8[:nc * K]
+
+        def run_all(nc=nc, x=x, r=r, ws=ws):
+            for Wc in copies:
+                G.gemv_fused_ex(Wc, 1, x, M, K, 4, r, r, ncols=nc, fwht_signs=step.signs, fwht_block=1024,
+                                fwht_workspace=ws, pdl=True)
+
+        with torch.cuda.stream(s):
+            run_all()
+        s.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            run_all()
+        with torch.cuda.stream(s):
+            gr.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(reps):
+                gr.replay()
+            e1.record(s)
+        s.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / (reps * ncopy)
+        path, _ = G.plan(W0, 1, x, M, K, 4, r, r, ncols=nc, fwht_signs=step.signs, fwht_block=1024,
+                         fwht_workspace=ws)
+        b = algo_bytes(1, M, K, 4, nc, True)
+        gbs = b / (us * 1e-6) / 1e9
+        out["ncols_%d" % nc] = {"us": round(us, 3), "bytes": b, "gbs": round(gbs, 1),
+                                "frac_of_peak": round(gbs / peak, 4),
+                                "kernel": {G.PATH_STREAM: "gemv_stream_kernel", G.PATH_TC: "gemv_tc_kernel"}.get(
+                                    path, "gemv_generic_kernel")}
+        del gr
+    del copies
+    return out
+
+
 def second_layer(torch, step):
     """A second set of the layer's weights (seeded apart from the step's), so that timed
     layers alternate between two sets and nothing stays in L2."""
@@ -571,21 +621,8 @@ def second_layer(torch, step):
     return step._layer2
 
 
-def layer_chains(G, step, layers, pdl=True):
-    """One persistent chain of the layer's eight calls per weight set (gf_prepare_chain)."""
-    specs = dict((n, (a, kw)) for (n, a, kw) in step.call_specs())
-    out = []
-    for Wl in layers:
-        calls = []
-        for n in CHAIN_NAMES:
-            a, kw = specs[n]
-            calls.append(G.prepare(Wl[n], *a[1:], pdl=pdl, split_k=False, **kw))
-        out.append(G.prepare_chain(calls))
-    return out
-
-
 def chain_measure(G, torch, step, s, args):
-    """Microseconds per decode layer: the persistent chain (one launch), the 8 fused
+    """Microseconds per decode layer: the step's four launches, the 8 fused
     launches and the 13-launch unfused chain (separate GEMV, add, silu, mul, sigmoid
     kernels), each captured in a CUDA graph, two layers' weights alternating so nothing
     stays in L2."""
@@ -644,10 +681,6 @@ def chain_measure(G, torch, step, s, args):
             e1.record(s)
         s.synchronize()
         res[label + "_us"] = round(1e3 * e0.elapsed_time(e1) / (2 * reps), 3)
-    chains = layer_chains(G, step, layers)
-    res["persistent_us"] = round(graph_us(torch, s, lambda i: chains[i].launch(), 2, reps), 3)
-    res["persistent_info"] = G.chain_info(chains[0])
-    del chains
     # the step's form: four launches
     res["step_form_us"] = round(graph_us(torch, s, lambda i: [step.layer_call(u, layers[i]) for u in LAYER_UNITS],
                                          2, reps), 3)
@@ -655,7 +688,6 @@ def chain_measure(G, torch, step, s, args):
     res["layer_bytes"] = layer_bytes
     res["step_form_bytes"] = sum(step.bytes[u] for u in LAYER_UNITS)
     res["fused_gbs"] = round(layer_bytes / (res["fused_us"] * 1e-6) / 1e9, 1)
-    res["persistent_gbs"] = round(layer_bytes / (res["persistent_us"] * 1e-6) / 1e9, 1)
     res["step_form_gbs"] = round(res["step_form_bytes"] / (res["step_form_us"] * 1e-6) / 1e9, 1)
     res["layers_timed"] = 2 * reps
     return res
@@ -756,24 +788,6 @@ def next_rows_measure(G, torch, step, s, args, peak):
     out["chain_multi_glu"] = {"us_per_layer": round(us4, 3), "launches_per_layer": 4, "layer_bytes": lb,
                               "gbs": round(lb / (us4 * 1e-6) / 1e9, 1),
                               "note": "q, k, v and the sigmoid head in one gemv_multi launch (separate buffers)"}
-
-    # 1a''. the same four calls prepared and run as one persistent chain
-    def fused_chain(Wl):
-        return G.prepare_chain([
-            G.prepare_multi([(Wl["chain_q"], 4096, 0, None, q), (Wl["chain_k"], 4096, 0, None, k),
-                             (Wl["chain_v"], 4096, 0, None, v), (Wl["chain_beta_sigmoid"], 32, 1, None, beta)],
-                            3, x, 4096, pdl=True),
-            G.prepare(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True, split_k=False),
-            G.prepare_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, r, 14336, 4096, g, pdl=True, split_k=False),
-            G.prepare(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True, split_k=False)])
-
-    fchains = [fused_chain(layers[0]), fused_chain(layers[1])]
-    us1 = graph_us(torch, s, lambda i: fchains[i].launch(), 2, max(20, min(args.steps, 500)))
-    out["chain_persistent_multi_glu"] = {"us_per_layer": round(us1, 3), "launches_per_layer": 1, "layer_bytes": lb,
-                                         "gbs": round(lb / (us1 * 1e-6) / 1e9, 1),
-                                         "info": G.chain_info(fchains[0]),
-                                         "note": "the four calls above as one gf_prepare_chain launch"}
-    del fchains
 
     # 1b. the same layer in Q4_K (a format the pages' decode-layer measurements name),
     # 8 launches and 7 with the dual GEMV
@@ -896,8 +910,9 @@ def epilogue_cost(G, torch, s):
 
 def e2e_measure(G, torch, step, s, args):
     """The same step through the public API from pinned host memory: every step copies its
-    activations host->device (one copy), launches the step's graph of the prepared calls
-    (the layer's eight as one chain) and copies every result back (one copy)."""
+    activations host->device (one copy), launches the step's prepared calls (the layer as
+    its four launches) recorded as one CUDA graph, and copies every result back (one
+    copy)."""
     arena, host, (i0, i1), (o0, o1) = step.pack_for_e2e()
     # the decode loop's calls, planned once on the step's buffers (gf_prepare) and
     # recorded as one graph (gf_graph_create); each step is one gf_graph_launch
@@ -957,14 +972,18 @@ def _oracle_inputs(seed0=0):
     return _ORACLE_INPUTS[seed0]
 
 
-def oracle_step(frac, seed0=0):
+def oracle_step(frac, seed0=0, part=(0, 1)):
     """Run the fp64 oracle on a row sample (every frac-th row) of every launch of the
-    step; returns (algorithmic bytes of the sample, seconds of oracle work)."""
+    step -- of that sample, share `part` = (w, n): the w-th of n contiguous row ranges of
+    each launch; returns (algorithmic bytes of the share, seconds of oracle work)."""
     from oracle import fwht as ofwht
     from oracle import gemv as ogemv
+    w, n = part
     total_b, total_t = 0, 0.0
     for (name, wt, M, K, epi, nc, fw), (raw, X, aux, s) in zip(step_spec(), _oracle_inputs(seed0)):
-        rows = np.arange(0, M, frac)
+        rows = np.array_split(np.arange(0, M, frac), n)[w]
+        if rows.size == 0:
+            continue
         t = time.perf_counter()
         if fw:
             X = np.stack([ofwht.fwht_signed(X[c], s, 1024) for c in range(nc)])
@@ -975,34 +994,78 @@ def oracle_step(frac, seed0=0):
     return total_b, total_t
 
 
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_part(w, n, frac, nsteps, barrier, q):
+    """One process of the row-parallel oracle: its inputs first (untimed), then nsteps
+    steps of its row share, each started together with the other processes."""
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    _oracle_inputs()
+    spans = []
+    for _ in range(nsteps):
+        barrier.wait()
+        t0 = time.monotonic()
+        oracle_step(frac, part=(w, n))
+        spans.append((t0, time.monotonic()))
+    q.put((w, spans))
+
+
+def oracle_parallel(frac, nsteps, nproc=None):
+    """The oracle (as it stands, one thread per process) over nproc processes, each a
+    contiguous share of every launch's sampled rows; per step the wall time from the
+    common start to the last process's end.  Processes are spawned (no inherited CUDA
+    state).  Returns (per-step seconds, processes)."""
+    import multiprocessing as mp
+    n = nproc or host_cores()
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(n)
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_part, args=(w, n, frac, nsteps, barrier, q), daemon=True) for w in range(n)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=1800) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+    spans = [r[1] for r in res]
+    per_step = [max(sp[i][1] for sp in spans) - min(sp[i][0] for sp in spans) for i in range(nsteps)]
+    return per_step, n
+
+
 def cpu_baseline(reps=3):
-    """The oracle over every row of every launch of the step, `reps` times (~10 s)."""
-    b, t = 0, 0.0
+    """The oracle over every row of every launch of the step, `reps` times: row-parallel
+    over every host core (the reported value) and on one core (~10 s)."""
+    b1, t1 = 0, 0.0
     for _ in range(reps):
         bi, ti = oracle_step(1)
-        b += bi
-        t += ti
-    return {"value": round(b / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+        b1 += bi
+        t1 += ti
+    per_step, n = oracle_parallel(1, reps)
+    tn = sum(per_step)
+    return {"value": round(b1 / tn / 1e9, 4), "unit": UNIT, "cores": n, "kind": "oracle",
             "sample": "%d full decode steps (every row of every launch, %.0f MB of algorithmic bytes each), "
-                      "numpy fp64 oracle, one thread" % (reps, b / reps / 1e6),
-            "seconds": round(t, 2)}
+                      "numpy fp64 oracle, row-parallel: %d processes of one thread, each a contiguous share of "
+                      "every launch's rows" % (reps, b1 / reps / 1e6, n),
+            "seconds": round(tn, 2),
+            "one_core": {"value": round(b1 / t1 / 1e9, 4), "cores": 1, "seconds": round(t1, 2)}}
 
 
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
     frac = 16
-    _oracle_inputs()
-    for _ in range(max(args.warmup, 0)):
-        oracle_step(frac)
-    tb, wall = 0, 0.0
-    for _ in range(args.steps):
-        b, t = oracle_step(frac)
-        tb += b
-        wall += t
-    value = tb / wall / 1e9
-    cb = {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-          "sample": "every 16th row of every launch of one decode step per step (%d steps)" % args.steps}
+    tb = sum(algo_bytes(wt, np.arange(0, M, frac).size, K, epi, nc, fw)
+             for (name, wt, M, K, epi, nc, fw) in step_spec())
+    per_step, n = oracle_parallel(frac, max(args.warmup, 0) + args.steps)
+    wall = sum(per_step[max(args.warmup, 0):])
+    value = tb * args.steps / wall / 1e9
+    cb = {"value": round(value, 4), "unit": UNIT, "cores": n, "kind": "oracle",
+          "sample": "every 16th row of every launch of one decode step per step (%d steps), row-parallel over "
+                    "%d processes of one thread" % (args.steps, n)}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * wall / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

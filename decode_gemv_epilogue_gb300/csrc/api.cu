@@ -109,7 +109,6 @@ struct Call {
   float eps;
   int nseg = 0;         // several matrices sharing x (gemv_multi): M is their rows' sum
   gf_multi_item segs[kMaxSeg];
-  int force_ncw = 0;    // chain stage: plan exactly this many consumer warps (0: free)
 };
 
 static int validate(const Call& c) {
@@ -241,15 +240,6 @@ static bool plan_stream_s(const Call& c, const DeviceLimits& lim, int S, Plan& p
   int G = std::max(1, std::min(max_cw / wpg, (vr * rows_max + RT - 1) / RT));
   while (G > 1 && G * RT * seg_full > kStageMaxBytes) --G;
   int ncw = G * wpg;
-  if (c.force_ncw > 0) {
-    // a chain stage: the launch's consumer warps, as many row groups as they hold (the
-    // warps left over idle through this stage)
-    if (S != 1 || c.force_ncw < wpg || c.force_ncw > max_cw) return false;
-    G = c.force_ncw / wpg;
-    while (G > 1 && G * RT * seg_full > kStageMaxBytes) --G;
-    if (G * RT * seg_full > kStageMaxBytes) return false;
-    ncw = c.force_ncw;
-  }
   int R = G * RT;
   // With at least one full tile per CTA, hand out whole tiles: the CTAs with the highest
   // indices, which a launch behind another (PDL) starts last, take one tile fewer, and
@@ -377,11 +367,9 @@ static int plan_call(const Call& c, Plan& p, int* generic_smem, int* generic_gri
 
 // One kernel launch with every argument resolved: what a call plans, and what a
 // prepared call keeps (gf_prepare) so that launching it does no planning at all.
-enum { REC_FWHT = 0, REC_TC = 1, REC_STREAM = 2, REC_GENERIC = 3, REC_CHAIN = 4 };
+enum { REC_FWHT = 0, REC_TC = 1, REC_STREAM = 2, REC_GENERIC = 3 };
 struct LaunchRec {
   int kind;
-  const ChainArgs* chain;  // persistent chain (owned by its prepared call), with:
-  int cgrid, cthreads, csmem;
   bool pdl;
   int wtype, ncols;
   const void* W;  // tensor-core path: the matrix of the tensor map
@@ -470,8 +458,6 @@ static int issue(const LaunchRec& r, cudaStream_t st) {
     e = launch_fwht(r.fx, r.fsigns, r.fdst, r.fn, r.fB, r.fnsigns, st);
   } else if (r.kind == REC_TC) {
     e = launch_tc(r.tp, r.W, st, r.pdl);
-  } else if (r.kind == REC_CHAIN) {
-    e = launch_stream_chain(r.wtype, r.cgrid, r.cthreads, r.csmem, *r.chain, st, r.pdl);
   } else if (r.kind == REC_STREAM) {
     const StreamArgs& s = r.p.s;
     const int nc = r.ncols;
@@ -653,146 +639,6 @@ static int make_multi_call(const gf_multi_item* items, int n, int wtype, const f
   }
   c.nseg = n;
   *out = c;
-  return GF_OK;
-}
-
-// ------------------------------------------------------------------ chains
-// Byte ranges a call reads, writes and streams (weights), for the hazards between the
-// stages of a chain.
-struct Ranges {
-  int nr = 0, nw = 0, nm = 0;
-  const void* r[2 + kMaxSeg];
-  int64_t rn[2 + kMaxSeg];
-  const void* w[kMaxSeg];
-  int64_t wn[kMaxSeg];
-  const void* m[kMaxSeg + 1];
-  int64_t mn[kMaxSeg + 1];
-  void read(const void* p, int64_t n) { if (p && n > 0) { r[nr] = p; rn[nr++] = n; } }
-  void write(const void* p, int64_t n) { if (p && n > 0) { w[nw] = p; wn[nw++] = n; } }
-  void weights(const void* p, int64_t n) { if (p && n > 0) { m[nm] = p; mn[nm++] = n; } }
-};
-
-static Ranges ranges_of(const Call& c) {
-  Ranges g;
-  const int64_t rb = row_bytes_of(c.wtype, c.K);
-  g.read(c.x, c.ncols * c.K * 4);
-  g.read(c.gamma, c.K * 4);
-  if (c.nseg > 0) {
-    for (int i = 0; i < c.nseg; ++i) {
-      const gf_multi_item& it = c.segs[i];
-      g.read(it.aux, c.ncols * it.M * 4);  // nullptr unless the tail takes it
-      g.write(it.dst, c.ncols * it.M * 4);
-      g.weights(it.W, it.M * rb);
-    }
-  } else {
-    g.read(c.aux, c.ncols * c.M * 4);
-    g.write(c.dst, c.ncols * c.M * 4);
-    g.weights(c.W, c.M * rb);
-    g.weights(c.W2, c.M * rb);
-  }
-  return g;
-}
-
-static bool any_overlap(const void* const* a, const int64_t* an, int na, const void* const* b, const int64_t* bn,
-                        int nb) {
-  for (int i = 0; i < na; ++i)
-    for (int j = 0; j < nb; ++j)
-      if (ranges_overlap(a[i], an[i], b[j], bn[j])) return true;
-  return false;
-}
-
-// Plans calls[0 .. n) (one column each, streamed, no transform) as the stages of one
-// persistent launch: every stage gets the most consumer warps any of them needs, one
-// ring and one shared-memory layout.  A stage that reads or writes what an earlier stage
-// of its group writes, or writes what one reads, starts a new group behind a grid
-// barrier.  No stage may write another's weights: the weights of later stages are
-// streamed before the barriers.
-static_assert(sizeof(StreamArgs) % 8 == 0, "stage arguments are copied to 8-byte aligned shared memory");
-
-static int plan_chain(const Call* calls, int n, ChainArgs& ca, int& grid, int& threads, int& smem) {
-  const DeviceLimits lim = device_limits();
-  std::memset(&ca, 0, sizeof(ca));
-  Plan pl[kMaxChain];
-  Call cs[kMaxChain];
-  int ncw = 0;
-  for (int i = 0; i < n; ++i) {
-    cs[i] = calls[i];
-    cs[i].force_ncw = 0;
-    if (cs[i].ncols != 1 || cs[i].signs || cs[i].wtype != calls[0].wtype) return GF_ERR_UNSUPPORTED;
-    if (!plan_stream_s(cs[i], lim, 1, pl[i])) return GF_ERR_UNSUPPORTED;
-    ncw = std::max(ncw, pl[i].s.ncw);
-  }
-  for (int i = 0; i < n; ++i)
-    if (pl[i].s.ncw != ncw) {
-      cs[i].force_ncw = ncw;
-      if (!plan_stream_s(cs[i], lim, 1, pl[i])) return GF_ERR_UNSUPPORTED;
-    }
-  int xs = 0, aux = 0, red = 0, nrm = 0, stage_bytes = 0;
-  grid = 0;
-  for (int i = 0; i < n; ++i) {
-    const StreamArgs& a = pl[i].s;
-    xs = std::max(xs, a.off_aux - a.off_xs);
-    aux = std::max(aux, a.off_red - a.off_aux);
-    red = std::max(red, a.off_norm - a.off_red);
-    nrm = std::max(nrm, a.off_xchg - a.off_norm);
-    stage_bytes = std::max(stage_bytes, a.stage_bytes);
-    grid = std::max(grid, pl[i].grid);
-  }
-  // aux and partial-sum buffers twice: even and odd stages alternate
-  const int off_ring = kBarBytes + xs + 2 * aux + 2 * red + nrm;
-  const int args_bytes = n * static_cast<int>(sizeof(StreamArgs));
-  const int NS = std::min(kMaxStages, (lim.smem_optin - off_ring - kRingSlackBytes - 16 - args_bytes) / stage_bytes);
-  if (NS < 2) return GF_ERR_UNSUPPORTED;
-  threads = 32 * (1 + ncw);
-  ca.off_args = round_up(off_ring + NS * stage_bytes + kRingSlackBytes, 16);
-  smem = ca.off_args + args_bytes;
-  const int per_sm = stream_chain_ctas_per_sm(calls[0].wtype, threads, smem);
-  if (per_sm < 1 || grid > per_sm * lim.sm_count) return GF_ERR_UNSUPPORTED;  // every CTA resident at once
-  unsigned* err = device_error_word();
-  if (!err) return cuda_fail(cudaGetLastError());
-  Ranges rg[kMaxChain];
-  for (int i = 0; i < n; ++i) rg[i] = ranges_of(cs[i]);
-  for (int i = 0; i < n; ++i)
-    for (int j = 0; j < n; ++j)
-      if (any_overlap(rg[i].w, rg[i].wn, rg[i].nw, rg[j].m, rg[j].mn, rg[j].nm)) return GF_ERR_ALIAS;
-  int g0 = 0;   // first stage of the current group
-  int rot = 0;  // the CTAs with a granule more than the others move on from stage to stage
-  for (int i = 0; i < n; ++i) {
-    StreamArgs& a = ca.st[i];
-    a = pl[i].s;
-    fill_stream_ptrs(cs[i], const_cast<float*>(cs[i].dst), err, a);
-    a.rot = rot;
-    rot = (rot + (pl[i].grid < grid ? pl[i].grid : a.rows_extra)) % grid;
-    a.NS = NS;
-    a.stage_bytes = stage_bytes;
-    a.off_xs = kBarBytes;
-    a.off_aux = a.off_xs + xs;
-    a.off_red = a.off_aux + 2 * aux;
-    a.off_norm = a.off_red + 2 * red;
-    a.off_xchg = a.off_norm + nrm;
-    a.off_ring = off_ring;
-    bool hazard = false;
-    for (int t = g0; t < i && !hazard; ++t)
-      hazard = any_overlap(rg[t].w, rg[t].wn, rg[t].nw, rg[i].r, rg[i].rn, rg[i].nr) ||
-               any_overlap(rg[t].w, rg[t].wn, rg[t].nw, rg[i].w, rg[i].wn, rg[i].nw) ||
-               any_overlap(rg[t].r, rg[t].rn, rg[t].nr, rg[i].w, rg[i].wn, rg[i].nw);
-    if (hazard) {
-      a.cflags |= CHAIN_BAR;
-      ++ca.nbar;
-      g0 = i;
-    }
-    // the previous stage's staged x (and gamma) serve again when every CTA had rows there
-    // (x is never a stage's own output); each thread's converted x, too, when the
-    // threads own the same units of one K chunk (and no RMS prologue scales x)
-    const StreamArgs& b = ca.st[i > 0 ? i - 1 : 0];
-    const bool reuse = i > 0 && a.stage_x && b.stage_x && a.x == b.x && a.K == b.K && a.gamma == b.gamma &&
-                       pl[i - 1].grid == grid;
-    if (reuse) a.cflags |= CHAIN_REUSE;
-    if (reuse && a.n_kc == 1 && b.n_kc == 1 && a.wpg == b.wpg && a.wpc == b.wpc && !a.gamma) a.cflags |= CHAIN_KEEP;
-  }
-  ca.nst = n;
-  ca.off_aux2 = kBarBytes + xs + aux;
-  ca.off_red2 = kBarBytes + xs + 2 * aux + red;
   return GF_OK;
 }
 
@@ -1003,10 +849,6 @@ struct gf_prepared {
   int device;
   int n;
   gf::LaunchRec recs[gf::kMaxRecs];
-  gf::Call call;                     // what was prepared (not for a chain)
-  bool chainable = false;            // call is set
-  gf::ChainArgs* chain = nullptr;    // a chain: its stages and barrier counter
-  unsigned long long* gbar = nullptr;
 };
 
 static int prepare(const Call& c, const gf_opts* opts, gf_prepared** out) {
@@ -1027,8 +869,6 @@ static int prepare(const Call& c, const gf_opts* opts, gf_prepared** out) {
     delete p;
     return v;
   }
-  p->call = c;
-  p->chainable = true;
   *out = p;
   return GF_OK;
 }
@@ -1070,85 +910,8 @@ int gf_launch_prepared(const gf_prepared* const* calls, int n, void* stream) {
   return GF_OK;
 }
 
-int gf_prepare_chain(const gf_prepared* const* calls, int n, gf_prepared** out) {
-  if (!out) return GF_ERR_INVALID;
-  *out = nullptr;
-  if (!calls || n < 1) return GF_ERR_INVALID;
-  for (int i = 0; i < n; ++i)
-    if (!calls[i]) return GF_ERR_INVALID;
-  if (n > kMaxChain) return GF_ERR_UNSUPPORTED;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError());
-  Call cs[kMaxChain];
-  int m = 0;
-  for (int i = 0; i < n; ++i) {
-    const gf_prepared& c = *calls[i];
-    if (c.device != dev) return GF_ERR_INVALID;
-    if (!c.chainable) return GF_ERR_UNSUPPORTED;
-    if (c.n == 0) continue;  // no rows: nothing to run
-    if (c.n != 1 || c.recs[0].kind == REC_FWHT) return GF_ERR_UNSUPPORTED;
-    cs[m++] = c.call;
-  }
-  gf_prepared* p = new (std::nothrow) gf_prepared;
-  if (!p) return GF_ERR_INVALID;
-  p->device = dev;
-  p->n = 0;
-  if (m == 0) {
-    *out = p;
-    return GF_OK;
-  }
-  p->chain = new (std::nothrow) ChainArgs;
-  if (!p->chain) {
-    delete p;
-    return GF_ERR_INVALID;
-  }
-  LaunchRec& r = p->recs[0];
-  std::memset(&r, 0, sizeof(r));
-  int v = plan_chain(cs, m, *p->chain, r.cgrid, r.cthreads, r.csmem);
-  if (v == GF_OK) {
-    cudaError_t e = cudaMalloc(&p->gbar, sizeof(unsigned long long));
-    if (e == cudaSuccess) e = cudaMemset(p->gbar, 0, sizeof(unsigned long long));
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) v = cuda_fail(e);
-  }
-  if (v != GF_OK) {
-    gf_free_prepared(p);
-    return v;
-  }
-  p->chain->gbar = p->gbar;
-  r.kind = REC_CHAIN;
-  r.chain = p->chain;
-  r.pdl = (cs[0].flags & GF_FLAG_PDL) != 0;
-  r.wtype = cs[0].wtype;
-  r.ncols = 1;
-  p->n = 1;
-  *out = p;
-  return GF_OK;
-}
-
-int gf_chain_info(const gf_prepared* chain, int64_t info[8]) {
-  if (!chain || !info) return GF_ERR_INVALID;
-  for (int i = 0; i < 8; ++i) info[i] = 0;
-  if (!chain->chain) return chain->chainable ? GF_ERR_INVALID : GF_OK;  // an empty chain: zeros
-  const ChainArgs& ca = *chain->chain;
-  const LaunchRec& r = chain->recs[0];
-  info[0] = ca.nst;
-  info[1] = ca.nbar;
-  for (int s = 0; s < ca.nst; ++s) {
-    if (ca.st[s].cflags & CHAIN_BAR) info[2] |= int64_t{1} << s;
-    if (ca.st[s].cflags & CHAIN_REUSE) info[3] |= int64_t{1} << s;
-  }
-  info[4] = r.cgrid;
-  info[5] = r.cthreads;
-  info[6] = r.csmem;
-  info[7] = ca.st[0].NS;
-  return GF_OK;
-}
-
 void gf_free_prepared(gf_prepared* p) {
   if (!p) return;
-  if (p->gbar) cudaFree(p->gbar);
-  delete p->chain;
   delete p;
 }
 

@@ -40,9 +40,9 @@
 //
 // Each (format, columns) pair is compiled three times (FEAT): the plain GEMV, the
 // extended one (dual GEMV, several matrices, RMS prologue) and the split-K one
-// (clusters, with the same extensions); each format once more with one column for
-// persistent chains (several calls in one launch, grid barriers between dependent ones).  The plain kernel carries none of the extension code: cluster
-// instructions in a kernel image alone add about a microsecond per launch on GB300.
+// (clusters, with the same extensions).  The plain kernel carries none of the
+// extension code: cluster instructions in a kernel image alone add about a
+// microsecond per launch on GB300.
 //
 // Every wait is bounded; a timeout sets the device error word and the kernel returns
 // after draining its own copies.
@@ -194,6 +194,36 @@ __device__ __forceinline__ void consume_tile_q4k(uint32_t st, int seg, int rows,
   }
 }
 
+// The fp32 products of a Q4_K chunk that the integer path cannot carry, for unit n (0 or
+// 1) of the thread's pair only, with that unit's x (one column), so that only one unit's
+// x is held in registers.  Each weight d*sc[j]*q - dmin*m[j] is formed first (both terms
+// are exact in fp32, one rounding for the difference), so a zero weight stays zero and
+// an infinite x gives the infinity or NaN of the definition.
+template <int RT>
+__device__ __forceinline__ void consume_tile_q4k_unit(uint32_t st, int seg, int rows, int units, int tg, int g,
+                                                      int G, int n, const float2 (&xn)[8], float2 (&acc)[RT][1]) {
+  if (2 * tg >= units) return;
+#pragma unroll 1
+  for (int j = 0; j < RT; ++j) {
+    const int r = g + j * G;
+    if (r < rows) {
+      const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
+      float dsc[2], dmn[2];
+      const uint4 q = q4k_load_pair(ld, static_cast<uint32_t>(tg), dsc, dmn);
+      float2 v[8];
+      q4k_nibbles(q, static_cast<uint32_t>(n), v);
+      const float ds = n ? dsc[1] : dsc[0], dm = n ? dmn[1] : dmn[0];
+      float2 p0 = acc[j][0], p1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        p0 = ffma2(ffma2(make_float2(ds, ds), v[k], make_float2(-dm, -dm)), xn[k], p0);
+        p1 = ffma2(ffma2(make_float2(ds, ds), v[k + 1], make_float2(-dm, -dm)), xn[k + 1], p1);
+      }
+      acc[j][0] = fadd2(p0, p1);
+    }
+  }
+}
+
 // Q4_K through integer dot products: per row, one 16-byte code load and one unpack of the
 // scales for the thread's unit pair; each unit's nibbles against its XInt, scaled by
 // d * sc[j] * 2^-s, and the min term through the unit's sum of x.  Every row's loads
@@ -327,86 +357,16 @@ __device__ __forceinline__ void consume_tile(uint32_t st, int seg, int rows, int
   }
 }
 
-// Kernel argument block: one call, or a chain of calls (FEAT_CHAIN).
-template <int FEAT>
-struct KernelArgsOf {
-  using type = StreamArgs;
-};
-template <>
-struct KernelArgsOf<FEAT_CHAIN> {
-  using type = ChainArgs;
-};
-__device__ __forceinline__ const StreamArgs& first_args(const StreamArgs& p) { return p; }
-__device__ __forceinline__ const StreamArgs& first_args(const ChainArgs& p) { return p.st[0]; }
-
-// Rows [r0, r0 + nrows) of call a owned by the CTA (cluster) with row-range index rg of
-// nrg; none for an index past the call's CTAs (a chain stage with fewer rows than the
-// grid).  A chain stage rotates the indices (a.rot) so that the CTAs given one granule
-// more than the others differ from stage to stage.
-__device__ __forceinline__ void cta_rows(const StreamArgs& a, int rg, int nrg, int64_t& r0, int& nrows) {
-  if (a.rot) rg = (rg + nrg - a.rot) % nrg;
+// Rows [r0, r0 + nrows) of call a owned by the CTA (cluster) with row-range index rg.
+__device__ __forceinline__ void cta_rows(const StreamArgs& a, int rg, int64_t& r0, int& nrows) {
   r0 = (static_cast<int64_t>(rg) * a.rows_base + min(rg, a.rows_extra)) * a.gran;
   const int64_t n = min(static_cast<int64_t>((a.rows_base + (rg < a.rows_extra ? 1 : 0)) * a.gran), a.M - r0);
   nrows = static_cast<int>(max(n, static_cast<int64_t>(0)));
 }
 
-// Grid barrier of a chain.  Arrival: the caller's CTA has passed a barrier after all of
-// its consumers' stores; the release add publishes them (cumulatively), and the proxy
-// fence orders them before later bulk copies that read the same bytes.  Returns the
-// counter's value before the add.
-__device__ __forceinline__ unsigned long long grid_arrive(unsigned long long* ctr) {
-  unsigned long long old;
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
-  return old;
-}
-
-// Wait (acquire, bounded) until the counter reaches target.  On timeout: error word,
-// abort flag, false.
-__device__ __forceinline__ bool grid_wait(const unsigned long long* ctr, unsigned long long target,
-                                          volatile int* abort, unsigned* err) {
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
-    if (v >= target) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      set_error(err, ERRBIT_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-// The chain's producer learns of passed grid barriers from the consumer thread that
-// waited for them (a count in shared memory, release / acquire at CTA scope); its bulk
-// copies after that read what the other CTAs published (the proxy fence).
-__device__ __forceinline__ void publish_count(volatile unsigned* p, unsigned v) {
-  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(const_cast<unsigned*>(p))), "r"(v)
-               : "memory");
-}
-__device__ __forceinline__ bool wait_count(volatile unsigned* p, unsigned v, volatile int* abort, unsigned* err) {
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    unsigned c;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(c) : "r"(smem_u32(const_cast<unsigned*>(p))) : "memory");
-    if (c >= v) break;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      set_error(err, ERRBIT_TIMEOUT);
-      return false;
-    }
-  }
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-  return true;
-}
-
 template <int WT, int NC, int FEAT>
 __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
-    gemv_stream_kernel(const __grid_constant__ typename KernelArgsOf<FEAT>::type prm) {
-  constexpr bool kChain = FEAT == FEAT_CHAIN;   // several calls, grid barriers between dependent ones
+    gemv_stream_kernel(const __grid_constant__ StreamArgs a) {
   constexpr bool kExt = FEAT != FEAT_PLAIN;     // dual GEMV / several matrices / RMS prologue compiled in
   constexpr bool kSplit = FEAT == FEAT_SPLIT;   // cluster split K compiled in
   constexpr int U = stream_u(WT, NC);
@@ -417,78 +377,48 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
   // the extension code)
   constexpr bool kBatch = !(kExt && WT == WT_F16 && NCT > 1);
   static_assert(U * NCT * 16 <= 64, "x registers per thread");
-  // launch-wide values (equal in every stage of a chain): ring, consumer warps, layout
-  const StreamArgs& a0 = first_args(prm);
-  int nst = 1, nbar = 0;
-  if constexpr (kChain) {
-    nst = prm.nst;
-    nbar = prm.nbar;
-  }
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t full0 = sbase, empty0 = sbase + 8u * a0.NS, xbar = sbase + 16u * a0.NS;
+  const uint32_t full0 = sbase, empty0 = sbase + 8u * a.NS, xbar = sbase + 16u * a.NS;
   const uint32_t xchbar = xbar + 8u;  // split K: arrivals of the peer CTAs (rank 0 only)
-  const uint32_t xfree = xbar + 16u;  // chain: the consumers are done with the staged x
-  float* xs = reinterpret_cast<float*>(smem + a0.off_xs);
-  float* auxs0 = reinterpret_cast<float*>(smem + a0.off_aux);
-  float* red0 = reinterpret_cast<float*>(smem + a0.off_red);
-  float* auxs_alt = auxs0;
-  float* red_alt = red0;
-  if constexpr (kChain) {
-    auxs_alt = reinterpret_cast<float*>(smem + prm.off_aux2);
-    red_alt = reinterpret_cast<float*>(smem + prm.off_red2);
-  }
-  float* normv = reinterpret_cast<float*>(smem + a0.off_norm);  // [wpc][NC] sums of squares
-  float* xch = reinterpret_cast<float*>(smem + a0.off_xchg);    // split K: [S][NC][XR], then [S][NC]
-  const uint32_t ring = sbase + static_cast<uint32_t>(a0.off_ring);
+  float* xs = reinterpret_cast<float*>(smem + a.off_xs);
+  float* auxs = reinterpret_cast<float*>(smem + a.off_aux);
+  float* red = reinterpret_cast<float*>(smem + a.off_red);
+  float* normv = reinterpret_cast<float*>(smem + a.off_norm);  // [wpc][NC] sums of squares
+  float* xch = reinterpret_cast<float*>(smem + a.off_xchg);    // split K: [S][NC][XR], then [S][NC]
+  const uint32_t ring = sbase + static_cast<uint32_t>(a.off_ring);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarBytes - 8);
-  // chain: grid barriers the consumers have passed (for the producer)
-  volatile unsigned* bars_passed = reinterpret_cast<volatile unsigned*>(smem + kBarBytes - 16);
 
-  const int S = kSplit ? a0.S : 1;
+  const int S = kSplit ? a.S : 1;
   int crank = 0;
   if constexpr (kSplit) crank = static_cast<int>(cluster_ctarank());
   const int rg = static_cast<int>(blockIdx.x) / S;  // row range of this CTA (its cluster's)
-  const int nrg = static_cast<int>(gridDim.x) / S;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < a0.NS; ++i) {
+    for (int i = 0; i < a.NS; ++i) {
       mbar_init(full0 + 8u * i, 1);
-      mbar_init(empty0 + 8u * i, static_cast<uint32_t>(a0.ncw));
+      mbar_init(empty0 + 8u * i, static_cast<uint32_t>(a.ncw));
     }
     mbar_init(xbar, 1);
-    mbar_init(xchbar, static_cast<uint32_t>(S > 1 ? (S - 1) * a0.ncw * 32 : 1));
-    if constexpr (kChain) {
-      mbar_init(xfree, 1);
-      *bars_passed = 0u;
-    }
+    mbar_init(xchbar, static_cast<uint32_t>(S > 1 ? (S - 1) * a.ncw * 32 : 1));
     fence_mbar_init();
   }
-  // chain: every stage's arguments copied to shared memory, where any stage's are read
-  // with plain shared loads
-  const StreamArgs* sargs = nullptr;
-  if constexpr (kChain) {
-    sargs = reinterpret_cast<const StreamArgs*>(smem + prm.off_args);
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(&prm.st[0]);
-    uint32_t* dstw = reinterpret_cast<uint32_t*>(smem + prm.off_args);
-    const int nw = nst * static_cast<int>(sizeof(StreamArgs) / 4);
-    for (int i = threadIdx.x; i < nw; i += blockDim.x) dstw[i] = src[i];
-  }
-  auto stage = [&](int s) -> const StreamArgs& {
-    if constexpr (kChain)
-      return sargs[s];
-    else
-      return prm;
-  };
   if constexpr (kSplit)
     cluster_sync_all();  // peers arrive on rank 0's barrier only after it is initialised
   else
     __syncthreads();
-  // A chain lets the next grid in only after its last grid barrier: that grid may be this
-  // chain again, whose first arrival takes its base from the counter.
-  if (nbar == 0) pdl_trigger();
+  pdl_trigger();
+
+  int64_t r0;
+  int nrows;
+  cta_rows(a, rg, r0, nrows);
+  const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
+  const bool dual = kExt && a.W2 != nullptr;
+  const bool multi = kExt && a.nseg > 0;  // several matrices sharing x (never with dual)
+  const bool norm = kExt && a.gamma != nullptr;
+  const bool xnew = a.stage_x && nrows > 0;  // the producer copies x (and gamma) into xs
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -497,33 +427,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
       int it = 0, slot = 0;  // tiles issued; ring slot of the next one
       uint32_t ephase = 1u;   // parity of the empty-barrier phase that frees `slot`
       bool ok = true;
-      int nx = 0;             // x copies issued
-      bool waited = false;    // preceding grid waited for
-      int bars = 0, bars_seen = 0;  // chain: grid barriers up to this stage; the last waited for
-      for (int s = 0; s < nst && ok; ++s) {
-      const StreamArgs& a = stage(s);
-      if constexpr (kChain) bars += (a.cflags & CHAIN_BAR) ? 1 : 0;
-      int64_t r0;
-      int nrows;
-      cta_rows(a, rg, nrg, r0, nrows);
-      const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
-      const bool dual = kExt && a.W2 != nullptr;
-      const bool multi = kExt && a.nseg > 0;
-      const bool norm = kExt && a.gamma != nullptr;
-      bool xnew = a.stage_x && nrows > 0;  // this stage copies x (and gamma) into xs
-      if constexpr (kChain) xnew = xnew && !(a.cflags & CHAIN_REUSE);
-      // x goes right behind the launch's first weight tile; in a later stage of a chain,
-      // behind as many of the stage's tiles as the ring holds (their slots free up as the
-      // previous stage ends, and x is not needed earlier)
-      int x_after = 1, its = 0;
-      if (kChain && s > 0) {
-        int ntl = 0;
-        for (int rc0 = 0; rc0 < nrows; rc0 += a.RC) {
-          const int nvr = (dual ? 2 : 1) * min(a.RC, nrows - rc0);
-          ntl += (kc_hi - kc_lo) * ((nvr + a.R - 1) / a.R);
-        }
-        x_after = max(1, min(a.NS, ntl));
-      }
+      bool x_issued = false;
       for (int rc0 = 0; rc0 < nrows && ok; rc0 += a.RC) {
         const int nrc = min(a.RC, nrows - rc0);
         const int nvr = dual ? 2 * nrc : nrc;
@@ -581,52 +485,34 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
               slot = 0;
               ephase ^= 1u;
             }
-            if (xnew && ++its == x_after) {
-              // x staged by bulk copy behind the weight tiles above, once the preceding
-              // grid (which may write x) has finished: later in the queue it waits behind
-              // the whole ring of weight tiles (with the RMS prologue, gamma follows x on
-              // the same barrier).  In a chain, also once the consumers are done with the
-              // previous x and, after a grid barrier, once every CTA has passed it.
-              if (!waited) {
-                pdl_wait();
-                waited = true;
-              }
-              if constexpr (kChain) {
-                if (nx > 0 && !mbar_wait_or_abort(xfree, static_cast<uint32_t>((nx - 1) & 1), abort_flag, a.err)) {
-                  ok = false;
-                  break;
-                }
-                if (bars > bars_seen) {
-                  if (!wait_count(bars_passed, static_cast<unsigned>(bars), abort_flag, a.err)) {
-                    ok = false;
-                    break;
-                  }
-                  bars_seen = bars;
-                }
-              }
+            if (xnew && !x_issued) {
+              // x staged by bulk copy right behind the first weight tile, once the preceding
+              // grid (which may write x) has finished: later in the queue it would wait
+              // behind the whole ring of weight tiles (with the RMS prologue, gamma follows
+              // x on the same barrier)
+              pdl_wait();
               mbar_arrive_expect_tx(xbar, static_cast<uint32_t>((NC + (norm ? 1 : 0)) * a.K * 4));
               for (int c = 0; c < NC; ++c)
                 bulk_g2s(smem_u32(xs + c * a.K), a.x + static_cast<int64_t>(c) * a.K,
                          static_cast<uint32_t>(a.K * 4), xbar);
               if (norm) bulk_g2s(smem_u32(xs + NC * a.K), a.gamma, static_cast<uint32_t>(a.K * 4), xbar);
-              ++nx;
+              x_issued = true;
             }
           }
         }
       }
-      }  // stages
       if (!ok) {
         // Drain: wait (bounded) until every copy this thread issued has landed.
-        for (int i = max(0, it - a0.NS); i < it; ++i)
-          (void)mbar_wait(full0 + 8u * (i % a0.NS), static_cast<uint32_t>((i / a0.NS) & 1));
-        if (nx > 0) (void)mbar_wait(xbar, static_cast<uint32_t>((nx - 1) & 1));
+        for (int i = max(0, it - a.NS); i < it; ++i)
+          (void)mbar_wait(full0 + 8u * (i % a.NS), static_cast<uint32_t>((i / a.NS) & 1));
+        if (x_issued) (void)mbar_wait(xbar, 0u);
       }
     }
   } else {
     // ------------------------------------------------------------ consumers
     // Every consumer thread runs the same sequence of named barriers whether or not a
     // wait gave up; after an abort the remaining work is skipped, not the barriers.
-    const int cw = warp - 1, ctid = threadIdx.x - 32, nt = a0.ncw * 32;
+    const int cw = warp - 1, ctid = threadIdx.x - 32, nt = a.ncw * 32;
     const uint32_t qr = lane_quad_rot<WT>(lane);
     auto epi_aux = [](int e) { return e == EPI_SILU_MUL || e == EPI_ADD; };
     const bool finalizer = (crank == 0);
@@ -636,46 +522,12 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
     uint32_t xphase = 0;
     bool ok = true;
     auto cbar = [&]() { named_bar_sync(1, static_cast<uint32_t>(nt)); };
-    int bars = 0;                  // chain: grid barriers passed
-    unsigned long long gbase = 0;  // chain (thread ctid 0): the counter when the launch began
-    // this thread's x for the current K chunk (a chain keeps it from stage to stage)
-    struct XRegs {
-      float2 xr[kInt ? 1 : U][NCT][8];
-      XInt xq[kInt ? U : 1][kInt ? NCT : 1];
-      float xsum[U][NCT];
-    };
-    XRegs x_chain;
-    for (int s = 0; s < nst; ++s) {
-    const StreamArgs& a = stage(s);
-    if constexpr (kChain) {
-      if (a.cflags & CHAIN_BAR) {
-        // this CTA arrived at the end of the previous stage; wait for every other one
-        ++bars;
-        if (ctid == 0) {
-          if (ok) (void)grid_wait(prm.gbar, gbase + static_cast<unsigned long long>(bars) * gridDim.x, abort_flag, a.err);
-          publish_count(bars_passed, static_cast<unsigned>(bars));
-        }
-        cbar();
-        ok = ok && !*abort_flag;
-        if (bars == nbar) pdl_trigger();
-      }
-    }
-    int64_t r0;
-    int nrows;
-    cta_rows(a, rg, nrg, r0, nrows);
-    const int kc_lo = crank * a.n_kc / S, kc_hi = (crank + 1) * a.n_kc / S;
-    const bool dual = kExt && a.W2 != nullptr;
-    const bool multi = kExt && a.nseg > 0;  // several matrices sharing x (never with dual)
-    const bool norm = kExt && a.gamma != nullptr;
     const int XR = dual ? 2 * a.RC : a.RC;  // virtual rows per row chunk
-    bool xnew = a.stage_x && nrows > 0;     // x (and gamma) copied into xs for this stage
-    if constexpr (kChain) xnew = xnew && !(a.cflags & CHAIN_REUSE);
-    const int g = cw / a.wpg;                  // row group of this warp
-    const bool live = !kChain || g < a.G;      // chain: warps past the stage's row groups idle
-    const int wr = cw - g * a.wpg;             // warp within the row group
-    const int cgi = wr / a.wpc;                // column group
-    const int wc = wr - cgi * a.wpc;           // warp within the column group
-    const int c0 = cgi * NCT;                  // first column of this thread
+    const int g = cw / a.wpg;               // row group of this warp
+    const int wr = cw - g * a.wpg;          // warp within the row group
+    const int cgi = wr / a.wpc;             // column group
+    const int wc = wr - cgi * a.wpc;        // warp within the column group
+    const int c0 = cgi * NCT;               // first column of this thread
     const int tg = wc * 32 + lane, tg_n = a.wpc * 32;
     bool need_aux = epi_aux(a.epi);
     if (multi)
@@ -690,12 +542,6 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
       return a.seg_aux[i][c * mi + local];
     };
     bool x_loaded = false;
-    // chain: this thread's x (converted) survives the stage when the next one keeps it
-    const bool keep_x = kChain && (a.cflags & CHAIN_KEEP);
-    // chain: odd stages use the second aux / partial-sum buffers, so that a stage's
-    // finalisation may overlap the next stage's start (no CTA barrier between them)
-    float* const auxs = (kChain && (s & 1)) ? auxs_alt : auxs0;
-    float* const red = (kChain && (s & 1)) ? red_alt : red0;
     float ssq[NCT];  // this thread's share of the sum of squares of x (first row chunk)
 #pragma unroll
     for (int c = 0; c < NCT; ++c) ssq[c] = 0.0f;
@@ -741,22 +587,18 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
         const bool x_smem = a.fwht_B > 0 || a.stage_x;
         const float* xsrc = x_smem ? xs : a.x + static_cast<int64_t>(kc) * a.kc_len;
         const int64_t xstride = x_smem ? klen : a.K;
-        // (integer path: each unit's x is converted as soon as it is loaded)
-        XRegs x_chunk;
-        XRegs& xreg = kChain ? x_chain : x_chunk;
-        auto& xr = xreg.xr;
-        auto& xq = xreg.xq;
-        auto& xsum = xreg.xsum;
         const float* gsrc = !norm ? nullptr
                             : a.stage_x ? xs + NC * a.K  // staged after x
                                         : a.gamma + static_cast<int64_t>(kc) * a.kc_len;
-        // a chain reloads x only for a new K chunk: not for a later row chunk of a one-chunk
-        // row, nor for a stage that keeps the previous stage's x
-        const bool load_x = !kChain || !(a.n_kc == 1 && (rc0 > 0 || keep_x));
+        // (integer path: each unit's x is converted as soon as it is loaded)
+        float2 xr[kInt ? 1 : U][NCT][8];
+        XInt xq[kInt ? U : 1][kInt ? NCT : 1];
+        float xsum[U][NCT];
+        bool xbad = false;  // a unit of this thread the integer path cannot carry
 #pragma unroll
         for (int i = 0; i < U; ++i) {
           const int u = unit_index<WT, U>(tg, i, tg_n);
-          if (u < units && ok && load_x) {
+          if (u < units && ok) {
             float2 (&xv)[NCT][8] = xr[kInt ? 0 : i];
             if (norm)
               load_unit_x<WT, NCT, kExt>(xsrc, xstride, gsrc, u, qr, c0, NC, xv, rc0 == 0, ssq);
@@ -773,54 +615,93 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
             }
             if constexpr (kInt) {
 #pragma unroll
-              for (int c = 0; c < NCT; ++c) x_to_int(xv[c], xq[i][c]);
+              for (int c = 0; c < NCT; ++c) xbad = x_to_int(xv[c], xq[i][c]) || xbad;
             }
           }
         }
-        for (int t0 = 0; t0 < nvr; t0 += a.R) {
-          const int rows = min(a.R, nvr - t0);
-          ok = ok && mbar_wait_or_abort(full0 + 8u * slot, fphase, abort_flag, a.err);
-          float2 acc[RT][NCT];
+        // The chunk's tiles: wait for the stage, `consume` it into the per-row partial
+        // sums, release it, reduce the sums over the warp and store them.
+        auto tiles = [&](auto&& consume) {
+          for (int t0 = 0; t0 < nvr; t0 += a.R) {
+            const int rows = min(a.R, nvr - t0);
+            ok = ok && mbar_wait_or_abort(full0 + 8u * slot, fphase, abort_flag, a.err);
+            float2 acc[RT][NCT];
 #pragma unroll
-          for (int j = 0; j < RT; ++j)
+            for (int j = 0; j < RT; ++j)
 #pragma unroll
-            for (int c = 0; c < NCT; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
-          if (ok && live) {
-            if constexpr (WT == WT_Q4_K && kInt)
-              consume_tile_q4k_int<RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg, g,
-                                       a.G, xq, xsum, acc);
-            else if constexpr (WT == WT_Q4_K)
-              consume_tile_q4k<NCT, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
-                                        g, a.G, xr, xsum, acc);
-            else if constexpr (kInt)
-              consume_tile_int<WT, NCT, U, RT>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows, units, tg,
-                                           tg_n, g, a.G, xq, acc);
-            else
-              consume_tile<WT, NCT, U, RT, kBatch>(ring + static_cast<uint32_t>(slot) * a.stage_bytes, seg, rows,
-                                                   units, tg, tg_n, g, a.G, qr, xr, acc);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty0 + 8u * slot);
-          if (++slot == a.NS) {
-            slot = 0;
-            fphase ^= 1u;
-          }
-          // warp reduction of the RT*NCT partial sums (padded to a power of two)
-          constexpr int V = RT * NCT;
-          constexpr int VP = V > 16 ? 32 : V > 8 ? 16 : V > 4 ? 8 : V > 2 ? 4 : V > 1 ? 2 : 1;
-          float vals[VP];
+              for (int c = 0; c < NCT; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
+            if (ok) consume(ring + static_cast<uint32_t>(slot) * a.stage_bytes, rows, acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+            if (++slot == a.NS) {
+              slot = 0;
+              fphase ^= 1u;
+            }
+            // warp reduction of the RT*NCT partial sums (padded to a power of two)
+            constexpr int V = RT * NCT;
+            constexpr int VP = V > 16 ? 32 : V > 8 ? 16 : V > 4 ? 8 : V > 2 ? 4 : V > 1 ? 2 : 1;
+            float vals[VP];
 #pragma unroll
-          for (int j = 0; j < VP; ++j)
-            vals[j] = j < V ? acc[j / NCT][j % NCT].x + acc[j / NCT][j % NCT].y : 0.0f;
-          const float sum = WarpVecReduce<VP>::run(vals, lane);
-          const int jv = lane >> (5 - WarpVecReduce<VP>::kLog);
-          if (live && lane == WarpVecReduce<VP>::owner(jv) && jv < V) {
-            const int r = g + (jv / NCT) * a.G, c = c0 + jv % NCT;
-            if (r < rows && c < NC) {
-              float* p = red + ((t0 + r) * a.wpc + wc) * NC + c;
-              *p = (kc == kc_lo) ? sum : (*p + sum);
+            for (int j = 0; j < VP; ++j)
+              vals[j] = j < V ? acc[j / NCT][j % NCT].x + acc[j / NCT][j % NCT].y : 0.0f;
+            const float sum = WarpVecReduce<VP>::run(vals, lane);
+            const int jv = lane >> (5 - WarpVecReduce<VP>::kLog);
+            if (lane == WarpVecReduce<VP>::owner(jv) && jv < V) {
+              const int r = g + (jv / NCT) * a.G, c = c0 + jv % NCT;
+              if (r < rows && c < NC) {
+                float* p = red + ((t0 + r) * a.wpc + wc) * NC + c;
+                *p = (kc == kc_lo) ? sum : (*p + sum);
+              }
             }
           }
+        };
+        if constexpr (kInt) {
+          // A warp holding a unit that the integer path cannot carry (an outlier, a
+          // sparse unit, a NaN or an infinity) takes fp32 products for the whole chunk,
+          // on x reloaded as floats (it stays in shared or global memory for the chunk).
+          if (__any_sync(0xffffffffu, xbad)) {
+            auto load_xf = [&](int i, float2 (&xv)[NCT][8]) {
+              const int u = unit_index<WT, U>(tg, i, tg_n);
+              if (u < units) {
+                if (norm)
+                  load_unit_x<WT, NCT, kExt>(xsrc, xstride, gsrc, u, qr, c0, NC, xv);
+                else
+                  load_unit_x<WT, NCT, false>(xsrc, xstride, nullptr, u, qr, c0, NC, xv);
+              }
+            };
+            if constexpr (WT == WT_Q4_K) {
+              // one unit of the pair at a time, its x loaded per tile
+              tiles([&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
+#pragma unroll 1
+                for (int n = 0; n < 2; ++n) {
+                  float2 xv[NCT][8];
+                  load_xf(n, xv);
+                  consume_tile_q4k_unit<RT>(st, seg, rows, units, tg, g, a.G, n, xv[0], acc);
+                }
+              });
+            } else {
+              float2 xf[U][NCT][8];
+#pragma unroll
+              for (int i = 0; i < U; ++i) load_xf(i, xf[i]);
+              tiles([&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
+                consume_tile<WT, NCT, U, RT, false>(st, seg, rows, units, tg, tg_n, g, a.G, qr, xf, acc);
+              });
+            }
+          } else {
+            tiles([&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
+              if constexpr (WT == WT_Q4_K)
+                consume_tile_q4k_int<RT>(st, seg, rows, units, tg, g, a.G, xq, xsum, acc);
+              else
+                consume_tile_int<WT, NCT, U, RT>(st, seg, rows, units, tg, tg_n, g, a.G, xq, acc);
+            });
+          }
+        } else {
+          tiles([&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
+            if constexpr (WT == WT_Q4_K)
+              consume_tile_q4k<NCT, RT>(st, seg, rows, units, tg, g, a.G, xr, xsum, acc);
+            else
+              consume_tile<WT, NCT, U, RT, kBatch>(st, seg, rows, units, tg, tg_n, g, a.G, qr, xr, acc);
+          });
         }
       }
       if (norm && rc0 == 0 && g == 0) {
@@ -920,36 +801,8 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
           a.dst[c * a.M + r0 + rc0 + r] = out;
         }
       }
-      // red / auxs may be reused by the next row chunk; a chain's next stage uses the other
-      // buffers and may start at once, unless it waits at a grid barrier (which publishes
-      // this stage's outputs) or writes the sums of squares read above
-      bool sync_end = true;
-      if constexpr (kChain)
-        sync_end = rc0 + a.RC < nrows || s + 1 == nst || (stage(s + 1).cflags & CHAIN_BAR) ||
-                   stage(s + 1).gamma != nullptr;
-      if (sync_end) cbar();
+      cbar();  // red / auxs may be reused by the next row chunk
     }
-    if constexpr (kChain) {
-      // The staged x is free once no later stage reuses it (the barrier above ended every
-      // read of it); the grid barrier's arrival publishes this CTA's outputs.
-      if (a.stage_x && nrows > 0 && ctid == 0) {
-        bool keep = false;
-        if (s + 1 < nst && (stage(s + 1).cflags & CHAIN_REUSE)) {
-          int64_t r0n;
-          int nrn;
-          cta_rows(stage(s + 1), rg, nrg, r0n, nrn);
-          keep = nrn > 0;
-        }
-        if (!keep) mbar_arrive(xfree);
-      }
-      if (s + 1 < nst && (stage(s + 1).cflags & CHAIN_BAR) && ctid == 0) {
-        // no CTA completes the launch's first barrier before this one arrives, and the
-        // previous launch on this counter made all of its arrivals before this one began
-        const unsigned long long old = grid_arrive(prm.gbar);
-        if (bars == 0) gbase = old - old % gridDim.x;
-      }
-    }
-    }  // stages
   }
   __syncthreads();
   if constexpr (kSplit) cluster_sync_all();  // no CTA leaves while a peer may still store into it
@@ -1017,51 +870,6 @@ int max_active_clusters_t(const Plan& p) {
   cfg.numAttrs = 1;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
-// Persistent chain of one-column calls (one instantiation per format).
-template <int WT>
-int launch_chain_t(int grid, int threads, int smem, const ChainArgs& a, cudaStream_t st, bool pdl) {
-  auto kern = gemv_stream_kernel<WT, 1, FEAT_CHAIN>;
-  static int configured_smem[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && configured_smem[dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured_smem[dev] = smem;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a);
-}
-
-// CTAs of the chain kernel resident per SM (0 if the query fails).
-template <int WT>
-int chain_ctas_per_sm_t(int threads, int smem) {
-  auto kern = gemv_stream_kernel<WT, 1, FEAT_CHAIN>;
-  int dev = 0, smem_max = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-      smem_max < smem ||
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, static_cast<size_t>(smem)) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }

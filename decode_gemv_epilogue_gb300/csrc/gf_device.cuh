@@ -502,16 +502,25 @@ __device__ __forceinline__ void q4k_nibbles(const uint4 q, uint32_t n, float2 (&
 }
 
 // ---- integer dot products (Q4_0, Q8_0 and Q4_K, single columns)
-// A unit's 16 x values become integers X_j = trunc(x_j * 2^s) that share the exponent s
-// (chosen so that max |x_j| * 2^s lies in [2^22, 2^23), hence |X_j| <= 2^23 - 1).  Each
-// X_j is split into three bytes X = D2 * 2^16 + D1 * 2^8 + D0 (D2 signed, D1 and D0
-// unsigned), packed four elements to a register in the order of the unit's code bytes:
-// group g holds the elements of the low nibbles (g = 0, 1) or high nibbles (g = 2, 3) of
-// code word g % 2.  sum_j (q_j - 8) X_j is then exact in 32-bit integers (|.| < 2^30):
-// three chains of four dp4a (one per digit) on the unpacked nibbles, combined at the end
-// with -8 sum_j X_j (modulo 2^32; the result fits).  The block's d times 2^-s scales the
-// converted sum.  Truncating x * 2^s changes each product by less than
-// |w_j| * 2^-s <= |w_j| * 2^-22 * max_unit |x|.
+// A unit's 16 x values become integers X_j = rn(x_j * 2^s) (round to nearest) that share
+// the exponent s, chosen so that m * 2^s lies in [2^22, 2^23) for m = max |x_j|; when
+// m's significand is all ones (m * 2^s would round up to 2^23) s is one less.  Hence
+// -2^23 <= X_j <= 2^23 - 1.  Each X_j is split into three bytes
+// X = D2 * 2^16 + D1 * 2^8 + D0 (D2 signed, D1 and D0 unsigned), packed four elements
+// to a register in the order of the unit's code bytes: group g holds the elements of the
+// low nibbles (g = 0, 1) or high nibbles (g = 2, 3) of code word g % 2.
+// sum_j (q_j - 8) X_j is then exact in 32-bit integers (|.| <= 2^30): three chains of
+// four dp4a (one per digit) on the unpacked nibbles, combined at the end with
+// -8 sum_j X_j (modulo 2^32; the result fits).  The block's d times 2^-s scales the
+// converted sum.  Rounding x * 2^s moves each x_j by at most 2^-s / 2 <= m * 2^-23.
+//
+// That absolute error is small next to |x_j| only for the unit's larger values, so a
+// unit takes the integer path only when at least half of its 16 values have magnitude
+// >= m / 16 (then every one of those is carried to 2^-19 relative, and the unit's
+// smaller values are at most as many as its larger ones), and all 16 are finite.  A
+// unit with an outlier (one or a few values far above the rest), a sparse unit, or a
+// NaN / Inf is flagged: the warp that holds it decodes its tiles to floats and takes
+// fp32 products instead (exact IEEE semantics for non-finite x).
 struct XInt {
   uint32_t d2[4], d1[4], d0[4];  // digit bytes of the four element groups
   uint32_t c;                    // -8 * sum_j X_j (two's complement)
@@ -552,25 +561,38 @@ __device__ __forceinline__ void pack_digits(uint32_t a, uint32_t b, uint32_t c, 
 // x of one unit (eight pairs in decode_unit()'s pair order: pairs 2g and 2g+1 form group
 // g) -> XInt.  The exponent is kept in [-126, 126] so that 2^s and 2^-s are normal
 // floats; below |x| = 2^-103 the integers get shorter (absolute error under 2^-126).
-__device__ __forceinline__ void x_to_int(const float2 (&xv)[8], XInt& xi) {
+// Returns true when the unit must not take the integer path (see above): fewer than 8
+// of its values reach m / 16, or one of them is NaN or infinite.
+__device__ __forceinline__ bool x_to_int(const float2 (&xv)[8], XInt& xi) {
   float m = 0.0f;
+  float2 z = make_float2(0.0f, 0.0f);  // stays 0 unless some x is NaN or infinite (x * 0)
 #pragma unroll
-  for (int k = 0; k < 8; ++k) m = fmaxf(m, fmaxf(fabsf(xv[k].x), fabsf(xv[k].y)));
-  // m = f * 2^E with f in [0.5, 1): E = biased exponent - 126 (m = 0: any s works)
-  const int E = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu) - 126;
-  const int s = max(-126, min(126, 23 - E));
+  for (int k = 0; k < 8; ++k) {
+    m = fmaxf(m, fmaxf(fabsf(xv[k].x), fabsf(xv[k].y)));
+    z = ffma2(xv[k], make_float2(0.0f, 0.0f), z);
+  }
+  const float thr = m * 0.0625f;  // exact: a power of two (m = 0: every value counts)
+  int nbig = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) nbig += (fabsf(xv[k].x) >= thr ? 1 : 0) + (fabsf(xv[k].y) >= thr ? 1 : 0);
+  // m = f * 2^E with f in [0.5, 1): E = biased exponent - 126 (m = 0: any s works); one
+  // less when f = 1 - 2^-24, whose m * 2^(23 - E) would round to 2^23
+  const uint32_t mb = __float_as_uint(m);
+  const int E = static_cast<int>((mb >> 23) & 0xFFu) - 126;
+  const int s = max(-126, min(126, 23 - E - ((mb & 0x7FFFFFu) == 0x7FFFFFu ? 1 : 0)));
   const float up = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
   xi.sc = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
   int sum = 0;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    const int X0 = __float2int_rz(xv[2 * g].x * up), X1 = __float2int_rz(xv[2 * g].y * up);
-    const int X2 = __float2int_rz(xv[2 * g + 1].x * up), X3 = __float2int_rz(xv[2 * g + 1].y * up);
+    const int X0 = __float2int_rn(xv[2 * g].x * up), X1 = __float2int_rn(xv[2 * g].y * up);
+    const int X2 = __float2int_rn(xv[2 * g + 1].x * up), X3 = __float2int_rn(xv[2 * g + 1].y * up);
     sum += (X0 + X1) + (X2 + X3);
     pack_digits(static_cast<uint32_t>(X0), static_cast<uint32_t>(X1), static_cast<uint32_t>(X2),
                 static_cast<uint32_t>(X3), xi.d2[g], xi.d1[g], xi.d0[g]);
   }
   xi.c = static_cast<uint32_t>(-8 * sum);
+  return nbig < 8 || !(z.x == 0.0f && z.y == 0.0f);
 }
 
 // Four registers of unsigned codes (byte k of n[g] is element 4g + k) against the XInt of

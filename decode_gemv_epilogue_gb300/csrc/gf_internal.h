@@ -23,7 +23,6 @@ constexpr int kMaxFusedFwhtBlock = 8192;
 constexpr int kUnitElems = 16;              // weights per decode unit (half a quant block)
 constexpr int kMaxSplit = 8;                // CTAs of a split-K cluster (portable cluster size)
 constexpr int kMaxSeg = 4;                  // matrices sharing x in one multi-matrix launch
-constexpr int kMaxChain = 8;                // calls run by one persistent chain launch
 
 // Tiling of the consumer warps, per (format, columns):
 //  U   units (16 weights) per thread per K chunk, RT rows per thread per tile;
@@ -104,30 +103,7 @@ struct StreamArgs {
   float* seg_dst[kMaxSeg];
   int S;             // CTAs per cluster sharing a row range, each a slice of the K chunks
   int stage_x;       // 1: the producer bulk-copies x (one K chunk, every column) into xs
-  int rot;           // chain stage: row range of CTA rg is that of index (rg - rot) mod CTAs
-  int cflags;        // chain stage: CHAIN_* bits
   int off_xs, off_aux, off_red, off_norm, off_xchg, off_ring;
-};
-
-// Several single-column streamed calls run by one persistent launch (FEAT_CHAIN).  Stage s
-// is the call st[s], planned with the launch's common consumer warps, ring stages and
-// shared-memory layout; the producer streams the stages' weight tiles back to back.
-// Before a stage flagged CHAIN_BAR, every CTA's consumers have finished and published the
-// stages before it: a grid barrier on *gbar, a counter that only grows (each CTA adds one
-// per barrier, so it is a multiple of the grid whenever no launch is in flight).
-// Chain stage flags (StreamArgs.cflags):
-enum {
-  CHAIN_BAR = 1,     // a grid barrier before the stage
-  CHAIN_REUSE = 2,   // x staged for the previous stage is this stage's x (no copy)
-  CHAIN_KEEP = 4,    // and each thread keeps its converted x of the previous stage
-};
-struct ChainArgs {
-  StreamArgs st[kMaxChain];
-  unsigned long long* gbar;
-  int nst;       // stages
-  int nbar;      // grid barriers
-  int off_args;  // shared-memory copy of st[0 .. nst) (8-byte aligned)
-  int off_aux2, off_red2;  // odd stages' aux and partial-sum buffers (even ones: off_aux, off_red)
 };
 
 struct GenericArgs {
@@ -213,7 +189,7 @@ struct DeviceLimits {
 };
 
 // Kernel feature sets of the streamed GEMV (separate instantiations).
-enum { FEAT_PLAIN = 0, FEAT_EXT = 1, FEAT_SPLIT = 2, FEAT_CHAIN = 3 };
+enum { FEAT_PLAIN = 0, FEAT_EXT = 1, FEAT_SPLIT = 2 };
 
 // Launchers (return cudaError_t).  `pdl` requests programmatic stream serialization.
 // FEAT_SPLIT launches group the grid into clusters of p.s.S CTAs.  One function per
@@ -231,11 +207,6 @@ int launch_stream_q4k_split(int ncols, const Plan& p, cudaStream_t st, bool pdl)
 int stream_split_max_clusters_float(int wtype, int ncols, const Plan& p);
 int stream_split_max_clusters_block(int wtype, int ncols, const Plan& p);
 int stream_split_max_clusters_q4k(int ncols, const Plan& p);
-// Persistent chain (one column, the extended kernel's features): launch, and CTAs of
-// `threads` threads and `smem` bytes resident per SM (0 if unknown).
-int launch_stream_chain(int wtype, int grid, int threads, int smem, const ChainArgs& a, cudaStream_t st,
-                        bool pdl);
-int stream_chain_ctas_per_sm(int wtype, int threads, int smem);
 int launch_generic(int wtype, int ncols, const GenericArgs& a, int grid, int smem,
                    cudaStream_t st, bool pdl);
 int launch_fwht(const float* x, const float* signs, float* dst, int64_t n, int B, int nsigns,

@@ -10,7 +10,10 @@
 // Host code cannot use the array's name as a device address, so the address is looked
 // up once per device with cudaGetSymbolAddress (the first call on a device does this,
 // with that device current) and handed to the kernels through gemv_fused_ex's
-// workspace option.  Nothing is allocated or freed, here or below.
+// workspace option.  Nothing is allocated or freed, here or below.  The address stays
+// valid as long as the device's primary context does: a cudaDeviceReset by the host
+// invalidates it (and the device error word of api.cu), so the library must be
+// reloaded after one.
 #include <cstdint>
 #include <mutex>
 

@@ -75,9 +75,6 @@ MULTI_MAX = 4
 _gemv_multi = _sig("gemv_multi", [ctypes.POINTER(MultiItem), _i32, _i32, _vp, _i64, ctypes.POINTER(GfOpts), _vp])
 _prepare_multi = _sig("gf_prepare_multi", [ctypes.POINTER(MultiItem), _i32, _i32, _vp, _i64,
                                            ctypes.POINTER(GfOpts), ctypes.POINTER(_vp)])
-CHAIN_MAX = 8
-_prepare_chain = _sig("gf_prepare_chain", [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp)])
-_chain_info = _sig("gf_chain_info", [_vp, ctypes.POINTER(_i64 * 8)])
 _graph_create = _sig("gf_graph_create", [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp)])
 _graph_launch = _sig("gf_graph_launch", [_vp, _vp])
 _graph_free = _sig("gf_graph_free", [_vp], None)
@@ -299,30 +296,6 @@ def prepare_multi(items, wtype, x, K, ncols=1, fwht_signs=None, fwht_block=0, ns
     if check:
         _check(st, "gf_prepare_multi")
     return Prepared(h.value, (items, x, fwht_signs, fwht_workspace, rms_norm_weight)) if st == OK else st
-
-
-def prepare_chain(calls, check=True):
-    """gf_prepare_chain: the prepared calls (one column each, one weight format) run by one
-    persistent launch, grid barriers only between dependent calls (see include/gemvfuse.h).
-    The given Prepared objects stay valid; the returned one keeps them (and their buffers)
-    referenced."""
-    arr = (_vp * max(1, len(calls)))(*[c.handle.value if isinstance(c, Prepared) else c for c in calls])
-    h = _vp()
-    st = _prepare_chain(arr, len(calls), ctypes.byref(h))
-    if check:
-        _check(st, "gf_prepare_chain")
-    return Prepared(h.value, list(calls)) if st == OK else st
-
-
-def chain_info(chain, check=True):
-    """gf_chain_info of a chain handle: dict of stages, barriers, barrier_mask, reuse_mask,
-    grid, threads, smem, ring_stages."""
-    info = (_i64 * 8)()
-    st = _chain_info(chain.handle if isinstance(chain, Prepared) else chain, ctypes.byref(info))
-    if check:
-        _check(st, "gf_chain_info")
-    keys = ("stages", "barriers", "barrier_mask", "reuse_mask", "grid", "threads", "smem", "ring_stages")
-    return dict(zip(keys, list(info)))
 
 
 def gemv_fused_fwht_noalloc(W, wtype, x, M, K, epilogue, aux, dst, ncols, fwht_signs, fwht_block, nsigns=None,

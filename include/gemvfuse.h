@@ -21,8 +21,8 @@
  * Conventions for every entry point:
  *  - All array pointers are DEVICE pointers owned by the caller.  The library never
  *    allocates, frees or keeps a pointer after the call returns, except for handles:
- *    a prepared call keeps its pointers, and a chain (gf_prepare_chain) allocates one
- *    8-byte device counter, freed with the handle.
+ *    a prepared call keeps its pointers (host memory only), and a step graph owns its
+ *    CUDA graph.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is enqueued
  *    asynchronously; the call returns once it is launched.
  *  - Arguments are validated on the host before anything is launched.  A non-zero
@@ -220,41 +220,6 @@ GF_API int gf_launch_prepared(const gf_prepared* const* calls, int n, void* stre
 /* Releases a handle (NULL is ignored).  Launches already issued are not affected. */
 GF_API void gf_free_prepared(gf_prepared* p);
 
-/* A persistent chain: the prepared calls calls[0..n) run by ONE launch of the streamed
- * kernel, in order, with the results of running them one after another (bit for bit,
- * except that a call planned with split K runs unsplit here: the same sums in another
- * order).  The pages fuse
- * the element-wise tail into each GEMV; a decode layer still pays a launch, a ramp and a
- * drain per GEMV, and a chain pays them once.  The kernel streams every stage's weights
- * back to back (the next stage's tiles load while the current one finishes) and puts a
- * grid barrier only before a stage that reads or writes what an earlier stage since the
- * last barrier writes, or writes what one reads (e.g. up -> gate silu*m -> down + add).
- *  calls : 1 <= n <= GF_CHAIN_MAX (more: GF_ERR_UNSUPPORTED) handles from gf_prepare,
- *          gf_prepare_glu or gf_prepare_multi on the current device (else GF_ERR_INVALID),
- *          each with ncols == 1, no FWHT prologue, one weight format for all, and a
- *          shape the streamed kernel takes; handles with M == 0 are skipped.  Anything
- *          else (a chain among the calls, a tensor-core or generic-kernel shape):
- *          GF_ERR_UNSUPPORTED.
- *  out   : a new handle, launched like any prepared call (gf_launch_prepared, graphs)
- *          with the first call's GF_FLAG_PDL, freed with gf_free_prepared.  The given
- *          handles stay valid and independent.
- *  Aliasing: no call may write any call's W (GF_ERR_ALIAS); the rest as in each call.
- *  The handle owns an 8-byte device counter for its grid barriers: launches of ONE
- *  chain handle must not overlap in time (issue them on one stream, as a decode step
- *  does); different handles are independent.  Every CTA of the launch must be resident
- *  at once (one per SM): checked here against the device's occupancy; a GPU shared
- *  with concurrent kernels can delay that, which ends in GF_ERR_TIMEOUT from
- *  gf_device_status, never a hang.  After a timeout, free the handle and prepare it
- *  again. */
-#define GF_CHAIN_MAX 8
-GF_API int gf_prepare_chain(const gf_prepared* const* calls, int n, gf_prepared** out);
-/* What a chain handle runs: info[0] stages, [1] grid barriers, [2] bit s set = a barrier
- * before stage s, [3] bit s set = stage s reuses stage s-1's x in shared memory, [4] CTAs,
- * [5] threads per CTA, [6] dynamic shared memory bytes, [7] ring stages.  Stages count
- * the non-empty calls in order.  GF_ERR_INVALID for NULL arguments or a handle that is not
- * a chain; a chain of empty calls gives zeros. */
-GF_API int gf_chain_info(const gf_prepared* chain, int64_t info[8]);
-
 /* A decode step as one launch: gf_graph_create records the launches of calls[0..n)
  * (n >= 1, in order, as gf_launch_prepared would issue them, programmatic dependent
  * launches included) into a CUDA graph and instantiates it; gf_graph_launch replays it
@@ -283,7 +248,10 @@ GF_API void gf_graph_free(gf_graph* g);
  *    with that device current); make that first call before any stream capture.
  *  - Every call on a device shares the one array and overwrites it before reading it;
  *    calls whose work overlaps on the GPU (e.g. on different streams without ordering)
- *    race on it and give undefined results: order them, e.g. on one stream. */
+ *    race on it and give undefined results: order them, e.g. on one stream.
+ *  - The address is kept for the life of the process.  Destroying the device's primary
+ *    context (cudaDeviceReset) invalidates it, as it does the library's device error
+ *    word: after a reset, reload the library before calling it again. */
 #define GF_NOALLOC_MAX_WORKSPACE_FLOATS 262144
 GF_API int gemv_fused_fwht_noalloc(const void* W, int wtype, const float* x, int64_t M, int64_t K,
                                    int epilogue, const float* aux, float* dst, int64_t ncols,

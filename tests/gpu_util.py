@@ -8,10 +8,6 @@ from oracle import gemv as ogemv
 
 TOL_REL = 2e-5   # |gpu - oracle| <= 2e-5 * sum_k |W_ik x_k| + 1e-6 (fp32 accumulation)
 TOL_ABS = 1e-6
-# Q4_0, Q8_0 and Q4_K integer dot products truncate each x to 24 bits relative to the
-# largest |x| of its 16-element unit (a subset of its 32-element block): less than
-# 2^-22 * max_block |x| per weight magnitude (for Q4_K, per |d sc q| <= |d sc q| + |dmin m|).
-INT_DOT_REL = 2.0 ** -22
 
 
 def dev_tensor(a, device="cuda"):
@@ -20,17 +16,20 @@ def dev_tensor(a, device="cuda"):
 
 
 def gemv_bound(raw, wt, x, M, K, rows=None, x_err=None):
-    """Per-element tolerance [ncols, rows]: the literal bound, plus the propagated
-    error of an on-chip prologue (x_err: per-element bound on |x' - x'_exact|)."""
+    """Per-element tolerance [ncols, rows]: the literal bound, for every weight format,
+    plus the propagated error of an on-chip prologue (x_err: per-element bound on
+    |x' - x'_exact|)."""
     b = TOL_REL * ogemv.abs_dot(raw, wt, x, M, K, rows) + TOL_ABS
     if x_err is not None:
         b = b + ogemv.abs_w_dot(raw, wt, x_err, M, K, rows)
-    if wt in (2, 3, 4):  # Q8_0, Q4_0, Q4_K
-        xa = np.abs(np.asarray(x, dtype=np.float64))
-        if x_err is not None:
-            xa = xa + np.asarray(x_err, dtype=np.float64).reshape(xa.shape)
-        b = b + INT_DOT_REL * ogemv.block_max_dot(raw, wt, xa, M, K, rows)
     return b
+
+
+def int_rounding_scale(raw, wt, x, M, K, rows=None):
+    """sum over 32-element blocks of max_block |x| * sum_block |w|: the scale of the error
+    the integer dot products would make if they rounded every x of a block relative to
+    its largest |x| (2^-23 of this).  Reported next to the gate, never added to it."""
+    return ogemv.block_max_dot(raw, wt, np.abs(np.asarray(x, dtype=np.float64)), M, K, rows)
 
 
 def fwht_err_bound(x, block):

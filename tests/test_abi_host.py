@@ -27,8 +27,7 @@ def test_header_declares_the_abi():
     assert {"gemv_fused", "gemv_fused_ex", "gemv_glu", "fwht_signed", "gf_elementwise", "gf_dequantize",
             "gf_plan", "gf_plan_glu", "gf_device_status", "gf_status_string", "gf_last_cuda_error",
             "gf_version", "gf_prepare", "gf_prepare_glu", "gf_launch_prepared", "gf_free_prepared",
-            "gf_graph_create", "gf_graph_launch", "gf_graph_free", "gemv_multi", "gf_prepare_multi",
-            "gf_prepare_chain", "gf_chain_info"} <= names
+            "gf_graph_create", "gf_graph_launch", "gf_graph_free", "gemv_multi", "gf_prepare_multi"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -362,21 +361,6 @@ def test_launch_prepared_arguments(lib):
     assert lib.raw.gf_launch_prepared(None, 1, None) == lib.ERR_INVALID
     assert lib.raw.gf_launch_prepared(arr, -1, None) == lib.ERR_INVALID
     lib.raw.gf_free_prepared(None)  # ignored
-
-
-def test_chain_arguments(lib):
-    h = ctypes.c_void_p(7)
-    none = (ctypes.c_void_p * 1)(None)
-    assert lib.raw.gf_prepare_chain(none, 1, None) == lib.ERR_INVALID
-    assert lib.raw.gf_prepare_chain(None, 1, ctypes.byref(h)) == lib.ERR_INVALID and not h.value
-    assert lib.raw.gf_prepare_chain(none, 0, ctypes.byref(h)) == lib.ERR_INVALID
-    assert lib.raw.gf_prepare_chain(none, 1, ctypes.byref(h)) == lib.ERR_INVALID  # a NULL handle
-    # more stages than a chain holds: refused before any handle is read
-    nine = (ctypes.c_void_p * 9)(*[ctypes.c_void_p(64 + i) for i in range(9)])
-    assert lib.raw.gf_prepare_chain(nine, 9, ctypes.byref(h)) == lib.ERR_UNSUPPORTED and not h.value
-    assert lib.CHAIN_MAX == 8
-    info = (ctypes.c_int64 * 8)()
-    assert lib.raw.gf_chain_info(None, ctypes.byref(info)) == lib.ERR_INVALID
 
 
 def test_graph_arguments(lib):

@@ -128,17 +128,15 @@ def test_glu_with_fwht_prologue_on_chip_and_workspace(G):
     assert_within(via_ws, want, bound, "glu + fwht workspace")
 
 
-def test_full_q4_0_ffn_gate_up_sampled_rows(G):
+def test_full_q4_0_ffn_gate_up_every_row(G):
     # the FFN gate/up pair of the Q4_0 decode layer (d_model 4096, ffn 14336) in one launch
     wt, M, K = synth.Q4_0, 14336, 4096
     rg, ru = synth.weights(wt, M, K, seed=270), synth.weights(wt, M, K, seed=271)
     X = synth.normal(K, seed=272).reshape(1, K)
     got, path, info = run_glu(G, rg, ru, wt, X, M, K, pdl=True)
     assert path == G.PATH_STREAM and info["grid"] == torch.cuda.get_device_properties(0).multi_processor_count
-    rng = np.random.default_rng(273)
-    rows = np.unique(np.concatenate([rng.choice(M, 600, replace=False), [0, 1, M - 2, M - 1]]))
-    want = ogemv.gemv_glu(rg, ru, wt, X, M, K, rows=rows)
-    assert_within(got[:, rows], want, glu_bound(rg, ru, wt, X, M, K, rows=rows), "full glu")
+    want = ogemv.gemv_glu(rg, ru, wt, X, M, K)
+    assert_within(got, want, glu_bound(rg, ru, wt, X, M, K), "full glu")
 
 
 # ----------------------------------------------------------------------------- RMS normalisation prologue

@@ -145,7 +145,7 @@ def test_q4_k_glu_and_rms_norm(G):
                   "q4_k rms")
 
 
-def test_q4_k_full_ffn_down_sampled_rows(G):
+def test_q4_k_full_ffn_down_every_row(G):
     # the FFN down projection of a decode layer in Q4_K: 4096 x 14336, residual add in place
     M, K = 4096, 14336
     raw = synth.weights(Q4K, M, K, seed=560)
@@ -153,6 +153,5 @@ def test_q4_k_full_ffn_down_sampled_rows(G):
     r = synth.normal(M, seed=562).reshape(1, M)
     got, path, _ = run(G, raw, X, M, K, ogemv.EPI_ADD, r, pdl=True)
     assert path == G.PATH_STREAM
-    rows = np.unique(np.concatenate([np.random.default_rng(563).choice(M, 500, replace=False), [0, M - 1]]))
-    want = ogemv.gemv(raw, Q4K, X, M, K, ogemv.EPI_ADD, r, rows=rows)
-    assert_within(got[:, rows], want, gemv_bound(raw, Q4K, X, M, K, rows=rows), "q4_k full down")
+    want = ogemv.gemv(raw, Q4K, X, M, K, ogemv.EPI_ADD, r)
+    assert_within(got, want, gemv_bound(raw, Q4K, X, M, K), "q4_k full down")

@@ -115,11 +115,10 @@ def test_tc_full_fwht_f16_5120_workspace(G, ncols):
     ws = torch.empty(ncols * K, device="cuda")
     got, _ = run(G, raw, X, M, K, ogemv.EPI_ADD, r, expect_path=G.PATH_TC, fwht_signs=dev_tensor(s), fwht_block=B,
                  fwht_workspace=ws, pdl=True)
-    rows = np.unique(np.concatenate([np.random.default_rng(754).choice(M, 400, replace=False), [0, M - 1]]))
     Xp = np.stack([ofwht.fwht_signed(X[c], s, B) for c in range(ncols)])
     E = np.stack([fwht_err_bound(X[c], B) for c in range(ncols)])
-    want = ogemv.gemv(raw, F16, Xp, M, K, ogemv.EPI_ADD, r, rows=rows)
-    assert_within(got[:, rows], want, gemv_bound(raw, F16, Xp, M, K, rows=rows, x_err=E), "tc fwht ws")
+    want = ogemv.gemv(raw, F16, Xp, M, K, ogemv.EPI_ADD, r)
+    assert_within(got, want, gemv_bound(raw, F16, Xp, M, K, x_err=E), "tc fwht ws")
 
 
 def test_tc_wide_batch_blocks_of_16(G):

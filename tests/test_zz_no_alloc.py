@@ -3,10 +3,13 @@
 Callers that cannot allocate a device workspace (a C host with no device allocator of
 its own, or a serving process whose device memory is fixed at start-up) use this entry
 point: the signed-FWHT prologue's scratch comes from a static device array inside the
-library.  The test calls it through the C ABI twice in a row, with different inputs, and
-checks each result against the existing entry point (gemv_fused_ex) within the parity
-tolerance the other GPU tests use.  It must pass on its own in a fresh process and after
-the rest of the suite, so it keeps no state between tests."""
+library.  Two calls are issued back to back on one stream, with different inputs and
+separate outputs and a single synchronisation after both (once without and once with
+programmatic dependent launch): each result is checked against the oracle (the GEMV of
+the oracle's signed FWHT of x, within the parity bound of the other tests) and bit for
+bit against gemv_fused_ex with a caller-allocated workspace, the path it runs.  The
+module is collected last and keeps no state between tests, so it passes alone in a
+fresh process and after the rest of the suite."""
 
 import numpy as np
 import pytest
@@ -30,43 +33,55 @@ def G(lib):
     assert lib.device_status() == 0
 
 
-def _tolerance(raw, wt, X, s, M, K, B):
-    """The parity bound of the other tests for a GEMV on the transformed input."""
+def _oracle(raw, wt, X, s, M, K, B, epi, aux):
+    """The oracle's result and the parity bound for a GEMV on the transformed input."""
     ncols = X.shape[0]
     Xp = np.stack([ofwht.fwht_signed(X[c], s, B) for c in range(ncols)])
     E = np.stack([fwht_err_bound(X[c], B) for c in range(ncols)])
-    return gemv_bound(raw, wt, Xp, M, K, x_err=E)
+    want = ogemv.gemv(raw, wt, Xp, M, K, epi, aux)
+    return want, gemv_bound(raw, wt, Xp, M, K, x_err=E)
 
 
+@pytest.mark.parametrize("pdl", [False, True])
 @pytest.mark.parametrize("wt,M,K,ncols,epi", [
     (synth.F16, 700, 5120, 3, ogemv.EPI_ADD),
     (synth.Q4_0, 333, 8192, 1, ogemv.EPI_SILU_MUL),
+    (synth.F16, 5120, 5120, 8, ogemv.EPI_ADD),
 ])
-def test_noalloc_matches_gemv_fused_ex_on_two_calls(G, wt, M, K, ncols, epi):
+def test_noalloc_two_calls_back_to_back(G, wt, M, K, ncols, epi, pdl):
     B = 1024
     raw = synth.weights(wt, M, K, seed=120)
     Wd = dev_tensor(raw)
     s = synth.rademacher(B, seed=121)
     sd = dev_tensor(s)
-    for call, seed in enumerate((130, 140)):  # two calls in a row, different inputs
+    st = torch.cuda.Stream()
+    calls = []
+    for seed in (130, 140):  # two calls, different inputs, separate outputs
         X = synth.normal(ncols * K, seed=seed).reshape(ncols, K)
         aux = synth.normal(ncols * M, seed=seed + 1).reshape(ncols, M)
         xd = dev_tensor(X.reshape(-1))
+        auxd = dev_tensor(aux.reshape(-1))
+        dst = auxd if epi == ogemv.EPI_ADD else torch.full((ncols * M,), float("nan"), device="cuda")
+        calls.append((X, aux, xd, auxd, dst))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        for (X, aux, xd, auxd, dst) in calls:
+            assert G.gemv_fused_fwht_noalloc(Wd, wt, xd, M, K, epi, auxd, dst, ncols, sd, B, pdl=pdl,
+                                             stream=st) == G.OK
+    st.synchronize()
+    for i, (X, aux, xd, auxd, dst) in enumerate(calls):
+        got = dst.cpu().numpy().astype(np.float64).reshape(ncols, M)
+        assert np.all(np.isfinite(got)), "call %d left outputs unwritten" % i
+        want, bound = _oracle(raw, wt, X, s, M, K, B, epi, aux)
+        assert_within(got, want, bound, "no-alloc call %d" % i)
+        # the path it reduces to: a caller-allocated workspace, the same kernels
         ref_aux = dev_tensor(aux.reshape(-1))
-        new_aux = dev_tensor(aux.reshape(-1))
-        if epi == ogemv.EPI_ADD:  # residual add in place: dst is the aux buffer
-            ref_dst, new_dst = ref_aux, new_aux
-        else:
-            ref_dst = torch.full((ncols * M,), float("nan"), device="cuda")
-            new_dst = torch.full((ncols * M,), float("nan"), device="cuda")
-        G.gemv_fused_ex(Wd, wt, xd, M, K, epi, ref_aux, ref_dst, ncols=ncols, fwht_signs=sd, fwht_block=B)
-        st = G.gemv_fused_fwht_noalloc(Wd, wt, xd, M, K, epi, new_aux, new_dst, ncols, sd, B)
-        assert st == G.OK
+        ref_dst = ref_aux if epi == ogemv.EPI_ADD else torch.full((ncols * M,), float("nan"), device="cuda")
+        ws = torch.empty(ncols * K, device="cuda")
+        G.gemv_fused_ex(Wd, wt, xd, M, K, epi, ref_aux, ref_dst, ncols=ncols, fwht_signs=sd, fwht_block=B,
+                        fwht_workspace=ws)
         torch.cuda.synchronize()
-        ref = ref_dst.cpu().numpy().astype(np.float64).reshape(ncols, M)
-        got = new_dst.cpu().numpy().astype(np.float64).reshape(ncols, M)
-        assert np.all(np.isfinite(got)), "call %d left outputs unwritten" % call
-        assert_within(got, ref, _tolerance(raw, wt, X, s, M, K, B), "no-alloc call %d" % call)
+        assert torch.equal(dst.view(torch.int32), ref_dst.view(torch.int32)), "call %d differs from the workspace path" % i
 
 
 def test_noalloc_rejects_oversize_and_missing_signs(G):
