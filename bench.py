@@ -132,7 +132,12 @@ class Step:
         # chain
         self.cx = up(synth.normal(4096, seed=seed0 + 6))
         self.ca = up(synth.normal(4096, seed=seed0 + 7))
-        self.cr = up(synth.normal(4096, seed=seed0 + 8))
+        # the layer's residual: the o-proj add reads r0 (N(0,1), as the workload draws it) and
+        # writes r, which gate/up read and down adds to in place; so every step starts from
+        # the same distribution instead of feeding its output back (which would grow
+        # without bound and end in Inf/NaN after a few steps)
+        self.cr0 = up(synth.normal(4096, seed=seed0 + 8))
+        self.cr = self.cr0.clone()
         self.cq, self.ck, self.cv = (torch.empty(4096, device=dev) for _ in range(3))
         self.cup = torch.empty(14336, device=dev)
         self.cg = torch.empty(14336, device=dev)
@@ -187,7 +192,7 @@ class Step:
             ("chain_q", (W["chain_q"], 3, self.cx, 4096, 4096, 0, None, self.cq), {}),
             ("chain_k", (W["chain_k"], 3, self.cx, 4096, 4096, 0, None, self.ck), {}),
             ("chain_v", (W["chain_v"], 3, self.cx, 4096, 4096, 0, None, self.cv), {}),
-            ("chain_o_add", (W["chain_o_add"], 3, self.ca, 4096, 4096, 4, self.cr, self.cr), {}),
+            ("chain_o_add", (W["chain_o_add"], 3, self.ca, 4096, 4096, 4, self.cr0, self.cr), {}),
             ("chain_up", (W["chain_up"], 3, self.cr, 14336, 4096, 0, None, self.cup), {}),
             ("chain_gate_silu_mul", (W["chain_gate_silu_mul"], 3, self.cr, 14336, 4096, 3, self.cup, self.cg), {}),
             ("chain_down_add", (W["chain_down_add"], 3, self.cg, 4096, 14336, 4, self.cr, self.cr), {}),
@@ -216,7 +221,7 @@ class Step:
             return fn(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, self.cr, f, d, self.cg, pdl=pdl, split_k=False)
         fn = G.prepare if prepare else G.gemv_fused_ex
         if unit == "layer_o_add":
-            return fn(Wl["chain_o_add"], 3, self.ca, d, d, 4, self.cr, self.cr, pdl=pdl, split_k=False)
+            return fn(Wl["chain_o_add"], 3, self.ca, d, d, 4, self.cr0, self.cr, pdl=pdl, split_k=False)
         return fn(Wl["chain_down_add"], 3, self.cg, d, f, 4, self.cr, self.cr, pdl=pdl, split_k=False)
 
     def prepared(self, pdl=True):
@@ -240,7 +245,7 @@ class Step:
         torch = self.torch
         res_only = ["sig_out", "gate_out", "cq", "ck", "cv", "cbeta"]
         inplace = ["r4096", "cr", "fr1", "fr8"]
-        inputs = ["x4096", "xsig", "xq8", "m", "cx", "ca", "fx1", "fx8"]
+        inputs = ["x4096", "xsig", "xq8", "m", "cx", "ca", "cr0", "fx1", "fx8"]
         names = res_only + inplace + inputs
         sizes = [getattr(self, n).numel() for n in names]
         total = sum(sizes)
@@ -630,7 +635,7 @@ def chain_measure(G, torch, step, s, args):
     names = ["chain_q", "chain_k", "chain_v", "chain_o_add", "chain_up", "chain_gate_silu_mul",
              "chain_down_add", "chain_beta_sigmoid"]
     layers = [{n: step.W[n] for n in names}, second_layer(torch, step)]
-    x, a, r = step.cx, step.ca, step.cr
+    x, a, r, r0 = step.cx, step.ca, step.cr, step.cr0
     q, k, v, u, g, beta = step.cq, step.ck, step.cv, step.cup, step.cg, step.cbeta
     y4 = torch.empty(4096, device=dev)
     y14 = torch.empty(14336, device=dev)
@@ -639,7 +644,7 @@ def chain_measure(G, torch, step, s, args):
         G.gemv_fused_ex(Wl["chain_q"], 3, x, 4096, 4096, 0, None, q, pdl=True)
         G.gemv_fused_ex(Wl["chain_k"], 3, x, 4096, 4096, 0, None, k, pdl=True)
         G.gemv_fused_ex(Wl["chain_v"], 3, x, 4096, 4096, 0, None, v, pdl=True)
-        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r0, r, pdl=True)
         G.gemv_fused_ex(Wl["chain_up"], 3, r, 14336, 4096, 0, None, u, pdl=True)
         G.gemv_fused_ex(Wl["chain_gate_silu_mul"], 3, r, 14336, 4096, 3, u, g, pdl=True)
         G.gemv_fused_ex(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True)
@@ -650,7 +655,7 @@ def chain_measure(G, torch, step, s, args):
         G.gemv_fused(Wl["chain_k"], 3, x, 4096, 4096, 0, None, k)
         G.gemv_fused(Wl["chain_v"], 3, x, 4096, 4096, 0, None, v)
         G.gemv_fused(Wl["chain_o_add"], 3, a, 4096, 4096, 0, None, y4)
-        G.elementwise(G.EW_ADD, y4, r, r, 4096)
+        G.elementwise(G.EW_ADD, y4, r0, r, 4096)
         G.gemv_fused(Wl["chain_up"], 3, r, 14336, 4096, 0, None, u)
         G.gemv_fused(Wl["chain_gate_silu_mul"], 3, r, 14336, 4096, 0, None, y14)
         G.elementwise(G.EW_SILU, y14, None, y14, 14336)
@@ -735,7 +740,7 @@ def next_rows_measure(G, torch, step, s, args, peak):
              "chain_down_add", "chain_beta_sigmoid"]
     shapes = {n: (M, K) for (n, wt, M, K, e, nc, fw) in step_spec() if n in names}
     layers = [{n: step.W[n] for n in names}, second_layer(torch, step)]
-    x, a, r = step.cx, step.ca, step.cr
+    x, a, r, r0 = step.cx, step.ca, step.cr, step.cr0
     q, k, v, g, beta = step.cq, step.ck, step.cv, step.cg, step.cbeta
 
     def glu_layer(i):
@@ -743,7 +748,7 @@ def next_rows_measure(G, torch, step, s, args, peak):
         G.gemv_fused_ex(Wl["chain_q"], 3, x, 4096, 4096, 0, None, q, pdl=True)
         G.gemv_fused_ex(Wl["chain_k"], 3, x, 4096, 4096, 0, None, k, pdl=True)
         G.gemv_fused_ex(Wl["chain_v"], 3, x, 4096, 4096, 0, None, v, pdl=True)
-        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r0, r, pdl=True)
         G.gemv_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, r, 14336, 4096, g, pdl=True)
         G.gemv_fused_ex(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True)
         G.gemv_fused_ex(Wl["chain_beta_sigmoid"], 3, x, 32, 4096, 1, None, beta, pdl=True)
@@ -762,7 +767,7 @@ def next_rows_measure(G, torch, step, s, args, peak):
     def qkv_layer(i):
         Wl = layers[i]
         G.gemv_fused_ex(qkv[i], 3, x, 3 * 4096, 4096, 0, None, qkv_out, pdl=True)
-        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r0, r, pdl=True)
         G.gemv_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, r, 14336, 4096, g, pdl=True)
         G.gemv_fused_ex(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True)
         G.gemv_fused_ex(Wl["chain_beta_sigmoid"], 3, x, 32, 4096, 1, None, beta, pdl=True)
@@ -780,7 +785,7 @@ def next_rows_measure(G, torch, step, s, args, peak):
         G.gemv_multi([(Wl["chain_q"], 4096, 0, None, q), (Wl["chain_k"], 4096, 0, None, k),
                       (Wl["chain_v"], 4096, 0, None, v), (Wl["chain_beta_sigmoid"], 32, 1, None, beta)],
                      3, x, 4096, pdl=True)
-        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 3, a, 4096, 4096, 4, r0, r, pdl=True)
         G.gemv_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 3, r, 14336, 4096, g, pdl=True)
         G.gemv_fused_ex(Wl["chain_down_add"], 3, g, 4096, 14336, 4, r, r, pdl=True)
 
@@ -799,7 +804,7 @@ def next_rows_measure(G, torch, step, s, args, peak):
         G.gemv_fused_ex(Wl["chain_q"], 4, x, 4096, 4096, 0, None, q, pdl=True)
         G.gemv_fused_ex(Wl["chain_k"], 4, x, 4096, 4096, 0, None, k, pdl=True)
         G.gemv_fused_ex(Wl["chain_v"], 4, x, 4096, 4096, 0, None, v, pdl=True)
-        G.gemv_fused_ex(Wl["chain_o_add"], 4, a, 4096, 4096, 4, r, r, pdl=True)
+        G.gemv_fused_ex(Wl["chain_o_add"], 4, a, 4096, 4096, 4, r0, r, pdl=True)
         if glu:
             G.gemv_glu(Wl["chain_gate_silu_mul"], Wl["chain_up"], 4, r, 14336, 4096, g, pdl=True)
         else:

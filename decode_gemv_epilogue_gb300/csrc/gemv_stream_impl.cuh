@@ -194,36 +194,6 @@ __device__ __forceinline__ void consume_tile_q4k(uint32_t st, int seg, int rows,
   }
 }
 
-// The fp32 products of a Q4_K chunk that the integer path cannot carry, for unit n (0 or
-// 1) of the thread's pair only, with that unit's x (one column), so that only one unit's
-// x is held in registers.  Each weight d*sc[j]*q - dmin*m[j] is formed first (both terms
-// are exact in fp32, one rounding for the difference), so a zero weight stays zero and
-// an infinite x gives the infinity or NaN of the definition.
-template <int RT>
-__device__ __forceinline__ void consume_tile_q4k_unit(uint32_t st, int seg, int rows, int units, int tg, int g,
-                                                      int G, int n, const float2 (&xn)[8], float2 (&acc)[RT][1]) {
-  if (2 * tg >= units) return;
-#pragma unroll 1
-  for (int j = 0; j < RT; ++j) {
-    const int r = g + j * G;
-    if (r < rows) {
-      const SmemLoader ld{st + static_cast<uint32_t>(r * seg)};
-      float dsc[2], dmn[2];
-      const uint4 q = q4k_load_pair(ld, static_cast<uint32_t>(tg), dsc, dmn);
-      float2 v[8];
-      q4k_nibbles(q, static_cast<uint32_t>(n), v);
-      const float ds = n ? dsc[1] : dsc[0], dm = n ? dmn[1] : dmn[0];
-      float2 p0 = acc[j][0], p1 = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int k = 0; k < 8; k += 2) {
-        p0 = ffma2(ffma2(make_float2(ds, ds), v[k], make_float2(-dm, -dm)), xn[k], p0);
-        p1 = ffma2(ffma2(make_float2(ds, ds), v[k + 1], make_float2(-dm, -dm)), xn[k + 1], p1);
-      }
-      acc[j][0] = fadd2(p0, p1);
-    }
-  }
-}
-
 // Q4_K through integer dot products: per row, one 16-byte code load and one unpack of the
 // scales for the thread's unit pair; each unit's nibbles against its XInt, scaled by
 // d * sc[j] * 2^-s, and the min term through the unit's sum of x.  Every row's loads
@@ -364,6 +334,107 @@ __device__ __forceinline__ void cta_rows(const StreamArgs& a, int rg, int64_t& r
   nrows = static_cast<int>(max(n, static_cast<int64_t>(0)));
 }
 
+// A consumer warp's walk over the tiles of one K chunk: wait for each stage, let
+// `consume` add the warp's products into its per-row partial sums, release the stage,
+// reduce the sums over the warp and store them to `red` (the first K chunk of the CTA
+// stores, later ones add).  The ring position and the status carry over between chunks.
+struct TileWalk {
+  uint32_t ring, full0, empty0;
+  float* red;
+  volatile int* abort_flag;
+  unsigned* err;
+  int stage_bytes, NS, R, G, wpc;
+  int nvr;    // virtual rows of the row chunk
+  bool first; // the CTA's first K chunk
+  int g, c0, wc, lane;
+  int slot;
+  uint32_t fphase;
+  bool ok;
+};
+
+template <int NC, int NCT, int RT, class F>
+__device__ __forceinline__ void walk_tiles(TileWalk& w, F&& consume) {
+  for (int t0 = 0; t0 < w.nvr; t0 += w.R) {
+    const int rows = min(w.R, w.nvr - t0);
+    w.ok = w.ok && mbar_wait_or_abort(w.full0 + 8u * w.slot, w.fphase, w.abort_flag, w.err);
+    float2 acc[RT][NCT];
+#pragma unroll
+    for (int j = 0; j < RT; ++j)
+#pragma unroll
+      for (int c = 0; c < NCT; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
+    if (w.ok) consume(w.ring + static_cast<uint32_t>(w.slot) * w.stage_bytes, rows, acc);
+    __syncwarp();
+    if (w.lane == 0) mbar_arrive(w.empty0 + 8u * w.slot);
+    if (++w.slot == w.NS) {
+      w.slot = 0;
+      w.fphase ^= 1u;
+    }
+    // warp reduction of the RT*NCT partial sums (padded to a power of two)
+    constexpr int V = RT * NCT;
+    constexpr int VP = V > 16 ? 32 : V > 8 ? 16 : V > 4 ? 8 : V > 2 ? 4 : V > 1 ? 2 : 1;
+    float vals[VP];
+#pragma unroll
+    for (int j = 0; j < VP; ++j) vals[j] = j < V ? acc[j / NCT][j % NCT].x + acc[j / NCT][j % NCT].y : 0.0f;
+    const float sum = WarpVecReduce<VP>::run(vals, w.lane);
+    const int jv = w.lane >> (5 - WarpVecReduce<VP>::kLog);
+    if (w.lane == WarpVecReduce<VP>::owner(jv) && jv < V) {
+      const int r = w.g + (jv / NCT) * w.G, c = w.c0 + jv % NCT;
+      if (r < rows && c < NC) {
+        float* p = w.red + ((t0 + r) * w.wpc + w.wc) * NC + c;
+        *p = w.first ? sum : (*p + sum);
+      }
+    }
+  }
+}
+
+// fp32 dot product of one row's K chunk (weights from global memory through the
+// 16-bit-load decoders, x from where the chunk lives) over the 32 lanes of a warp: the
+// repair of rows whose x the integer path cannot carry.  Single column.  Every lane gets
+// the sum.  IEEE semantics throughout (an infinite x gives the definition's Inf or NaN).
+template <int WT, bool GAMMA>
+__device__ __forceinline__ float repair_dot(const uint8_t* rowp, int units, const float* xsrc, int64_t xstride,
+                                            const float* gsrc, bool norm, int lane) {
+  const GmemLoader ld{rowp};
+  float s = 0.0f;
+  auto load_x = [&](int u, float2 (&xv)[1][8]) {
+    if (norm)
+      load_unit_x<WT, 1, GAMMA>(xsrc, xstride, gsrc, u, 0u, 0, 1, xv);
+    else
+      load_unit_x<WT, 1, false>(xsrc, xstride, nullptr, u, 0u, 0, 1, xv);
+  };
+  if constexpr (WT == WT_Q4_K) {
+    for (int p = lane; 2 * p < units; p += 32) {
+      float dsc[2], dmn[2];
+      const uint4 q = q4k_load_pair(ld, static_cast<uint32_t>(p), dsc, dmn);
+#pragma unroll 1
+      for (int n = 0; n < 2; ++n) {
+        float2 v[8], xv[1][8];
+        q4k_nibbles(q, static_cast<uint32_t>(n), v);
+        load_x(2 * p + n, xv);
+        float2 t = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // the weight d*sc*q - dmin*m first, then its product
+          t = ffma2(ffma2(make_float2(dsc[n], dsc[n]), v[k], make_float2(-dmn[n], -dmn[n])), xv[0][k], t);
+        s += t.x + t.y;
+      }
+    }
+  } else {
+    for (int u = lane; u < units; u += 32) {
+      float2 v[8], xv[1][8];
+      float d;
+      decode_unit<WT>(ld, static_cast<uint32_t>(u), v, d);
+      load_x(u, xv);
+      float2 t = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t = ffma2(v[k], xv[0][k], t);
+      s = fmaf(d, t.x + t.y, s);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  return s;
+}
+
 template <int WT, int NC, int FEAT>
 __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
     gemv_stream_kernel(const __grid_constant__ StreamArgs a) {
@@ -389,6 +460,8 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
   float* xch = reinterpret_cast<float*>(smem + a.off_xchg);    // split K: [S][NC][XR], then [S][NC]
   const uint32_t ring = sbase + static_cast<uint32_t>(a.off_ring);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarBytes - 8);
+  // integer path: some unit of x cannot be carried (its rows are recomputed in fp32)
+  volatile int* xflag = reinterpret_cast<volatile int*>(smem + kBarBytes - 16);
 
   const int S = kSplit ? a.S : 1;
   int crank = 0;
@@ -397,6 +470,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    *xflag = 0;
     for (int i = 0; i < a.NS; ++i) {
       mbar_init(full0 + 8u * i, 1);
       mbar_init(empty0 + 8u * i, static_cast<uint32_t>(a.ncw));
@@ -541,6 +615,68 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
       const int64_t mi = a.seg_end[i] - (i ? a.seg_end[i - 1] : 0);
       return a.seg_aux[i][c * mi + local];
     };
+    // Repair (integer path): when some unit of x could not be carried (xflag), the sums
+    // of the row chunk starting at global row rb are recomputed in fp32 -- a warp per
+    // virtual row, every K chunk of the row, x' rebuilt in shared memory chunk by chunk
+    // with the on-chip prologue -- and stored where the finalisation reads them: red
+    // (warp slot 0) or, with split K, slice 0 of rank 0's exchange buffer.  Every
+    // consumer thread takes every barrier; after an abort the work is skipped.
+    auto repair = [&](int64_t rb, int nrc_, int nvr_) {
+      if constexpr (kInt) {
+        if constexpr (kSplit) {
+          for (int i = ctid; i < S * NC * XR; i += nt) xch[i] = 0.0f;
+        } else {
+          for (int i = ctid; i < nvr_ * a.wpc * NC; i += nt) red[i] = 0.0f;
+        }
+        cbar();
+        const int H = a.R / 2;
+        for (int kc2 = 0; kc2 < a.n_kc; ++kc2) {
+          const int klen2 = min(a.kc_len, a.K - kc2 * a.kc_len);
+          const float* xsrc2;
+          int64_t xstride2;
+          if (a.fwht_B > 0) {
+            for (int i = ctid; i < NC * klen2; i += nt) {
+              const int c = i / klen2, e = i - c * klen2;
+              xs[i] = a.x[static_cast<int64_t>(c) * a.K + static_cast<int64_t>(kc2) * a.kc_len + e];
+            }
+            cbar();
+            fwht_smem(xs, NC * klen2, a.fwht_B, klen2, static_cast<int64_t>(kc2) * a.kc_len, a.signs, a.nsigns,
+                      a.fwht_scale, ctid, nt, cbar);
+            xsrc2 = xs;
+            xstride2 = klen2;
+          } else if (a.stage_x) {
+            xsrc2 = xs;
+            xstride2 = a.K;
+          } else {
+            xsrc2 = a.x + static_cast<int64_t>(kc2) * a.kc_len;
+            xstride2 = a.K;
+          }
+          const float* gsrc2 = !norm ? nullptr
+                               : a.stage_x ? xs + NC * a.K
+                                           : a.gamma + static_cast<int64_t>(kc2) * a.kc_len;
+          const int64_t segoff = seg_bytes_of<WT>(kc2 * a.kc_len);
+          for (int v = cw; v < nvr_ && !*abort_flag; v += a.ncw) {
+            const uint8_t* rowp;
+            if (dual) {  // tile t: gate rows t*H .. t*H+ht-1, then the same up rows
+              const int t = v / a.R, l = v - t * a.R, ht = min(H, nrc_ - t * H);
+              rowp = l < ht ? a.W + (rb + t * H + l) * a.row_bytes : a.W2 + (rb + t * H + l - ht) * a.row_bytes;
+            } else if (multi) {
+              int64_t local;
+              const int i = seg_of(a, rb + v, local);
+              rowp = a.seg_W[i] + local * a.row_bytes;
+            } else {
+              rowp = a.W + (rb + v) * a.row_bytes;
+            }
+            const float y = repair_dot<WT, kExt>(rowp + segoff, klen2 / kUnitElems, xsrc2, xstride2, gsrc2, norm, lane);
+            if (lane == 0) {
+              float* slot = kSplit ? xch + v : red + v * a.wpc * NC;
+              *slot += y;
+            }
+          }
+          cbar();  // the next chunk's x' overwrites xs
+        }
+      }
+    };
     bool x_loaded = false;
     float ssq[NCT];  // this thread's share of the sum of squares of x (first row chunk)
 #pragma unroll
@@ -594,7 +730,10 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
         float2 xr[kInt ? 1 : U][NCT][8];
         XInt xq[kInt ? U : 1][kInt ? NCT : 1];
         float xsum[U][NCT];
-        bool xbad = false;  // a unit of this thread the integer path cannot carry
+        // integer path: per unit, whether its own values allow it, its largest |x| and the
+        // sum of its 14 smaller |x| (see x_to_int)
+        bool xlocal[U];
+        float xmax[U], xrest[U];
 #pragma unroll
         for (int i = 0; i < U; ++i) {
           const int u = unit_index<WT, U>(tg, i, tg_n);
@@ -613,96 +752,51 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
                 xsum[i][c] = t.x + t.y;
               }
             }
-            if constexpr (kInt) {
-#pragma unroll
-              for (int c = 0; c < NCT; ++c) xbad = x_to_int(xv[c], xq[i][c]) || xbad;
-            }
+            if constexpr (kInt) xlocal[i] = x_to_int(xv[0], xq[i][0], xmax[i], xrest[i]);
           }
         }
-        // The chunk's tiles: wait for the stage, `consume` it into the per-row partial
-        // sums, release it, reduce the sums over the warp and store them.
-        auto tiles = [&](auto&& consume) {
-          for (int t0 = 0; t0 < nvr; t0 += a.R) {
-            const int rows = min(a.R, nvr - t0);
-            ok = ok && mbar_wait_or_abort(full0 + 8u * slot, fphase, abort_flag, a.err);
-            float2 acc[RT][NCT];
-#pragma unroll
-            for (int j = 0; j < RT; ++j)
-#pragma unroll
-              for (int c = 0; c < NCT; ++c) acc[j][c] = make_float2(0.0f, 0.0f);
-            if (ok) consume(ring + static_cast<uint32_t>(slot) * a.stage_bytes, rows, acc);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8u * slot);
-            if (++slot == a.NS) {
-              slot = 0;
-              fphase ^= 1u;
-            }
-            // warp reduction of the RT*NCT partial sums (padded to a power of two)
-            constexpr int V = RT * NCT;
-            constexpr int VP = V > 16 ? 32 : V > 8 ? 16 : V > 4 ? 8 : V > 2 ? 4 : V > 1 ? 2 : 1;
-            float vals[VP];
-#pragma unroll
-            for (int j = 0; j < VP; ++j)
-              vals[j] = j < V ? acc[j / NCT][j % NCT].x + acc[j / NCT][j % NCT].y : 0.0f;
-            const float sum = WarpVecReduce<VP>::run(vals, lane);
-            const int jv = lane >> (5 - WarpVecReduce<VP>::kLog);
-            if (lane == WarpVecReduce<VP>::owner(jv) && jv < V) {
-              const int r = g + (jv / NCT) * a.G, c = c0 + jv % NCT;
-              if (r < rows && c < NC) {
-                float* p = red + ((t0 + r) * a.wpc + wc) * NC + c;
-                *p = (kc == kc_lo) ? sum : (*p + sum);
-              }
-            }
-          }
-        };
+        TileWalk w{ring, full0, empty0, red, abort_flag, a.err, a.stage_bytes, a.NS, a.R, a.G, a.wpc,
+                   nvr, kc == kc_lo, g, c0, wc, lane, slot, fphase, ok};
         if constexpr (kInt) {
-          // A warp holding a unit that the integer path cannot carry (an outlier, a
-          // sparse unit, a NaN or an infinity) takes fp32 products for the whole chunk,
-          // on x reloaded as floats (it stays in shared or global memory for the chunk).
-          if (__any_sync(0xffffffffu, xbad)) {
-            auto load_xf = [&](int i, float2 (&xv)[NCT][8]) {
-              const int u = unit_index<WT, U>(tg, i, tg_n);
-              if (u < units) {
-                if (norm)
-                  load_unit_x<WT, NCT, kExt>(xsrc, xstride, gsrc, u, qr, c0, NC, xv);
-                else
-                  load_unit_x<WT, NCT, false>(xsrc, xstride, nullptr, u, qr, c0, NC, xv);
-              }
-            };
-            if constexpr (WT == WT_Q4_K) {
-              // one unit of the pair at a time, its x loaded per tile
-              tiles([&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
-#pragma unroll 1
-                for (int n = 0; n < 2; ++n) {
-                  float2 xv[NCT][8];
-                  load_xf(n, xv);
-                  consume_tile_q4k_unit<RT>(st, seg, rows, units, tg, g, a.G, n, xv[0], acc);
-                }
-              });
-            } else {
-              float2 xf[U][NCT][8];
+          // the warp's typical magnitude: the mean over its units of their trimmed means;
+          // a unit the integer path cannot carry sets xflag: the rows are recomputed in
+          // fp32 before the tails (the integer sums stay finite meanwhile)
+          float rsum = 0.0f, nun = 0.0f;
 #pragma unroll
-              for (int i = 0; i < U; ++i) load_xf(i, xf[i]);
-              tiles([&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
-                consume_tile<WT, NCT, U, RT, false>(st, seg, rows, units, tg, tg_n, g, a.G, qr, xf, acc);
-              });
+          for (int i = 0; i < U; ++i)
+            if (unit_index<WT, U>(tg, i, tg_n) < units) {
+              rsum += xrest[i];
+              nun += 14.0f;
             }
-          } else {
-            tiles([&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
-              if constexpr (WT == WT_Q4_K)
-                consume_tile_q4k_int<RT>(st, seg, rows, units, tg, g, a.G, xq, xsum, acc);
-              else
-                consume_tile_int<WT, NCT, U, RT>(st, seg, rows, units, tg, tg_n, g, a.G, xq, acc);
-            });
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+            rsum += __shfl_xor_sync(0xffffffffu, rsum, off);
+            nun += __shfl_xor_sync(0xffffffffu, nun, off);
           }
+          const float mu = rsum / fmaxf(nun, 1.0f);
+          bool xbad = false;
+#pragma unroll
+          for (int i = 0; i < U; ++i)
+            if (unit_index<WT, U>(tg, i, tg_n) < units && ok)
+              xbad = xbad || !(xlocal[i] || xmax[i] <= 256.0f * mu);
+          if (xbad) *xflag = 1;
+          walk_tiles<NC, NCT, RT>(w, [&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
+            if constexpr (WT == WT_Q4_K)
+              consume_tile_q4k_int<RT>(st, seg, rows, units, tg, g, a.G, xq, xsum, acc);
+            else
+              consume_tile_int<WT, NCT, U, RT>(st, seg, rows, units, tg, tg_n, g, a.G, xq, acc);
+          });
         } else {
-          tiles([&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
+          walk_tiles<NC, NCT, RT>(w, [&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
             if constexpr (WT == WT_Q4_K)
               consume_tile_q4k<NCT, RT>(st, seg, rows, units, tg, g, a.G, xr, xsum, acc);
             else
               consume_tile<WT, NCT, U, RT, kBatch>(st, seg, rows, units, tg, tg_n, g, a.G, qr, xr, acc);
           });
         }
+        slot = w.slot;
+        fphase = w.fphase;
+        ok = w.ok;
       }
       if (norm && rc0 == 0 && g == 0) {
         // sum of squares: row group 0's column groups saw every x value of this CTA's K
@@ -716,6 +810,9 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
         }
       }
       cbar();  // all partial sums of this row chunk are in `red` (and `normv`)
+      if constexpr (kInt && !kSplit) {
+        if (*xflag) repair(r0 + rc0, nrc, nvr);
+      }
       // sum of squares of column c over this CTA's K range, warps in order
       auto ssum = [&](int c) -> float {
         float t = 0.0f;
@@ -743,11 +840,17 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
           else
             st_cluster_f32(map_to_rank(smem_u32(slot), 0), t);
         }
+        if constexpr (kInt) {  // rank 0 repairs if any rank's x could not be carried
+          if (!finalizer && ctid == 0 && *xflag) st_cluster_u32(map_to_rank(smem_u32(const_cast<int*>(xflag)), 0), 1u);
+        }
         if (!finalizer)
           mbar_arrive_remote(map_to_rank(xchbar, 0));
         else
           ok = ok && mbar_wait_cluster_or_abort(xchbar, 0, abort_flag, a.err);
         cbar();  // rank 0: its own slice is complete too
+        if constexpr (kInt) {
+          if (finalizer && *xflag) repair(r0 + rc0, nrc, nvr);
+        }
       }
       if (ok && finalizer) {
         // sum of virtual row v for column c: the consumer warps' partials (one CTA),

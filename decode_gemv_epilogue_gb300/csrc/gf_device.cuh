@@ -122,6 +122,10 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
@@ -514,13 +518,23 @@ __device__ __forceinline__ void q4k_nibbles(const uint4 q, uint32_t n, float2 (&
 // -8 sum_j X_j (modulo 2^32; the result fits).  The block's d times 2^-s scales the
 // converted sum.  Rounding x * 2^s moves each x_j by at most 2^-s / 2 <= m * 2^-23.
 //
-// That absolute error is small next to |x_j| only for the unit's larger values, so a
-// unit takes the integer path only when at least half of its 16 values have magnitude
-// >= m / 16 (then every one of those is carried to 2^-19 relative, and the unit's
-// smaller values are at most as many as its larger ones), and all 16 are finite.  A
-// unit with an outlier (one or a few values far above the rest), a sparse unit, or a
-// NaN / Inf is flagged: the warp that holds it decodes its tiles to floats and takes
-// fp32 products instead (exact IEEE semantics for non-finite x).
+// That error is m * 2^-23 at most for every value of the unit: small next to the row's
+// products unless m stands far above the values around it.  A unit is carried by the
+// integer path when all 16 values are finite and
+//  - m <= 1024 * (mean |x| of its 14 values left after the two largest): each value moves
+//    by at most 1.2e-4 of that mean, even when the two largest carry zero weights; or
+//  - at most two values are non-zero and the second is within 2^7 of m (one-hot and
+//    two-hot units); or
+//  - m <= 256 * mu, mu the mean of that trimmed mean over the 32 units of the warp
+//    (512 values of x): the unit's rounding is then small next to the typical products of
+//    the row, however small its own other values are (a SwiGLU output, whose units often
+//    hold a few large values among near-zero ones, stays on the integer path).
+// The roundings of independent values add with random signs, so the error stays a few
+// thousandths of the tolerance on every input measured.  A unit failing all three (one
+// or two outliers far above everything near them, or a NaN / Inf) flags its CTA: the
+// CTA's rows are then recomputed in fp32 from the weights in global memory before the
+// tails (exact IEEE semantics for non-finite x).  That costs a second read of the
+// CTA's weights, so the rule is no stricter than the tolerance needs.
 struct XInt {
   uint32_t d2[4], d1[4], d0[4];  // digit bytes of the four element groups
   uint32_t c;                    // -8 * sum_j X_j (two's complement)
@@ -561,20 +575,24 @@ __device__ __forceinline__ void pack_digits(uint32_t a, uint32_t b, uint32_t c, 
 // x of one unit (eight pairs in decode_unit()'s pair order: pairs 2g and 2g+1 form group
 // g) -> XInt.  The exponent is kept in [-126, 126] so that 2^s and 2^-s are normal
 // floats; below |x| = 2^-103 the integers get shorter (absolute error under 2^-126).
-// Returns true when the unit must not take the integer path (see above): fewer than 8
-// of its values reach m / 16, or one of them is NaN or infinite.
-__device__ __forceinline__ bool x_to_int(const float2 (&xv)[8], XInt& xi) {
-  float m = 0.0f;
-  float2 z = make_float2(0.0f, 0.0f);  // stays 0 unless some x is NaN or infinite (x * 0)
+// Returns whether the unit's own values allow the integer path (the first two rules
+// above); m gets the unit's largest |x| and rest the sum of |x| over its 14 smaller
+// values (NaN or Inf when a value is not finite; the third rule needs the warp's rests).
+__device__ __forceinline__ bool x_to_int(const float2 (&xv)[8], XInt& xi, float& m_out, float& rest_out) {
+  float m = 0.0f, m2 = 0.0f, sa = 0.0f;  // largest and second largest |x|, sum of |x|
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    m = fmaxf(m, fmaxf(fabsf(xv[k].x), fabsf(xv[k].y)));
-    z = ffma2(xv[k], make_float2(0.0f, 0.0f), z);
+    const float a = fabsf(xv[k].x), b = fabsf(xv[k].y);
+    sa += a + b;
+    m2 = fmaxf(m2, fmaxf(fminf(m, a), fminf(fmaxf(m, a), b)));
+    m = fmaxf(m, fmaxf(a, b));
   }
-  const float thr = m * 0.0625f;  // exact: a power of two (m = 0: every value counts)
-  int nbig = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) nbig += (fabsf(xv[k].x) >= thr ? 1 : 0) + (fabsf(xv[k].y) >= thr ? 1 : 0);
+  // both false for NaN or Inf (sa is then NaN or Inf, and the rest NaN); true for zeros
+  const float rest = sa - m - m2;  // |x| of the other 14 values (0 up to rounding: sparse)
+  const bool dense = m * 14.0f <= 1024.0f * rest ||
+                     (rest <= m * 0x1p-20f && (m2 == 0.0f || m <= 128.0f * m2));
+  m_out = m;
+  rest_out = rest;
   // m = f * 2^E with f in [0.5, 1): E = biased exponent - 126 (m = 0: any s works); one
   // less when f = 1 - 2^-24, whose m * 2^(23 - E) would round to 2^23
   const uint32_t mb = __float_as_uint(m);
@@ -592,7 +610,7 @@ __device__ __forceinline__ bool x_to_int(const float2 (&xv)[8], XInt& xi) {
                 static_cast<uint32_t>(X3), xi.d2[g], xi.d1[g], xi.d0[g]);
   }
   xi.c = static_cast<uint32_t>(-8 * sum);
-  return nbig < 8 || !(z.x == 0.0f && z.y == 0.0f);
+  return dense;
 }
 
 // Four registers of unsigned codes (byte k of n[g] is element 4g + k) against the XInt of

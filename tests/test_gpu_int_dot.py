@@ -95,7 +95,9 @@ def x_case(name, K, seed):
     return x.astype(np.float32)
 
 
-FINITE_CASES = ["zeros", "scale_3e4", "scale_1e-20", "mixed_1e3_1e-3", "spike_1e4", "spike_1e6",
+# spike_3e2 stays on the integer path (its spikes are below 1024 times the mean of their
+# units' other values); the larger spikes send their units to the fp32 products
+FINITE_CASES = ["zeros", "scale_3e4", "scale_1e-20", "mixed_1e3_1e-3", "spike_3e2", "spike_1e4", "spike_1e6",
                 "heavy_tail", "sparse"]
 
 
@@ -296,3 +298,59 @@ def test_rms_prologue_with_spike(G, fmt):
     # the literal bound on x', plus the kernel's own 1/rms (under 2e-6 relative)
     bound = literal_bound(raw, wt, xn, M, K)[0] + 2e-6 * ogemv.abs_dot(raw, wt, xn, M, K)[0]
     assert_within(got, want, bound, "rms %s spike" % fmt)
+
+
+# ----------------------------------------------------------------------------- on-chip FWHT prologue
+
+@pytest.mark.parametrize("M,K", [(512, 5120), (300, 32768), (8, 32768)])
+@pytest.mark.parametrize("bad", ["nan", "inf"])
+def test_fwht_prologue_non_finite(G, M, K, bad):
+    """Signed FWHT(1024) on chip ahead of a Q4_0 GEMV: one K chunk, several chunks, and
+    split K (8 rows).  A non-finite x spreads over its whole transform block, so the rows
+    are recomputed with x' rebuilt chunk by chunk; the non-finite pattern must match."""
+    B = 1024
+    wt = synth.Q4_0
+    raw = synth.weights(wt, M, K, seed=570)
+    x = x_case("heavy_tail", K, seed=571)
+    x[K - 700] = np.nan if bad == "nan" else np.inf
+    s = synth.rademacher(B, seed=572)
+    xd, sd = dev_tensor(x), dev_tensor(s)
+    dst = torch.full((M,), 7.0, device="cuda")
+    G.gemv_fused_ex(dev_tensor(raw), wt, xd, M, K, NONE, None, dst, fwht_signs=sd, fwht_block=B)
+    torch.cuda.synchronize()
+    got = dst.cpu().numpy().astype(np.float64)
+    from oracle import fwht as ofwht
+    with np.errstate(invalid="ignore", over="ignore"):
+        xp = ofwht.fwht_signed(x, s, B)
+        want = ogemv.gemv(raw, wt, xp, M, K)[0]
+    assert_classes(got, want, "fwht %s %dx%d" % (bad, M, K))
+
+
+@pytest.mark.parametrize("M,K", [(512, 5120), (300, 32768), (8, 32768)])
+def test_fwht_prologue_after_repair_matches_oracle(G, M, K):
+    """Finite x whose transform holds an outlier unit: x is chosen so that one 1024-block
+    of x' = H (s x) / 32 is a single spike (x = the block's inverse transform of a
+    one-hot, times 1e6) on top of N(0,1) elsewhere; the spike's column has zero weights.
+    Its unit is repaired in fp32; every row within the literal bound on x'."""
+    B = 1024
+    wt = synth.Q4_0
+    col = 1024 + 37
+    raw = zero_weight_columns(synth.weights(wt, M, K, seed=580), wt, M, K, (col,))
+    s = synth.rademacher(B, seed=581)
+    from oracle import fwht as ofwht
+    target = x_case("heavy_tail", K, seed=582).astype(np.float64)
+    target[col] = 1e6
+    # x with fwht_signed(x) == target: the normalised transform is its own inverse, then undo the signs
+    blocks = target.reshape(-1, B)
+    x = np.concatenate([ofwht.fwht_signed(b, np.ones(B), B) * s for b in blocks]).astype(np.float32)
+    xp = ofwht.fwht_signed(x, s, B)
+    dst = torch.full((M,), 7.0, device="cuda")
+    G.gemv_fused_ex(dev_tensor(raw), wt, dev_tensor(x), M, K, NONE, None, dst, fwht_signs=dev_tensor(s),
+                    fwht_block=B)
+    torch.cuda.synchronize()
+    got = dst.cpu().numpy().astype(np.float64)
+    want = ogemv.gemv(raw, wt, xp, M, K)[0]
+    from gpu_util import fwht_err_bound
+    E = fwht_err_bound(x, B).reshape(1, K)
+    bound = literal_bound(raw, wt, xp, M, K)[0] + ogemv.abs_w_dot(raw, wt, E, M, K)[0]
+    assert_within(got, want, bound, "fwht repaired %dx%d" % (M, K))
