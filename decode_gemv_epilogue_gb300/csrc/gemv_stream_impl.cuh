@@ -758,27 +758,34 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
         TileWalk w{ring, full0, empty0, red, abort_flag, a.err, a.stage_bytes, a.NS, a.R, a.G, a.wpc,
                    nvr, kc == kc_lo, g, c0, wc, lane, slot, fphase, ok};
         if constexpr (kInt) {
-          // the warp's typical magnitude: the mean over its units of their trimmed means;
-          // a unit the integer path cannot carry sets xflag: the rows are recomputed in
-          // fp32 before the tails (the integer sums stay finite meanwhile)
-          float rsum = 0.0f, nun = 0.0f;
-#pragma unroll
-          for (int i = 0; i < U; ++i)
-            if (unit_index<WT, U>(tg, i, tg_n) < units) {
-              rsum += xrest[i];
-              nun += 14.0f;
-            }
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
-            rsum += __shfl_xor_sync(0xffffffffu, rsum, off);
-            nun += __shfl_xor_sync(0xffffffffu, nun, off);
-          }
-          const float mu = rsum / fmaxf(nun, 1.0f);
+          // a unit the integer path cannot carry sets xflag: the rows are recomputed in fp32
+          // before the tails (the integer sums stay finite meanwhile).  Units whose own
+          // values do not allow it are judged against the warp's typical magnitude: the
+          // mean of the units' trimmed means (a non-finite unit never passes).
           bool xbad = false;
+          bool lbad = false;
 #pragma unroll
           for (int i = 0; i < U; ++i)
-            if (unit_index<WT, U>(tg, i, tg_n) < units && ok)
-              xbad = xbad || !(xlocal[i] || xmax[i] <= 256.0f * mu);
+            if (unit_index<WT, U>(tg, i, tg_n) < units && ok) lbad = lbad || !xlocal[i];
+          if (__any_sync(0xffffffffu, lbad)) {
+            float rsum = 0.0f, nun = 0.0f;
+#pragma unroll
+            for (int i = 0; i < U; ++i)
+              if (unit_index<WT, U>(tg, i, tg_n) < units && ok) {
+                rsum += fmaxf(xrest[i], 0.0f);  // 0 for a non-finite unit
+                nun += 14.0f;
+              }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+              rsum += __shfl_xor_sync(0xffffffffu, rsum, off);
+              nun += __shfl_xor_sync(0xffffffffu, nun, off);
+            }
+            const float mu = rsum / fmaxf(nun, 1.0f);
+#pragma unroll
+            for (int i = 0; i < U; ++i)
+              if (unit_index<WT, U>(tg, i, tg_n) < units && ok)
+                xbad = xbad || !(xlocal[i] || (xmax[i] <= 256.0f * mu && xrest[i] == xrest[i]));
+          }
           if (xbad) *xflag = 1;
           walk_tiles<NC, NCT, RT>(w, [&](uint32_t st, int rows, float2 (&acc)[RT][NCT]) {
             if constexpr (WT == WT_Q4_K)

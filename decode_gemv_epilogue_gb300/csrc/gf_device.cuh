@@ -577,15 +577,16 @@ __device__ __forceinline__ void pack_digits(uint32_t a, uint32_t b, uint32_t c, 
 // floats; below |x| = 2^-103 the integers get shorter (absolute error under 2^-126).
 // Returns whether the unit's own values allow the integer path (the first two rules
 // above); m gets the unit's largest |x| and rest the sum of |x| over its 14 smaller
-// values (NaN or Inf when a value is not finite; the third rule needs the warp's rests).
+// values (NaN when a value is not finite).
 __device__ __forceinline__ bool x_to_int(const float2 (&xv)[8], XInt& xi, float& m_out, float& rest_out) {
   float m = 0.0f, m2 = 0.0f, sa = 0.0f;  // largest and second largest |x|, sum of |x|
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const float a = fabsf(xv[k].x), b = fabsf(xv[k].y);
+    const float hi = fmaxf(a, b), lo = fminf(a, b);
     sa += a + b;
-    m2 = fmaxf(m2, fmaxf(fminf(m, a), fminf(fmaxf(m, a), b)));
-    m = fmaxf(m, fmaxf(a, b));
+    m2 = fmaxf(fmaxf(m2, lo), fminf(m, hi));
+    m = fmaxf(m, hi);
   }
   // both false for NaN or Inf (sa is then NaN or Inf, and the rest NaN); true for zeros
   const float rest = sa - m - m2;  // |x| of the other 14 values (0 up to rounding: sparse)
