@@ -430,6 +430,7 @@ def gpu_arm(args, rank, world, local_rank):
             s.synchronize()
     # ---------------------------------------------------------------- timed region
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    G.repair_count(reset=True)  # (synchronises) counted over the timed steps only
     barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
@@ -446,6 +447,9 @@ def gpu_arm(args, rank, world, local_rank):
     ms_per_step = ms / args.steps
     value = whole_job_gbs(world, step.step_bytes, ms_per_step)
 
+    # row chunks the integer-path kernels handed to their fp32 repair during the timed steps
+    # (0 for the workload's inputs: a repair reads the chunk's weights twice)
+    step_repairs = G.repair_count(reset=True)
     # ---------------------------------------------------------------- per-kernel durations
     per_call = launch_durations(G, torch, step, s, args)
     nl = len(calls)
@@ -511,7 +515,7 @@ def gpu_arm(args, rank, world, local_rank):
         "us_per_layer_8_launches": chain["fused_us"],
         "us_per_layer_unfused": chain["unfused_us"], "launches_per_layer_unfused": 13,
         "chain": chain, "epilogue_cost": epi_cost, "per_kernel": per_kernel, "per_workload": per_workload,
-        "next_rows": nxt,
+        "next_rows": nxt, "repairs_in_timed_steps": step_repairs,
         "e2e": e2e, "clocks": sampler.summary(),
     }
     if dist is not None:
@@ -813,9 +817,11 @@ def next_rows_measure(G, torch, step, s, args, peak):
         G.gemv_fused_ex(Wl["chain_down_add"], 4, g, 4096, 14336, 4, r, r, pdl=True)
         G.gemv_fused_ex(Wl["chain_beta_sigmoid"], 4, x, 32, 4096, 1, None, beta, pdl=True)
 
+    G.repair_count(reset=True)
     us8 = graph_us(torch, s, lambda i: k_layer(i, False), 2, max(20, min(args.steps, 500)))
     us7 = graph_us(torch, s, lambda i: k_layer(i, True), 2, max(20, min(args.steps, 500)))
     lbk = sum(layers_k[0][n].numel() for n in names) + 4 * (4096 * 3 + 4096 * 3 + 2 * 4096 * 2 + 14336 * 3 + 32)
+    out["chain_q4_k_repairs"] = G.repair_count(reset=True)
     out["chain_q4_k"] = {"us_per_layer": round(us8, 3), "launches_per_layer": 8,
                          "us_per_layer_glu": round(us7, 3), "launches_per_layer_glu": 7, "layer_bytes": lbk,
                          "gbs": round(lbk / (us8 * 1e-6) / 1e9, 1)}

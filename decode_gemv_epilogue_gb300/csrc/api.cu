@@ -21,7 +21,9 @@
 
 namespace gf {
 
-__device__ unsigned int g_error_word;
+// Per device: [0] the error bits of bounded waits that gave up, [1] the row chunks whose
+// sums the integer path handed to the fp32 repair (see the streamed kernel).
+__device__ unsigned int g_error_word[2];
 
 static thread_local int t_last_cuda_error = 0;
 
@@ -825,6 +827,23 @@ int gf_device_status(int reset) {
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return (v & ERRBIT_TIMEOUT) ? GF_ERR_TIMEOUT : GF_OK;
+}
+
+int64_t gf_repair_count(int reset) {
+  unsigned* err = device_error_word();
+  if (!err) return cuda_fail(cudaGetLastError());
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned v = 0;
+  e = cudaMemcpy(&v, err + 1, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (reset) {
+    e = cudaMemset(err + 1, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return static_cast<int64_t>(v);
 }
 
 const char* gf_status_string(int status) {

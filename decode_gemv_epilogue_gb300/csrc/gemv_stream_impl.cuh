@@ -623,6 +623,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
     // consumer thread takes every barrier; after an abort the work is skipped.
     auto repair = [&](int64_t rb, int nrc_, int nvr_) {
       if constexpr (kInt) {
+        if (ctid == 0 && a.err) atomicAdd(a.err + 1, 1u);  // counted for gf_repair_count
         if constexpr (kSplit) {
           for (int i = ctid; i < S * NC * XR; i += nt) xch[i] = 0.0f;
         } else {

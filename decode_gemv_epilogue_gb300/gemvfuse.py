@@ -365,6 +365,14 @@ def selftest_wait_timeout(limit_us, out, stream=None, check=True):
     return st
 
 
+_repair_count = _sig("gf_repair_count", [_i32], _i64)
+
+
+def repair_count(reset=False):
+    """gf_repair_count: row chunks recomputed in fp32 by the integer-path kernels."""
+    return _repair_count(1 if reset else 0)
+
+
 def device_status(reset=False):
     return _device_status(1 if reset else 0)
 

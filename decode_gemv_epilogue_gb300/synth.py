@@ -80,8 +80,12 @@ def weights(wtype, M, K, seed, dist=None):
     """Weight bytes (uint8 [M * row_bytes]) with the workload distributions:
     F32 ~ U(-1/sqrt(K), 1/sqrt(K)); F16 ~ N(0, 0.02);
     Q8_0 q ~ U{-127..127}, d ~ U(0.001, 0.01); Q4_0 q ~ U{0..15}, d ~ U(0.001, 0.02);
-    Q4_K q ~ U{0..15}, sc, m ~ U{0..63}, d ~ U(1e-4, 4e-4), dmin ~ U(5e-4, 2e-3) (the
-    scaled code and the sub-block min are then of the same order, ~0.05).
+    Q4_K q ~ U{0..15}, sc ~ U{1..63}, d ~ U(1e-4, 4e-4), and per super-block dmin = the
+    largest d * sc[j] * 7.5 / 63 of its sub-blocks times U(1, 1.25), with
+    m[j] = round(d * sc[j] * 7.5 / dmin) in 0..63: each sub-block's min centres its scaled
+    codes, so the weights have mean ~0 as the quantised weights of a trained layer do
+    (drawing m and dmin independently gives weights whose mean is ~40% of their size,
+    which a layer's residual stream turns into gates deep in silu's saturation).
     The fp16 scales are drawn in float64 and rounded to binary16 (nearest even)."""
     g = rng(seed)
     if wtype == F32:
@@ -95,10 +99,11 @@ def weights(wtype, M, K, seed, dist=None):
     if wtype == Q4_K:
         nsb = K // QK_K
         codes = g.integers(0, 16, size=(M, K), dtype=np.int16)
-        sc = g.integers(0, 64, size=(M, nsb, 8), dtype=np.int16)
-        mn = g.integers(0, 64, size=(M, nsb, 8), dtype=np.int16)
+        sc = g.integers(1, 64, size=(M, nsb, 8), dtype=np.int16)
         d = g.uniform(1e-4, 4e-4, size=(M, nsb)).astype(np.float16)
-        dmin = g.uniform(5e-4, 2e-3, size=(M, nsb)).astype(np.float16)
+        centre = d.astype(np.float64)[:, :, None] * sc * 7.5           # d * sc[j] * 7.5
+        dmin = (centre.max(axis=2) / 63.0 * g.uniform(1.0, 1.25, size=(M, nsb))).astype(np.float16)
+        mn = np.clip(np.rint(centre / dmin.astype(np.float64)[:, :, None]), 0, 63).astype(np.int16)
         return pack_q4_k(codes, sc, mn, d, dmin).reshape(-1)
     nb = K // QK
     if wtype == Q8_0:

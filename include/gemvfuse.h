@@ -30,8 +30,9 @@
  *    gf_last_cuda_error()).
  *  - Vectors are contiguous float32.  A batch of ncols columns is column-major:
  *    x is [ncols][K], aux and dst are [ncols][M].
- *  - The library holds no state between calls other than per-device launch limits
- *    and a device error word (see gf_device_status()).
+ *  - The library holds no state between calls other than per-device launch limits,
+ *    a device error word (see gf_device_status()) and a repair counter
+ *    (gf_repair_count()).
  */
 #ifndef GEMVFUSE_H
 #define GEMVFUSE_H
@@ -300,6 +301,15 @@ GF_API int gf_selftest_wait_timeout(int64_t limit_us, int* out, void* stream);
  * on a bounded wait since the last reset.  Synchronises with the device.  reset != 0
  * clears it. */
 GF_API int gf_device_status(int reset);
+
+/* Row chunks (a CTA's rows of one launch, or of one row chunk of it) whose sums the
+ * single-column Q4_0 / Q8_0 / Q4_K kernels recomputed in fp32 because some 16-element
+ * unit of x could not be carried by their integer dot products (an outlier far above
+ * the values around it, or a NaN / Inf): a count since the last reset, on the current
+ * device.  Such a launch reads its weights twice; the count says how often that
+ * happens for a workload.  Synchronises with the device; reset != 0 clears it.
+ * Negative: a gf_status (GF_ERR_CUDA). */
+GF_API int64_t gf_repair_count(int reset);
 
 /* Human-readable name of a gf_status value. */
 GF_API const char* gf_status_string(int status);

@@ -27,7 +27,8 @@ def test_header_declares_the_abi():
     assert {"gemv_fused", "gemv_fused_ex", "gemv_glu", "fwht_signed", "gf_elementwise", "gf_dequantize",
             "gf_plan", "gf_plan_glu", "gf_device_status", "gf_status_string", "gf_last_cuda_error",
             "gf_version", "gf_prepare", "gf_prepare_glu", "gf_launch_prepared", "gf_free_prepared",
-            "gf_graph_create", "gf_graph_launch", "gf_graph_free", "gemv_multi", "gf_prepare_multi"} <= names
+            "gf_graph_create", "gf_graph_launch", "gf_graph_free", "gemv_multi", "gf_prepare_multi",
+            "gf_repair_count"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):

@@ -101,6 +101,11 @@ FINITE_CASES = ["zeros", "scale_3e4", "scale_1e-20", "mixed_1e3_1e-3", "spike_3e
                 "heavy_tail", "sparse"]
 
 
+# cases whose units the integer path must hand to the fp32 repair, and ones it must carry
+REPAIRED = ("spike_1e4", "spike_1e6")
+NOT_REPAIRED = ("zeros", "scale_3e4", "scale_1e-20", "mixed_1e3_1e-3", "spike_3e2", "heavy_tail")
+
+
 def case_weights(wt, M, K, seed):
     raw = synth.weights(wt, M, K, seed=seed)
     return zero_weight_columns(raw, wt, M, K, SPIKE_COLS)
@@ -153,8 +158,14 @@ def test_gemv_fused_dynamic_range(G, fmt, M, K, case):
     Wd, xd = dev_tensor(raw), dev_tensor(x)
     for epi in (NONE, ADD):
         dst = dev_tensor(r) if epi == ADD else torch.full((M,), float("nan"), device="cuda")
+        G.repair_count(reset=True)
         G.gemv_fused(Wd, wt, xd, M, K, epi, dst if epi == ADD else None, dst)
         torch.cuda.synchronize()
+        repairs = G.repair_count()
+        if case in REPAIRED:
+            assert repairs > 0, "%s %s: the fp32 repair should have run" % (fmt, case)
+        elif case in NOT_REPAIRED:
+            assert repairs == 0, "%s %s: %d row chunks repaired" % (fmt, case, repairs)
         got = dst.cpu().numpy().astype(np.float64)
         want = ogemv.gemv(raw, wt, x, M, K, epi, r)[0]
         assert_within(got, want, literal_bound(raw, wt, x, M, K)[0], "%s %s epi %d" % (fmt, case, epi))
@@ -181,8 +192,10 @@ def test_gemv_fused_non_finite_x(G, fmt, M, K, bad):
     Wd, xd = dev_tensor(raw), dev_tensor(x)
     for epi in (NONE, SIG):
         dst = torch.zeros(M, device="cuda")
+        G.repair_count(reset=True)
         G.gemv_fused(Wd, wt, xd, M, K, epi, None, dst)
         torch.cuda.synchronize()
+        assert G.repair_count() > 0, "a non-finite x must go to the fp32 repair"
         got = dst.cpu().numpy().astype(np.float64)
         with np.errstate(invalid="ignore", over="ignore"):
             want = ogemv.gemv(raw, wt, x, M, K, epi)[0]
