@@ -1085,6 +1085,76 @@ def reference_arm(args, rank, world):
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ----------------------------------------------------------------------------- profiling cases
+
+PROFILE_CASES = ("q4_0_glu_14336x4096", "q4_0_multi_qkv_head", "q4_0_down_add_4096x14336", "q4_0_o_add_4096x4096",
+                 "q8_0_silu_mul_11008x4096", "f16_add_4096x4096", "fwht_f16_add_5120x5120_n1",
+                 "fwht_f16_add_5120x5120_n8")
+
+
+def profile_case(name, launches=6):
+    """A small workload for per-kernel ncu captures: one call of the decode step, issued
+    `launches` times (no graph, no timing) over enough weight copies that the weights
+    exceed L2; a few hundred MB on the device."""
+    import torch
+    import __graft_entry__ as ge
+    ge.build()
+    from decode_gemv_epilogue_gb300 import gemvfuse as G
+    from decode_gemv_epilogue_gb300 import synth
+    dev = torch.device("cuda")
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    d, f = 4096, 14336
+    x, a = up(synth.normal(d, seed=1)), up(synth.normal(d, seed=2))
+    r0, r = up(synth.normal(d, seed=3)), torch.empty(d, device=dev)
+    xf = up(synth.normal(f, seed=4))
+    signs = up(synth.rademacher(1024, seed=5))
+
+    def copies(wt, M, K, nbytes_per):
+        n = max(2, -(-2 * L2_BYTES // nbytes_per))
+        return [up(synth.weights(wt, M, K, seed=10 + i)) for i in range(n)]
+
+    if name == "q4_0_glu_14336x4096":
+        Wg = copies(3, f, d, 2 * row_bytes(3, d) * f)
+        Wu = [up(synth.weights(3, f, d, seed=50 + i)) for i in range(len(Wg))]
+        g = torch.empty(f, device=dev)
+        fn = lambda i: G.gemv_glu(Wg[i % len(Wg)], Wu[i % len(Wg)], 3, x, f, d, g, split_k=False)
+    elif name == "q4_0_multi_qkv_head":
+        Ws = [[up(synth.weights(3, M, d, seed=10 + 4 * i + j)) for j, M in enumerate((d, d, d, 32))] for i in range(6)]
+        outs = [torch.empty(M, device=dev) for M in (d, d, d, 32)]
+        fn = lambda i: G.gemv_multi([(Ws[i % 6][j], M, e, None, outs[j])
+                                     for j, (M, e) in enumerate(((d, 0), (d, 0), (d, 0), (32, 1)))], 3, x, d)
+    elif name == "q4_0_down_add_4096x14336":
+        Ws = copies(3, d, f, row_bytes(3, f) * d)
+        fn = lambda i: G.gemv_fused_ex(Ws[i % len(Ws)], 3, xf, d, f, 4, r, r, split_k=False)
+    elif name == "q4_0_o_add_4096x4096":
+        Ws = copies(3, d, d, row_bytes(3, d) * d)
+        fn = lambda i: G.gemv_fused_ex(Ws[i % len(Ws)], 3, a, d, d, 4, r0, r, split_k=False)
+    elif name == "q8_0_silu_mul_11008x4096":
+        Ws = copies(2, 11008, d, row_bytes(2, d) * 11008)
+        m, gout = up(synth.normal(11008, seed=6)), torch.empty(11008, device=dev)
+        fn = lambda i: G.gemv_fused_ex(Ws[i % len(Ws)], 2, x, 11008, d, 3, m, gout)
+    elif name == "f16_add_4096x4096":
+        Ws = copies(1, d, d, row_bytes(1, d) * d)
+        rr = up(synth.normal(d, seed=7))
+        fn = lambda i: G.gemv_fused_ex(Ws[i % len(Ws)], 1, x, d, d, 4, rr, rr, view=(32, 128))
+    elif name.startswith("fwht_f16_add_5120x5120_n"):
+        nc = int(name.rsplit("n", 1)[1])
+        Ws = copies(1, 5120, 5120, row_bytes(1, 5120) * 5120)
+        X = up(synth.normal(nc * 5120, seed=8))
+        rr = up(synth.normal(nc * 5120, seed=9))
+        ws = torch.empty(nc * 5120, device=dev)
+        fn = lambda i: G.gemv_fused_ex(Ws[i % len(Ws)], 1, X, 5120, 5120, 4, rr, rr, ncols=nc, fwht_signs=signs,
+                                       fwht_block=1024, fwht_workspace=ws)
+    else:
+        raise SystemExit("unknown profile case %r (one of %s)" % (name, ", ".join(PROFILE_CASES)))
+    for i in range(launches):
+        fn(i)
+    torch.cuda.synchronize()
+    assert G.device_status() == 0
+    print(json.dumps({"profile_case": name, "launches": launches}))
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 
 def main(argv=None):
@@ -1094,7 +1164,11 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="run one call of the step a few times (a small workload for ncu) and exit")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        return profile_case(args.profile_case)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
