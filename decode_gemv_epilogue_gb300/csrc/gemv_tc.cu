@@ -17,9 +17,10 @@
 // values are exact in fp32 and the accumulation is fp32.
 //
 // Rows alone give too few tiles for 152 SMs (e.g. 40 for 5120 rows), so K is split
-// over a cluster of S CTAs per tile (S = SMs / tiles, at most 8); ranks 1..S-1 store
-// their per-row partial sums into rank 0's shared memory and rank 0 adds them in rank
-// order (deterministic).  Every wait is bounded; on a timeout the kernel sets the error
+// over a cluster of S CTAs per tile (S = SMs / tiles, at most 8).  Column c of the batch
+// is finalised by rank c % S: every rank stores its per-row partial sums of the other
+// ranks' columns into their shared memory, and each owner adds the S partials in rank
+// order (deterministic) and writes its columns, so the ranks share the final stores.  Every wait is bounded; on a timeout the kernel sets the error
 // word, drains its copies and MMAs, frees its tensor memory and returns.
 #include <cuda.h>
 
@@ -43,7 +44,7 @@ constexpr int kTcMaxStages = 12;                // W tiles in flight
 // MMA m accumulates into accumulator m % kTcAcc: MMAs into the same TMEM columns wait
 // for each other's full latency, which a 128 x N x 16 MMA with small N does not amortise
 // (one accumulator held the kernel to ~240 cycles per MMA); the epilogue adds them.
-constexpr int kTcAcc = 8;
+constexpr int kTcAcc = 4;
 
 // ------------------------------------------------------------------ kernel
 // Shared memory from a 1024-aligned base: barriers and the TMEM address slot [0, 512);
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   float* smax = reinterpret_cast<float*>(base + 512);   // [4 warps][64] column maxima
   float* scl = reinterpret_cast<float*>(base + 1536);   // [64]
   float* iscl = scl + 64;                               // [64]
-  float* xch = reinterpret_cast<float*>(base + 2048);   // [S][Np][128]
+  float* xch = reinterpret_cast<float*>(base + 2048);   // [Np][128][SP] partial sums (split K)
   const uint32_t sA = sb + static_cast<uint32_t>(a.off_a), sB = sb + static_cast<uint32_t>(a.off_b);
   const uint32_t sX = sb + static_cast<uint32_t>(a.off_x);
 
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   const int st0 = crank * a.nst / S, st1 = (crank + 1) * a.nst / S;  // this CTA's K stages
   const int nmy = st1 - st0;
   const int Np = a.Np;
+  const int SP = S <= 4 ? 4 : 8;            // exchange slots per (column, row): S rounded up
   const int subs = a.subs;                  // 64-element sub-tiles per stage
   const int b_sub_bytes = 2 * Np * 128;     // B rows of one sub-tile
 
@@ -89,7 +91,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       mbar_init(empty0 + 8u * i, 1);
     }
     mbar_init(accbar, 1);
-    mbar_init(xchbar, static_cast<uint32_t>(SPLIT ? (S - 1) * 128 : 1));
+    mbar_init(xchbar, 1);
+    if constexpr (SPLIT) {  // the partials this CTA receives: S - 1 peers x its columns x 128 rows
+      const int nown = a.ncols > crank ? (a.ncols - 1 - crank) / S + 1 : 0;
+      mbar_arrive_expect_tx(xchbar, static_cast<uint32_t>((S - 1) * nown * kTcRows * 4));
+    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(a.tmem_cols));
@@ -258,61 +264,120 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         }
       }
     }
+    // This thread's epilogue row (TMEM lane quarter of its warp).  Column c is finalised
+    // by cluster rank c % S: own_tbl holds that rank in 4 bits per column, `mine` flags
+    // this CTA's columns (a chain of compares: the epilogue runs one warp per SM
+    // sub-partition, where every dependent instruction is paid in full, so integer
+    // division stays out of it).  Their aux values are loaded here, before the wait for
+    // the last MMAs hides their latency (at the start they would delay the scale pass;
+    // in the tail each would wait behind the previous column's dst store, as dst may
+    // alias aux).
+    const int q = warp & 3;           // TMEM lane quarter this warp can read
+    const int r = 32 * q + lane;      // row within the tile
+    const int64_t row = static_cast<int64_t>(row0) + r;
+    const bool need_aux = (a.epi == EPI_SILU_MUL || a.epi == EPI_ADD);
+    uint64_t own_tbl = 0;
+    uint32_t mine = 0;
+    {
+      int o = 0;
+#pragma unroll
+      for (int c = 0; c < kTcMaxCols; ++c) {
+        own_tbl |= static_cast<uint64_t>(o) << (4 * c);
+        if (o == crank && c < a.ncols) mine |= 1u << c;
+        o = (o + 1 == S) ? 0 : o + 1;
+      }
+    }
+    float auxv[kTcMaxCols];
+#pragma unroll
+    for (int c = 0; c < kTcMaxCols; ++c) {
+      auxv[c] = 0.0f;
+      if (need_aux && ((mine >> c) & 1u) && row < a.M) auxv[c] = a.aux[static_cast<int64_t>(c) * a.M + row];
+    }
     // epilogue: wait for every MMA (bounded, regardless of an abort: tensor memory is
     // freed below), then this warp's quarter of the accumulator rows
     const bool acc_ok = mbar_wait(accbar, 0);
     if (!acc_ok) set_error(a.err, ERRBIT_TIMEOUT);
     ok = ok && acc_ok && !*abort_flag;
     tc_fence_after();
-    const int q = warp & 3;           // TMEM lane quarter this warp can read
-    const int r = 32 * q + lane;      // row within the tile
-    const int64_t row = static_cast<int64_t>(row0) + r;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    const bool need_aux = (a.epi == EPI_SILU_MUL || a.epi == EPI_ADD);
     const int nacc = min(kTcAcc, nmy * subs * kTcKSteps);  // accumulators written
-    for (int c0 = 0; c0 < Np; c0 += 8) {
-      float hv[8], lv[8];
-      tmem_ld8(trow + static_cast<uint32_t>(c0), hv);
-      tmem_ld8(trow + static_cast<uint32_t>(Np + c0), lv);
-      for (int ac = 1; ac < nacc; ++ac) {  // the accumulators, in order
-        float h2[8], l2[8];
-        tmem_ld8(trow + static_cast<uint32_t>(ac * 2 * Np + c0), h2);
-        tmem_ld8(trow + static_cast<uint32_t>(ac * 2 * Np + Np + c0), l2);
+    float* const dcol = a.dst + row;                         // column c at dcol[c * M]
+    const bool plain_add = a.epi == EPI_ADD;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          hv[j] += h2[j];
-          lv[j] += l2[j];
+    for (int c0 = 0; c0 < kTcMaxCols; c0 += 8) {
+      if (c0 >= Np) break;
+      // all accumulators of these 8 columns (hi and lo) in flight, then one wait
+      uint32_t hr[kTcAcc][8], lr[kTcAcc][8];
+#pragma unroll
+      for (int t = 0; t < kTcAcc; ++t)
+        if (t < nacc) {
+          tmem_ld8_nowait(trow + static_cast<uint32_t>(t * 2 * Np + c0), hr[t]);
+          tmem_ld8_nowait(trow + static_cast<uint32_t>(t * 2 * Np + Np + c0), lr[t]);
         }
-      }
+      tmem_wait_ld();
+      float hv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+      float lv[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int t = 0; t < kTcAcc; ++t)  // the accumulators, in order
+        if (t < nacc) {
+          tmem_pin8(hr[t]);
+          tmem_pin8(lr[t]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            hv[j] += __uint_as_float(hr[t][j]);
+            lv[j] += __uint_as_float(lr[t][j]);
+          }
+        }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int c = c0 + j;
-        if (c >= a.ncols) continue;
+        if (c >= a.ncols) break;
         const float y = (hv[j] + lv[j]) * iscl[c];
-        if constexpr (SPLIT) {
-          float* slot = xch + (crank * Np + c) * kTcRows + r;
-          if (crank == 0)
+        if constexpr (SPLIT) {  // this rank's partial, into the exchange of the column's owner
+          const uint32_t own = static_cast<uint32_t>(own_tbl >> (4 * c)) & 15u;
+          float* slot = xch + (c * kTcRows + r) * SP + crank;
+          if (own == static_cast<uint32_t>(crank))
             *slot = y;
           else
-            st_cluster_f32(map_to_rank(smem_u32(slot), 0), y);
+            st_async_f32(map_to_rank(smem_u32(slot), own), y, map_to_rank(xchbar, own));
         } else if (ok && row < a.M) {
-          const int64_t o = static_cast<int64_t>(c) * a.M + row;
-          a.dst[o] = apply_tail(a.epi, y, need_aux ? a.aux[o] : 0.0f);
+          dcol[static_cast<int64_t>(c) * a.M] = plain_add ? y + auxv[c] : apply_tail(a.epi, y, auxv[c]);
         }
       }
     }
     if constexpr (SPLIT) {
-      if (crank != 0) {
-        mbar_arrive_remote(map_to_rank(xchbar, 0));
-      } else {
-        ok = mbar_wait_cluster_or_abort(xchbar, 0, abort_flag, a.err) && ok;
-        if (ok && row < a.M)
-          for (int c = 0; c < a.ncols; ++c) {
-            float y = 0.0f;
-            for (int sl = 0; sl < S; ++sl) y += xch[(sl * Np + c) * kTcRows + r];  // rank order
-            const int64_t o = static_cast<int64_t>(c) * a.M + row;
-            a.dst[o] = apply_tail(a.epi, y, need_aux ? a.aux[o] : 0.0f);
+      // wait until every peer's partials of this CTA's columns have landed, then add the
+      // S partials of each column in rank order and apply the tail
+      ok = mbar_wait_cluster_or_abort(xchbar, 0, abort_flag, a.err) && ok;
+      if (ok && row < a.M) {
+        float yv[kTcMaxCols];
+#pragma unroll
+        for (int c = 0; c < kTcMaxCols; ++c) {
+          yv[c] = 0.0f;
+          if ((mine >> c) & 1u) {
+            const float4* pp = reinterpret_cast<const float4*>(xch + (c * kTcRows + r) * SP);
+            const float4 p0 = pp[0];
+            yv[c] = (0.0f + p0.x) + p0.y;  // S >= 2 here
+            if (S >= 3) yv[c] += p0.z;
+            if (S >= 4) yv[c] += p0.w;
+            if (S >= 5) {
+              const float4 p1 = pp[1];
+              yv[c] += p1.x;
+              if (S >= 6) yv[c] += p1.y;
+              if (S >= 7) yv[c] += p1.z;
+              if (S >= 8) yv[c] += p1.w;
+            }
           }
+        }
+        if (plain_add) {
+#pragma unroll
+          for (int c = 0; c < kTcMaxCols; ++c)
+            if ((mine >> c) & 1u) dcol[static_cast<int64_t>(c) * a.M] = yv[c] + auxv[c];
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTcMaxCols; ++c)
+            if ((mine >> c) & 1u) dcol[static_cast<int64_t>(c) * a.M] = apply_tail(a.epi, yv[c], auxv[c]);
+        }
       }
     }
   }
@@ -401,14 +466,14 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
   const int nsub_all = static_cast<int>(K / kTcK);
   int S = static_cast<int>(std::min<int64_t>(kMaxSplit, lim.sm_count / std::max<int64_t>(tiles, 1)));
   S = std::min(S, nsub_all);
-  S = std::min(S, (64 * 1024) / (Np * kTcRows * 4));
+  while (S >= 2 && Np * kTcRows * 4 * (S <= 4 ? 4 : 8) > 64 * 1024) --S;
   while (S >= 2) {  // every cluster resident at once (when the device can say)
     const int fit = tc_max_clusters(S, lim.smem_optin);
     if (fit == 0 || tiles <= fit) break;
     --S;
   }
   if (S < 2) S = 1;
-  const int xch_bytes = S > 1 ? S * Np * kTcRows * 4 : 0;
+  const int xch_bytes = S > 1 ? Np * kTcRows * 4 * (S <= 4 ? 4 : 8) : 0;
   const int off_a = round_up_i(2048 + xch_bytes, 1024);
   const int avail = lim.smem_optin - 1024 - off_a;  // 1024: alignment slack of the dynamic base
   // stages of `subs` sub-tiles: the MMA thread's per-stage cost (its waits and commits) is
@@ -505,7 +570,7 @@ struct MapEntry {
   const void* W;
   int64_t M;
   int K;
-  alignas(64) CUtensorMap map;
+  CUtensorMap map;  // the type carries the 64-byte alignment the driver requires
 };
 constexpr int kMapCache = 64;
 std::mutex g_map_mu;
@@ -520,7 +585,7 @@ static int w_map(const void* W, int64_t M, int K, CUtensorMap* out) {
       *out = g_maps[i].map;
       return cudaSuccess;
     }
-  alignas(64) CUtensorMap fresh;
+  CUtensorMap fresh;
   const int r = encode_map_2d(&fresh, true, W, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
                               static_cast<uint64_t>(K) * 2, kTcK, kTcRows, true);
   if (r != cudaSuccess) return r;
@@ -536,7 +601,7 @@ static int w_map(const void* W, int64_t M, int K, CUtensorMap* out) {
 }
 
 int launch_tc(const TcPlan& p, const void* W, cudaStream_t st, bool pdl) {
-  alignas(64) CUtensorMap map;
+  CUtensorMap map;  // the type carries the 64-byte alignment the driver requires
   const int e = w_map(W, p.a.M, p.a.K, &map);
   if (e != cudaSuccess) return e;
   return p.a.S > 1 ? launch_tc_t<true>(map, p, st, pdl) : launch_tc_t<false>(map, p, st, pdl);

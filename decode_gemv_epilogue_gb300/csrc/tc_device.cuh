@@ -59,6 +59,28 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// The same load without the wait: several can be in flight before one tmem_wait_ld();
+// tmem_pin8 after the wait keeps the compiler from reading the registers before it.
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_pin8(uint32_t (&r)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// Asynchronous store of one float into the shared memory of a peer CTA of the cluster;
+// on arrival it completes 4 bytes of transaction on the peer's mbarrier `remote_bar`
+// (both addresses from mapa).  The sender does not wait for it.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr), "f"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand in the 128-byte swizzled layout
 // (rows of 128 bytes, 8-row groups 1024 bytes apart; the tile starts 1024-aligned).
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
