@@ -41,6 +41,7 @@ constexpr int kTcKSteps = kTcK / 16;            // MMAs per sub-tile (K = 16 eac
 constexpr int kTcThreads = 192;                 // warp 0 TMA, warp 1 MMA, warps 2..5 x / epilogue
 constexpr int kTcABytes = kTcRows * kTcK * 2;   // 16 KB per sub-tile (a stage holds a.subs of them)
 constexpr int kTcMaxStages = 12;                // W tiles in flight
+constexpr int kTcMaxSubs = 4;                   // sub-tiles per stage
 // MMA m accumulates into accumulator m % kTcAcc: MMAs into the same TMEM columns wait
 // for each other's full latency, which a 128 x N x 16 MMA with small N does not amortise
 // (one accumulator held the kernel to ~240 cycles per MMA); the epilogue adds them.
@@ -112,8 +113,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     // ------------------------------------------------------------ W tiles and x (TMA)
     if (lane == 0) {
       const int xrow = subs * kTcK;  // floats of one column per stage
-      auto issue_x = [&](int i) {
-        const int slot = i % NS;
+      auto issue_x = [&](int i, int slot) {
         for (int c = 0; c < a.ncols; ++c)
           bulk_g2s(sX + static_cast<uint32_t>(slot * a.x_stage_bytes + c * xrow * 4),
                    a.x + static_cast<int64_t>(c) * a.K + static_cast<int64_t>(st0 + i) * xrow,
@@ -121,11 +121,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       };
       int issued = 0, x_done = 0;  // stages whose W / x copies are out
       bool waited = false;
-      for (int i = 0; i < nmy; ++i) {
-        const int slot = i % NS, round = i / NS;
+      // slot = i % NS and the phase parity (i / NS) & 1, kept incrementally (no division
+      // on the issue path)
+      for (int i = 0, slot = 0, par = 0; i < nmy; ++i, slot = (slot + 1 == NS) ? 0 : slot + 1, par ^= (slot == 0)) {
         // the first NS stages are empty: no wait (see the stream kernel)
-        if (i >= NS && !mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>((round & 1) ^ 1), abort_flag,
-                                            a.err))
+        if (i >= NS && !mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>(par ^ 1), abort_flag, a.err))
           break;
         mbar_arrive_expect_tx(fullA0 + 8u * slot,
                               static_cast<uint32_t>(subs * kTcABytes + a.ncols * xrow * 4));
@@ -138,11 +138,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
           waited = true;
         }
         if (waited)
-          for (; x_done < issued; ++x_done) issue_x(x_done);
+          for (; x_done < issued; ++x_done) issue_x(x_done, x_done == i ? slot : x_done % NS);
       }
       if (issued < nmy) {  // aborted: complete the stages' x, then wait (bounded) for the copies in flight
         if (!waited) pdl_wait();
-        for (; x_done < issued; ++x_done) issue_x(x_done);
+        for (; x_done < issued; ++x_done) issue_x(x_done, x_done % NS);
         for (int i = max(0, issued - NS); i < issued; ++i)
           (void)mbar_wait(fullA0 + 8u * (i % NS), static_cast<uint32_t>((i / NS) & 1));
       }
@@ -152,10 +152,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_f16(kTcRows, 2 * Np);
       const uint32_t acc_cols = static_cast<uint32_t>(2 * Np);
-      for (int i = 0; i < nmy; ++i) {
-        const int slot = i % NS, round = i / NS;
-        if (!mbar_wait_or_abort(fullA0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag, a.err)) break;
-        if (!mbar_wait_or_abort(fullB0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag, a.err)) break;
+      for (int i = 0, slot = 0, par = 0; i < nmy; ++i, slot = (slot + 1 == NS) ? 0 : slot + 1, par ^= (slot == 0)) {
+        if (!mbar_wait_or_abort(fullA0 + 8u * slot, static_cast<uint32_t>(par), abort_flag, a.err)) break;
+        if (!mbar_wait_or_abort(fullB0 + 8u * slot, static_cast<uint32_t>(par), abort_flag, a.err)) break;
         tc_fence_after();
         for (int sbt = 0; sbt < subs; ++sbt) {
           const uint64_t da = umma_desc_sw128(sA + static_cast<uint32_t>((slot * subs + sbt) * kTcABytes));
@@ -219,50 +218,53 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     const bool has_chunk = ctid < Np * 8;
     const int n_own = ctid >> 3, c8_own = ctid & 7;
     const bool live = has_chunk && n_own < a.ncols;
-    const int nu = nmy * subs;  // sub-tiles of this CTA
     const float sc_own = live ? scl[n_own] : 1.0f;
+    const uint32_t sw_hi = sw128_offset(n_own, 8 * c8_own), sw_lo = sw128_offset(Np + n_own, 8 * c8_own);
     bool ok = true;
-    for (int u = 0; u < nu; ++u) {
-      {
-        const int i = u / subs, sbt = u - i * subs;
-        const int slot = i % NS, round = i / NS;
-        if (sbt == 0)
-          ok = ok && mbar_wait_or_abort(fullA0 + 8u * slot, static_cast<uint32_t>(round & 1), abort_flag, a.err);
-        float4 c0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), c1 = c0;
-        if (ok && live) {
-          const float* xs = reinterpret_cast<const float*>(base + a.off_x + slot * a.x_stage_bytes) +
-                            n_own * subs * kTcK + sbt * kTcK + 8 * c8_own;
-          c0 = reinterpret_cast<const float4*>(xs)[0];
-          c1 = reinterpret_cast<const float4*>(xs)[1];
-        }
-        if (ok && has_chunk) {
-          uint8_t* bt = base + a.off_b + slot * a.b_stage_bytes + sbt * b_sub_bytes;
-          uint4 hv = make_uint4(0u, 0u, 0u, 0u), lv = make_uint4(0u, 0u, 0u, 0u);
-          if (live) {
-            // hi = f16(x * 2^s), lo = f16(x * 2^s - hi), two elements per conversion
-            const float2 sc2 = make_float2(sc_own, sc_own);
-            const float2 v[4] = {fmul2(make_float2(c0.x, c0.y), sc2), fmul2(make_float2(c0.z, c0.w), sc2),
-                                 fmul2(make_float2(c1.x, c1.y), sc2), fmul2(make_float2(c1.z, c1.w), sc2)};
-            uint32_t hw[4], lw[4];
+    // per stage: one wait, the loads of every sub-tile in flight together, then the
+    // conversions and stores (one warp per SM sub-partition runs this, so independent
+    // work is what hides the latencies); ring slot and phase kept incrementally
+    for (int i = 0, slot = 0, par = 0; i < nmy; ++i, slot = (slot + 1 == NS) ? 0 : slot + 1, par ^= (slot == 0)) {
+      ok = ok && mbar_wait_or_abort(fullA0 + 8u * slot, static_cast<uint32_t>(par), abort_flag, a.err);
+      float4 c[kTcMaxSubs][2];
+      const float* xs = reinterpret_cast<const float*>(base + a.off_x + slot * a.x_stage_bytes) +
+                        n_own * subs * kTcK + 8 * c8_own;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const __half2 h = __floats2half2_rn(v[t].x, v[t].y);
-              const float2 r = fsub2(v[t], __half22float2(h));
-              const __half2 l = __floats2half2_rn(r.x, r.y);
-              hw[t] = *reinterpret_cast<const uint32_t*>(&h);
-              lw[t] = *reinterpret_cast<const uint32_t*>(&l);
-            }
-            hv = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            lv = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-          }
-          *reinterpret_cast<uint4*>(bt + sw128_offset(n_own, 8 * c8_own)) = hv;
-          *reinterpret_cast<uint4*>(bt + sw128_offset(Np + n_own, 8 * c8_own)) = lv;
-        }
-        if (sbt == subs - 1) {
-          if (ok && has_chunk) fence_proxy_async_smem();  // generic-proxy writes, read by the tensor cores
-          mbar_arrive(fullB0 + 8u * slot);
+      for (int sbt = 0; sbt < kTcMaxSubs; ++sbt) {
+        c[sbt][0] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        c[sbt][1] = c[sbt][0];
+        if (sbt < subs && ok && live) {
+          c[sbt][0] = reinterpret_cast<const float4*>(xs + sbt * kTcK)[0];
+          c[sbt][1] = reinterpret_cast<const float4*>(xs + sbt * kTcK)[1];
         }
       }
+      if (ok && has_chunk) {
+        uint8_t* bt = base + a.off_b + slot * a.b_stage_bytes;
+#pragma unroll
+        for (int sbt = 0; sbt < kTcMaxSubs; ++sbt) {
+          if (sbt >= subs) break;
+          // hi = f16(x * 2^s), lo = f16(x * 2^s - hi), two elements per conversion (zero
+          // rows for the padding columns)
+          const float2 sc2 = make_float2(sc_own, sc_own);
+          const float2 v[4] = {fmul2(make_float2(c[sbt][0].x, c[sbt][0].y), sc2),
+                               fmul2(make_float2(c[sbt][0].z, c[sbt][0].w), sc2),
+                               fmul2(make_float2(c[sbt][1].x, c[sbt][1].y), sc2),
+                               fmul2(make_float2(c[sbt][1].z, c[sbt][1].w), sc2)};
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const __half2 h = __floats2half2_rn(v[t].x, v[t].y);
+            const float2 rr = fsub2(v[t], __half22float2(h));
+            const __half2 l = __floats2half2_rn(rr.x, rr.y);
+            hw[t] = *reinterpret_cast<const uint32_t*>(&h);
+            lw[t] = *reinterpret_cast<const uint32_t*>(&l);
+          }
+          *reinterpret_cast<uint4*>(bt + sbt * b_sub_bytes + sw_hi) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(bt + sbt * b_sub_bytes + sw_lo) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        fence_proxy_async_smem();  // generic-proxy writes, read by the tensor cores
+      }
+      mbar_arrive(fullB0 + 8u * slot);
     }
     // This thread's epilogue row (TMEM lane quarter of its warp).  Column c is finalised
     // by cluster rank c % S: own_tbl holds that rank in 4 bits per column, `mine` flags
