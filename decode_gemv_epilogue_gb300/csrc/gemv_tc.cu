@@ -1,12 +1,13 @@
 // Tensor-core GEMV for F16 weights and a batch of columns (5th-generation tensor cores:
 // tcgen05.mma with the accumulator in tensor memory).
 //
-// A CTA owns one tile of 128 rows of W and a slice of its K range.  Per 64-element K
-// stage, warp 0 loads the 128 x 64 f16 tile of W with one 2-D TMA copy (128-byte
-// swizzle, K-major: the tensor cores read it straight from shared memory) and the
-// batch's x for the same elements with one bulk copy per column (issued once the
-// preceding grid, which may write x, has finished; the first W stage goes out before
-// that); warps 2..5 turn the staged x into f16 rows of B in the same swizzled layout.  x is fp32, so each column is scaled by an exact power of two
+// A CTA owns one tile of 128 rows of W and a slice of its K range.  Per stage of 64-element
+// K sub-tiles, warp 0 loads the 128 x 64 f16 tiles of W with 2-D TMA copies (128-byte
+// swizzle, K-major: the tensor cores read them straight from shared memory) and the
+// batch's x for the same elements (one bulk copy per column up to 8 columns, one 2-D copy
+// of all columns beyond), x once the preceding grid, which may write it, has finished
+// (the first W stage goes out before that); warps 2..5 turn the staged x into f16 rows
+// of B in the same swizzled layout.  x is fp32, so each column is scaled by an exact power of two
 // (its largest |x| over the CTA's K slice lands in [2^14, 2^15)) and split into
 // hi = f16(x) and lo = f16(x - hi): B holds Np rows of hi followed by Np rows of lo
 // (Np = columns rounded up to 8).  One thread of warp 1 issues four
@@ -54,6 +55,7 @@ constexpr int kTcAcc = 4;
 // off_b (2 Np rows of 128 bytes each).
 template <bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                const __grid_constant__ CUtensorMap xmap,
                                                                 const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -85,6 +87,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   const int b_sub_bytes = 2 * Np * 128;     // B rows of one sub-tile
 
   if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap);
+    if (a.ncols > 8) prefetch_tmap(&xmap);
     *abort_flag = 0;
     for (int i = 0; i < NS; ++i) {
       mbar_init(fullA0 + 8u * i, 1);
@@ -113,11 +117,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     // ------------------------------------------------------------ W tiles and x (TMA)
     if (lane == 0) {
       const int xrow = subs * kTcK;  // floats of one column per stage
+      // the stage's x: one 2-D copy of every column for wide batches, one bulk copy per
+      // column up to 8 columns (measured faster there behind the transform-once prologue)
+      const bool x2d = a.ncols > 8;
       auto issue_x = [&](int i, int slot) {
-        for (int c = 0; c < a.ncols; ++c)
-          bulk_g2s(sX + static_cast<uint32_t>(slot * a.x_stage_bytes + c * xrow * 4),
-                   a.x + static_cast<int64_t>(c) * a.K + static_cast<int64_t>(st0 + i) * xrow,
-                   static_cast<uint32_t>(xrow * 4), fullA0 + 8u * slot);
+        if (x2d) {
+          tma_load_2d(sX + static_cast<uint32_t>(slot * a.x_stage_bytes), &xmap, (st0 + i) * xrow, 0,
+                      fullA0 + 8u * slot);
+        } else {
+          for (int c = 0; c < a.ncols; ++c)
+            bulk_g2s(sX + static_cast<uint32_t>(slot * a.x_stage_bytes + c * xrow * 4),
+                     a.x + static_cast<int64_t>(c) * a.K + static_cast<int64_t>(st0 + i) * xrow,
+                     static_cast<uint32_t>(xrow * 4), fullA0 + 8u * slot);
+        }
       };
       int issued = 0, x_done = 0;  // stages whose W / x copies are out
       bool waited = false;
@@ -516,7 +528,7 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
 }
 
 template <bool SPLIT>
-static int launch_tc_t(const CUtensorMap& map, const TcPlan& p, cudaStream_t st, bool pdl) {
+static int launch_tc_t(const CUtensorMap& map, const CUtensorMap& xmap, const TcPlan& p, cudaStream_t st, bool pdl) {
   auto kern = gemv_tc_kernel<SPLIT>;
   static int configured[64] = {0};
   int dev = 0;
@@ -547,10 +559,10 @@ static int launch_tc_t(const CUtensorMap& map, const TcPlan& p, cudaStream_t st,
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kern, map, p.a);
+  return cudaLaunchKernelEx(&cfg, kern, map, xmap, p.a);
 }
 
-int encode_map_2d(CUtensorMap* map, bool f16, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
+int encode_map_2d(CUtensorMap* map, int dtype, const void* base, uint64_t inner, uint64_t rows, uint64_t stride_bytes,
                   uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
   const EncodeTiledFn enc = encode_tiled();
   if (!enc) return cudaErrorNotSupported;
@@ -558,20 +570,25 @@ int encode_map_2d(CUtensorMap* map, bool f16, const void* base, uint64_t inner, 
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride_bytes)};
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+  const CUresult r = enc(map,
+                         dtype == kMapF16   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                         : dtype == kMapF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                         2,
                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Encoded tensor maps of recent weight matrices: a map holds only the address, shape
-// and stride, so an entry with the same (W, M, K) is always the right one.
+// Encoded tensor maps of recent operands: a map holds only the address, shape, stride
+// and box, so an entry with the same key is always the right one.
 namespace {
 struct MapEntry {
-  const void* W;
-  int64_t M;
-  int K;
+  const void* base;
+  uint64_t inner, rows;
+  uint32_t box_inner, box_rows;
+  int dtype;
   CUtensorMap map;  // the type carries the 64-byte alignment the driver requires
 };
 constexpr int kMapCache = 64;
@@ -580,22 +597,30 @@ MapEntry g_maps[kMapCache];
 int g_map_used = 0, g_map_next = 0;
 }  // namespace
 
-static int w_map(const void* W, int64_t M, int K, CUtensorMap* out) {
+// A dense row-major [rows][inner] operand (rows `inner` elements apart).
+static int cached_map(const void* base, int dtype, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                      uint32_t box_rows, bool swizzle128, CUtensorMap* out) {
   std::lock_guard<std::mutex> lock(g_map_mu);
-  for (int i = 0; i < g_map_used; ++i)
-    if (g_maps[i].W == W && g_maps[i].M == M && g_maps[i].K == K) {
-      *out = g_maps[i].map;
+  for (int i = 0; i < g_map_used; ++i) {
+    const MapEntry& e = g_maps[i];
+    if (e.base == base && e.dtype == dtype && e.inner == inner && e.rows == rows && e.box_inner == box_inner &&
+        e.box_rows == box_rows) {
+      *out = e.map;
       return cudaSuccess;
     }
+  }
+  const uint64_t esize = dtype == kMapF32 ? 4 : dtype == kMapF16 ? 2 : 1;
   CUtensorMap fresh;
-  const int r = encode_map_2d(&fresh, true, W, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
-                              static_cast<uint64_t>(K) * 2, kTcK, kTcRows, true);
+  const int r = encode_map_2d(&fresh, dtype, base, inner, rows, inner * esize, box_inner, box_rows, swizzle128);
   if (r != cudaSuccess) return r;
   MapEntry& e = g_maps[g_map_next];
   e.map = fresh;
-  e.W = W;
-  e.M = M;
-  e.K = K;
+  e.base = base;
+  e.dtype = dtype;
+  e.inner = inner;
+  e.rows = rows;
+  e.box_inner = box_inner;
+  e.box_rows = box_rows;
   *out = e.map;
   g_map_next = (g_map_next + 1) % kMapCache;
   if (g_map_used < kMapCache) ++g_map_used;
@@ -603,10 +628,19 @@ static int w_map(const void* W, int64_t M, int K, CUtensorMap* out) {
 }
 
 int launch_tc(const TcPlan& p, const void* W, cudaStream_t st, bool pdl) {
-  CUtensorMap map;  // the type carries the 64-byte alignment the driver requires
-  const int e = w_map(W, p.a.M, p.a.K, &map);
+  CUtensorMap wmap, xmap;  // the type carries the 64-byte alignment the driver requires
+  // W: 128 x 64 f16 boxes, 128-byte swizzle; x (beyond 8 columns): [ncols][K] fp32, one
+  // stage of every column
+  int e = cached_map(W, kMapF16, static_cast<uint64_t>(p.a.K), static_cast<uint64_t>(p.a.M), kTcK, kTcRows, true,
+                     &wmap);
   if (e != cudaSuccess) return e;
-  return p.a.S > 1 ? launch_tc_t<true>(map, p, st, pdl) : launch_tc_t<false>(map, p, st, pdl);
+  std::memset(&xmap, 0, sizeof(xmap));  // unused up to 8 columns
+  if (p.a.ncols > 8) {
+    e = cached_map(p.a.x, kMapF32, static_cast<uint64_t>(p.a.K), static_cast<uint64_t>(p.a.ncols),
+                   static_cast<uint32_t>(p.a.subs * kTcK), static_cast<uint32_t>(p.a.ncols), false, &xmap);
+    if (e != cudaSuccess) return e;
+  }
+  return p.a.S > 1 ? launch_tc_t<true>(wmap, xmap, p, st, pdl) : launch_tc_t<false>(wmap, xmap, p, st, pdl);
 }
 
 }  // namespace gf

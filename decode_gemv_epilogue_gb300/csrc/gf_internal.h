@@ -161,10 +161,11 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
 // Encodes the tensor map of W ([M][K] f16, row stride 2K) and launches.
 int launch_tc(const TcPlan& p, const void* W, cudaStream_t st, bool pdl);
 
-// A 2-D tensor map (f16 or bytes) over rows of `inner` elements, `stride_bytes` apart,
-// with boxes of box_inner x box_rows (128-byte swizzle or none).  `map` points to a
-// 64-byte aligned CUtensorMap.  Returns a cudaError_t.
-int encode_map_2d(::CUtensorMap_st* map, bool f16, const void* base, uint64_t inner, uint64_t rows,
+// A 2-D tensor map of element type dtype (kMapU8, kMapF16, kMapF32) over rows of `inner`
+// elements, `stride_bytes` apart, with boxes of box_inner x box_rows (128-byte swizzle or
+// none).  `map` points to a 64-byte aligned CUtensorMap.  Returns a cudaError_t.
+enum { kMapU8 = 0, kMapF16 = 1, kMapF32 = 2 };
+int encode_map_2d(::CUtensorMap_st* map, int dtype, const void* base, uint64_t inner, uint64_t rows,
                   uint64_t stride_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 
 
