@@ -171,9 +171,10 @@ static int validate(const Call& c) {
 
 // The tensor-core kernel takes F16 weights with a batch of at least kTcMinCols
 // columns (no gated dual GEMV, no on-chip prologue), 16-byte aligned W and x, K a
-// multiple of 64.  Measured on GB300 (5120^2, graph + PDL): 2 columns 17.3 us vs
-// 12.8 us on the CUDA cores, 4 columns 18.1 vs 21.2 us, 8 columns 21.1 vs 31.9 us.
-constexpr int kTcMinCols = 4;
+// multiple of 64.  Measured on GB300 (signed FWHT + 5120^2, graph + PDL): 2 columns
+// 15.7 us vs 14.2 us on the CUDA cores, 3 columns 15.7 vs 21.4 us, 8 columns 17.0 vs
+// 31.9 us.
+constexpr int kTcMinCols = 3;
 
 static bool tc_eligible(const Call& c) {
   return c.wtype == GF_F16 && !c.W2 && !c.gamma && !c.signs && c.nseg == 0 && !(c.flags & GF_FLAG_NO_TENSOR_CORES) &&

@@ -314,7 +314,7 @@ def test_tc_plan(lib, M, K, ncols, expect_split):
 
 @pytest.mark.parametrize("kw,args", [
     ({"ncols": 1}, (W, 1, X, 4096, 4096)),                  # one column: CUDA cores
-    ({"ncols": 3}, (W, 1, X, 4096, 4096)),                  # below the tensor-core batch
+    ({"ncols": 2}, (W, 1, X, 4096, 4096)),                  # below the tensor-core batch
     ({"ncols": 8}, (W, 3, X, 4096, 4096)),                  # block formats: CUDA cores
     ({"ncols": 8}, (W, 1, X, 4096, 4096 + 32)),             # K % 64
     ({"ncols": 8}, (W + 2, 1, X, 4096, 4096)),              # W not 16-byte aligned

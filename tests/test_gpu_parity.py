@@ -182,7 +182,7 @@ def test_ncols_batch(G, ncols, wt):
     want = ogemv.gemv(raw, wt, X, M, K, ogemv.EPI_SILU_MUL, aux)
     for tc in (True, False):  # F16 batches default to the tensor cores
         got, path = run_gemv(G, raw, wt, X, M, K, ogemv.EPI_SILU_MUL, aux, ncols=ncols, tensor_cores=tc)
-        assert path == (G.PATH_TC if tc and wt == synth.F16 and ncols >= 4 else G.PATH_STREAM)
+        assert path == (G.PATH_TC if tc and wt == synth.F16 and ncols >= 3 else G.PATH_STREAM)
         assert_within(got, want, gemv_bound(raw, wt, X, M, K), "ncols %d tc %s" % (ncols, tc))
 
 

@@ -44,7 +44,7 @@ def run(G, raw, X, M, K, epi, aux=None, expect_path=None, **kw):
     return dst.cpu().numpy().astype(np.float64).reshape(ncols, M), info
 
 
-@pytest.mark.parametrize("M,K,ncols", [(128, 64, 4), (100, 4096, 8), (333, 1024, 5), (1000, 2048, 16),
+@pytest.mark.parametrize("M,K,ncols", [(128, 64, 4), (100, 4096, 8), (333, 1024, 5), (1000, 2048, 16), (200, 2048, 3),
                                        (4096, 512, 8), (640, 8192, 64), (257, 4096, 36)])
 def test_tc_shapes(G, M, K, ncols):
     raw = synth.weights(F16, M, K, seed=700 + ncols)
