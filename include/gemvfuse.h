@@ -95,9 +95,10 @@ typedef enum {
                             streams W before waiting for it.  Only valid when no kernel
                             still running in `stream` writes W. */
 #define GF_FLAG_NO_TENSOR_CORES 4u  /* use the CUDA-core kernels only.  By default F16 weights
-                            with 4..16 columns, K % 64 == 0 and 16-byte aligned W and x
-                            run on the tensor cores: tcgen05 MMAs of the f16 weights with
-                            x split into scaled f16 hi + lo parts, fp32 accumulation. */
+                            with 3 or more columns (16 per launch), K % 64 == 0 and
+                            16-byte aligned W and x run on the tensor cores: tcgen05 MMAs
+                            of the f16 weights with x split into scaled f16 hi + lo parts,
+                            fp32 accumulation. */
 #define GF_FLAG_NO_SPLIT_K 2u  /* never split K over a cluster of CTAs (by default a GEMV
                             with M <= SMs/2 rows gives each row range to a cluster of
                             2..8 CTAs that each stream a slice of K and add their
