@@ -1,4 +1,4 @@
-"""GPU parity of the tensor-core GEMV (F16 weights, batches of 2..16 columns per launch)
+"""GPU parity of the tensor-core GEMV (F16 weights, batches of 3..16 columns per launch)
 through the C ABI against the fp64 oracle, within 2e-5 * sum_k |W_ik x_k| + 1e-6: x
 enters as scaled f16 hi + lo parts (about 2^-22 relative), f16 products are exact and
 the accumulation is fp32.  Covers ragged tiles, split K, every tail, wide dynamic
@@ -129,3 +129,23 @@ def test_tc_wide_batch_blocks_of_16(G):
     got, _ = run(G, raw, X, M, K, ogemv.EPI_SILU_MUL, aux, expect_path=G.PATH_TC)
     want = ogemv.gemv(raw, F16, X, M, K, ogemv.EPI_SILU_MUL, aux)
     assert_within(got, want, gemv_bound(raw, F16, X, M, K), "tc 100 columns")
+
+
+@pytest.mark.parametrize("ncols", [3, 8, 13, 16])
+@pytest.mark.parametrize("epi", [ogemv.EPI_ADD, ogemv.EPI_SILU_MUL])
+def test_tc_every_split_width(G, ncols, epi):
+    """Row counts that give every cluster size the planner can pick (1..8 CTAs splitting K;
+    ragged last tiles), each with the batch widths whose column owners (column c belongs
+    to rank c % S) wrap differently: the split-K exchange and the per-rank tails."""
+    K = 1024
+    seen = set()
+    for M in (10240, 8192, 5184, 4196, 3800, 3100, 2600, 1000):
+        raw = synth.weights(F16, M, K, seed=770 + M % 97)
+        X = synth.normal(ncols * K, seed=771 + M % 89).reshape(ncols, K)
+        aux = synth.normal(ncols * M, seed=772 + M % 83).reshape(ncols, M)
+        got, info = run(G, raw, X, M, K, epi, aux, expect_path=G.PATH_TC)
+        seen.add(info["split"])
+        want = ogemv.gemv(raw, F16, X, M, K, epi, aux)
+        assert_within(got, want, gemv_bound(raw, F16, X, M, K),
+                      "tc %dx%d n%d split %d epi %d" % (M, K, ncols, info["split"], epi))
+    assert {1, 2, 8} <= seen and len(seen) >= 5, seen
