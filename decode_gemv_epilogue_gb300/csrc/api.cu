@@ -370,10 +370,13 @@ static int plan_call(const Call& c, Plan& p, int* generic_smem, int* generic_gri
 
 // One kernel launch with every argument resolved: what a call plans, and what a
 // prepared call keeps (gf_prepare) so that launching it does no planning at all.
-enum { REC_FWHT = 0, REC_TC = 1, REC_STREAM = 2, REC_GENERIC = 3 };
+enum { REC_FWHT = 0, REC_TC = 1, REC_STREAM = 2, REC_GENERIC = 3, REC_COPY = 4 };
 struct LaunchRec {
   int kind;
   bool pdl;
+  const void* csrc;  // host staging copy (device-addressable pointers)
+  void* cdst;
+  int64_t cbytes;
   int wtype, ncols;
   const void* W;  // tensor-core path: the matrix of the tensor map
   const float* fx;  // stand-alone FWHT
@@ -457,7 +460,9 @@ static int plan_one(const Call& c, float* dst, LaunchRec& r) {
 
 static int issue(const LaunchRec& r, cudaStream_t st) {
   int e;
-  if (r.kind == REC_FWHT) {
+  if (r.kind == REC_COPY) {
+    e = launch_copy(r.cdst, r.csrc, r.cbytes, st, r.pdl);
+  } else if (r.kind == REC_FWHT) {
     e = launch_fwht(r.fx, r.fsigns, r.fdst, r.fn, r.fB, r.fnsigns, st);
   } else if (r.kind == REC_TC) {
     e = launch_tc(r.tp, r.W, st, r.pdl);
@@ -862,7 +867,7 @@ const char* gf_status_string(int status) {
 
 int gf_last_cuda_error(void) { return t_last_cuda_error; }
 
-int gf_version(void) { return 4; }
+int gf_version(void) { return 5; }
 
 // ------------------------------------------------------------------ prepared calls
 struct gf_prepared {
@@ -933,6 +938,78 @@ int gf_launch_prepared(const gf_prepared* const* calls, int n, void* stream) {
 void gf_free_prepared(gf_prepared* p) {
   if (!p) return;
   delete p;
+}
+
+// ------------------------------------------------------------------ host staging copies
+// Checks a gf_copy request; on GF_OK *ks / *kd are the addresses the kernel uses (the
+// device view of pinned host memory).  Shape checks come first and need no device.
+static int check_copy(void* dst, const void* src, int64_t bytes, const void** ks, void** kd) {
+  if (bytes < 0 || bytes % 16 != 0) return GF_ERR_INVALID;
+  if (bytes == 0) return GF_OK;
+  if (!dst || !src) return GF_ERR_INVALID;
+  if (!aligned(dst, 16) || !aligned(src, 16)) return GF_ERR_ALIGN;
+  if (ranges_overlap(src, bytes, dst, bytes)) return GF_ERR_ALIAS;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError());
+  const void* in[2] = {src, dst};
+  void* outp[2] = {nullptr, nullptr};
+  for (int i = 0; i < 2; ++i) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, in[i]) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return GF_ERR_INVALID;
+    }
+    if (at.type == cudaMemoryTypeDevice) {
+      if (at.device != dev) return GF_ERR_INVALID;
+      outp[i] = const_cast<void*>(in[i]);
+    } else if (at.type == cudaMemoryTypeHost) {
+      if (!at.devicePointer) return GF_ERR_INVALID;
+      outp[i] = at.devicePointer;  // the address of `in[i]` in the device's view
+    } else if (at.type == cudaMemoryTypeManaged) {
+      outp[i] = const_cast<void*>(in[i]);
+    } else {  // pageable host memory: not taken, even where the device could read it
+      return GF_ERR_INVALID;
+    }
+  }
+  *ks = outp[0];
+  *kd = outp[1];
+  return GF_OK;
+}
+
+int gf_copy(void* dst, const void* src, int64_t bytes, uint32_t flags, void* stream) {
+  const void* ks = nullptr;
+  void* kd = nullptr;
+  const int v = check_copy(dst, src, bytes, &ks, &kd);
+  if (v != GF_OK || bytes == 0) return v;
+  const int e = gf::launch_copy(kd, ks, bytes, static_cast<cudaStream_t>(stream), (flags & GF_FLAG_PDL) != 0);
+  return e != cudaSuccess ? cuda_fail(static_cast<cudaError_t>(e)) : GF_OK;
+}
+
+int gf_prepare_copy(void* dst, const void* src, int64_t bytes, uint32_t flags, gf_prepared** out) {
+  if (!out) return GF_ERR_INVALID;
+  *out = nullptr;
+  const void* ks = nullptr;
+  void* kd = nullptr;
+  const int v = check_copy(dst, src, bytes, &ks, &kd);
+  if (v != GF_OK) return v;
+  gf_prepared* p = new (std::nothrow) gf_prepared;
+  if (!p) return GF_ERR_INVALID;
+  if (cudaGetDevice(&p->device) != cudaSuccess) {
+    delete p;
+    return cuda_fail(cudaGetLastError());
+  }
+  p->n = 0;
+  if (bytes > 0) {
+    gf::LaunchRec& r = p->recs[0];
+    r.kind = gf::REC_COPY;
+    r.pdl = (flags & GF_FLAG_PDL) != 0;
+    r.csrc = ks;
+    r.cdst = kd;
+    r.cbytes = bytes;
+    p->n = 1;
+  }
+  *out = p;
+  return GF_OK;
 }
 
 // ------------------------------------------------------------------ step graphs

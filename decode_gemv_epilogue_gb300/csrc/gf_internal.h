@@ -212,6 +212,8 @@ int launch_generic(int wtype, int ncols, const GenericArgs& a, int grid, int sme
                    cudaStream_t st, bool pdl);
 int launch_fwht(const float* x, const float* signs, float* dst, int64_t n, int B, int nsigns,
                 cudaStream_t st);
+// Kernel copy of `bytes` (a multiple of 16) between device-addressable ranges.
+int launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t st, bool pdl);
 int launch_elementwise(int op, const float* a, const float* b, int64_t nb, float* dst, int64_t n,
                        cudaStream_t st);
 int launch_dequantize(int wtype, const uint8_t* W, int64_t M, int64_t K, int64_t row_bytes,

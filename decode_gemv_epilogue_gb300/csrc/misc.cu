@@ -1,9 +1,42 @@
-// Stand-alone kernels: the signed FWHT, the unfused element-wise control ops and the
-// dequantize test hook.
+// Stand-alone kernels: the host staging copy, the signed FWHT, the unfused element-wise
+// control ops and the dequantize test hook.
+#include <algorithm>
+
 #include "gf_device.cuh"
 #include "gf_internal.h"
 
 namespace gf {
+
+// ------------------------------------------------------------------ host staging copy
+// dst[i] = src[i] for n16 16-byte words; either side may be host memory the device
+// addresses (pinned, registered, or pageable where the device reads it).  Waits for the
+// preceding grid first (src may be its output) and lets the next one start early.
+__global__ void __launch_bounds__(256) copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                     int64_t n16) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride)
+    dst[i] = src[i];
+}
+
+int launch_copy(void* dst, const void* src, int64_t bytes, cudaStream_t st, bool pdl) {
+  const int64_t n16 = bytes / 16;
+  if (n16 <= 0) return cudaSuccess;
+  // one word per thread up to 1024 CTAs (latency-bound sizes), then a grid-stride loop
+  const int64_t grid = std::min<int64_t>((n16 + 255) / 256, 1024);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, copy16_kernel, static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+}
 
 // ------------------------------------------------------------------ signed FWHT
 // Each CTA transforms E consecutive elements (a whole number of blocks) in shared

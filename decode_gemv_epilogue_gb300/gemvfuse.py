@@ -75,6 +75,8 @@ MULTI_MAX = 4
 _gemv_multi = _sig("gemv_multi", [ctypes.POINTER(MultiItem), _i32, _i32, _vp, _i64, ctypes.POINTER(GfOpts), _vp])
 _prepare_multi = _sig("gf_prepare_multi", [ctypes.POINTER(MultiItem), _i32, _i32, _vp, _i64,
                                            ctypes.POINTER(GfOpts), ctypes.POINTER(_vp)])
+_copy = _sig("gf_copy", [_vp, _vp, _i64, _u32, _vp])
+_prepare_copy = _sig("gf_prepare_copy", [_vp, _vp, _i64, _u32, ctypes.POINTER(_vp)])
 _graph_create = _sig("gf_graph_create", [ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp)])
 _graph_launch = _sig("gf_graph_launch", [_vp, _vp])
 _graph_free = _sig("gf_graph_free", [_vp], None)
@@ -379,3 +381,22 @@ def device_status(reset=False):
 
 def last_cuda_error():
     return _last_cuda_error()
+
+
+def copy(dst, src, nbytes, pdl=False, stream=None, check=True):
+    """gf_copy: nbytes from src to dst by a kernel (device memory, or host memory the
+    device addresses, e.g. a pinned tensor)."""
+    st = _copy(_ptr(dst), _ptr(src), nbytes, FLAG_PDL if pdl else 0, _stream(stream))
+    if check:
+        _check(st, "gf_copy")
+    return st
+
+
+def prepare_copy(dst, src, nbytes, pdl=False, check=True):
+    """gf_prepare_copy: the copy gf_copy would launch, as a prepared call (a graph may hold
+    it beside the GEMVs)."""
+    h = _vp()
+    st = _prepare_copy(_ptr(dst), _ptr(src), nbytes, FLAG_PDL if pdl else 0, ctypes.byref(h))
+    if check:
+        _check(st, "gf_prepare_copy")
+    return Prepared(h.value, (dst, src)) if st == OK else st

@@ -222,6 +222,25 @@ GF_API int gf_launch_prepared(const gf_prepared* const* calls, int n, void* stre
 /* Releases a handle (NULL is ignored).  Launches already issued are not affected. */
 GF_API void gf_free_prepared(gf_prepared* p);
 
+/* Host staging of a decode step by a kernel instead of the copy engine, so that a step's
+ * input upload, its GEMVs and its result download can be one stream sequence or one CUDA
+ * graph (gf_graph_create takes the handle of gf_prepare_copy like any prepared call).
+ * Copies `bytes` bytes from src to dst; each range may be device memory of the current
+ * device, managed memory, or pinned host memory (cudaHostAlloc / cudaMallocHost, or
+ * registered with cudaHostRegister).
+ *  - src and dst 16-byte aligned (GF_ERR_ALIGN), bytes >= 0 and a multiple of 16
+ *    (GF_ERR_INVALID), the ranges disjoint (GF_ERR_ALIAS); pageable host memory, or
+ *    device memory of another device: GF_ERR_INVALID (nothing launched).  bytes == 0
+ *    launches nothing.
+ *  - flags: GF_FLAG_PDL launches it with programmatic dependent launch; the kernel
+ *    waits for the preceding grid before reading src, so it may read what that grid
+ *    wrote, and the next launch may start early (every kernel of this library waits
+ *    before reading what a preceding grid writes).
+ *  - Host memory written here is complete when the stream (or graph launch) is; the
+ *    copy uses no copy engine and is not ordered with copies in other streams. */
+GF_API int gf_copy(void* dst, const void* src, int64_t bytes, uint32_t flags, void* stream);
+GF_API int gf_prepare_copy(void* dst, const void* src, int64_t bytes, uint32_t flags, gf_prepared** out);
+
 /* A decode step as one launch: gf_graph_create records the launches of calls[0..n)
  * (n >= 1, in order, as gf_launch_prepared would issue them, programmatic dependent
  * launches included) into a CUDA graph and instantiates it; gf_graph_launch replays it

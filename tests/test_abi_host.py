@@ -28,7 +28,7 @@ def test_header_declares_the_abi():
             "gf_plan", "gf_plan_glu", "gf_device_status", "gf_status_string", "gf_last_cuda_error",
             "gf_version", "gf_prepare", "gf_prepare_glu", "gf_launch_prepared", "gf_free_prepared",
             "gf_graph_create", "gf_graph_launch", "gf_graph_free", "gemv_multi", "gf_prepare_multi",
-            "gf_repair_count"} <= names
+            "gf_repair_count", "gf_copy", "gf_prepare_copy"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -51,7 +51,7 @@ def test_status_strings(lib):
     assert lib.status_string(0) == "GF_OK"
     for s in (-1, -2, -3, -4, -5, -6):
         assert lib.status_string(s).startswith("GF_ERR_")
-    assert lib.version() == 4
+    assert lib.version() == 5
 
 
 def g(lib, *a, **k):
@@ -325,6 +325,23 @@ def test_tc_plan(lib, M, K, ncols, expect_split):
 def test_tc_not_chosen(lib, kw, args):
     path, _ = lib.plan(*args, 0, None, D, **kw)
     assert path in (lib.PATH_STREAM, lib.PATH_GENERIC)
+
+
+@pytest.mark.parametrize("dst,src,nbytes,expect", [
+    (D, X, -16, -1),            # negative size
+    (D, X, 40, -1),             # not a multiple of 16
+    (None, X, 64, -1),          # null destination
+    (D, None, 64, -1),          # null source
+    (D + 8, X, 64, -4),         # destination not 16-byte aligned
+    (D, X + 4, 64, -4),         # source not 16-byte aligned
+    (X + 32, X, 64, -2),        # overlapping ranges
+    (D, X, 0, 0),               # nothing to copy: OK, nothing launched
+    (None, None, 0, 0),
+])
+def test_copy_validation(lib, dst, src, nbytes, expect):
+    assert lib.copy(dst, src, nbytes, stream=0, check=False) == expect
+    if expect != 0:  # (a valid handle needs a current device)
+        assert lib.prepare_copy(dst, src, nbytes, check=False) == expect
 
 
 def test_selftest_wait_validation(lib):
