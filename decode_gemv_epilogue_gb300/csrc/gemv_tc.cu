@@ -1,28 +1,30 @@
 // Tensor-core GEMV for F16 weights and a batch of columns (5th-generation tensor cores:
 // tcgen05.mma with the accumulator in tensor memory).
 //
-// A CTA owns one tile of 128 rows of W and a slice of its K range.  Per stage of 64-element
-// K sub-tiles, warp 0 loads the 128 x 64 f16 tiles of W with 2-D TMA copies (128-byte
-// swizzle, K-major: the tensor cores read them straight from shared memory) and the
-// batch's x for the same elements (one bulk copy per column up to 8 columns, one 2-D copy
-// of all columns beyond), x once the preceding grid, which may write it, has finished
-// (the first W stage goes out before that); warps 2..5 turn the staged x into f16 rows
-// of B in the same swizzled layout.  x is fp32, so each column is scaled by an exact power of two
-// (its largest |x| over the CTA's K slice lands in [2^14, 2^15)) and split into
-// hi = f16(x) and lo = f16(x - hi): B holds Np rows of hi followed by Np rows of lo
-// (Np = columns rounded up to 8).  One thread of warp 1 issues four
-// 128 x (2 Np) x 16 MMAs per stage into a TMEM accumulator and releases the stage
-// with tcgen05.commit.  After the last stage the same four warps read their lane
-// quarter of TMEM (one row per thread), form y = (hi part + lo part) * 2^-s, apply the
-// tail and write dst.  hi + lo represents x to about 2^-22 relative, products of f16
-// values are exact in fp32 and the accumulation is fp32.
+// A CTA owns one tile of 128 rows of W and a slice of its K range.  Per stage of
+// 64-element K sub-tiles, warp 0 loads the 128 x 64 f16 tiles of W with 2-D TMA copies
+// (128-byte swizzle, K-major: the tensor cores read them straight from shared memory)
+// and the batch's x for the same elements (one bulk copy per column up to 8 columns, one
+// 2-D copy of all columns beyond), x once the preceding grid, which may write it, has
+// finished (the first W stage goes out before that).  Warps 2..5 turn the staged x into
+// f16 rows of B in the same swizzled layout.  x is fp32, so each column is scaled by an
+// exact power of two (its largest |x| over the CTA's K slice lands in [2^14, 2^15)) and
+// split into hi = f16(x) and lo = f16(x - hi): B holds Np rows of hi followed by Np rows
+// of lo (Np = columns rounded up to 8).  One thread of warp 1 issues the stage's
+// 128 x (2 Np) x 16 MMAs, rotating over four TMEM accumulators, and releases the stage
+// with tcgen05.commit.  After the last stage the same four warps read their lane quarter
+// of TMEM (one row per thread), form y = (hi part + lo part) * 2^-s, apply the tail and
+// write dst.  hi + lo represents x to about 2^-22 relative, products of f16 values are
+// exact in fp32 and the accumulation is fp32.
 //
-// Rows alone give too few tiles for 152 SMs (e.g. 40 for 5120 rows), so K is split
-// over a cluster of S CTAs per tile (S = SMs / tiles, at most 8).  Column c of the batch
-// is finalised by rank c % S: every rank stores its per-row partial sums of the other
-// ranks' columns into their shared memory, and each owner adds the S partials in rank
-// order (deterministic) and writes its columns, so the ranks share the final stores.  Every wait is bounded; on a timeout the kernel sets the error
-// word, drains its copies and MMAs, frees its tensor memory and returns.
+// Rows alone give too few tiles for 152 SMs (e.g. 40 for 5120 rows), so K is split over
+// a cluster of S CTAs per tile (S = SMs / tiles, at most 8).  Column c of the batch is
+// finalised by rank c % S: every rank sends its per-row partial sums of the other ranks'
+// columns into their shared memory (st.async, completing bytes on the owner's mbarrier),
+// and each owner adds the S partials in rank order (deterministic) and writes its
+// columns, so the ranks share the final stores.  Every wait is bounded; on a timeout the
+// kernel sets the error word, drains its copies and MMAs, frees its tensor memory and
+// returns.
 #include <cuda.h>
 
 #include <algorithm>
