@@ -51,7 +51,9 @@ constexpr int kTcMaxSubs = 4;                   // sub-tiles per stage
 constexpr int kTcAcc = 4;
 
 // ------------------------------------------------------------------ kernel
-// Shared memory from a 1024-aligned base: barriers and the TMEM address slot [0, 512);
+// Shared memory from a 1024-aligned base: barriers (per stage: W landed, B written, slot
+// empty, x landed; the accumulator and exchange barriers) and the TMEM address slot
+// [0, 512);
 // per-warp column maxima [512, 1536); scales and inverse scales [1536, 2048); the
 // split-K exchange [2048, off_a); NS A stages (16 KB each) at off_a; NS B stages at
 // off_b (2 Np rows of 128 bytes each).
@@ -67,6 +69,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   const int NS = a.NS;
   const uint32_t fullA0 = sb, fullB0 = sb + 8u * NS, empty0 = sb + 16u * NS;
   const uint32_t accbar = sb + 24u * NS, xchbar = accbar + 8u;
+  const uint32_t xfull0 = sb + 24u * NS + 24u;  // NS barriers: a stage's x has landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 24 * NS + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + 24 * NS + 20);
   float* smax = reinterpret_cast<float*>(base + 512);   // [4 warps][64] column maxima
@@ -94,6 +97,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     *abort_flag = 0;
     for (int i = 0; i < NS; ++i) {
       mbar_init(fullA0 + 8u * i, 1);
+      mbar_init(xfull0 + 8u * i, 1);
       mbar_init(fullB0 + 8u * i, 128);
       mbar_init(empty0 + 8u * i, 1);
     }
@@ -122,15 +126,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       // the stage's x: one 2-D copy of every column for wide batches, one bulk copy per
       // column up to 8 columns (measured faster there behind the transform-once prologue)
       const bool x2d = a.ncols > 8;
+      // x lands on its own barrier: the converters start on a stage as soon as its x is
+      // there (an L2 read) instead of waiting for its W tiles (a DRAM read), and the MMAs
+      // find B ready when W lands.  x of stage i goes out after the producer saw the slot
+      // empty, so its arrival also tells the converters that the slot's B is free.
       auto issue_x = [&](int i, int slot) {
+        const uint32_t xb = xfull0 + 8u * slot;
+        mbar_arrive_expect_tx(xb, static_cast<uint32_t>(a.ncols * xrow * 4));
         if (x2d) {
-          tma_load_2d(sX + static_cast<uint32_t>(slot * a.x_stage_bytes), &xmap, (st0 + i) * xrow, 0,
-                      fullA0 + 8u * slot);
+          tma_load_2d(sX + static_cast<uint32_t>(slot * a.x_stage_bytes), &xmap, (st0 + i) * xrow, 0, xb);
         } else {
           for (int c = 0; c < a.ncols; ++c)
             bulk_g2s(sX + static_cast<uint32_t>(slot * a.x_stage_bytes + c * xrow * 4),
                      a.x + static_cast<int64_t>(c) * a.K + static_cast<int64_t>(st0 + i) * xrow,
-                     static_cast<uint32_t>(xrow * 4), fullA0 + 8u * slot);
+                     static_cast<uint32_t>(xrow * 4), xb);
         }
       };
       int issued = 0, x_done = 0;  // stages whose W / x copies are out
@@ -141,8 +150,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         // the first NS stages are empty: no wait (see the stream kernel)
         if (i >= NS && !mbar_wait_or_abort(empty0 + 8u * slot, static_cast<uint32_t>(par ^ 1), abort_flag, a.err))
           break;
-        mbar_arrive_expect_tx(fullA0 + 8u * slot,
-                              static_cast<uint32_t>(subs * kTcABytes + a.ncols * xrow * 4));
+        mbar_arrive_expect_tx(fullA0 + 8u * slot, static_cast<uint32_t>(subs * kTcABytes));
         for (int sbt = 0; sbt < subs; ++sbt)
           tma_load_2d(sA + static_cast<uint32_t>((slot * subs + sbt) * kTcABytes), &tmap,
                       ((st0 + i) * subs + sbt) * kTcK, row0, fullA0 + 8u * slot);
@@ -157,8 +165,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       if (issued < nmy) {  // aborted: complete the stages' x, then wait (bounded) for the copies in flight
         if (!waited) pdl_wait();
         for (; x_done < issued; ++x_done) issue_x(x_done, x_done % NS);
-        for (int i = max(0, issued - NS); i < issued; ++i)
+        for (int i = max(0, issued - NS); i < issued; ++i) {
           (void)mbar_wait(fullA0 + 8u * (i % NS), static_cast<uint32_t>((i / NS) & 1));
+          (void)mbar_wait(xfull0 + 8u * (i % NS), static_cast<uint32_t>((i / NS) & 1));
+        }
       }
     }
   } else if (warp == 1) {
@@ -239,7 +249,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     // conversions and stores (one warp per SM sub-partition runs this, so independent
     // work is what hides the latencies); ring slot and phase kept incrementally
     for (int i = 0, slot = 0, par = 0; i < nmy; ++i, slot = (slot + 1 == NS) ? 0 : slot + 1, par ^= (slot == 0)) {
-      ok = ok && mbar_wait_or_abort(fullA0 + 8u * slot, static_cast<uint32_t>(par), abort_flag, a.err);
+      ok = ok && mbar_wait_or_abort(xfull0 + 8u * slot, static_cast<uint32_t>(par), abort_flag, a.err);
       float4 c[kTcMaxSubs][2];
       const float* xs = reinterpret_cast<const float*>(base + a.off_x + slot * a.x_stage_bytes) +
                         n_own * subs * kTcK + 8 * c8_own;
@@ -505,7 +515,7 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
       break;
     }
   }
-  if (NS < 2 || 24 * NS + 24 > 512) return false;
+  if (NS < 2 || 32 * NS + 24 > 512) return false;
   if (tiles * S > INT32_MAX) return false;
   TcArgs& a = p.a;
   std::memset(&a, 0, sizeof(a));
