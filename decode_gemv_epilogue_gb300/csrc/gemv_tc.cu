@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   const uint32_t fullA0 = sb, fullB0 = sb + 8u * NS, empty0 = sb + 16u * NS;
   const uint32_t accbar = sb + 24u * NS, xchbar = accbar + 8u;
   const uint32_t xfull0 = sb + 24u * NS + 24u;  // NS barriers: a stage's x has landed
+  const uint32_t tmemdone = xfull0 + 8u * NS;    // every epilogue thread's TMEM reads are done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 24 * NS + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + 24 * NS + 20);
   float* smax = reinterpret_cast<float*>(base + 512);   // [4 warps][64] column maxima
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
       mbar_init(empty0 + 8u * i, 1);
     }
     mbar_init(accbar, 1);
+    mbar_init(tmemdone, 128);
     mbar_init(xchbar, 1);
     if constexpr (SPLIT) {  // the partials this CTA receives: S - 1 peers x its columns x 128 rows
       const int nown = a.ncols > crank ? (a.ncols - 1 - crank) / S + 1 : 0;
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
     }
     fence_mbar_init();
   }
+  __syncwarp();  // warp 0 reaches the CTA-wide barrier below converged
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(a.tmem_cols));
   tc_fence_before();
   if constexpr (SPLIT)
@@ -371,6 +374,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
         }
       }
     }
+    // the tensor memory may be freed once every epilogue thread is past its reads (an
+    // explicit barrier: the freeing warp does not rely on the CTA-wide one below)
+    tc_fence_before();
+    mbar_arrive(tmemdone);
     if constexpr (SPLIT) {
       // wait until every peer's partials of this CTA's columns have landed, then add the
       // S partials of each column in rank order and apply the tail
@@ -411,6 +418,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(const __grid_con
   __syncthreads();
   if constexpr (SPLIT) cluster_sync_all();  // no CTA leaves while a peer may still store into it
   if (warp == 1) {
+    (void)mbar_wait(tmemdone, 0u);  // bounded; every epilogue thread arrives, also after an abort
+    __syncwarp();                    // the dealloc is a warp-wide instruction
     tc_fence_after();
     tmem_dealloc(tmem, static_cast<uint32_t>(a.tmem_cols));
   }
@@ -515,7 +524,7 @@ bool plan_tc(int64_t M, int64_t K, int ncols, int epi, const DeviceLimits& lim, 
       break;
     }
   }
-  if (NS < 2 || 32 * NS + 24 > 512) return false;
+  if (NS < 2 || 32 * NS + 32 > 512) return false;
   if (tiles * S > INT32_MAX) return false;
   TcArgs& a = p.a;
   std::memset(&a, 0, sizeof(a));
