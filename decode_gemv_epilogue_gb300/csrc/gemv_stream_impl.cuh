@@ -479,6 +479,7 @@ __global__ void __launch_bounds__(stream_threads(WT, NC), 1)
     mbar_init(xchbar, static_cast<uint32_t>(S > 1 ? (S - 1) * a.ncw * 32 : 1));
     fence_mbar_init();
   }
+  __syncwarp();  // warp 0 reaches the CTA-wide barrier below converged
   if constexpr (kSplit)
     cluster_sync_all();  // peers arrive on rank 0's barrier only after it is initialised
   else
