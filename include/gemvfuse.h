@@ -19,10 +19,10 @@
  *         the RMS_NORM + MUL pair ahead of a matmul (the RMS-normalisation prologue).
  *
  * Conventions for every entry point:
- *  - All array pointers are DEVICE pointers owned by the caller.  The library never
- *    allocates, frees or keeps a pointer after the call returns, except for handles:
- *    a prepared call keeps its pointers (host memory only), and a step graph owns its
- *    CUDA graph.
+ *  - All array pointers are DEVICE pointers owned by the caller (gf_copy's may also be
+ *    pinned host memory).  The library never allocates, frees or keeps a pointer after
+ *    the call returns, except for handles: a prepared call keeps its pointers (host
+ *    memory only), and a step graph owns its CUDA graph.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is enqueued
  *    asynchronously; the call returns once it is launched.
  *  - Arguments are validated on the host before anything is launched.  A non-zero
@@ -31,8 +31,10 @@
  *  - Vectors are contiguous float32.  A batch of ncols columns is column-major:
  *    x is [ncols][K], aux and dst are [ncols][M].
  *  - The library holds no state between calls other than per-device launch limits,
- *    a device error word (see gf_device_status()) and a repair counter
- *    (gf_repair_count()).
+ *    a device error word (see gf_device_status()), a repair counter
+ *    (gf_repair_count()) and a host-side cache of encoded tensor maps (address, shape
+ *    and box of recent tensor-core operands; an entry never goes stale, as it holds
+ *    no data).
  */
 #ifndef GEMVFUSE_H
 #define GEMVFUSE_H
