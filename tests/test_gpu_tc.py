@@ -105,7 +105,7 @@ def test_tc_deterministic(G):
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("ncols", [4, 8])
+@pytest.mark.parametrize("ncols", [3, 4, 8, 12, 16])  # 12, 16: x by one 2-D copy per stage
 def test_tc_full_fwht_f16_5120_workspace(G, ncols):
     M, K, B = 5120, 5120, 1024
     raw = synth.weights(F16, M, K, seed=750)
@@ -149,3 +149,34 @@ def test_tc_every_split_width(G, ncols, epi):
         assert_within(got, want, gemv_bound(raw, F16, X, M, K),
                       "tc %dx%d n%d split %d epi %d" % (M, K, ncols, info["split"], epi))
     assert {1, 2, 8} <= seen and len(seen) >= 5, seen
+
+
+def test_tc_with_staging_copies_through_launch_prepared(G):
+    """Upload, the 8-column tensor-core call with its transform, download: issued with
+    gf_launch_prepared (no graph), twice with new host inputs."""
+    M, K, B, nc = 1000, 4096, 1024, 8
+    raw = synth.weights(F16, M, K, seed=780)
+    Wd = dev_tensor(raw)
+    s = synth.rademacher(B, seed=781)
+    sd = dev_tensor(s)
+    xh = torch.empty(nc * K, dtype=torch.float32).pin_memory()
+    rh = torch.empty(nc * M, dtype=torch.float32).pin_memory()
+    yh = torch.empty(nc * M, dtype=torch.float32).pin_memory()
+    xd, rd, ws = (torch.empty(nc * K, device="cuda"), torch.empty(nc * M, device="cuda"),
+                  torch.empty(nc * K, device="cuda"))
+    calls = [G.prepare_copy(xd, xh, 4 * nc * K), G.prepare_copy(rd, rh, 4 * nc * M, pdl=True),
+             G.prepare(Wd, F16, xd, M, K, ogemv.EPI_ADD, rd, rd, ncols=nc, fwht_signs=sd, fwht_block=B,
+                       fwht_workspace=ws, pdl=True),
+             G.prepare_copy(yh, rd, 4 * nc * M, pdl=True)]
+    for step in range(2):
+        X = synth.normal(nc * K, seed=782 + step).reshape(nc, K)
+        R = synth.normal(nc * M, seed=784 + step).reshape(nc, M)
+        xh.copy_(torch.from_numpy(X.astype(np.float32).reshape(-1)))
+        rh.copy_(torch.from_numpy(R.astype(np.float32).reshape(-1)))
+        G.launch_prepared(calls)
+        torch.cuda.synchronize()
+        Xp = np.stack([ofwht.fwht_signed(X[c], s, B) for c in range(nc)])
+        E = np.stack([fwht_err_bound(X[c], B) for c in range(nc)])
+        want = ogemv.gemv(raw, F16, Xp, M, K, ogemv.EPI_ADD, R)
+        assert_within(yh.numpy().astype(np.float64).reshape(nc, M), want,
+                      gemv_bound(raw, F16, Xp, M, K, x_err=E), "step %d" % step)
