@@ -94,6 +94,7 @@ def test_gemv_fused_guard_bands(G, wt, M, K):
 
 
 @pytest.mark.parametrize("wt,M,K,ncols", [(synth.F16, 611, 1024, 3), (synth.F16, 611, 1024, 8),
+                                           (synth.F16, 611, 1024, 12), (synth.F16, 8200, 1024, 13),
                                            (synth.Q4_0, 611, 2048, 5), (synth.F32, 65, 33, 2)])
 def test_batch_and_fwht_workspace_guard_bands(G, wt, M, K, ncols):
     B = 1024 if K % 1024 == 0 else 0
@@ -196,3 +197,21 @@ def test_noalloc_guard_bands(G):
     E = np.stack([fwht_err_bound(X[c], B) for c in range(ncols)])
     want = ogemv.gemv(raw, synth.F16, Xp, M, K, ogemv.EPI_ADD, r)
     assert_within(aux.host().reshape(ncols, M), want, gemv_bound(raw, synth.F16, Xp, M, K, x_err=E), "noalloc")
+
+
+@pytest.mark.parametrize("nbytes", [16, 4112, 1 << 20])
+def test_copy_guard_bands(G, nbytes):
+    """The staging copy writes exactly its range of a device buffer and reads exactly its
+    range of another; host to device and device to host."""
+    n = nbytes // 4
+    src = np.random.default_rng(nbytes).standard_normal(n).astype(np.float32)
+    host_in = torch.from_numpy(src).pin_memory()
+    dst = Guarded(n=n, fill=0.0)
+    assert G.copy(dst.t, host_in, nbytes) == G.OK
+    check_all(dst)
+    assert np.array_equal(dst.t.cpu().numpy(), src)
+    srcd = Guarded(src)
+    host_out = torch.zeros(n, dtype=torch.float32).pin_memory()
+    assert G.copy(host_out, srcd.t, nbytes) == G.OK
+    check_all(srcd)
+    assert np.array_equal(host_out.numpy(), src)
