@@ -327,6 +327,21 @@ def test_tc_not_chosen(lib, kw, args):
     assert path in (lib.PATH_STREAM, lib.PATH_GENERIC)
 
 
+@pytest.mark.parametrize("M,split", [(10240, 1), (8192, 2), (5184, 3), (4196, 4), (3800, 5), (3100, 6),
+                                     (2600, 7), (1000, 8)])
+@pytest.mark.parametrize("ncols", [3, 8, 13, 16])
+def test_tc_plan_split_sizes(lib, M, split, ncols):
+    """F16 batches of 3..16 columns plan onto the tensor cores; K is split over a cluster
+    of SMs // tiles CTAs (at most 8; without a device no residency limit lowers it), the
+    grid fits the 152 SMs at once, and the shared memory fits a CTA."""
+    path, info = lib.plan(W, 1, X, M, 1024, 4, A, A, ncols=ncols)
+    tiles = -(-M // 128)
+    assert path == lib.PATH_TC
+    assert info["split"] == split == min(8, 152 // tiles)
+    assert info["grid"] == tiles * split <= 152
+    assert info["threads"] == 192 and 3 <= info["stages"] <= 12 and info["smem"] <= 232448
+
+
 @pytest.mark.parametrize("dst,src,nbytes,expect", [
     (D, X, -16, -1),            # negative size
     (D, X, 40, -1),             # not a multiple of 16
